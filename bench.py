@@ -1,0 +1,375 @@
+"""Benchmark of the gated delta-rule chunked-prefill forward on GB300.
+
+One *step* is one complete forward (every kernel of the call: gate cumsum,
+gated K K^T, inverse, WY form, state scan, output, plus the chunk-parallel
+split when planned) over one batch of synthetic input resident in HBM.
+Default workload: B=4, H=16, T=4096, dk=dv=128, bf16 q/k/v, fp32 gates and
+state, h0 given, final state written.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunked-prefill fwd tokens/s and TFLOP/s (% of roofline), 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic_work(w, N, total_tokens):
+    """FLOP and bytes per call, implementation-independent.
+
+    Per token-head: FLOP = 4 C (dk + dv) + 6 dk dv (K K^T, Q K^T, A V-delta,
+    P V', K S, Q S, K^T V' as dense tiles); bytes = e (2 dk + 2 dv) + 8
+    (+ 4 dk for per-channel gates): read q, k, v, g, beta, write o.  Plus
+    4 dk dv per (sequence, head) for each of h0 (when given) and ht.
+    """
+    C, dk, dv, HV = w.chunk, w.K, w.V, w.hv
+    e = 2 if w.dtype == "bf16" else 4
+    flop = total_tokens * HV * (4 * C * (dk + dv) + 6 * dk * dv)
+    qk_bytes = total_tokens * w.H * e * 2 * dk          # q, k (per query/key head)
+    hv_bytes = total_tokens * HV * (e * 2 * dv + 8 + (4 * dk if w.gate == "channel" else 0))
+    state = N * HV * dk * dv * 4 * (2 if w.h0 else 1)   # h0 read, ht write
+    return float(flop), float(qk_bytes + hv_bytes + state)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_sha():
+    import glob
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gated_deltanet_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name, kernel):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(f"{workload_name}:{kernel}")
+    if not ent or ent.get("sources_sha") != kernel_sources_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import gated_deltanet_gb300 as gdn
+    from gdn_inputs import make_inputs, workload
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gdn.load_library()
+    w = workload(args.workload)
+    x = make_inputs(w, device=dev)
+    N = x["N"]
+    tokens = int(x["q"].shape[0] * x["q"].shape[1])
+    opts = dict(keys_unit_norm=True)  # the workloads L2-normalise k and use beta = sigmoid(.)
+    info = gdn.plan(int(x["q"].shape[0]), int(x["q"].shape[1]), w.H, w.hv, w.K, w.V, w.dtype, w.gate,
+                    num_seqs=N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
+                    max_seq_len=(w.T if w.varlen else 0), **opts)
+    o = torch.empty_like(x["v"])
+    ht = torch.empty(N, w.hv, w.K, w.V, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 2x L2 (129 MB)
+
+    def step():
+        gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
+                                   x["cu_seqlens"], out=o, final_state=ht,
+                                   max_seq_len=(w.T if w.varlen else 0), **opts)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if gdn.read_device_status() != 0:
+        raise RuntimeError("device status not clean after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.05)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flushed between timed steps (not timed)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if ws > 1:
+        dist.barrier()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    dev_ms = sum(per_step)
+    if ws > 1:
+        t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    status = gdn.read_device_status()
+
+    # end-to-end through the C ABI on pinned host buffers (copies inside the timed region)
+    xh = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+
+    def e2e_step():
+        gdn.chunk_gated_delta_rule_host(xh["q"], xh["k"], xh["v"], xh["g"], xh["beta"], xh["scale"], xh["h0"],
+                                        True, xh["cu_seqlens"], out=oh, final_state=hh, device=dev,
+                                        max_seq_len=(w.T if w.varlen else 0), **opts)
+    e2e_step()
+    n_e2e = max(3, min(20, args.steps // 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    h2d = sum(int(xh[k].numel() * xh[k].element_size()) for k in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")
+              if xh[k] is not None)
+    d2h = int(oh.numel() * oh.element_size() + hh.numel() * hh.element_size())
+
+    flop, byts = algorithmic_work(w, N, tokens)
+    peaks, peak_kind = read_peaks()
+    t_step = dev_ms / 1e3 / args.steps
+    value = ws * tokens * args.steps / (dev_ms / 1e3)
+    # dominant kernel: the fused scan; with a one-kernel plan the step time is its launch time
+    achieved = byts / t_step / 1e9
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dev_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded; q,k L2-normalised, beta=sigmoid(N(0,1)), g=logsigmoid(N(%g,%g)))"
+                % (w.g_mu, w.g_sigma),
+        "config": {"workload": w.name, "B": int(x["q"].shape[0]), "T": int(x["q"].shape[1]), "H": w.H,
+                   "HV": w.hv, "dk": w.K, "dv": w.V, "chunk": w.chunk, "gate": w.gate, "h0": w.h0,
+                   "sequences": N, "l2": "flushed (512 MiB write) before every timed step",
+                   "plan": {"engine": ["auto", "simt", "tc"][info.engine],
+                            "cp": ["auto", "off", "exact", "warmup"][info.cp_mode],
+                            "segments": info.segments, "kernels": info.kernels},
+                   "parallelism": f"replicas x{ws}"},
+        "tflops": flop / t_step / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind,
+                     "traffic": ncu_traffic(w.name, "scan"),
+                     "algorithmic_bytes": byts, "algorithmic_flop": flop,
+                     "roofline_ms": max(byts / (peaks["hbm_gbs"] * 1e9),
+                                        flop / (peaks["bf16_tflops"] * 1e12)) * 1e3},
+        "e2e": {"value": ws * tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": info.kernels * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _oracle_sample(w, x, T_s):
+    from oracle import recurrence
+    sl = slice(0, T_s)
+    if x["cu_seqlens"] is not None:
+        # packed input: the first sequences whose lengths add up to about T_s tokens
+        cu = x["cu_seqlens"].numpy()
+        n = int(max(1, (cu <= T_s).sum() - 1))
+        e = int(cu[n])
+        return (lambda: recurrence(x["q"][:, :e], x["k"][:, :e], x["v"][:, :e], x["g"][:, :e],
+                                   x["beta"][:, :e], x["scale"], x["h0"][:n] if x["h0"] is not None else None,
+                                   x["cu_seqlens"][:n + 1])), e
+    return (lambda: recurrence(x["q"][:, sl], x["k"][:, sl], x["v"][:, sl], x["g"][:, sl], x["beta"][:, sl],
+                               x["scale"], x["h0"], None, gate=x["gate"])), x["q"].shape[0] * min(T_s, x["q"].shape[1])
+
+
+def _calibrated_sample(w, seconds):
+    """Pick a token prefix whose oracle run takes about `seconds` on the host."""
+    from gdn_inputs import make_inputs
+    x = make_inputs(w)
+    T_full = int(x["q"].shape[1])
+    T_s = min(T_full, 64)
+    fn, ntok = _oracle_sample(w, x, T_s)
+    t0 = time.perf_counter()
+    fn()
+    dt = max(time.perf_counter() - t0, 1e-4)
+    if dt < seconds and T_s < T_full:
+        T_s = int(min(T_full, max(T_s + 1, T_s * seconds / dt)))
+        fn, ntok = _oracle_sample(w, x, T_s)
+    return x, fn, ntok, T_s
+
+
+def _describe(w, x, ntok, T_s, dt):
+    from oracle.recurrence import host_cores
+    cores = min(host_cores(), x["N"] * w.hv)
+    return {"unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 C recurrence (pthreads over sequence x head) on the first {T_s} tokens of "
+                      f"the workload ({ntok} tokens x {w.hv} heads, {dt:.2f} s wall per run)"}
+
+
+def cpu_baseline(w, seconds):
+    """Time the fp64 oracle (as it stands) on the host cores, on a prefix of
+    the workload sized to about `seconds` of CPU work."""
+    x, fn, ntok, T_s = _calibrated_sample(w, seconds)
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    d = _describe(w, x, ntok, T_s, dt)
+    d["value"] = ntok / dt
+    return d
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from gdn_inputs import workload
+    w = workload(args.workload)
+    # every step is a bounded sample: the whole run stays within about two minutes
+    per_step_s = max(0.05, min(args.cpu_seconds, 120.0 / (args.steps + args.warmup)))
+    x, fn, ntok, T_s = _calibrated_sample(w, per_step_s)
+    for _ in range(args.warmup):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    value = ntok * len(times) / sum(times)
+    cb = _describe(w, x, ntok, T_s, statistics.mean(times))
+    cb["value"] = value
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (same seeded inputs as the GPU arm)",
+           "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.hv, "dk": w.K, "dv": w.V,
+                      "sample_tokens_per_sequence": T_s},
+           "cpu_baseline": cb,
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="batched_bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

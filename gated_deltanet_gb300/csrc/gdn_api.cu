@@ -1,0 +1,403 @@
+// C-ABI layer: argument validation, planning, workspace management and the
+// launch sequence of one gated delta-rule chunked-prefill forward.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gdn_internal.cuh"
+
+using namespace gdn;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+    gdn_engine engine;
+    gdn_cp_mode cp;
+    int seg_chunks, n_seg, value_tiles, kernels, max_nt;
+    float log2_eps;
+    // workspace layout
+    size_t off_warm, off_segout, off_seginit, bytes;
+};
+
+bool is_varlen(const gdn_shape *s, const int64_t *cu) { return cu != nullptr; }
+
+gdn_status validate_shape(const gdn_shape *s, int chunk_size, const gdn_options *opt)
+{
+    if (!s) return GDN_ERR_INVALID;
+    if (s->B < 0 || s->T < 0 || s->H <= 0 || s->HV <= 0 || s->K <= 0 || s->V <= 0 || s->num_seqs < 0)
+        return GDN_ERR_INVALID;
+    if (s->HV % s->H != 0) return GDN_ERR_INVALID;
+    if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_INVALID;
+    if (s->gate_kind != GDN_GATE_SCALAR && s->gate_kind != GDN_GATE_CHANNEL) return GDN_ERR_INVALID;
+    if (opt) {
+        if (opt->cp_mode < GDN_CP_AUTO || opt->cp_mode > GDN_CP_WARMUP) return GDN_ERR_INVALID;
+        if (opt->engine < GDN_ENGINE_AUTO || opt->engine > GDN_ENGINE_TC) return GDN_ERR_INVALID;
+        if (opt->segment_chunks < 0 || opt->max_seq_len < 0) return GDN_ERR_INVALID;
+        if (!(opt->warmup_log2_eps <= 0.f)) return GDN_ERR_INVALID;
+    }
+    if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
+    if (s->K != 32 && s->K != 64 && s->K != 128) return GDN_ERR_UNSUPPORTED;
+    if (s->V > 4096) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_options *optp, int num_sms,
+                     Plan *p)
+{
+    gdn_status st = validate_shape(s, chunk_size, optp);
+    if (st != GDN_OK) return st;
+    gdn_options opt;
+    if (optp) opt = *optp; else gdn_default_options(&opt);
+    if (varlen && s->B != 1) return GDN_ERR_INVALID;
+    if (!varlen && s->num_seqs != s->B) return GDN_ERR_INVALID;
+    if (num_sms <= 0) num_sms = 148;
+
+    const int N = s->num_seqs;
+    int maxlen = s->T;
+    if (varlen && opt.max_seq_len > 0) maxlen = std::min(opt.max_seq_len, s->T);
+    const int max_nt = ceil_div(maxlen, kChunk);
+
+    *p = Plan{};
+    p->engine = GDN_ENGINE_SIMT;
+    if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_UNSUPPORTED;
+    p->value_tiles = ceil_div(s->V, 32);
+    p->max_nt = max_nt;
+    p->log2_eps = opt.warmup_log2_eps < 0.f ? opt.warmup_log2_eps : -24.f;
+
+    gdn_cp_mode cp = opt.cp_mode;
+    const long pairs = (long)N * s->HV;
+    if (cp == GDN_CP_AUTO) {
+        const long base = pairs * p->value_tiles;
+        if (pairs > 0 && base * 2 <= num_sms && max_nt >= 8)
+            cp = opt.keys_unit_norm ? GDN_CP_WARMUP : GDN_CP_EXACT;
+        else
+            cp = GDN_CP_OFF;
+    }
+    if (max_nt <= 1) cp = GDN_CP_OFF;
+    int L;
+    if (cp == GDN_CP_OFF) {
+        L = std::max(max_nt, 1);
+    } else if (opt.segment_chunks > 0) {
+        L = opt.segment_chunks;
+    } else {
+        const long base = std::max(1L, pairs * p->value_tiles);
+        long segs = std::max(2L, (long)num_sms / base);
+        segs = std::min<long>(segs, std::max(2, max_nt / 4));
+        L = ceil_div(max_nt, (int)segs);
+    }
+    L = std::max(L, 1);
+    p->cp = cp;
+    p->seg_chunks = L;
+    p->n_seg = std::max(1, ceil_div(max_nt, L));
+    if (p->n_seg == 1 && cp != GDN_CP_OFF) { p->cp = GDN_CP_OFF; cp = GDN_CP_OFF; p->seg_chunks = std::max(max_nt, 1); }
+
+    size_t off = kStatusBytes;
+    p->off_warm = p->off_segout = p->off_seginit = 0;
+    const size_t nsegs = (size_t)N * s->HV * p->n_seg;
+    if (cp == GDN_CP_WARMUP) {
+        p->off_warm = off;
+        off = align_up(off + nsegs * sizeof(int), 256);
+        if ((size_t)p->n_seg * L * sizeof(float) > 227 * 1024) return GDN_ERR_UNSUPPORTED;
+        p->kernels = 2;
+    } else if (cp == GDN_CP_EXACT) {
+        p->off_segout = off;
+        off = align_up(off + nsegs * s->K * (size_t)(s->V + s->K) * sizeof(float), 256);
+        p->off_seginit = off;
+        off = align_up(off + nsegs * s->K * (size_t)s->V * sizeof(float), 256);
+        p->kernels = 3;
+    } else {
+        p->kernels = 1;
+    }
+    p->bytes = off;
+    return GDN_OK;
+}
+
+int current_sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return sms;
+}
+
+gdn_status check_ptrs(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, const void *o)
+{
+    const bool any = (size_t)s->B * s->T > 0;
+    if (any && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID;
+    return GDN_OK;
+}
+
+gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+               const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size, void *o,
+               float *ht, const gdn_options *opt, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    Plan p;
+    gdn_status st = make_plan(s, is_varlen(s, cu), chunk_size, opt, current_sm_count(), &p);
+    if (st != GDN_OK) return st;
+    if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
+    if (!std::isfinite(scale)) return GDN_ERR_INVALID;
+    if (!ws || ws_bytes < p.bytes) return GDN_ERR_WORKSPACE;
+    if (((uintptr_t)ws & 255u) != 0) return GDN_ERR_INVALID;
+
+    char *wsb = (char *)ws;
+    unsigned *status = (unsigned *)wsb;
+    const int N = s->num_seqs;
+
+    ScanArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu_seqlens = cu;
+    a.o = o; a.ht = ht;
+    a.B = s->B; a.T = s->T; a.H = s->H; a.HV = s->HV; a.K = s->K; a.V = s->V; a.N = N;
+    a.scale = scale;
+    a.seg_chunks = p.seg_chunks; a.n_seg = p.n_seg;
+    a.mode = kModeForward; a.vext = s->V; a.status = status;
+
+    cudaError_t e = cudaSuccess;
+    if (p.cp == GDN_CP_WARMUP) {
+        GateStatsArgs gs{};
+        gs.g = g; gs.beta = beta; gs.cu_seqlens = cu;
+        gs.warm_start = (int *)(wsb + p.off_warm);
+        gs.T = s->T; gs.HV = s->HV; gs.K = s->K; gs.N = N;
+        gs.seg_chunks = p.seg_chunks; gs.n_seg = p.n_seg;
+        gs.channel = s->gate_kind == GDN_GATE_CHANNEL;
+        gs.log2_eps = p.log2_eps;
+        gs.max_warm_chunks = 1 << 30;
+        e = launch_gate_stats(gs, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        a.warm_start = gs.warm_start;
+    } else if (p.cp == GDN_CP_EXACT) {
+        ScanArgs pre = a;
+        pre.mode = kModePrepass;
+        pre.vext = s->V + s->K;
+        pre.seg_out = (float *)(wsb + p.off_segout);
+        e = launch_simt_scan(pre, s->qkv_dtype, s->gate_kind, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        CombineArgs cb{};
+        cb.h0 = h0; cb.cu_seqlens = cu; cb.seg_out = pre.seg_out;
+        cb.seg_init = (float *)(wsb + p.off_seginit);
+        cb.T = s->T; cb.HV = s->HV; cb.K = s->K; cb.V = s->V; cb.N = N;
+        cb.seg_chunks = p.seg_chunks; cb.n_seg = p.n_seg;
+        e = launch_cp_combine(cb, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        a.seg_init = cb.seg_init;
+    }
+    e = launch_simt_scan(a, s->qkv_dtype, s->gate_kind, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+// ---------------------------------------------------------------- library-managed workspaces
+struct WsEntry {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+
+gdn_status managed_ws(size_t need, cudaStream_t stream, void **out, size_t *out_bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    WsEntry &w = g_ws[{dev, stream}];
+    if (w.bytes < need) {
+        if (w.ptr) cudaFreeAsync(w.ptr, stream);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        size_t bytes = align_up(std::max<size_t>(need, 1 << 20), 1 << 20);
+        if (cudaMallocAsync(&w.ptr, bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_NOMEM;
+        }
+        if (cudaMemsetAsync(w.ptr, 0, kStatusBytes, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    *out_bytes = w.bytes;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void gdn_default_options(gdn_options *opt)
+{
+    if (!opt) return;
+    std::memset(opt, 0, sizeof(*opt));
+    opt->cp_mode = GDN_CP_AUTO;
+    opt->engine = GDN_ENGINE_AUTO;
+}
+
+const char *gdn_status_string(gdn_status st)
+{
+    switch (st) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID: return "GDN_ERR_INVALID: invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: valid but not supported";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime error";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait ran out";
+    case GDN_ERR_NOMEM: return "GDN_ERR_NOMEM: workspace allocation failed";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace too small";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+int gdn_version(void) { return 100; }
+
+size_t gdn_workspace_size(const gdn_shape *s, int chunk_size, const gdn_options *opt)
+{
+    if (!s) return 0;
+    Plan p;
+    // Sized for the worst case over SM counts the planner may see: use the
+    // device's count when a device is current, else a nominal one.
+    if (make_plan(s, false, chunk_size, opt, current_sm_count(), &p) != GDN_OK &&
+        make_plan(s, true, chunk_size, opt, current_sm_count(), &p) != GDN_OK)
+        return 0;
+    Plan pv;
+    if (s->B == 1 && make_plan(s, true, chunk_size, opt, current_sm_count(), &pv) == GDN_OK)
+        p.bytes = std::max(p.bytes, pv.bytes);
+    return p.bytes;
+}
+
+gdn_status gdn_plan(const gdn_shape *s, int chunk_size, const gdn_options *opt, int num_sms, gdn_plan_info *out)
+{
+    if (!out || !s) return GDN_ERR_INVALID;
+    Plan p;
+    const bool varlen = s->num_seqs != s->B || (opt && opt->max_seq_len > 0);
+    gdn_status st = make_plan(s, varlen, chunk_size, opt, num_sms, &p);
+    if (st != GDN_OK) return st;
+    out->engine = p.engine;
+    out->cp_mode = p.cp;
+    out->segment_chunks = p.seg_chunks;
+    out->segments = p.n_seg;
+    out->value_tiles = p.value_tiles;
+    out->kernels = p.kernels;
+    out->workspace_bytes = p.bytes;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd_ws(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size,
+                            void *o, float *ht, const gdn_options *opt, void *workspace, size_t ws_bytes,
+                            gdn_stream_t stream)
+{
+    return run(s, q, k, v, g, beta, scale, h0, cu, chunk_size, o, ht, opt, workspace, ws_bytes,
+               (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_fwd_ex(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size,
+                            void *o, float *ht, const gdn_options *opt, gdn_stream_t stream)
+{
+    Plan p;
+    gdn_status st = make_plan(s, cu != nullptr, chunk_size, opt, current_sm_count(), &p);
+    if (st != GDN_OK) return st;
+    if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
+    if (!std::isfinite(scale)) return GDN_ERR_INVALID;
+    void *ws = nullptr;
+    size_t bytes = 0;
+    st = managed_ws(p.bytes, (cudaStream_t)stream, &ws, &bytes);
+    if (st != GDN_OK) return st;
+    return run(s, q, k, v, g, beta, scale, h0, cu, chunk_size, o, ht, opt, ws, bytes, (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size,
+                         void *o, float *ht, gdn_stream_t stream)
+{
+    return gdn_chunk_fwd_ex(s, q, k, v, g, beta, scale, h0, cu, chunk_size, o, ht, nullptr, stream);
+}
+
+gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream)
+{
+    cudaStream_t st = (cudaStream_t)stream;
+    void *ws = workspace;
+    if (!ws) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_ws.find({dev, st});
+        if (it == g_ws.end() || !it->second.ptr) return GDN_OK;
+        ws = it->second.ptr;
+    }
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof(unsigned), st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word & kStatusTimeout) return GDN_ERR_TIMEOUT;
+    if (word & (kStatusPlan | kStatusNormBound)) return GDN_ERR_INVALID;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size,
+                              void *o, float *ht, const gdn_options *opt, gdn_stream_t stream)
+{
+    Plan p;
+    gdn_status st = make_plan(s, cu != nullptr, chunk_size, opt, current_sm_count(), &p);
+    if (st != GDN_OK) return st;
+    if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const size_t esz = s->qkv_dtype == GDN_BF16 ? 2 : 4;
+    const size_t tok = (size_t)s->B * s->T;
+    const size_t n_q = tok * s->H * s->K, n_v = tok * s->HV * s->V;
+    const size_t n_g = tok * s->HV * (s->gate_kind == GDN_GATE_CHANNEL ? s->K : 1);
+    const size_t n_b = tok * s->HV, n_h = (size_t)s->num_seqs * s->HV * s->K * s->V;
+    const size_t sizes[9] = {n_q * esz, n_q * esz, n_v * esz, n_g * 4, n_b * 4, h0 ? n_h * 4 : 0,
+                             cu ? (size_t)(s->num_seqs + 1) * 8 : 0, n_v * esz, ht ? n_h * 4 : 0};
+    size_t offs[9], total = 0;
+    for (int i = 0; i < 9; ++i) {
+        offs[i] = total;
+        total = align_up(total + sizes[i], 256);
+    }
+    void *arena = nullptr;
+    size_t arena_bytes = 0;
+    {
+        // the host path keeps its own arena per (device, stream), keyed apart from the workspaces
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+        static std::map<std::pair<int, cudaStream_t>, WsEntry> arenas;
+        std::lock_guard<std::mutex> lock(g_mu);
+        WsEntry &w = arenas[{dev, cs}];
+        if (w.bytes < total) {
+            if (w.ptr) cudaFreeAsync(w.ptr, cs);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            const size_t bytes = align_up(std::max<size_t>(total, 1 << 20), 1 << 20);
+            if (cudaMallocAsync(&w.ptr, bytes, cs) != cudaSuccess) {
+                cudaGetLastError();
+                return GDN_ERR_NOMEM;
+            }
+            w.bytes = bytes;
+        }
+        arena = w.ptr;
+        arena_bytes = w.bytes;
+    }
+    (void)arena_bytes;
+    char *A = (char *)arena;
+    const void *src[7] = {q, k, v, g, beta, h0, cu};
+    for (int i = 0; i < 7; ++i)
+        if (sizes[i] && cudaMemcpyAsync(A + offs[i], src[i], sizes[i], cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    st = gdn_chunk_fwd_ex(s, A + offs[0], A + offs[1], A + offs[2], (const float *)(A + offs[3]),
+                          (const float *)(A + offs[4]), scale, h0 ? (const float *)(A + offs[5]) : nullptr,
+                          cu ? (const int64_t *)(A + offs[6]) : nullptr, chunk_size, A + offs[7],
+                          ht ? (float *)(A + offs[8]) : nullptr, opt, stream);
+    if (st != GDN_OK) return st;
+    if (sizes[7] && cudaMemcpyAsync(o, A + offs[7], sizes[7], cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (sizes[8] && cudaMemcpyAsync(ht, A + offs[8], sizes[8], cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal declarations shared by the GB300 gated delta-rule kernels and the
+// C-ABI layer.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;               // chunk size C
+constexpr float kRcpLn2 = 1.4426950408889634f;  // 1 / ln 2: log-gates are kept in base 2
+
+// Device status word bits (first 16 bytes of every workspace).
+enum : unsigned {
+    kStatusTimeout = 1u << 0,      // a bounded mbarrier / flag wait ran out
+    kStatusPlan = 1u << 1,         // a kernel found a plan inconsistency and skipped work
+    kStatusNormBound = 1u << 2,    // warmup split used although beta*||k||^2 > 2 was seen
+};
+
+enum Mode : int { kModeForward = 0, kModePrepass = 1 };
+
+// Arguments of one scan launch (one engine pass over segments).
+struct ScanArgs {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    const int64_t *cu_seqlens;  // nullable
+    void *o;
+    float *ht;
+    int B, T, H, HV, K, V, N;
+    float scale;
+    // segmentation
+    int seg_chunks;         // chunks per segment
+    int n_seg;              // segments per sequence (grid.y bound)
+    const int *warm_start;  // [N*HV*n_seg] first chunk a segment processes (warmup), nullable
+    const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
+    float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
+    int mode;               // Mode
+    int vext;               // value columns processed: V (forward) or V + K (prepass)
+    unsigned *status;
+};
+
+struct CombineArgs {
+    const float *h0;
+    const int64_t *cu_seqlens;
+    const float *seg_out;  // [N*HV*n_seg][K][V+K]
+    float *seg_init;       // [N*HV*n_seg][K][V]
+    int T, HV, K, V, N, seg_chunks, n_seg;
+};
+
+struct GateStatsArgs {
+    const float *g;
+    const float *beta;
+    const int64_t *cu_seqlens;
+    int *warm_start;       // [N*HV*n_seg]
+    int T, HV, K, N, seg_chunks, n_seg, channel;
+    float log2_eps;        // threshold on the window's accumulated log2-decay
+    int max_warm_chunks;   // walk at most this far back, else start from the sequence start
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_simt_scan(const ScanArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
+cudaError_t launch_cp_combine(const CombineArgs &a, cudaStream_t st);
+cudaError_t launch_gate_stats(const GateStatsArgs &a, cudaStream_t st);
+size_t simt_smem_bytes(int K, gdn_gate_kind gate);
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace gdn

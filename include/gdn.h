@@ -1,0 +1,193 @@
+/*
+ * gdn.h -- C ABI of the GB300 gated delta-rule chunked-prefill forward.
+ *
+ * The operation (per sequence n, value head h; key/query head h / (HV/H)):
+ *
+ *   S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = scale * S_t^T q_t,        S_0 = h0[n,h] (or 0),  ht[n,h] = S_T
+ *
+ * with alpha_t = exp(g_t) for a scalar gate (FlashQLA blog, "Further
+ * optimisation via gate decay", the recurrence; "Key problems in FLA's GDN
+ * chunked prefill", the chunk form) or alpha_t,d = exp(gk_t,d) for a
+ * per-key-channel gate ("KDA source walkthrough", chunk_kda_fwd and the gk
+ * branch of chunk_gated_delta_rule_fwd_h).  It is evaluated chunkwise
+ * (chunk size C = 64): gate cumsum, gated strictly-lower K K^T, its
+ * unit-lower-triangular inverse, the WY form, the serial inter-chunk state
+ * scan and the output, optionally split over sequence segments on one GPU
+ * (FlashQLA blog, "A balanced solution": the S* / M correction, and "Further
+ * optimisation via gate decay": the gate-driven warmup).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers (except in gdn_chunk_fwd_host),
+ *    contiguous (row-major, last index fastest) and owned by the caller.
+ *  - Shapes (FlashQLA blog, "Usage"; GDN-in-FLA notes, forward signature):
+ *      q, k   [B, T, H,  K]    qkv_dtype
+ *      v      [B, T, HV, V]    qkv_dtype
+ *      o      [B, T, HV, V]    qkv_dtype (written)
+ *      g      [B, T, HV]       fp32, natural-log gate (gate_kind SCALAR)
+ *      gk     [B, T, HV, K]    fp32, natural-log gate (gate_kind CHANNEL)
+ *      beta   [B, T, HV]       fp32
+ *      h0     [N, HV, K, V]    fp32, nullable (= zero initial state)
+ *      ht     [N, HV, K, V]    fp32, nullable (final state not written)
+ *      cu_seqlens [N+1]        int64 token offsets, nullable.  When given the
+ *                              input is packed: B must be 1, T is the total
+ *                              token count and sequence n spans tokens
+ *                              [cu[n], cu[n+1]) ("Flash Linear Attention"
+ *                              page, sec. 2, varlen: FlashAttention semantics).
+ *                              Without it N = B and each batch row is one
+ *                              sequence of T tokens.
+ *  - State layout is [K][V] row-major (FLA's default, not state_v_first).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising.  Argument errors
+ *    are reported before anything is enqueued; errors found on the device
+ *    (a bounded wait that ran out, a failed plan check) are recorded in the
+ *    workspace status word, read with gdn_read_device_status().
+ *  - Nothing aborts the process and no entry point calls exit().
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gdn_stream_t; /* identical to cudaStream_t */
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_CHANNEL = 1 } gdn_gate_kind;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID = -1,     /* null pointer, negative or inconsistent size       */
+    GDN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. chunk_size != 64) */
+    GDN_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed              */
+    GDN_ERR_TIMEOUT = -4,     /* a bounded device wait ran out (device status)     */
+    GDN_ERR_NOMEM = -5,       /* library-managed workspace could not be allocated  */
+    GDN_ERR_WORKSPACE = -6    /* caller workspace smaller than gdn_workspace_size  */
+} gdn_status;
+
+typedef struct {
+    int B, T, H, HV, K, V;   /* varlen: B == 1 and T == total tokens               */
+    gdn_dtype qkv_dtype;     /* q, k, v and o share it; g/beta/h0/ht are fp32      */
+    gdn_gate_kind gate_kind; /* SCALAR: g [B,T,HV];  CHANNEL: gk [B,T,HV,K]        */
+    int num_seqs;            /* N: B, or len(cu_seqlens) - 1 for packed input       */
+} gdn_shape;
+
+/* How a long sequence is split over the GPU (FlashQLA blog, in-GPU CP). */
+typedef enum {
+    GDN_CP_AUTO = 0,   /* planner decides (split only when (seq, head) pairs are few) */
+    GDN_CP_OFF = 1,    /* one serial scan per (sequence, head)                        */
+    GDN_CP_EXACT = 2,  /* segments start from S* = 0, M = I; serial S* / M combine      */
+    GDN_CP_WARMUP = 3  /* segments re-derive their start state from zero over a
+                          warmup window sized from the gate statistics               */
+} gdn_cp_mode;
+
+typedef enum {
+    GDN_ENGINE_AUTO = 0, /* tensor-core engine where supported, else SIMT            */
+    GDN_ENGINE_SIMT = 1, /* fp32 CUDA-core engine (any supported shape, fp32 inputs) */
+    GDN_ENGINE_TC = 2    /* tcgen05/TMEM engine (bf16, K = V = 128, scalar gate)     */
+} gdn_engine;
+
+typedef struct {
+    gdn_cp_mode cp_mode;
+    int segment_chunks;    /* chunks per segment when split (0 = planner's choice)  */
+    gdn_engine engine;
+    int keys_unit_norm;    /* caller asserts ||k_t||_2 <= 1 and 0 <= beta_t <= 2, so
+                              every transition has spectral norm <= its decay; lets
+                              AUTO choose the warmup split                           */
+    float warmup_log2_eps; /* warmup stops once the window's decay <= 2^this (0 = -24) */
+    int max_seq_len;       /* packed input: bound on one sequence's length, used to
+                              size the split grid (0 = T)                             */
+} gdn_options;
+
+/* Fill `opt` with the defaults (AUTO everywhere, no assertions). */
+void gdn_default_options(gdn_options *opt);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gdn_status_string(gdn_status st);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+/*
+ * Bytes of device workspace gdn_chunk_fwd_ws needs for this problem and
+ * options (at least 256: the first 256 bytes hold the device status word).
+ * Returns 0 if the arguments are invalid or unsupported.
+ */
+size_t gdn_workspace_size(const gdn_shape *s, int chunk_size, const gdn_options *opt);
+
+/*
+ * The forward pass with a caller-provided workspace (`workspace`, at least
+ * gdn_workspace_size bytes, 256-byte aligned, device memory).  The
+ * workspace must not be used by another call that can run concurrently.
+ * Returns GDN_OK once all work is enqueued on `stream`.
+ */
+gdn_status gdn_chunk_fwd_ws(const gdn_shape *s,
+                            const void *q, const void *k, const void *v,
+                            const float *g_or_gk, const float *beta, float scale,
+                            const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                            void *o, float *ht, const gdn_options *opt,
+                            void *workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/*
+ * The forward pass with default options and a library-managed workspace,
+ * cached per (device, stream) and grown stream-ordered (cudaMallocAsync on
+ * `stream`) when a call needs more.  Arguments as in gdn_chunk_fwd_ws.
+ */
+gdn_status gdn_chunk_fwd(const gdn_shape *s,
+                         const void *q, const void *k, const void *v,
+                         const float *g_or_gk, const float *beta, float scale,
+                         const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                         void *o, float *ht, gdn_stream_t stream);
+
+/* As gdn_chunk_fwd with explicit options (NULL = defaults). */
+gdn_status gdn_chunk_fwd_ex(const gdn_shape *s,
+                            const void *q, const void *k, const void *v,
+                            const float *g_or_gk, const float *beta, float scale,
+                            const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                            void *o, float *ht, const gdn_options *opt, gdn_stream_t stream);
+
+/*
+ * End-to-end call on HOST buffers (pageable or pinned): copies the inputs to
+ * a library-owned device arena on `stream`, runs gdn_chunk_fwd_ex, copies o
+ * (and ht when non-NULL) back, and synchronises `stream` before returning.
+ * `cu_seqlens` is a host array here too.  Same shapes as above.
+ */
+gdn_status gdn_chunk_fwd_host(const gdn_shape *s,
+                              const void *q, const void *k, const void *v,
+                              const float *g_or_gk, const float *beta, float scale,
+                              const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                              void *o, float *ht, const gdn_options *opt,
+                              gdn_stream_t stream);
+
+/*
+ * Synchronise `stream`, return the status the device recorded in the
+ * workspace since the last read, and clear it.  `workspace` is the buffer
+ * given to gdn_chunk_fwd_ws, or NULL for the library-managed workspace of
+ * (current device, stream).
+ */
+gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream);
+
+/* Plan summary (host only, no GPU needed) -- what a call would launch. */
+typedef struct {
+    gdn_engine engine;    /* engine the call would use                    */
+    gdn_cp_mode cp_mode;  /* OFF, EXACT or WARMUP after AUTO is resolved   */
+    int segment_chunks;   /* chunks per segment (huge when OFF)            */
+    int segments;         /* segments per sequence (grid bound)            */
+    int value_tiles;      /* CTAs per (sequence, head, segment)            */
+    int kernels;          /* kernel launches per call                      */
+    size_t workspace_bytes;
+} gdn_plan_info;
+
+gdn_status gdn_plan(const gdn_shape *s, int chunk_size, const gdn_options *opt,
+                    int num_sms, gdn_plan_info *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

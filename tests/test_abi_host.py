@@ -1,0 +1,85 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function ``include/gdn.h`` declares, validates arguments and plans on the host
+(no compute calls without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_deltanet_gb300 as g
+    g.load_library()
+    return g
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(gdn):
+    names = declared_functions()
+    assert "gdn_chunk_fwd" in names and len(names) >= 9
+    lib = ctypes.CDLL(gdn.build.lib_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(gdn):
+    L = gdn.lib()
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert L.gdn_status_string(code).startswith(b"GDN_")
+    assert L.gdn_version() >= 100
+
+
+def _shape(**kw):
+    from gated_deltanet_gb300 import GdnShape
+    d = dict(B=4, T=4096, H=16, HV=16, K=128, V=128, qkv_dtype=1, gate_kind=0, num_seqs=4)
+    d.update(kw)
+    return GdnShape(**d)
+
+
+def test_validation_before_any_gpu_work(gdn):
+    L = gdn.lib()
+    null = None
+    s = _shape()
+    # null data pointers with a non-empty problem: invalid, reported on the host
+    assert L.gdn_chunk_fwd_ex(ctypes.byref(s), null, null, null, null, null, ctypes.c_float(0.1), null, null,
+                              64, null, null, None, None) == -1
+    # chunk size other than 64: unsupported
+    assert L.gdn_chunk_fwd_ex(ctypes.byref(s), null, null, null, null, null, ctypes.c_float(0.1), null, null,
+                              32, null, null, None, None) == -2
+    bad = [dict(H=0), dict(HV=24, H=16), dict(K=-1), dict(qkv_dtype=7), dict(gate_kind=3), dict(num_seqs=3)]
+    for kw in bad:
+        s = _shape(**kw)
+        assert L.gdn_chunk_fwd_ex(ctypes.byref(s), null, null, null, null, null, ctypes.c_float(0.1), null,
+                                  null, 64, null, null, None, None) == -1, kw
+    assert L.gdn_workspace_size(ctypes.byref(_shape(K=96)), 64, None) == 0
+
+
+def test_plans(gdn):
+    # many (sequence, head) pairs: one serial scan each
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152)
+    assert p.cp_mode == 1 and p.segments == 1 and p.kernels == 1
+    # few pairs and a long sequence: the split is planned
+    p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152)
+    assert p.cp_mode == 2 and p.segments > 1 and p.kernels == 3
+    p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, keys_unit_norm=True)
+    assert p.cp_mode == 3 and p.kernels == 2
+    p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="off")
+    assert p.cp_mode == 1 and p.segments == 1
+    p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="exact", segment_chunks=64)
+    assert p.segments == 16 and p.segment_chunks == 64
+    # workspace grows with the split's per-segment states
+    assert p.workspace_bytes >= 8 * 16 * 128 * (128 + 128) * 4
+    # a one-chunk sequence never splits
+    p = gdn.plan(1, 64, 1, 1, 64, 64, num_sms=152, cp_mode="exact")
+    assert p.cp_mode == 1

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs.
+
+Tolerances (written here, from the target statement of the method):
+  * fp32 q/k/v: max |gpu - oracle| <= 1e-4 on o and on the final state;
+  * bf16 q/k/v: relative L2 <= 5e-3 and max abs <= 2e-2 on o and on the final
+    state (fp32 state, bf16 output).
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from gdn_inputs import WORKLOADS, Workload, make_inputs, to_f64
+from oracle import recurrence
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_deltanet_gb300 as g
+    g.load_library()
+    return g
+
+
+def tol_check(name, gpu, ref, dtype):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    mx = float(err.max()) if err.size else 0.0
+    nrm = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(gpu - ref) / nrm) if nrm > 0 else float(np.linalg.norm(gpu))
+    if dtype == "f32":
+        assert mx <= 1e-4, f"{name}: max abs {mx:.3e} > 1e-4"
+    else:
+        assert rel <= 5e-3, f"{name}: rel L2 {rel:.3e} > 5e-3"
+        assert mx <= 2e-2, f"{name}: max abs {mx:.3e} > 2e-2"
+    return mx, rel
+
+
+@functools.lru_cache(maxsize=16)
+def oracle_for(w: Workload):
+    x = make_inputs(w)
+    return recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], x["cu_seqlens"],
+                      gate=x["gate"])
+
+
+def run_gpu(gdn, w: Workload, **opts):
+    x = make_inputs(w, device="cuda")
+    o, ht = gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
+                                       x["cu_seqlens"], **opts)
+    torch.cuda.synchronize()
+    assert gdn.read_device_status() == 0
+    return to_f64(o), to_f64(ht)
+
+
+def check(gdn, w: Workload, **opts):
+    go, gh = run_gpu(gdn, w, **opts)
+    ro, rh = oracle_for(w)
+    tol_check(f"{w.name} o", go, ro, w.dtype)
+    tol_check(f"{w.name} ht", gh, rh, w.dtype)
+
+
+SMALL = {
+    "f32_d64_ragged": Workload("f32_d64_ragged", B=2, T=200, H=2, K=64, V=64, dtype="f32", h0=True, seed=1),
+    "f32_d32_T1": Workload("f32_d32_T1", B=3, T=1, H=2, K=32, V=32, dtype="f32", h0=True, seed=2),
+    "f32_v_not_mult32": Workload("f32_v_not_mult32", B=1, T=130, H=1, K=64, V=40, dtype="f32", h0=True, seed=3),
+    "bf16_d128_ragged": Workload("bf16_d128_ragged", B=2, T=333, H=3, K=128, V=128, h0=True, seed=4),
+    "bf16_gva": Workload("bf16_gva", B=1, T=150, H=2, HV=4, K=128, V=128, h0=True, seed=5),
+    "bf16_varlen": Workload("bf16_varlen", B=1, T=300, H=2, K=128, V=128, h0=True, varlen=7, seed=6),
+    "f32_channel": Workload("f32_channel", B=1, T=190, H=2, K=64, V=64, dtype="f32", gate="channel",
+                            h0=True, seed=7),
+    "bf16_channel": Workload("bf16_channel", B=2, T=140, H=2, K=128, V=128, gate="channel", seed=8),
+    "f32_strong_decay": Workload("f32_strong_decay", B=1, T=256, H=2, K=64, V=64, dtype="f32", g_mu=-2.0,
+                                 h0=True, seed=9),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases(gdn, name):
+    check(gdn, SMALL[name])
+
+
+@pytest.mark.parametrize("mode", ["exact", "warmup"])
+@pytest.mark.parametrize("seg", [1, 3, 8])
+def test_split_modes_small(gdn, mode, seg):
+    w = Workload("split", B=1, T=64 * 20 + 17, H=2, K=64, V=64, dtype="f32", h0=True, seed=10, g_mu=2.0)
+    check(gdn, w, cp_mode=mode, segment_chunks=seg, keys_unit_norm=True)
+
+
+def test_split_modes_varlen(gdn):
+    w = Workload("split_varlen", B=1, T=900, H=2, K=64, V=64, dtype="f32", h0=True, varlen=5, seed=11)
+    for mode in ("exact", "warmup"):
+        check(gdn, w, cp_mode=mode, segment_chunks=2, keys_unit_norm=True, max_seq_len=900)
+
+
+def test_empty_and_single_token_sequences(gdn):
+    cu = torch.tensor([0, 0, 1, 65, 65, 130], dtype=torch.int64)
+    w = Workload("edge_varlen", B=1, T=130, H=2, K=64, V=64, dtype="f32", h0=True, seed=12)
+    x = make_inputs(w)
+    x["cu_seqlens"] = cu
+    x["h0"] = 0.1 * torch.randn(5, 2, 64, 64, generator=torch.Generator().manual_seed(3))
+    ro, rh = recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], cu)
+    xd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    o, ht = gdn.chunk_gated_delta_rule(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], x["scale"], xd["h0"],
+                                       True, xd["cu_seqlens"])
+    torch.cuda.synchronize()
+    tol_check("edge o", to_f64(o), ro, "f32")
+    tol_check("edge ht", to_f64(ht), rh, "f32")
+    # an empty sequence passes its initial state through unchanged
+    assert torch.equal(ht[0].cpu(), x["h0"][0]) and torch.equal(ht[3].cpu(), x["h0"][3])
+
+
+def test_outputs_stay_in_bounds(gdn):
+    """Canary-padded output buffers: nothing outside o / ht is written."""
+    w = SMALL["bf16_d128_ragged"]
+    x = make_inputs(w, device="cuda")
+    pad = 4096
+    n_o = x["v"].numel()
+    buf = torch.full((n_o + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = buf[pad:pad + n_o].view_as(x["v"])
+    hbuf = torch.full((x["h0"].numel() + 2 * pad,), 5.0, dtype=torch.float32, device="cuda")
+    ht = hbuf[pad:pad + x["h0"].numel()].view_as(x["h0"])
+    gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True, None,
+                               out=o, final_state=ht)
+    torch.cuda.synchronize()
+    assert bool((buf[:pad] == 7.0).all()) and bool((buf[-pad:] == 7.0).all())
+    assert bool((hbuf[:pad] == 5.0).all()) and bool((hbuf[-pad:] == 5.0).all())
+    ro, rh = oracle_for(w)
+    tol_check("canary o", to_f64(o), ro, "bf16")
+
+
+def test_workspace_variant_and_host_variant_agree(gdn):
+    w = Workload("ws", B=1, T=64 * 12 + 5, H=2, K=64, V=64, dtype="f32", h0=True, seed=13)
+    x = make_inputs(w, device="cuda")
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True, None)
+    nbytes = gdn.workspace_size(x["q"], x["v"], x["g"], cp_mode="exact", segment_chunks=3)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    o1, h1 = gdn.chunk_gated_delta_rule(*args, cp_mode="exact", segment_chunks=3, workspace=ws)
+    o2, h2 = gdn.chunk_gated_delta_rule(*args, cp_mode="exact", segment_chunks=3)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    assert gdn.read_device_status(ws) == 0
+    xc = make_inputs(w)
+    o3, h3 = gdn.chunk_gated_delta_rule_host(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["scale"],
+                                             xc["h0"], True, None, cp_mode="exact", segment_chunks=3)
+    assert torch.equal(o3, o1.cpu()) and torch.equal(h3, h1.cpu())
+
+
+# ------------------------------------------------------------------ full-size workloads
+def test_workload_tiny_f32(gdn):
+    check(gdn, WORKLOADS["tiny_f32"])
+
+
+def test_workload_batched_bf16(gdn):
+    check(gdn, WORKLOADS["batched_bf16"])
+
+
+@pytest.mark.parametrize("mode", ["auto", "exact", "warmup", "off"])
+def test_workload_long_bf16(gdn, mode):
+    check(gdn, WORKLOADS["long_bf16"], cp_mode=mode, keys_unit_norm=True)
+
+
+def test_workload_varlen_bf16_sampled(gdn):
+    """All sequences on the GPU; the oracle recomputes a sample of them one by one
+    (the longest, the shortest and four more)."""
+    w = WORKLOADS["varlen_bf16"]
+    x = make_inputs(w)
+    go, gh = run_gpu(gdn, w)
+    cu = x["cu_seqlens"].numpy()
+    lens = np.diff(cu)
+    pick = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] +
+                      list(np.random.default_rng(0).choice(len(lens), 4, replace=False))))
+    for n in pick:
+        s, e = cu[n], cu[n + 1]
+        ro, rh = recurrence(x["q"][:, s:e], x["k"][:, s:e], x["v"][:, s:e], x["g"][:, s:e], x["beta"][:, s:e],
+                            x["scale"], x["h0"][n:n + 1])
+        tol_check(f"varlen seq {n} o", go[:, s:e], ro, "bf16")
+        tol_check(f"varlen seq {n} ht", gh[n:n + 1], rh, "bf16")
+
+
+def test_workload_channel_bf16(gdn):
+    check(gdn, WORKLOADS["channel_bf16"])
