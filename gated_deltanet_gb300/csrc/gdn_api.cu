@@ -183,7 +183,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         cb.h0 = h0; cb.cu_seqlens = cu; cb.seg_out = pre.seg_out;
         cb.seg_init = (float *)(wsb + p.off_seginit);
         cb.T = s->T; cb.HV = s->HV; cb.K = s->K; cb.V = s->V; cb.N = N;
-        cb.seg_chunks = p.seg_chunks; cb.n_seg = p.n_seg;
+        cb.seg_chunks = p.seg_chunks; cb.n_seg = p.n_seg; cb.status = status;
         e = launch_cp_combine(cb, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         a.seg_init = cb.seg_init;

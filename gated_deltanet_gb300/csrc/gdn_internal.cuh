@@ -48,6 +48,7 @@ struct CombineArgs {
     const float *seg_out;  // [N*HV*n_seg][K][V+K]
     float *seg_init;       // [N*HV*n_seg][K][V]
     int T, HV, K, V, N, seg_chunks, n_seg;
+    unsigned *status;
 };
 
 struct GateStatsArgs {

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
     const int c0 = seg * a.seg_chunks;
     if (seg > 0 && c0 >= NT) return;
     const int c1 = min(c0 + a.seg_chunks, NT);
+    if (seg == a.n_seg - 1 && c1 < NT && tid == 0 && vt == 0) atomicOr(a.status, kStatusPlan);
     const int col0 = vt * kBV;
     const bool fwd = a.mode == kModeForward;
     const size_t sidx = ((size_t)n * a.HV + hv) * a.n_seg + seg;
@@ -389,7 +390,11 @@ __global__ void __launch_bounds__(kThreads) cp_combine_kernel(const CombineArgs 
     const int n = pair / a.HV, hv = pair % a.HV;
     const int64_t len = a.cu_seqlens ? a.cu_seqlens[n + 1] - a.cu_seqlens[n] : (int64_t)a.T;
     const int NT = (int)((len + kChunk - 1) / kChunk);
-    const int nseg = max(1, ceil_div(NT, a.seg_chunks));
+    int nseg = max(1, ceil_div(NT, a.seg_chunks));
+    if (nseg > a.n_seg) {  // a sequence longer than the plan's bound: never index past the grid
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.status, kStatusPlan);
+        nseg = a.n_seg;
+    }
     const int V = a.V, VE = a.V + K;
     for (int e = tid; e < K * kBV; e += kThreads) {
         const int d = e / kBV, col = col0 + e % kBV;

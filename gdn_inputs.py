@@ -23,7 +23,7 @@ gate logits, h0.  ``N(mu, sigma)`` means mean mu and standard deviation sigma.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 from typing import Optional
 
 import torch
@@ -48,7 +48,6 @@ class Workload:
     varlen: int = 0              # >0: that many packed sequences, lengths U{1..T}
     seed: int = 0
     chunk: int = 64
-    extra: dict = field(default_factory=dict)
 
     @property
     def hv(self) -> int:
