@@ -65,20 +65,24 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     const int max_nt = ceil_div(maxlen, kChunk);
 
     *p = Plan{};
-    p->engine = GDN_ENGINE_SIMT;
-    if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_UNSUPPORTED;
-    p->value_tiles = ceil_div(s->V, 32);
+    const bool tc_ok = tc_shape_ok(s);
+    if (opt.engine == GDN_ENGINE_TC && !tc_ok) return GDN_ERR_UNSUPPORTED;
+    p->engine = (opt.engine != GDN_ENGINE_SIMT && tc_ok) ? GDN_ENGINE_TC : GDN_ENGINE_SIMT;
+    p->value_tiles = p->engine == GDN_ENGINE_TC ? 1 : ceil_div(s->V, 32);
     p->max_nt = max_nt;
     p->log2_eps = opt.warmup_log2_eps < 0.f ? opt.warmup_log2_eps : -24.f;
 
     gdn_cp_mode cp = opt.cp_mode;
     const long pairs = (long)N * s->HV;
     if (cp == GDN_CP_AUTO) {
+        // Split only when the (sequence, head) pairs leave most SMs idle.  The
+        // warmup split costs a few extra chunks per segment; the exact split a
+        // pre-pass over the whole sequence plus a serial combine, so it needs
+        // a larger idle share to pay off.
         const long base = pairs * p->value_tiles;
-        if (pairs > 0 && base * 2 <= num_sms && max_nt >= 8)
-            cp = opt.keys_unit_norm ? GDN_CP_WARMUP : GDN_CP_EXACT;
-        else
-            cp = GDN_CP_OFF;
+        cp = GDN_CP_OFF;
+        if (pairs > 0 && opt.keys_unit_norm && base * 2 <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
+        else if (pairs > 0 && base * 4 <= num_sms && max_nt >= 16) cp = GDN_CP_EXACT;
     }
     if (max_nt <= 1) cp = GDN_CP_OFF;
     int L;
@@ -88,7 +92,10 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         L = opt.segment_chunks;
     } else {
         const long base = std::max(1L, pairs * p->value_tiles);
-        long segs = std::max(2L, (long)num_sms / base);
+        // exact: the pre-pass runs S* and M (two value tiles on the tensor-core
+        // engine), so leave room for both in one wave
+        const long per = cp == GDN_CP_EXACT ? 2 * base : base;
+        long segs = std::max(2L, (long)num_sms / per);
         segs = std::min<long>(segs, std::max(2, max_nt / 4));
         L = ceil_div(max_nt, (int)segs);
     }
@@ -135,12 +142,25 @@ gdn_status check_ptrs(const gdn_shape *s, const void *q, const void *k, const vo
     return GDN_OK;
 }
 
+cudaError_t scan_prepass(const ScanArgs &pre, bool tc, const gdn_shape *s, cudaStream_t stream)
+{
+    if (tc) return launch_tc_scan(pre, 2, stream);
+    return launch_simt_scan(pre, s->qkv_dtype, s->gate_kind, stream);
+}
+
 gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
                const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size, void *o,
-               float *ht, const gdn_options *opt, void *ws, size_t ws_bytes, cudaStream_t stream)
+               float *ht, const gdn_options *optp, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     Plan p;
-    gdn_status st = make_plan(s, is_varlen(s, cu), chunk_size, opt, current_sm_count(), &p);
+    gdn_options opt;
+    if (optp) opt = *optp; else gdn_default_options(&opt);
+    // the tensor-core engine needs 16-byte aligned q/k/v/o for its TMA maps
+    if (opt.engine != GDN_ENGINE_SIMT && tc_shape_ok(s) && !tc_supported(s, q, k, v, o)) {
+        if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_INVALID;
+        opt.engine = GDN_ENGINE_SIMT;
+    }
+    gdn_status st = make_plan(s, is_varlen(s, cu), chunk_size, &opt, current_sm_count(), &p);
     if (st != GDN_OK) return st;
     if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
     if (!std::isfinite(scale)) return GDN_ERR_INVALID;
@@ -160,6 +180,11 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     a.mode = kModeForward; a.vext = s->V; a.status = status;
 
     cudaError_t e = cudaSuccess;
+    const bool tc = p.engine == GDN_ENGINE_TC;
+    auto scan = [&](const ScanArgs &sa) -> cudaError_t {
+        if (tc) return launch_tc_scan(sa, sa.mode == kModePrepass ? 2 : 1, stream);
+        return launch_simt_scan(sa, s->qkv_dtype, s->gate_kind, stream);
+    };
     if (p.cp == GDN_CP_WARMUP) {
         GateStatsArgs gs{};
         gs.g = g; gs.beta = beta; gs.cu_seqlens = cu;
@@ -177,7 +202,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         pre.mode = kModePrepass;
         pre.vext = s->V + s->K;
         pre.seg_out = (float *)(wsb + p.off_segout);
-        e = launch_simt_scan(pre, s->qkv_dtype, s->gate_kind, stream);
+        e = scan_prepass(pre, tc, s, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         CombineArgs cb{};
         cb.h0 = h0; cb.cu_seqlens = cu; cb.seg_out = pre.seg_out;
@@ -188,7 +213,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         a.seg_init = cb.seg_init;
     }
-    e = launch_simt_scan(a, s->qkv_dtype, s->gate_kind, stream);
+    e = scan(a);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }

@@ -67,6 +67,13 @@ cudaError_t launch_cp_combine(const CombineArgs &a, cudaStream_t st);
 cudaError_t launch_gate_stats(const GateStatsArgs &a, cudaStream_t st);
 size_t simt_smem_bytes(int K, gdn_gate_kind gate);
 
+// Tensor-core engine (bf16, K = V = 128, scalar gate).  `value_tiles` is 1 for
+// the forward pass and 2 for the exact split's pre-pass (S* and M columns).
+bool tc_shape_ok(const gdn_shape *s);
+bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o);
+cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st);
+size_t tc_smem_bytes();
+
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace gdn

@@ -66,9 +66,18 @@ def test_validation_before_any_gpu_work(gdn):
 
 
 def test_plans(gdn):
-    # many (sequence, head) pairs: one serial scan each
+    # bf16, dk = dv = 128, scalar gate: tensor-core engine, one CTA per (sequence, head)
     p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152)
+    assert p.engine == 2 and p.value_tiles == 1
     assert p.cp_mode == 1 and p.segments == 1 and p.kernels == 1
+    # 64 pairs leave half the SMs idle: with unit-norm keys asserted, the warmup split
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152, keys_unit_norm=True)
+    assert p.cp_mode == 3 and p.segments == 2
+    # fp32 or other head dims: CUDA-core engine
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, dtype="f32", num_sms=152)
+    assert p.engine == 1 and p.value_tiles == 4
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152)
+    assert p.engine == 1
     # few pairs and a long sequence: the split is planned
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152)
     assert p.cp_mode == 2 and p.segments > 1 and p.kernels == 3

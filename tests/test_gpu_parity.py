@@ -78,12 +78,31 @@ SMALL = {
     "bf16_channel": Workload("bf16_channel", B=2, T=140, H=2, K=128, V=128, gate="channel", seed=8),
     "f32_strong_decay": Workload("f32_strong_decay", B=1, T=256, H=2, K=64, V=64, dtype="f32", g_mu=-2.0,
                                  h0=True, seed=9),
+    "bf16_T1": Workload("bf16_T1", B=2, T=1, H=2, K=128, V=128, h0=True, seed=14),
+    "bf16_T64": Workload("bf16_T64", B=1, T=64, H=2, K=128, V=128, h0=True, seed=15),
+    "bf16_T65": Workload("bf16_T65", B=1, T=65, H=2, K=128, V=128, h0=True, seed=16),
+    "bf16_strong_decay": Workload("bf16_strong_decay", B=1, T=300, H=2, K=128, V=128, g_mu=-2.0, h0=True,
+                                  seed=17),
+    "bf16_no_decay": Workload("bf16_no_decay", B=1, T=700, H=2, K=128, V=128, g_mu=30.0, h0=True, seed=18),
 }
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_cases(gdn, name):
     check(gdn, SMALL[name])
+
+
+@pytest.mark.parametrize("engine", ["simt", "tc"])
+@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_T65"])
+def test_engines_match_oracle(gdn, engine, name):
+    check(gdn, SMALL[name], engine=engine)
+
+
+@pytest.mark.parametrize("mode", ["exact", "warmup"])
+@pytest.mark.parametrize("seg", [1, 3, 8])
+def test_split_modes_tc(gdn, mode, seg):
+    w = Workload("split_tc", B=1, T=64 * 20 + 17, H=2, K=128, V=128, h0=True, seed=19, g_mu=2.0)
+    check(gdn, w, cp_mode=mode, segment_chunks=seg, keys_unit_norm=True, engine="tc")
 
 
 @pytest.mark.parametrize("mode", ["exact", "warmup"])
