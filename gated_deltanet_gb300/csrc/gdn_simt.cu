@@ -444,21 +444,25 @@ __global__ void __launch_bounds__(kThreads) gate_stats_kernel(const GateStatsArg
     const int NT = (int)((len + kChunk - 1) / kChunk);
     const int nseg = max(1, ceil_div(NT, a.seg_chunks));
     const int cap = a.n_seg * a.seg_chunks;  // shared-memory capacity in chunks
-    for (int c = tid; c < NT && c < cap; c += blockDim.x) {
-        float s = 0.f;
-        const int rows = (int)rows_in_chunk(len, c);
-        for (int r = 0; r < rows; ++r) {
+    const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    for (int c = warp; c < NT && c < cap; c += nwarps) {
+        // one warp per chunk: lane l takes tokens l and l + 32
+        const int rows = (int)min((int64_t)kChunk, len - (int64_t)c * kChunk);
+        float part = 0.f;
+        for (int r = lane; r < rows; r += 32) {
             const size_t t = (size_t)(bos + (int64_t)c * kChunk + r);
             if (a.channel) {
                 const float *gt = a.g + (t * a.HV + hv) * a.K;
                 float mx = gt[0];
                 for (int d = 1; d < a.K; ++d) mx = fmaxf(mx, gt[d]);
-                s += mx;
+                part += mx;
             } else {
-                s += a.g[t * a.HV + hv];
+                part += a.g[t * a.HV + hv];
             }
         }
-        csum[c] = s * kRcpLn2;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) csum[c] = part * kRcpLn2;
     }
     __syncthreads();
     int *ws = a.warm_start + ((size_t)n * a.HV + hv) * a.n_seg;

@@ -56,8 +56,8 @@ constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), 2^
 constexpr uint32_t OFF_GATE = OFF_X + 64 * kLdX * 4;
 constexpr uint32_t OFF_PG = OFF_GATE + 2 * kGateBytes;      // prep copy: gam, rgam, G [3][64], flag
 constexpr uint32_t OFF_SCR = OFF_PG + 1024;                 // prep per-warp scratch [4][256] f32
-constexpr uint32_t OFF_EG = OFF_SCR + 4096;                 // output: scale * gam, per warp [4][64]
-constexpr uint32_t OFF_BAR = OFF_EG + 1024;
+constexpr uint32_t OFF_EG = OFF_SCR + 4096;                 // scale * gam per chunk, ring of 8 [8][64]
+constexpr uint32_t OFF_BAR = OFF_EG + 2048;
 constexpr uint32_t kSmemTC = OFF_BAR + 256 + 1024;          // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
@@ -270,6 +270,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             gt[GT_RGAM + r1] = exp2f(-G1);
             gt[GT_NBG + r0] = -b0 * gm0;
             gt[GT_NBG + r1] = -b1 * gm1;
+            // output scales of this chunk; read by the output warps after x_ready of the chunk,
+            // which the prep warps release after acquiring this stage (so the writes are visible)
+            float *osc = (float *)(sm + OFF_EG) + (i & 7) * 64;
+            osc[r0] = a.scale * gm0;
+            osc[r1] = a.scale * gm1;
             ok = mbar_wait(&bars[B_TMA + s], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -837,9 +842,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     } else {
         // ================================================================ output (lane = dv)
         const int et = tid - 384, dv = et;
-        const int ew = warp - 12;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
-        float *eg = (float *)(sm + OFF_EG) + ew * 64;
         const float *sX = (const float *)(sm + OFF_X);
         const float *pG = (const float *)(sm + OFF_PG);
         bool ok = true;
@@ -887,21 +890,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (!(fwd && c >= c0)) continue;
             const int64_t t0 = bos + (int64_t)c * kChunk;
             const int rows = rows_in(len, c);
-            // scale * 2^G for this chunk, from the raw gates (independent of the stage ring)
-            {
-                const int r0 = 2 * lane, r1 = r0 + 1;
-                const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2 : 0.f;
-                const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2 : 0.f;
-                float sp = g0 + g1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, sp, off);
-                    if (lane >= off) sp += y;
-                }
-                eg[r0] = a.scale * exp2f(sp - g1);
-                eg[r1] = a.scale * exp2f(sp);
-                __syncwarp();
-            }
+            const float *eg = (const float *)(sm + OFF_EG) + ((it - 1) & 7) * 64;  // scale * 2^G of the chunk
             ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
