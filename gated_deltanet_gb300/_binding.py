@@ -66,7 +66,9 @@ def load_library(path: str | None = None):
         lib.gdn_chunk_fwd_ex.argtypes = fwd_args + [OP, VP]
         lib.gdn_chunk_fwd_ws.argtypes = fwd_args + [OP, VP, ctypes.c_size_t, VP]
         lib.gdn_chunk_fwd_host.argtypes = fwd_args + [OP, VP]
-        for f in (lib.gdn_chunk_fwd, lib.gdn_chunk_fwd_ex, lib.gdn_chunk_fwd_ws, lib.gdn_chunk_fwd_host):
+        lib.gdn_chunk_fwd_noalloc.argtypes = fwd_args + [OP, VP]
+        for f in (lib.gdn_chunk_fwd, lib.gdn_chunk_fwd_ex, lib.gdn_chunk_fwd_ws, lib.gdn_chunk_fwd_host,
+                  lib.gdn_chunk_fwd_noalloc):
             f.restype = ctypes.c_int
         lib.gdn_workspace_size.argtypes = [SP, ctypes.c_int, OP]
         lib.gdn_workspace_size.restype = ctypes.c_size_t

@@ -172,6 +172,36 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s,
  */
 gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream);
 
+/*
+ * The forward pass without any allocation (no counterpart in the paper; an
+ * interface for callers that cannot allocate device memory when they run the
+ * forward: code running inside a memory pool it does not own, runtimes that
+ * forbid cudaMalloc on their hot path because it synchronises the device, or
+ * embeddings that reserved all device memory up front).  Arguments as in
+ * gdn_chunk_fwd_ex; the caller still provides every input and output.
+ *
+ * Scratch (the device status word and the chunk-parallel split's tables)
+ * lives in one fixed 4 MiB device array owned by the library, which every
+ * GPU that loads the library holds until the process exits.  A plan that
+ * needs more scratch than that (gdn_workspace_size > 4 MiB, e.g. the exact
+ * split over many segments) is rejected with GDN_ERR_WORKSPACE before
+ * anything is enqueued; choose GDN_CP_OFF or GDN_CP_WARMUP, or use
+ * gdn_chunk_fwd_ws with a larger workspace.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress with that device current); make that first call
+ * before any stream capture.  Every call uses the same array, which keeps
+ * the previous call's contents (the status word is cleared at the start of
+ * each call): calls that can overlap on the GPU -- on different streams, or
+ * from different threads -- race on it and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+gdn_status gdn_chunk_fwd_noalloc(const gdn_shape *s,
+                                 const void *q, const void *k, const void *v,
+                                 const float *g_or_gk, const float *beta, float scale,
+                                 const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                                 void *o, float *ht, const gdn_options *opt, gdn_stream_t stream);
+
 /* Plan summary (host only, no GPU needed) -- what a call would launch. */
 typedef struct {
     gdn_engine engine;    /* engine the call would use                    */
