@@ -108,7 +108,9 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     size_t off = kStatusBytes;
     p->off_warm = p->off_segout = p->off_seginit = 0;
     const size_t nsegs = (size_t)N * s->HV * p->n_seg;
-    if (cp == GDN_CP_WARMUP) {
+    if (cp == GDN_CP_WARMUP && p->engine == GDN_ENGINE_TC) {
+        p->kernels = 1;  // each CTA of the scan finds its own warmup start
+    } else if (cp == GDN_CP_WARMUP) {
         p->off_warm = off;
         off = align_up(off + nsegs * sizeof(int), 256);
         if ((size_t)p->n_seg * L * sizeof(float) > 227 * 1024) return GDN_ERR_UNSUPPORTED;
@@ -185,7 +187,10 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         if (tc) return launch_tc_scan(sa, sa.mode == kModePrepass ? 2 : 1, stream);
         return launch_simt_scan(sa, s->qkv_dtype, s->gate_kind, stream);
     };
-    if (p.cp == GDN_CP_WARMUP) {
+    if (p.cp == GDN_CP_WARMUP && tc) {
+        a.warm_in_kernel = 1;
+        a.warm_log2_eps = p.log2_eps;
+    } else if (p.cp == GDN_CP_WARMUP) {
         GateStatsArgs gs{};
         gs.g = g; gs.beta = beta; gs.cu_seqlens = cu;
         gs.warm_start = (int *)(wsb + p.off_warm);

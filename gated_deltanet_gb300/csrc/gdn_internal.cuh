@@ -35,6 +35,8 @@ struct ScanArgs {
     int seg_chunks;         // chunks per segment
     int n_seg;              // segments per sequence (grid.y bound)
     const int *warm_start;  // [N*HV*n_seg] first chunk a segment processes (warmup), nullable
+    int warm_in_kernel;     // tensor-core engine: each CTA finds its own warmup start from g
+    float warm_log2_eps;    // threshold of that search (accumulated log2-decay)
     const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
     float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
     int mode;               // Mode

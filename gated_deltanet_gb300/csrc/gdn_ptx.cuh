@@ -39,11 +39,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 
 // Waits for the phase with the given parity to complete; gives up after
 // `limit_ns` of wall time, records kStatusTimeout-style `flag` in *status and
-// returns false.  Never spins without a bound.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
-                                          uint64_t limit_ns)
+// returns false.  Never spins without a bound.  The polling loop is kept out
+// of line: the kernels wait at many places and their code has to stay small.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
+                                                   uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer() - t0 > limit_ns) {
@@ -52,6 +52,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
         }
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
+                                          uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, status, flag, limit_ns);
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
@@ -67,10 +73,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 
 // Latency-critical variant: polls without suspending (a suspended waiter can
 // wake up hundreds of cycles after the phase completes), still bounded in time.
-__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
-                                          uint64_t limit_ns)
+static __device__ __noinline__ bool mbar_spin_slow(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
+                                                   uint64_t limit_ns)
 {
-    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_test_wait(bar, parity)) return true;
@@ -79,6 +84,12 @@ __device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity, unsign
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity, unsigned *status, unsigned flag,
+                                          uint64_t limit_ns)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_spin_slow(bar, parity, status, flag, limit_ns);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -203,6 +214,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r)
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x with the MUFU approximation (relative error ~2^-22, flushes denormals): the
+// gate factors it feeds are rounded to bf16 or multiplied into fp32 sums
+__device__ __forceinline__ float ex2(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 
 // two floats -> packed bf16x2 (lo in the low half)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)

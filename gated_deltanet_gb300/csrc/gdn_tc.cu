@@ -3,31 +3,29 @@
 //
 // One CTA owns one (sequence, value head, segment) and walks its chunks
 // serially.  The state is kept transposed, S^T [dv x dk] fp32, in tensor
-// memory (lane = dv), so every product of the chunk step is an M = 128
-// tcgen05 MMA with dv as M.  The chunk step is the FlashQLA restructured form
-// (FlashQLA blog, "A balanced solution", step 3), with A0 from step 1:
+// memory (lane = dv), so every product is an M = 128 tcgen05 MMA.  Per chunk
+// (G = chunk-local inclusive cumsum of the log-gate in base 2, gam = 2^G,
+// Gam_ij = 2^(G_i - G_j), gC = gam of the last row):
 //
-//   A0    = (I + StrictLower(diag(beta) K K^T))^-1        (prep warps)
-//   A_g   = Gam * A0,  P_g = scale Lower(Gam) * (Q K^T)    (prep / aux warps)
-//   D^T   = S^T K^T - (V diag(1/gam))^T                    (MMA; the second term
-//                                                            through a resident -I)
-//   Y^T   = -D^T diag(beta gam) = (V^T - X^T diag(gam)) diag(beta)
-//   V'^T  = Y^T A_g^T                                      (MMA)
-//   O^T   = scale (S^T Q^T) diag(gam) + V'^T P_g^T         (MMA x2, output warps)
-//   S^T  <- gC S^T + (V'^T diag(gC / gam)) K               (MMA, B = K MN-major)
+//   X    = (I + StrictLower(diag(beta) K K^T))^-1       gate-free inverse (FlashQLA
+//                                                       blog, "A balanced solution")
+//   A_g  = Gam * X                                       gated inverse (same page)
+//   U    = A_g diag(beta) V,  W = A_g diag(beta gam) K   WY form (FLA page, sec. 4)
+//   V'   = U - W S                                       the only state-dependent product
+//   O    = Q~ S + P V',  Q~ = diag(scale gam) Q,  P = scale Lower(Gam) * (Q K^T)
+//   S   <- gC S + K^T diag(gC / gam) V'
 //
-// with G the chunk-local inclusive cumsum of the log-gate (kept in base 2),
-// gam = 2^G, Gam_ij = 2^(G_i - G_j), gC = gam of the last valid row.  When a
-// chunk decays by more than 2^-100 the 1/gam scaling is skipped and Y is
-// formed from V directly.
+// Everything but V' = U - W S and the state update is independent of the
+// state, so the serial chain per chunk is: S -> bf16 copy, one MMA group
+// (V'^T = U^T - S^T W^T), V' -> bf16, one MMA group (the state update).
 //
-// Warp roles (16 warps): 0 TMA producer (+ gate statistics), 1 MMA issuer,
-// 2-3 aux (TMEM allocation, V / gam in place, P_g), 4-7 chain (state, Y,
-// V'), 8-11 prep (K K^T -> L -> blockwise inverse), 12-15 output (A_g of
-// the next chunk, then O of the previous one).
-// All waits are bounded in wall time; a wait that runs out records a timeout
-// in the status word and every role leaves its loop, so the kernel always
-// ends and frees its tensor memory.
+// Warp roles (16 warps): 0 TMA producer + gate statistics (and the warmup
+// start), 1 MMA issuer (event driven), 2-3 aux (Q~ in place, P), 4-7 chain
+// (state copy, V'), 8-11 prep (L, blockwise inverse), 12-15 output (U / W
+// operand tiles, W^T -> shared memory, O epilogue).
+// Every wait is bounded in wall time; a wait that runs out records a timeout
+// in the status word and the roles leave their loops, so the kernel always
+// ends, waits for its copies and products in flight and frees its tensor memory.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -39,42 +37,40 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreadsTC = 512;
+constexpr int kStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kStageBytes = 49152;  // K0 | Q0 | K1 | Q1 | V0 | V1, 8 KB each
+constexpr uint32_t kStageBytes = 49152;  // K0 | Q0 | K1 | Q1 | V0 | V1, 8 KB each (64 rows x 64 bf16)
 constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, sV1 = 40960;
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_NEGI = OFF_STAGE + 2 * kStageBytes;  // -I [128 x 128] bf16 SW128 (2 boxes of 16 KB)
-constexpr uint32_t OFF_A = OFF_NEGI + 32768;                // A_g  [64 x 64] bf16 SW128, x2
-constexpr uint32_t OFF_P = OFF_A + 2 * 8192;                // P_g  [64 x 64] bf16 SW128, x2
-constexpr uint32_t OFF_VP = OFF_P + 2 * 8192;               // V'^T [128 x 64] bf16 SW128
-constexpr int kLdX = 68;                                    // row pitch (floats) of the 64 x 64 fp32 tiles
-constexpr uint32_t OFF_L = OFF_VP + 16384;                  // L  fp32 [64][68]
-constexpr uint32_t OFF_X = OFF_L + 64 * kLdX * 4;           // X  fp32 [64][68]
-constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), 2^-G, -beta*gam  [64] f32 each
-constexpr uint32_t OFF_GATE = OFF_X + 64 * kLdX * 4;
-constexpr uint32_t OFF_PG = OFF_GATE + 2 * kGateBytes;      // prep copy: gam, rgam, G [3][64], flag
-constexpr uint32_t OFF_SCR = OFF_PG + 1024;                 // prep per-warp scratch [4][256] f32
-constexpr uint32_t OFF_EG = OFF_SCR + 4096;                 // scale * gam per chunk, ring of 8 [8][64]
-constexpr uint32_t OFF_BAR = OFF_EG + 2048;
-constexpr uint32_t kSmemTC = OFF_BAR + 256 + 1024;          // + slack for the 1024-byte alignment
+constexpr uint32_t OFF_TU = OFF_STAGE + kStages * kStageBytes;  // A_g diag(beta) [64 x 64] bf16, x2
+constexpr uint32_t OFF_TW = OFF_TU + 2 * 8192;                  // A_g diag(beta gam) [64 x 64] bf16
+constexpr uint32_t OFF_P = OFF_TW + 8192;                       // P [64 x 64] bf16, x2
+constexpr uint32_t OFF_WS = OFF_P + 2 * 8192;                      // -W^T [128 (dk) x 64] bf16, MN-major
+constexpr int kLdX = 68;                                        // row pitch (floats) of the L / X tile
+constexpr uint32_t OFF_LX = OFF_WS + 16384;                     // L (lower) and X^T (upper), fp32 [64][68]
+constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each
+constexpr uint32_t OFF_GATE = OFF_LX + 64 * kLdX * 4;
+constexpr uint32_t OFF_SCR = OFF_GATE + kStages * kGateBytes;  // merge scratch, 4 warps x 32 x 8 fp32
+constexpr uint32_t OFF_BAR = OFF_SCR + 4096;
+constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_RGAM = 256, GT_NBG = 320;
-constexpr float kFactorFloor = -100.f;  // chunks with G_C below this skip the 1/gam factorisations
+constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_RGAM = 256, GT_SGAM = 320;
 
-// ---- tensor memory columns
-constexpr uint32_t TM_S = 0, TM_XV = 128, TM_O1 = 192, TM_O2 = 256, TM_KQ = 320, TM_SBF = 384,
-                   TM_YBF = 448, TM_VTB = 480;
+// ---- tensor memory columns (512 allocated)
+constexpr uint32_t TM_S = 0, TM_VP = 128, TM_O = 192, TM_W = 256, TM_SBF = 320, TM_VB = 384, TM_VTB = 416,
+                   TM_KQ = 448;
+
+// ---- named barriers (0 is __syncthreads)
+constexpr int NB_PREP = 1;
 
 enum Bar {
-    B_FULL = 0, B_EMPTY = 2, B_TMA = 4, B_VH = 6, B_AF = 8, B_AE = 10, B_KQF = 12, B_KQE, B_SBF, B_XF, B_YF,
-    B_VPF, B_VTF, B_SF, B_OF, B_OE, B_XR, B_XFREE, B_COUNT
+    B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_TUF, B_TUF1, B_TUE, B_TUE1, B_TWF, B_WF,
+    B_WC, B_XR, B_XFREE, B_SBF, B_VPF, B_VTF, B_SF, B_PF, B_PF1, B_PE, B_PE1, B_OF, B_OE, B_FIN, B_COUNT
 };
-constexpr uint32_t kEmptyArrivals = 1 + 4 + 4 + 2;  // MMA commit, chain, prep, aux warps
-constexpr uint32_t kKqArrivals = 4 + 2;             // prep + aux warps read the K K^T / Q K^T tile
-constexpr uint32_t kAfArrivals = 4 + 2;             // output warps write A_g, aux writes P_g
+static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");
 
 struct TcMaps {
     CUtensorMap q, k, v;
@@ -99,23 +95,18 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
     return r < kChunk ? (int)r : kChunk;
 }
 
-__device__ __forceinline__ uint32_t tf32(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
 
-// d += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation (one warp)
+// d += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation (one warp; the merges of the
+// blockwise inverse, whose result is rounded to bf16 for the MMA operands afterwards).  The fp32
+// operands go in as they are: the tensor core reads their top 19 bits (tf32 by truncation).
 __device__ __forceinline__ void mma_tf32(float *d, float a0, float a1, float a2, float a3, float b0, float b1)
 {
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                  "{%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(tf32(a0)), "r"(tf32(a1)), "r"(tf32(a2)), "r"(tf32(a3)), "r"(tf32(b0)), "r"(tf32(b1)));
+                 : "r"(f2u(a0)), "r"(f2u(a1)), "r"(f2u(a2)), "r"(f2u(a3)), "r"(f2u(b0)), "r"(f2u(b1)));
 }
-
-__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
 
 __device__ __forceinline__ uint4 pack8(const float *v)
 {
@@ -127,6 +118,42 @@ __device__ __forceinline__ uint4 pack8(const float *v)
     return pk;
 }
 
+// Warmup start of a segment beginning at chunk c0: walk back over whole chunks,
+// adding their log2-decays, until the window has decayed to log2_eps or below;
+// the chunk where that happens is the start.  If the sequence start is reached
+// first, start there (the exact prefix).  One warp; lane l sums tokens l and
+// l + 32 of a chunk, eight chunks per round trip to memory.
+__device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t len, int HV, int hv, int c0,
+                                          float log2_eps)
+{
+    const int lane = threadIdx.x & 31;
+    float acc = 0.f;
+    for (int c = c0; c > 0; c -= 8) {
+        // lane l: tokens l and l + 32 of the chunks c - 1, ..., c - 8 (loads issued together)
+        float v[16];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int cc = c - 1 - b;
+            const int rows = cc >= 0 ? rows_in(len, cc) : 0;
+            const float *gp = g + ((size_t)(bos + (int64_t)(cc >= 0 ? cc : 0) * kChunk) + lane) * HV + hv;
+            v[2 * b] = lane < rows ? gp[0] : 0.f;
+            v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+        }
+#pragma unroll 1
+        for (int b = 0; b < 8 && c - 1 - b >= 0; ++b) {
+            float part = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q == b) part = v[2 * q] + v[2 * q + 1];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            acc += part * kRcpLn2;
+            if (acc <= log2_eps) return c - 1 - b;
+        }
+    }
+    return 0;
+}
+
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a, const __grid_constant__ TcMaps m)
 {
     extern __shared__ __align__(1024) uint8_t smraw[];
@@ -136,6 +163,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const uint32_t sbase = smem_u32(sm);
     uint64_t *bars = (uint64_t *)(sm + OFF_BAR);
     uint32_t *tslot = (uint32_t *)(sm + OFF_BAR + 8 * B_COUNT);
+    int *s_cs = (int *)(sm + OFF_BAR + 8 * B_COUNT + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int vt = blockIdx.x, seg = blockIdx.y, pair = blockIdx.z;
@@ -155,72 +183,82 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const int c1 = min(c0 + a.seg_chunks, NT);
     const bool fwd = a.mode == kModeForward;
     const size_t sidx = ((size_t)n * HV + hv) * a.n_seg + seg;
-    int cs = c0;
-    if (fwd && a.warm_start) {
-        cs = a.warm_start[sidx];
-        if (cs < 0 || cs > c0) cs = 0;
-    }
-    const int nch = c1 - cs;
     const bool zero_values = !fwd && vt == 1;   // pre-pass: the M columns carry no values
-    const bool check_norm = fwd && a.warm_start != nullptr;
+    const bool check_norm = fwd && (a.warm_start != nullptr || a.warm_in_kernel != 0);
 
-    if (tid == 0) {
-        if (seg == a.n_seg - 1 && c1 < NT) atomicOr(a.status, kStatusPlan);
-        if (fwd && a.warm_start && (a.warm_start[sidx] < 0 || a.warm_start[sidx] > c0))
-            atomicOr(a.status, kStatusPlan);
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(&bars[B_FULL + j], 1);
-            mbar_init(&bars[B_EMPTY + j], kEmptyArrivals);
+    if (warp == 0) {
+        int cs = c0;
+        if (fwd && seg > 0) {
+            if (a.warm_in_kernel) {
+                cs = warm_start_of(a.g, bos, len, HV, hv, c0, a.warm_log2_eps);
+            } else if (a.warm_start) {
+                cs = a.warm_start[sidx];
+                if (cs < 0 || cs > c0) {
+                    if (lane == 0) atomicOr(a.status, kStatusPlan);
+                    cs = 0;
+                }
+            }
+        }
+        if (lane == 0) {
+            *s_cs = cs;
+            if (seg == a.n_seg - 1 && c1 < NT) atomicOr(a.status, kStatusPlan);
+        }
+    }
+    if (tid == 32) {
+        for (int j = 0; j < kStages; ++j) {
             mbar_init(&bars[B_TMA + j], 1);
-            mbar_init(&bars[B_VH + j], 2);
-            mbar_init(&bars[B_AF + j], kAfArrivals);
-            mbar_init(&bars[B_AE + j], 1);
+            mbar_init(&bars[B_FULL + j], 1);
+            mbar_init(&bars[B_EMPTY + j], 1);
+            mbar_init(&bars[B_QS + j], 2);
         }
         mbar_init(&bars[B_KQF], 1);
-        mbar_init(&bars[B_KQE], kKqArrivals);
+        mbar_init(&bars[B_KQE], 4);
+        mbar_init(&bars[B_TUF], 4);
+        mbar_init(&bars[B_TUF1], 4);
+        mbar_init(&bars[B_TUE], 1);
+        mbar_init(&bars[B_TUE1], 1);
+        mbar_init(&bars[B_TWF], 4);
+        mbar_init(&bars[B_WF], 1);
+        mbar_init(&bars[B_WC], 4);
+        mbar_init(&bars[B_XR], 4);
+        mbar_init(&bars[B_XFREE], 4);
         mbar_init(&bars[B_SBF], 4);
-        mbar_init(&bars[B_XF], 1);
-        mbar_init(&bars[B_YF], 4);
         mbar_init(&bars[B_VPF], 1);
         mbar_init(&bars[B_VTF], 4);
         mbar_init(&bars[B_SF], 1);
+        mbar_init(&bars[B_PF], 2);
+        mbar_init(&bars[B_PF1], 2);
+        mbar_init(&bars[B_PE], 1);
+        mbar_init(&bars[B_PE1], 1);
         mbar_init(&bars[B_OF], 1);
         mbar_init(&bars[B_OE], 4);
-        mbar_init(&bars[B_XR], 4);
-        mbar_init(&bars[B_XFREE], 4);
+        mbar_init(&bars[B_FIN], 1);
         fence_mbar_init();
     }
-    // the resident -I operand (K-major, 128-byte swizzle; two 64-column boxes)
-    for (int e = tid; e < 128 * 16; e += kThreadsTC) {
-        const int r = e >> 4, ch = e & 15, bx = ch >> 3, cl = ch & 7;
-        uint4 z = make_uint4(0, 0, 0, 0);
-        if ((r >> 6) == bx && ((r & 63) >> 3) == cl) {
-            const uint32_t neg1 = 0xBF80u;  // bf16 -1.0
-            const int w = (r & 7) >> 1;
-            const uint32_t word = (r & 1) ? (neg1 << 16) : neg1;
-            if (w == 0) z.x = word; else if (w == 1) z.y = word; else if (w == 2) z.z = word; else z.w = word;
-        }
-        *(uint4 *)(sm + OFF_NEGI + bx * 16384 + sw128(r, 8 * cl)) = z;
-    }
-    fence_proxy_async();
     if (warp == 2) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *tslot;
+    const int cs = *s_cs;
+    const int nch = c1 - cs;
     unsigned *status = a.status;
+    float *sLX = (float *)(sm + OFF_LX);
+    auto gates = [&](int i) { return (float *)(sm + OFF_GATE + (i % kStages) * kGateBytes); };
+    auto emit_of = [&](int i) { return fwd && cs + i >= c0; };
 
     if (warp == 0) {
         // ================================================================ producer
         bool ok = true;
+        int issued = 0, landed = 0;
         for (int i = 0; i < nch && ok; ++i) {
-            const int c = cs + i, s = i & 1;
-            if (i >= 2) ok = mbar_wait(&bars[B_EMPTY + s], ((i >> 1) - 1) & 1, status, kStatusTimeout, kWaitNs);
+            const int c = cs + i, s = i % kStages;
+            if (i >= kStages) ok = mbar_wait(&bars[B_EMPTY + s], ((i / kStages) - 1) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const int64_t t0 = bos + (int64_t)c * kChunk;
             const int rows = rows_in(len, c);
-            const bool emit = fwd && c >= c0;
+            const bool emit = emit_of(i);
             uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
             if (lane == 0) {
                 const uint32_t bytes = 16384u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
@@ -237,6 +275,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
                 }
             }
+            ++issued;
             // gate statistics while the tiles land: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
             const int r0 = 2 * lane, r1 = r0 + 1;
             float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
@@ -256,28 +295,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             }
             const float G0 = sp - g1, G1 = sp;
             const float GC = __shfl_sync(0xffffffffu, sp, 31);
-            float *gt = (float *)(sm + OFF_GATE + s * kGateBytes);
-            const float gm0 = exp2f(G0), gm1 = exp2f(G1);
-            gt[GT_G + r0] = G0;
-            gt[GT_G + r1] = G1;
-            gt[GT_BETA + r0] = b0;
-            gt[GT_BETA + r1] = b1;
-            gt[GT_GAM + r0] = gm0;
-            gt[GT_GAM + r1] = gm1;
-            gt[GT_RDEC + r0] = exp2f(GC - G0);
-            gt[GT_RDEC + r1] = exp2f(GC - G1);
-            gt[GT_RGAM + r0] = exp2f(-G0);
-            gt[GT_RGAM + r1] = exp2f(-G1);
-            gt[GT_NBG + r0] = -b0 * gm0;
-            gt[GT_NBG + r1] = -b1 * gm1;
-            // output scales of this chunk; read by the output warps after x_ready of the chunk,
-            // which the prep warps release after acquiring this stage (so the writes are visible)
-            float *osc = (float *)(sm + OFF_EG) + (i & 7) * 64;
-            osc[r0] = a.scale * gm0;
-            osc[r1] = a.scale * gm1;
-            ok = mbar_wait(&bars[B_TMA + s], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
+            float *gt = gates(i);
+            const float gm0 = ex2(G0), gm1 = ex2(G1);
+            *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
+            *(float2 *)(gt + GT_BETA + r0) = make_float2(b0, b1);
+            *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
+            *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
+            *(float2 *)(gt + GT_RGAM + r0) = make_float2(ex2(-G0), ex2(-G1));
+            *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
+            ok = mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            ++landed;
             if (rows < kChunk) {
                 // rows past the end of the sequence belong to the next one: make them inert zeros
                 const uint4 z = make_uint4(0, 0, 0, 0);
@@ -295,192 +324,202 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_FULL + s]);
         }
+        // copies still in flight after a failure land before the CTA releases its shared memory
+        for (int i = landed; i < issued; ++i)
+            mbar_wait(&bars[B_TMA + i % kStages], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
     } else if (warp == 1) {
-        // ================================================================ MMA issuer
+        // ================================================================ MMA issuer (event driven)
         if (lane == 0 && nch > 0) {
-            const uint32_t idN64 = idesc_bf16_f32(128, 64, 0, 0);
-            const uint32_t idN128MN = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t negi = sbase + OFF_NEGI;
-            bool ok = mbar_wait(&bars[B_FULL], 0, status, kStatusTimeout, kWaitNs);
-            auto issue_kq = [&](int j) {
-                const uint32_t st = sbase + OFF_STAGE + (j & 1) * kStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ss(tb + TM_KQ, kmaj(st + off), kmaj(st + off), idN64, ks > 0);
-                }
-                mma_commit(&bars[B_KQF]);
-            };
-            // -(V diag(1/gam))^T of chunk j into the D region: needs no state, so it is issued
-            // as soon as the previous chunk's V' has been read out of that region
-            auto vhat_of = [&](int j) {
-                const float *gt = (const float *)(sm + OFF_GATE + (j & 1) * kGateBytes);
-                return !zero_values && gt[GT_G + 63] >= kFactorFloor;
-            };
-            auto issue_negv = [&](int j) -> bool {
-                if (!vhat_of(j)) return true;
-                if (!mbar_wait(&bars[B_VH + (j & 1)], (j >> 1) & 1, status, kStatusTimeout, kWaitNs)) return false;
-                tc_fence_after();
-                const uint32_t st = sbase + OFF_STAGE + (j & 1) * kStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    const uint32_t voff = (ks >> 2) * 8192 + (ks & 3) * 32;
-                    mma_ss(tb + TM_XV, kmaj(negi + off), kmaj(st + sV0 + voff), idN64, ks > 0);
-                }
-                return true;
-            };
-            if (ok) {
-                tc_fence_after();
-                issue_kq(0);
-                ok = issue_negv(0);
-            }
-            int e = 0;
-            for (int i = 0; i < nch && ok; ++i) {
-                const int s = i & 1, b = i & 1, c = cs + i;
-                const bool emit = fwd && c >= c0;
-                const uint32_t st = sbase + OFF_STAGE + s * kStageBytes;
-                const bool vhat = vhat_of(i);
-                ok = mbar_spin(&bars[B_SBF], i & 1, status, kStatusTimeout, kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-                // D^T (+)= S^T K^T
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ts(tb + TM_XV, tb + TM_SBF + ks * 8, kmaj(st + sK0 + off), idN64, vhat || ks > 0);
-                }
-                mma_commit(&bars[B_XF]);
-                // K K^T / Q K^T of the next chunk, so its preparation overlaps this chunk's chain
-                if (i + 1 < nch) {
-                    ok = mbar_wait(&bars[B_FULL + ((i + 1) & 1)], ((i + 1) >> 1) & 1, status, kStatusTimeout, kWaitNs) &&
-                         mbar_wait(&bars[B_KQE], i & 1, status, kStatusTimeout, kWaitNs);
-                    if (!ok) break;
+            const uint32_t idKQ = idesc_bf16_f32(128, 64, 0, 0);   // K-major A and B
+            const uint32_t idMN = idesc_bf16_f32(128, 64, 1, 0);   // MN-major A (V^T, K^T), K-major B
+            const uint32_t idV1 = idesc_bf16_f32(128, 64, 0, 1);   // A in TMEM, MN-major B (-W^T)
+            const uint32_t idO = idesc_bf16_f32(128, 64, 0, 0);    // A in TMEM, K-major B (Q~, P)
+            const uint32_t idS = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, MN-major B (K), N = dk
+            auto rdy = [&](int b, int ph) { return mbar_test_wait(&bars[b], (uint32_t)ph & 1u); };
+            auto stage = [&](int i) { return sbase + OFF_STAGE + (i % kStages) * kStageBytes; };
+            int kq = 0, u = 0, w = 0, c = 0, e = 0, cst = 0;
+            uint64_t t_last = globaltimer();
+            uint32_t idle = 0;
+            while (c < nch) {
+                bool prog = false;
+                const bool em = emit_of(c);
+                const uint32_t st = stage(c);
+                if (cst == 0 && u > c && rdy(B_SBF, c) && rdy(B_WC, c)) {
+                    // V'^T (holding U^T) -= S^T W^T
                     tc_fence_after();
-                    issue_kq(i + 1);
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
+                               idV1, (ks > 0 || !zero_values) ? 1u : 0u);
+                    mma_commit(&bars[B_VPF]);
+                    cst = em ? 1 : 2;
+                    prog = true;
                 }
-                ok = mbar_spin(&bars[B_YF], i & 1, status, kStatusTimeout, kWaitNs) &&
-                     mbar_spin(&bars[B_AF + b], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-                // V'^T = Y^T A_g^T
-                const uint32_t abuf = sbase + OFF_A + b * 8192;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ts(tb + TM_XV, tb + TM_YBF + ks * 8, kmaj(abuf + ks * 32), idN64, ks > 0);
-                mma_commit(&bars[B_VPF]);
-                if (emit) {
-                    // O1^T = S^T Q^T, in the window where the chain converts V'
-                    if (e > 0) ok = mbar_wait(&bars[B_OE], (e - 1) & 1, status, kStatusTimeout, kWaitNs);
-                    if (!ok) break;
+                if (cst == 1 && rdy(B_QS + c % kStages, c / kStages) && (e == 0 || rdy(B_OE, e - 1))) {
+                    // O^T = S^T Q~^T
                     tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ts(tb + TM_O1, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idN64, ks > 0);
+                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idO, ks > 0 ? 1u : 0u);
+                    }
+                    cst = 2;
+                    prog = true;
+                }
+                if (cst == 2 && rdy(B_VTF, c)) {
+                    // S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                    mma_commit(&bars[B_SF]);
+                    cst = em ? 3 : 4;
+                    prog = true;
+                }
+                if (cst == 3 && rdy(B_PF + (e & 1), e >> 1)) {
+                    // O^T += V'^T P^T
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + (e & 1) * 8192 + ks * 32), idO, 1u);
+                    mma_commit(&bars[B_OF]);
+                    mma_commit(&bars[B_PE + (e & 1)]);
+                    ++e;
+                    cst = 4;
+                    prog = true;
+                }
+                if (cst == 4) {
+                    mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                    ++c;
+                    cst = 0;
+                }
+                // ---- state-independent products, issued as soon as their inputs are ready
+                if (kq < nch && rdy(B_FULL + kq % kStages, kq / kStages) && (kq == 0 || rdy(B_KQE, kq - 1))) {
+                    // [K; Q] K^T: K K^T in lanes 0-63, Q K^T in lanes 64-127
+                    tc_fence_after();
+                    const uint32_t s2 = stage(kq);
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars[B_KQF]);
+                    ++kq;
+                    prog = true;
+                }
+                if (w < kq && rdy(B_TWF, w) && (w == 0 || rdy(B_WC, w - 1))) {
+                    // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
+                    tc_fence_after();
+                    const uint32_t s2 = stage(w);
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024),
+                               kmaj(sbase + OFF_TW + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                    mma_commit(&bars[B_WF]);
+                    ++w;
+                    prog = true;
+                }
+                if (u < kq && rdy(B_TUF + (u & 1), u >> 1) && (u == 0 || rdy(B_VTF, u - 1))) {
+                    // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
+                    tc_fence_after();
+                    if (!zero_values) {
+                        const uint32_t s2 = stage(u);
+#pragma unroll 1
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024),
+                                   kmaj(sbase + OFF_TU + (u & 1) * 8192 + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars[B_TUE + (u & 1)]);
+                    ++u;
+                    prog = true;
+                }
+                if (prog) {
+                    idle = 0;
+                    t_last = globaltimer();
+                } else {
+                    __nanosleep(20);  // polling competes with the other warps for the shared-memory pipe
+                    if ((++idle & 255u) == 0 && globaltimer() - t_last > kWaitNs) {
+                        atomicOr(status, kStatusTimeout);
+                        break;
                     }
                 }
-                ok = mbar_spin(&bars[B_VTF], i & 1, status, kStatusTimeout, kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-                // S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024),
-                           idN128MN, 1);
-                mma_commit(&bars[B_SF]);
-                // the next chunk's -(V / gam)^T (its stage was waited for before K K^T above)
-                if (i + 1 < nch && !issue_negv(i + 1)) {
-                    ok = false;
-                    break;
-                }
-                if (emit) {
-                    // O2^T = V'^T P_g^T
-                    const uint32_t pbuf = sbase + OFF_P + b * 8192, vp = sbase + OFF_VP;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tb + TM_O2, kmaj(vp + ks * 32), kmaj(pbuf + ks * 32), idN64, ks > 0);
-                    mma_commit(&bars[B_OF]);
-                    ++e;
-                }
-                mma_commit(&bars[B_EMPTY + s]);
-                mma_commit(&bars[B_AE + b]);
             }
+            // every product issued so far has finished before the CTA frees its tensor memory
+            mma_commit(&bars[B_FIN]);
+            mbar_wait(&bars[B_FIN], 0, status, kStatusTimeout, kWaitNs);
         }
     } else if (warp == 2 || warp == 3) {
-        // ================================================================ aux: V / gam in place, P_g
-        const int at = tid - 64;  // 0..63; TMEM lanes 64..127 = Q K^T rows
+        // ================================================================ aux: Q~ in place, P (lane = row of Q K^T)
+        const int r = tid - 64;  // 0..63; TMEM lanes 64..127
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
         bool ok = true;
+        int e = 0;
         for (int i = 0; i < nch && ok; ++i) {
-            const int s = i & 1, b = i & 1, c = cs + i;
-            const bool emit = fwd && c >= c0;
-            ok = mbar_wait(&bars[B_FULL + s], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const float *gt = (const float *)(sm + OFF_GATE + s * kGateBytes);
-            const bool factored = gt[GT_G + 63] >= kFactorFloor;
-            if (!zero_values && factored) {
-                // V <- V diag(2^-G): 16-byte pieces (8 values of one row c)
-                uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-#pragma unroll 4
-                for (int p = at; p < 1024; p += 64) {
-                    const int bx = p >> 9, w = p & 511, r = w >> 3;
-                    uint4 *ptr = (uint4 *)(st + sV0 + bx * 8192 + w * 16);
-                    uint4 x = *ptr;
-                    const float f = gt[GT_RGAM + r];
-                    __nv_bfloat162 *h2 = (__nv_bfloat162 *)&x;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float2 fv = __bfloat1622float2(h2[u]);
-                        h2[u] = __floats2bfloat162_rn(fv.x * f, fv.y * f);
-                    }
-                    *ptr = x;
-                }
-                fence_proxy_async();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_VH + s]);  // every chunk, so the phases follow the stage uses
-            // P_g row r = scale * Gam[r, j <= r] * (Q K^T)[r, j] -> bf16, 128-byte swizzled
-            if (i >= 2) ok = mbar_wait(&bars[B_AE + b], ((i >> 1) - 1) & 1, status, kStatusTimeout, kWaitNs);
+            const int s = i % kStages;
+            const bool emit = emit_of(i);
+            ok = mbar_wait(&bars[B_FULL + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             if (ok) ok = mbar_wait(&bars[B_KQF], i & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            const float *gt = gates(i);
+            // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j] -> bf16 into buffer e & 1, once O2 of
+            // the chunk that used it before has finished
             if (emit) {
-                const int r = at;
-                const float Gr = gt[GT_G + r], fr = a.scale * gt[GT_GAM + r];
-                uint8_t *prow = sm + OFF_P + b * 8192;
+                if (e >= 2) ok = mbar_wait(&bars[B_PE + (e & 1)], ((e >> 1) - 1) & 1, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const float Gr = gt[GT_G + r], sc = a.scale;
+                uint8_t *prow = sm + OFF_P + (e & 1) * 8192;
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t kq[32];
                     tmem_ld32(tl + TM_KQ + 32 * hf, kq);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const int j0 = 32 * hf + 8 * qq;
-                        const float4 rg0 = *(const float4 *)(gt + GT_RGAM + j0);
-                        const float4 rg1 = *(const float4 *)(gt + GT_RGAM + j0 + 4);
-                        const float rgv[8] = {rg0.x, rg0.y, rg0.z, rg0.w, rg1.x, rg1.y, rg1.z, rg1.w};
+                    for (int q = 0; q < 4; ++q) {
                         float v[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            const int j = j0 + u;
-                            const float gij = factored ? fr * rgv[u] : a.scale * exp2f(Gr - gt[GT_G + j]);
-                            v[u] = (j <= r) ? gij * u2f(kq[8 * qq + u]) : 0.f;
+                            const int j = 32 * hf + 8 * q + u;
+                            v[u] = (j <= r) ? sc * ex2(Gr - gt[GT_G + j]) * u2f(kq[8 * q + u]) : 0.f;
                         }
-                        *(uint4 *)(prow + sw128(r, j0)) = pack8(v);
+                        *(uint4 *)(prow + sw128(r, 32 * hf + 8 * q)) = pack8(v);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_KQE]);
+            if (emit) {
+                // Q~ row r = scale * gam_r * q_r, in place (the K K^T / Q K^T product has read Q);
+                // the 16-byte pieces are visited in a row-rotated order to spread the banks
+                uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
+                const float f = gt[GT_SGAM + r];
+#pragma unroll 1
+                for (int bx = 0; bx < 2; ++bx) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const int ch = (c8 + r) & 7;
+                        uint4 *ptr = (uint4 *)(st + (bx ? sQ1 : sQ0) + r * 128 + ch * 16);
+                        uint4 x = *ptr;
+                        __nv_bfloat162 *h2 = (__nv_bfloat162 *)&x;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 fv = __bfloat1622float2(h2[q]);
+                            h2[q] = __floats2bfloat162_rn(fv.x * f, fv.y * f);
+                        }
+                        *ptr = x;
                     }
                 }
                 fence_proxy_async();
             }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_KQE]);
-                mbar_arrive(&bars[B_AF + b]);
-                mbar_arrive(&bars[B_EMPTY + s]);
-            }
+            if (lane == 0) mbar_arrive(&bars[B_QS + s]);
+            if (!emit) continue;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_PF + (e & 1)]);
+            ++e;
         }
     } else if (warp >= 4 && warp < 8) {
         // ================================================================ chain (lane = dv)
@@ -497,136 +536,86 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             identity = true;
         }
         bool ok = true;
+        if (nch > 0) {
+            // the segment's initial state into the state accumulator (no product touches it yet)
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t r[32];
+                if (init) {
+                    const float *src = init + (size_t)(32 * q4) * V + dv;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = f2u(__ldg(src + j * V));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = f2u(identity && 32 * q4 + j == dv ? 1.f : 0.f);
+                }
+                tmem_st32(tl + TM_S + 32 * q4, r);
+            }
+            tmem_st_wait();
+        }
         for (int i = 0; i < nch && ok; ++i) {
-            const int s = i & 1, c = cs + i;
-            const bool emit = fwd && c >= c0;
-            ok = mbar_wait(&bars[B_FULL + s], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
-            if (ok && i > 0) ok = mbar_spin(&bars[B_SF], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
+            const int s = i % kStages;
+            ok = mbar_wait(&bars[B_FULL + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
+            if (ok && i > 0) ok = mbar_wait(&bars[B_SF], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const float *gt = (const float *)(sm + OFF_GATE + s * kGateBytes);
+            const float *gt = gates(i);
             const float dec = gt[GT_GAM + 63];  // gC = 2^G_C
-            const bool vhat = !zero_values && gt[GT_G + 63] >= kFactorFloor;
             // ---- S_i -> bf16 copy (MMA operand) and gC * S_i (accumulator of this chunk's update)
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t r[32], p[16];
-                if (i == 0) {
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[64];
+                tmem_ld32(tl + TM_S + 64 * h, r);
+                tmem_ld32(tl + TM_S + 64 * h + 32, r + 32);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int d = 32 * q4 + j;
-                        float x = 0.f;
-                        if (init) x = init[(size_t)d * V + dv];
-                        else if (identity) x = (d == dv) ? 1.f : 0.f;
-                        r[j] = f2u(x);
-                    }
-                } else {
-                    tmem_ld32(tl + TM_S + 32 * q4, r);
-                    tmem_ld_wait();
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t p[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) p[j] = pack_bf16(u2f(r[32 * q + 2 * j]), u2f(r[32 * q + 2 * j + 1]));
+                    tmem_st16(tl + TM_SBF + 32 * h + 16 * q, p);
                 }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) p[j] = pack_bf16(u2f(r[2 * j]), u2f(r[2 * j + 1]));
-                tmem_st16(tl + TM_SBF + 16 * q4, p);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = f2u(u2f(r[j]) * dec);
-                tmem_st32(tl + TM_S + 32 * q4, r);
+                for (int j = 0; j < 64; ++j) r[j] = f2u(u2f(r[j]) * dec);
+                tmem_st32(tl + TM_S + 64 * h, r);
+                tmem_st32(tl + TM_S + 64 * h + 32, r + 32);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_SBF]);
 
-            // ---- Y^T = beta (V^T - gam X^T)
-            ok = mbar_spin(&bars[B_XF], i & 1, status, kStatusTimeout, kWaitNs);
+            // ---- V'^T -> bf16: as the output operand (TMEM) and scaled by gC/gam as the update operand
+            ok = mbar_wait(&bars[B_VPF], i & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             {
-                const uint8_t *vbox = sm + OFF_STAGE + s * kStageBytes + (dv < 64 ? sV0 : sV1);
-                const int dl = dv & 63;
-                uint32_t rr[2][32];
-                tmem_ld32(tl + TM_XV, rr[0]);
-                tmem_ld32(tl + TM_XV + 32, rr[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t *r = rr[h];
-                    uint32_t y[16];
-                    if (vhat) {
-                        // the tensor core already formed X^T - (V diag(1/gam))^T: Y = -beta gam (that)
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 nb = *(const float4 *)(gt + GT_NBG + 32 * h + 4 * j4);
-                            y[2 * j4] = pack_bf16(nb.x * u2f(r[4 * j4 + 0]), nb.y * u2f(r[4 * j4 + 1]));
-                            y[2 * j4 + 1] = pack_bf16(nb.z * u2f(r[4 * j4 + 2]), nb.w * u2f(r[4 * j4 + 3]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const int cc = 32 * h + 4 * j4;
-                            const float4 bt = *(const float4 *)(gt + GT_BETA + cc);
-                            const float4 gm = *(const float4 *)(gt + GT_GAM + cc);
-                            float v[4] = {0.f, 0.f, 0.f, 0.f};
-                            if (!zero_values) {
-#pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    v[u] = __bfloat162float(*(const __nv_bfloat16 *)(vbox + sw128(cc + u, dl)));
-                            }
-                            y[2 * j4] = pack_bf16(bt.x * (v[0] - gm.x * u2f(r[4 * j4 + 0])),
-                                                  bt.y * (v[1] - gm.y * u2f(r[4 * j4 + 1])));
-                            y[2 * j4 + 1] = pack_bf16(bt.z * (v[2] - gm.z * u2f(r[4 * j4 + 2])),
-                                                      bt.w * (v[3] - gm.w * u2f(r[4 * j4 + 3])));
-                        }
-                    }
-                    tmem_st16(tl + TM_YBF + 16 * h, y);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_YF]);
-
-            // ---- V'^T -> bf16 (output operand, smem) and V'^T diag(gC/gam) (state operand, TMEM)
-            ok = mbar_spin(&bars[B_VPF], i & 1, status, kStatusTimeout, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            {
-                uint8_t *vprow = sm + OFF_VP;
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t r[32], vtl[16];
-                    tmem_ld32(tl + TM_XV + 32 * h, r);
+                    uint32_t r[32];
+                    tmem_ld32(tl + TM_VP + 32 * h, r);
                     tmem_ld_wait();
-                    float4 rd[8];
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) rd[j4] = *(const float4 *)(gt + GT_RDEC + 32 * h + 4 * j4);
+                    uint32_t vb[16], vtb[16];
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        vtl[2 * j4] = pack_bf16(u2f(r[4 * j4 + 0]) * rd[j4].x, u2f(r[4 * j4 + 1]) * rd[j4].y);
-                        vtl[2 * j4 + 1] = pack_bf16(u2f(r[4 * j4 + 2]) * rd[j4].z, u2f(r[4 * j4 + 3]) * rd[j4].w);
+                        const float4 rd = *(const float4 *)(gt + GT_RDEC + 32 * h + 4 * j4);
+                        const float x0 = u2f(r[4 * j4 + 0]), x1 = u2f(r[4 * j4 + 1]);
+                        const float x2 = u2f(r[4 * j4 + 2]), x3 = u2f(r[4 * j4 + 3]);
+                        vb[2 * j4] = pack_bf16(x0, x1);
+                        vb[2 * j4 + 1] = pack_bf16(x2, x3);
+                        vtb[2 * j4] = pack_bf16(x0 * rd.x, x1 * rd.y);
+                        vtb[2 * j4 + 1] = pack_bf16(x2 * rd.z, x3 * rd.w);
                     }
-                    tmem_st16(tl + TM_VTB + 16 * h, vtl);
-                    if (emit) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float f[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) f[u] = u2f(r[8 * q + u]);
-                            *(uint4 *)(vprow + sw128(dv, 32 * h + 8 * q)) = pack8(f);
-                        }
-                    }
+                    tmem_st16(tl + TM_VTB + 16 * h, vtb);
+                    tmem_st16(tl + TM_VB + 16 * h, vb);
                 }
-                if (emit) fence_proxy_async();
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_VTF]);
-                mbar_arrive(&bars[B_EMPTY + s]);  // done with this stage's V and gates
-            }
+            if (lane == 0) mbar_arrive(&bars[B_VTF]);
         }
         // ---- final state of the segment
         const bool write_ht = fwd && c1 == NT && a.ht != nullptr;
@@ -642,6 +631,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 dstride = V + 128;
             }
             if (nch == 0) {
+#pragma unroll 1
                 for (int d = 0; d < 128; ++d) {
                     float x = 0.f;
                     if (init) x = init[(size_t)d * V + dv];
@@ -658,276 +648,297 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                         uint32_t r[32];
                         tmem_ld32(tl + TM_S + 32 * q4, r);
                         tmem_ld_wait();
+                        float *p = dst + (size_t)(32 * q4) * dstride;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) dst[(size_t)(32 * q4 + j) * dstride] = u2f(r[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            *p = u2f(r[j]);
+                            p += dstride;
+                        }
                     }
                 }
             }
         }
     } else if (warp >= 8 && warp < 12) {
-        // ================================================================ prep (lane = row of K K^T)
+        // ================================================================ prep: L and the blockwise inverse
+        // sLX holds L = diag(beta) StrictLower(K K^T) in its lower triangle and X = (I + L)^-1
+        // transposed in its upper triangle: X(r, j), j < r, at sLX[j * kLdX + r]; X(r, r) = 1.
+        // Blocks are merged exactly: [[A, 0], [C, D]]^-1 = [[A^-1, 0], [-D^-1 C A^-1, D^-1]].
         const int pt = tid - 256, pw = warp - 8;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
-        float *sL = (float *)(sm + OFF_L);
-        float *sX = (float *)(sm + OFF_X);
-        float *pG = (float *)(sm + OFF_PG);               // gam, rgam, G of the chunk being prepared
-        float *scr = (float *)(sm + OFF_SCR) + pw * 256;  // per-warp scratch for the block products
-        const int g = lane >> 2, tg = lane & 3;
+        float *scr = (float *)(sm + OFF_SCR);
+        auto Lx = [&](int r, int j) -> float { return sLX[r * kLdX + j]; };
+        auto Xt = [&](int r, int j) -> float { return sLX[j * kLdX + r]; };  // X(r, j), j < r
+        auto Xm = [&](int r, int j) -> float { return r > j ? sLX[j * kLdX + r] : (r == j ? 1.f : 0.f); };  // X(r, j)
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
-            const int s = i & 1;
-            ok = mbar_wait(&bars[B_FULL + s], (i >> 1) & 1, status, kStatusTimeout, kWaitNs);
+            const int s = i % kStages;
+            ok = mbar_wait(&bars[B_FULL + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             if (ok) ok = mbar_wait(&bars[B_KQF], i & 1, status, kStatusTimeout, kWaitNs);
-            ok = bar_and(1, 128, ok);
+            ok = bar_and(NB_PREP, 128, ok);
             if (!ok) break;
             tc_fence_after();
-            const float *gt = (const float *)(sm + OFF_GATE + s * kGateBytes);
-            const float factored = gt[GT_G + 63] >= kFactorFloor ? 1.f : 0.f;
-            float pg_gam = 0.f, pg_rgam = 0.f, pg_G = 0.f;
+            const float *gt = gates(i);
             if (pt < 64) {
-                // L row r = beta_r * (K K^T)[r, j < r]   (gate-free: the gates enter as Gam * A0)
+                // L row r = beta_r * (K K^T)[r, j < r]   (lower triangle only: X of the previous chunk
+                // in the upper triangle may still be read by the output warps)
                 const int r = pt;
                 const float br = gt[GT_BETA + r];
-                pg_gam = gt[GT_GAM + r];
-                pg_rgam = gt[GT_RGAM + r];
-                pg_G = gt[GT_G + r];
-                float diag = 0.f;
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t kq[32];
-                    tmem_ld32(tl + TM_KQ + 32 * hf, kq);
-                    tmem_ld_wait();
+                uint32_t kq[64];
+                tmem_ld32(tl + TM_KQ, kq);
+                tmem_ld32(tl + TM_KQ + 32, kq + 32);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_KQE]);
+                float bdiag = 0.f;  // beta_r ||k_r||^2 (<= 2 keeps every transition non-expansive)
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const int j = 32 * hf + 4 * j4;
-                        float4 w;
-                        w.x = (j + 0 < r) ? br * u2f(kq[4 * j4 + 0]) : 0.f;
-                        w.y = (j + 1 < r) ? br * u2f(kq[4 * j4 + 1]) : 0.f;
-                        w.z = (j + 2 < r) ? br * u2f(kq[4 * j4 + 2]) : 0.f;
-                        w.w = (j + 3 < r) ? br * u2f(kq[4 * j4 + 3]) : 0.f;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (j + u == r) diag = u2f(kq[4 * j4 + u]);
-                        *(float4 *)(sL + r * kLdX + j) = w;
+                for (int j4 = 0; j4 < 16; ++j4) {
+                    const int j = 4 * j4;
+                    const float4 w4 = make_float4(br * u2f(kq[j]), br * u2f(kq[j + 1]), br * u2f(kq[j + 2]),
+                                                  br * u2f(kq[j + 3]));
+                    if (j + 3 < r) {
+                        *(float4 *)(sLX + r * kLdX + j) = w4;
+                    } else if (j <= r) {
+                        // the quad holding the diagonal: strictly lower part stored, diagonal kept
+                        if (j < r) sLX[r * kLdX + j] = w4.x;
+                        if (j + 1 < r) sLX[r * kLdX + j + 1] = w4.y;
+                        if (j + 2 < r) sLX[r * kLdX + j + 2] = w4.z;
+                        bdiag = (r & 1) ? ((r & 2) ? w4.w : w4.y) : ((r & 2) ? w4.z : w4.x);
                     }
                 }
-                if (check_norm && br * diag > 2.0001f) atomicOr(status, kStatusNormBound);
+                if (check_norm && bdiag > 2.0001f) atomicOr(status, kStatusNormBound);
             }
-            tc_fence_before();
-            bar_sync(1, 128);
-            if (lane == 0) {
-                mbar_arrive(&bars[B_KQE]);
-                mbar_arrive(&bars[B_EMPTY + s]);  // gates copied; stage no longer read here
-            }
-            // X / gate copies of the previous chunk must have been turned into A_g
+            // X of the previous chunk has been turned into the operand tiles
             if (i >= 1) ok = mbar_wait(&bars[B_XFREE], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
-            ok = bar_and(1, 128, ok);
+            ok = bar_and(NB_PREP, 128, ok);
             if (!ok) break;
-            if (pt < 64) {
-                pG[pt] = pg_gam;
-                pG[64 + pt] = pg_rgam;
-                pG[128 + pt] = pg_G;
-                if (pt == 0) pG[192] = factored;
-            }
 
-            // ---- (I + L_bb)^-1 for the four 16 x 16 diagonal blocks: 2 threads per (block, column)
+            // ---- A: the eight 8 x 8 diagonal blocks by forward substitution; 2 threads per (block, column)
             {
                 const int task = pt >> 1, hh = pt & 1;
-                const int bb = task >> 4, cc = task & 15;
-                const int base = 16 * bb;
-                const float *Lb = sL + base * kLdX + base;
-                float x[16];
+                const int base = 8 * (task >> 3), cc = task & 7;
+                float x[8];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+                for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-                for (int r = 1; r < 16; ++r) {
+                for (int r = 1; r < 8; ++r) {
                     float part = 0.f;
 #pragma unroll
                     for (int j = 0; j < r; ++j)
-                        if ((j & 1) == hh) part = fmaf(Lb[r * kLdX + j], x[j], part);
+                        if ((j & 1) == hh) part = fmaf(Lx(base + r, base + j), x[j], part);
                     part += __shfl_xor_sync(0xffffffffu, part, 1);
                     if (r > cc) x[r] = -part;
                 }
-                float *Xb = sX + base * kLdX + base;
                 if (hh == 0) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) Xb[r * kLdX + cc] = x[r];
-                } else if (bb == 0 || bb == 2) {
-                    // zero the strictly upper 16 x 16 blocks that the 32 x 32 merge reads
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) Xb[r * kLdX + 16 + cc] = 0.f;
+                    for (int r = 1; r < 8; ++r)
+                        if (r > cc) sLX[(base + cc) * kLdX + base + r] = x[r];
                 }
             }
-            bar_sync(1, 128);
-            // ---- exact block merges (16 -> 32 -> 64), tf32 tensor-core products (the result is
-            //      rounded to bf16 for the MMA operand, well above tf32's rounding):
-            //      [[A00, 0], [A10, A11]]^-1 = [[X00, 0], [-X11 A10 X00, X11]]
+            bar_sync(NB_PREP, 128);
+            // ---- B: 8 -> 16, one warp per merge:  X(B, A) = -X(B, B) (L(B, A) X(A, A))
             {
-                // 16 -> 32: warps 0,1 merge blocks (1,0); warps 2,3 merge (3,2); one 8-column tile each
-                const int ra = (pw >> 1) ? 3 : 1, rb = ra - 1, nt = pw & 1;
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                const int A = 16 * pw, Bb = A + 8;
+                const int r = lane >> 2, cp = (lane & 3) * 2;
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float l = Lx(Bb + r, A + k);
+                    const float x0 = k > cp ? Xt(A + k, A + cp) : (k == cp ? 1.f : 0.f);
+                    const float x1 = k > cp + 1 ? Xt(A + k, A + cp + 1) : (k == cp + 1 ? 1.f : 0.f);
+                    t0 = fmaf(l, x0, t0);
+                    t1 = fmaf(l, x1, t1);
+                }
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float tk0 = __shfl_sync(0xffffffffu, t0, 4 * k + (lane & 3));
+                    const float tk1 = __shfl_sync(0xffffffffu, t1, 4 * k + (lane & 3));
+                    const float xb = k < r ? Xt(Bb + r, Bb + k) : (k == r ? 1.f : 0.f);
+                    a0 = fmaf(xb, tk0, a0);
+                    a1 = fmaf(xb, tk1, a1);
+                }
+                sLX[(A + cp) * kLdX + Bb + r] = -a0;
+                sLX[(A + cp + 1) * kLdX + Bb + r] = -a1;
+            }
+            bar_sync(NB_PREP, 128);
+            // ---- C: 16 -> 32 on the tensor cores (tf32 m16n8k8); warp = (merge, 8-column tile):
+            //      T = L(B, A) X(A, A)[:, tile], then X(B, A)[:, tile] = -X(B, B) T
+            {
+                const int g = lane >> 2, t = lane & 3;
+                const int A = 32 * (pw >> 1), Bb = A + 16, n0 = 8 * (pw & 1);
+                float *T = scr + pw * 128;  // T[m][n], 16 x 8, private to the warp
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
-                    const float *Lr = sL + (16 * ra) * kLdX + 16 * rb + 8 * ks;
-                    const float *Xr = sX + (16 * rb + 8 * ks) * kLdX + 16 * rb + 8 * nt;
-                    mma_tf32(t, Lr[g * kLdX + tg], Lr[(g + 8) * kLdX + tg], Lr[g * kLdX + tg + 4],
-                               Lr[(g + 8) * kLdX + tg + 4], Xr[tg * kLdX + g], Xr[(tg + 4) * kLdX + g]);
+                    const int k0 = 8 * ks;
+                    mma_tf32(d, Lx(Bb + g, A + k0 + t), Lx(Bb + g + 8, A + k0 + t), Lx(Bb + g, A + k0 + t + 4),
+                             Lx(Bb + g + 8, A + k0 + t + 4), Xm(A + k0 + t, A + n0 + g), Xm(A + k0 + t + 4, A + n0 + g));
                 }
-                scr[g * 8 + 2 * tg] = t[0];
-                scr[g * 8 + 2 * tg + 1] = t[1];
-                scr[(g + 8) * 8 + 2 * tg] = t[2];
-                scr[(g + 8) * 8 + 2 * tg + 1] = t[3];
+                *(float2 *)(T + g * 8 + 2 * t) = make_float2(d[0], d[1]);
+                *(float2 *)(T + (g + 8) * 8 + 2 * t) = make_float2(d[2], d[3]);
                 __syncwarp();
-                float u4[4] = {0.f, 0.f, 0.f, 0.f};
+                float u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
-                    const float *Xa = sX + (16 * ra) * kLdX + 16 * ra + 8 * ks;
-                    mma_tf32(u4, Xa[g * kLdX + tg], Xa[(g + 8) * kLdX + tg], Xa[g * kLdX + tg + 4],
-                               Xa[(g + 8) * kLdX + tg + 4], scr[(8 * ks + tg) * 8 + g], scr[(8 * ks + tg + 4) * 8 + g]);
+                    const int k0 = 8 * ks;
+                    mma_tf32(u, Xm(Bb + g, Bb + k0 + t), Xm(Bb + g + 8, Bb + k0 + t), Xm(Bb + g, Bb + k0 + t + 4),
+                             Xm(Bb + g + 8, Bb + k0 + t + 4), T[(k0 + t) * 8 + g], T[(k0 + t + 4) * 8 + g]);
                 }
-                float *dst = sX + (16 * ra) * kLdX + 16 * rb + 8 * nt;
-                dst[g * kLdX + 2 * tg] = -u4[0];
-                dst[g * kLdX + 2 * tg + 1] = -u4[1];
-                dst[(g + 8) * kLdX + 2 * tg] = -u4[2];
-                dst[(g + 8) * kLdX + 2 * tg + 1] = -u4[3];
+                sLX[(A + n0 + 2 * t) * kLdX + Bb + g] = -u[0];
+                sLX[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = -u[1];
+                sLX[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = -u[2];
+                sLX[(A + n0 + 2 * t + 1) * kLdX + Bb + g + 8] = -u[3];
             }
-            bar_sync(1, 128);
+            bar_sync(NB_PREP, 128);
+            // ---- D: 32 -> 64 on the tensor cores; warp = 8-column tile of the lower-left 32 x 32 block:
+            //      T = L(32:64, 0:32) X(0:32, tile), then X(32:64, tile) = -X(32:64, 32:64) T
             {
-                // 32 -> 64: X[32:64, 0:32] = -X[32:64, 32:64] * (L[32:64, 0:32] * X[0:32, 0:32]); warp = 8-column tile
-                const int nt = pw;
-                float t[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const int g = lane >> 2, t = lane & 3, n0 = 8 * pw;
+                float *T = scr + pw * 256;  // T[m][n], 32 x 8, private to the warp
+                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const float *Xr = sX + (8 * ks) * kLdX + 8 * nt;
-                    const float b0 = Xr[tg * kLdX + g], b1 = Xr[(tg + 4) * kLdX + g];
+                    if (ks < pw) continue;  // X(k, n) = 0 for k < n
+                    const int k0 = 8 * ks;
+                    const float b0 = Xm(k0 + t, n0 + g), b1 = Xm(k0 + t + 4, n0 + g);
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
-                        const float *Lr = sL + (32 + 16 * mt) * kLdX + 8 * ks;
-                        mma_tf32(t[mt], Lr[g * kLdX + tg], Lr[(g + 8) * kLdX + tg], Lr[g * kLdX + tg + 4],
-                                   Lr[(g + 8) * kLdX + tg + 4], b0, b1);
+                        const int m0 = 32 + 16 * mt;
+                        mma_tf32(d[mt], Lx(m0 + g, k0 + t), Lx(m0 + g + 8, k0 + t), Lx(m0 + g, k0 + t + 4),
+                                 Lx(m0 + g + 8, k0 + t + 4), b0, b1);
                     }
                 }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    scr[(16 * mt + g) * 8 + 2 * tg] = t[mt][0];
-                    scr[(16 * mt + g) * 8 + 2 * tg + 1] = t[mt][1];
-                    scr[(16 * mt + g + 8) * 8 + 2 * tg] = t[mt][2];
-                    scr[(16 * mt + g + 8) * 8 + 2 * tg + 1] = t[mt][3];
+                    *(float2 *)(T + (16 * mt + g) * 8 + 2 * t) = make_float2(d[mt][0], d[mt][1]);
+                    *(float2 *)(T + (16 * mt + g + 8) * 8 + 2 * t) = make_float2(d[mt][2], d[mt][3]);
                 }
                 __syncwarp();
-                float u4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const float b0 = scr[(8 * ks + tg) * 8 + g], b1 = scr[(8 * ks + tg + 4) * 8 + g];
+                    const int k0 = 8 * ks;
+                    const float b0 = T[(k0 + t) * 8 + g], b1 = T[(k0 + t + 4) * 8 + g];
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
-                        const float *Xa = sX + (32 + 16 * mt) * kLdX + 32 + 8 * ks;
-                        mma_tf32(u4[mt], Xa[g * kLdX + tg], Xa[(g + 8) * kLdX + tg], Xa[g * kLdX + tg + 4],
-                                   Xa[(g + 8) * kLdX + tg + 4], b0, b1);
+                        if (k0 > 16 * mt + 15) continue;  // X(32 + m, 32 + k) = 0 for k > m
+                        const int m0 = 32 + 16 * mt;
+                        mma_tf32(u[mt], Xm(m0 + g, 32 + k0 + t), Xm(m0 + g + 8, 32 + k0 + t), Xm(m0 + g, 32 + k0 + t + 4),
+                                 Xm(m0 + g + 8, 32 + k0 + t + 4), b0, b1);
                     }
                 }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    float *dst = sX + (32 + 16 * mt) * kLdX + 8 * nt;
-                    dst[g * kLdX + 2 * tg] = -u4[mt][0];
-                    dst[g * kLdX + 2 * tg + 1] = -u4[mt][1];
-                    dst[(g + 8) * kLdX + 2 * tg] = -u4[mt][2];
-                    dst[(g + 8) * kLdX + 2 * tg + 1] = -u4[mt][3];
+                    const int m0 = 32 + 16 * mt;
+                    sLX[(n0 + 2 * t) * kLdX + m0 + g] = -u[mt][0];
+                    sLX[(n0 + 2 * t + 1) * kLdX + m0 + g] = -u[mt][1];
+                    sLX[(n0 + 2 * t) * kLdX + m0 + g + 8] = -u[mt][2];
+                    sLX[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
                 }
             }
-            bar_sync(1, 128);
-            // X (and the gate copies) are ready for the output warps, which form A_g
+            // X is complete once all four warps have arrived
+            __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_XR]);
         }
     } else {
-        // ================================================================ output (lane = dv)
-        const int et = tid - 384, dv = et;
+        // ================================================================ output warps
+        const int et = tid - 384;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
-        const float *sX = (const float *)(sm + OFF_X);
-        const float *pG = (const float *)(sm + OFF_PG);
         bool ok = true;
         int e = 0;
-        for (int it = 0; it <= nch && ok; ++it) {
-            if (it < nch) {
-                // ---- A_g = Gam * X (lower incl. diagonal) -> bf16, 128-byte swizzled rows, for chunk it
-                const int b = it & 1;
-                ok = mbar_wait(&bars[B_XR], it & 1, status, kStatusTimeout, kWaitNs);
-                if (ok && it >= 2) ok = mbar_wait(&bars[B_AE + b], ((it >> 1) - 1) & 1, status, kStatusTimeout, kWaitNs);
-                ok = bar_and(3, 128, ok);
+        // operand tiles of chunk j: T_U = A_g diag(beta), T_W = A_g diag(beta gam) = diag(gam) X diag(beta)
+        auto tiles = [&](int j) -> bool {
+            const int b = j & 1;
+            bool k2 = mbar_wait(&bars[B_XR], j & 1, status, kStatusTimeout, kWaitNs);
+            if (k2 && j >= 2) k2 = mbar_wait(&bars[B_TUE + b], ((j - 2) >> 1) & 1, status, kStatusTimeout, kWaitNs);
+            if (k2 && j >= 1) k2 = mbar_wait(&bars[B_WF], (j - 1) & 1, status, kStatusTimeout, kWaitNs);
+            k2 = __all_sync(0xffffffffu, k2);  // warps work on their own rows: no group barrier
+            if (!k2) return false;
+            const float *gt = gates(j);
+            const int r = et >> 1, h = et & 1;
+            const float gr = gt[GT_GAM + r], Gr = gt[GT_G + r];
+            uint8_t *tu = sm + OFF_TU + b * 8192, *tw = sm + OFF_TW;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                const int j0 = 32 * h + 8 * q;
+                float vu[8], vw[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = j0 + u;
+                    const float x = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                    const float bx = gt[GT_BETA + jj] * x;
+                    vw[u] = gr * bx;
+                    vu[u] = jj <= r ? ex2(Gr - gt[GT_G + jj]) * bx : 0.f;
+                }
+                *(uint4 *)(tu + sw128(r, j0)) = pack8(vu);
+                *(uint4 *)(tw + sw128(r, j0)) = pack8(vw);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[B_XFREE]);
+                mbar_arrive(&bars[B_TUF + b]);
+                mbar_arrive(&bars[B_TWF]);
+            }
+            return true;
+        };
+        for (int it = -1; it <= nch && ok; ++it) {
+            if (it >= 0 && it < nch) {
+                // ---- -W^T of chunk it (lane = dk) -> shared memory, MN-major operand of V' = U - W S
+                ok = mbar_wait(&bars[B_WF], it & 1, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const int r = et >> 1, h = et & 1;
-                const bool factored = pG[192] != 0.f;
-                const float gr = pG[r], Gr = pG[128 + r];
-                uint8_t *arow = sm + OFF_A + b * 8192;
+                tc_fence_after();
+                uint32_t r[64];
+                tmem_ld32(tl + TM_W, r);
+                tmem_ld32(tl + TM_W + 32, r + 32);
+                tmem_ld_wait();
+                if (it >= 1) ok = mbar_wait(&bars[B_VPF], (it - 1) & 1, status, kStatusTimeout, kWaitNs);  // -W^T free
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                uint8_t *wrow = sm + OFF_WS;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j0 = 32 * h + 8 * q;
-                    const float4 x0 = *(const float4 *)(sX + r * kLdX + j0);
-                    const float4 x1 = *(const float4 *)(sX + r * kLdX + j0 + 4);
-                    const float4 rg0 = *(const float4 *)(pG + 64 + j0);
-                    const float4 rg1 = *(const float4 *)(pG + 64 + j0 + 4);
-                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                    const float rgv[8] = {rg0.x, rg0.y, rg0.z, rg0.w, rg1.x, rg1.y, rg1.z, rg1.w};
-                    float v[8];
+                for (int q = 0; q < 8; ++q) {
+                    float f[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int j = j0 + u;
-                        const float gij = factored ? gr * rgv[u] : exp2f(Gr - pG[128 + j]);
-                        v[u] = (j <= r) ? gij * xv[u] : 0.f;
-                    }
-                    *(uint4 *)(arow + sw128(r, j0)) = pack8(v);
+                    for (int u = 0; u < 8; ++u) f[u] = -u2f(r[8 * q + u]);
+                    *(uint4 *)(wrow + sw128(et, 8 * q)) = pack8(f);
                 }
                 fence_proxy_async();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[B_AF + b]);
-                    mbar_arrive(&bars[B_XFREE]);
-                }
+                if (lane == 0) mbar_arrive(&bars[B_WC]);
             }
-            if (it < 1) continue;
-            // ---- O of chunk it - 1
-            const int c = cs + it - 1;
-            if (!(fwd && c >= c0)) continue;
-            const int64_t t0 = bos + (int64_t)c * kChunk;
-            const int rows = rows_in(len, c);
-            const float *eg = (const float *)(sm + OFF_EG) + ((it - 1) & 7) * 64;  // scale * 2^G of the chunk
-            ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            __nv_bfloat16 *og = (__nv_bfloat16 *)a.o + ((size_t)t0 * HV + hv) * V + dv;
-            const size_t ostride = (size_t)HV * V;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r1[32], r2[32];
-                tmem_ld32(tl + TM_O1 + 32 * h, r1);
-                tmem_ld32(tl + TM_O2 + 32 * h, r2);
+            if (it >= 1 && emit_of(it - 1)) {
+                // ---- O of chunk it - 1 (lane = dv)
+                const int c = cs + it - 1;
+                const int64_t t0 = bos + (int64_t)c * kChunk;
+                const int rows = rows_in(len, c);
+                ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t r[64];
+                tmem_ld32(tl + TM_O, r);
+                tmem_ld32(tl + TM_O + 32, r + 32);
                 tmem_ld_wait();
-                if (h == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[B_OE]);  // O regions drained
-                }
-                float ov[32];
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_OE]);  // O region drained
+                __nv_bfloat16 *og = (__nv_bfloat16 *)a.o + ((size_t)t0 * HV + hv) * V + et;
+                const size_t ostride = (size_t)HV * V;
+                {
+                    __nv_bfloat16 *p = og;  // (incremented pointer: keeps the unrolled stores compact)
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 e4 = *(const float4 *)(eg + 32 * h + 4 * j4);
-                    ov[4 * j4 + 0] = e4.x * u2f(r1[4 * j4 + 0]) + u2f(r2[4 * j4 + 0]);
-                    ov[4 * j4 + 1] = e4.y * u2f(r1[4 * j4 + 1]) + u2f(r2[4 * j4 + 1]);
-                    ov[4 * j4 + 2] = e4.z * u2f(r1[4 * j4 + 2]) + u2f(r2[4 * j4 + 2]);
-                    ov[4 * j4 + 3] = e4.w * u2f(r1[4 * j4 + 3]) + u2f(r2[4 * j4 + 3]);
+                    for (int j = 0; j < 64; ++j) {
+                        if (j < rows) *p = __float2bfloat16_rn(u2f(r[j]));
+                        p += ostride;
+                    }
                 }
-                if (rows == kChunk) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) og[(size_t)(32 * h + j) * ostride] = __float2bfloat16_rn(ov[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (32 * h + j < rows) og[(size_t)(32 * h + j) * ostride] = __float2bfloat16_rn(ov[j]);
-                }
+                ++e;
             }
-            ++e;
-            __syncwarp();
+            if (it + 1 < nch) ok = tiles(it + 1);
         }
     }
 

@@ -82,7 +82,7 @@ def test_plans(gdn):
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152)
     assert p.cp_mode == 2 and p.segments > 1 and p.kernels == 3
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, keys_unit_norm=True)
-    assert p.cp_mode == 3 and p.kernels == 2
+    assert p.cp_mode == 3 and p.kernels == 1  # the tensor-core scan finds its own warmup starts
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="off")
     assert p.cp_mode == 1 and p.segments == 1
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="exact", segment_chunks=64)
