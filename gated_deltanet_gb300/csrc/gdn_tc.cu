@@ -21,8 +21,8 @@
 //
 // Warp roles (16 warps): 0 TMA producer + gate statistics (and the warmup
 // start), 1 MMA issuer (event driven), 2-3 aux (Q~ in place, P), 4-7 chain
-// (state copy, V'), 8-11 prep (L, blockwise inverse), 12-15 output (U / W
-// operand tiles, W^T -> shared memory, O epilogue).
+// (state copy, V'), 8-11 prep (L, blockwise inverse, U / W operand tiles), 12-15
+// output (W^T -> shared memory, O epilogue).
 // Every wait is bounded in wall time; a wait that runs out records a timeout
 // in the status word and the roles leave their loops, so the kernel always
 // ends, waits for its copies and products in flight and frees its tensor memory.
@@ -68,7 +68,7 @@ constexpr int NB_PREP = 1;
 
 enum Bar {
     B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_TUF, B_TUF1, B_TUE, B_TUE1, B_TWF, B_WF,
-    B_WC, B_XR, B_XFREE, B_SBF, B_VPF, B_VTF, B_SF, B_PF, B_PF1, B_PE, B_PE1, B_OF, B_OE, B_FIN, B_COUNT
+    B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF, B_PF1, B_PE, B_PE1, B_OF, B_OE, B_FIN, B_COUNT
 };
 static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");
 
@@ -96,6 +96,14 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 }
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
+
+// true on one lane of a converged warp (the MMA issue of the warp)
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
 
 // d += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation (one warp; the merges of the
 // blockwise inverse, whose result is rounded to bf16 for the MMA operands afterwards).  The fp32
@@ -220,8 +228,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         mbar_init(&bars[B_TWF], 4);
         mbar_init(&bars[B_WF], 1);
         mbar_init(&bars[B_WC], 4);
-        mbar_init(&bars[B_XR], 4);
-        mbar_init(&bars[B_XFREE], 4);
         mbar_init(&bars[B_SBF], 4);
         mbar_init(&bars[B_VPF], 1);
         mbar_init(&bars[B_VTF], 4);
@@ -329,17 +335,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             mbar_wait(&bars[B_TMA + i % kStages], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
     } else if (warp == 1) {
         // ================================================================ MMA issuer (event driven)
-        if (lane == 0 && nch > 0) {
+        // The whole warp runs the loop with warp-uniform decisions and one elected lane issues:
+        // the operands of tcgen05.mma are then warp-uniform values and unrolled groups issue at
+        // the tensor core's rate (a divergent single-thread issuer is several times slower).
+        if (nch > 0) {
             const uint32_t idKQ = idesc_bf16_f32(128, 64, 0, 0);   // K-major A and B
             const uint32_t idMN = idesc_bf16_f32(128, 64, 1, 0);   // MN-major A (V^T, K^T), K-major B
             const uint32_t idV1 = idesc_bf16_f32(128, 64, 0, 1);   // A in TMEM, MN-major B (-W^T)
             const uint32_t idO = idesc_bf16_f32(128, 64, 0, 0);    // A in TMEM, K-major B (Q~, P)
             const uint32_t idS = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, MN-major B (K), N = dk
-            auto rdy = [&](int b, int ph) { return mbar_test_wait(&bars[b], (uint32_t)ph & 1u); };
+            // readiness as seen by lane 0, shared by the warp
+            auto rdy = [&](int b, int ph) {
+                return __shfl_sync(0xffffffffu, (int)mbar_test_wait(&bars[b], (uint32_t)ph & 1u), 0) != 0;
+            };
             auto stage = [&](int i) { return sbase + OFF_STAGE + (i % kStages) * kStageBytes; };
             int kq = 0, u = 0, w = 0, c = 0, e = 0, cst = 0;
             uint64_t t_last = globaltimer();
             uint32_t idle = 0;
+            bool ok = true;
             while (c < nch) {
                 bool prog = false;
                 const bool em = emit_of(c);
@@ -347,49 +360,62 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (cst == 0 && u > c && rdy(B_SBF, c) && rdy(B_WC, c)) {
                     // V'^T (holding U^T) -= S^T W^T
                     tc_fence_after();
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
-                               idV1, (ks > 0 || !zero_values) ? 1u : 0u);
-                    mma_commit(&bars[B_VPF]);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
+                                   idV1, (ks > 0 || !zero_values) ? 1u : 0u);
+                        mma_commit(&bars[B_VPF]);
+                    }
+                    __syncwarp();
                     cst = em ? 1 : 2;
                     prog = true;
                 }
                 if (cst == 1 && rdy(B_QS + c % kStages, c / kStages) && (e == 0 || rdy(B_OE, e - 1))) {
                     // O^T = S^T Q~^T
                     tc_fence_after();
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idO, ks > 0 ? 1u : 0u);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idO, ks > 0 ? 1u : 0u);
+                        }
                     }
+                    __syncwarp();
                     cst = 2;
                     prog = true;
                 }
                 if (cst == 2 && rdy(B_VTF, c)) {
                     // S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
                     tc_fence_after();
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
-                    mma_commit(&bars[B_SF]);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                        mma_commit(&bars[B_SF]);
+                    }
+                    __syncwarp();
                     cst = em ? 3 : 4;
                     prog = true;
                 }
                 if (cst == 3 && rdy(B_PF + (e & 1), e >> 1)) {
                     // O^T += V'^T P^T
                     tc_fence_after();
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + (e & 1) * 8192 + ks * 32), idO, 1u);
-                    mma_commit(&bars[B_OF]);
-                    mma_commit(&bars[B_PE + (e & 1)]);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + (e & 1) * 8192 + ks * 32), idO, 1u);
+                        mma_commit(&bars[B_OF]);
+                        mma_commit(&bars[B_PE + (e & 1)]);
+                    }
+                    __syncwarp();
                     ++e;
                     cst = 4;
                     prog = true;
                 }
                 if (cst == 4) {
-                    mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                    if (elect_one()) mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                    __syncwarp();
                     ++c;
                     cst = 0;
                 }
@@ -398,12 +424,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     // [K; Q] K^T: K K^T in lanes 0-63, Q K^T in lanes 64-127
                     tc_fence_after();
                     const uint32_t s2 = stage(kq);
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars[B_KQF]);
                     }
-                    mma_commit(&bars[B_KQF]);
+                    __syncwarp();
                     ++kq;
                     prog = true;
                 }
@@ -411,25 +440,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
                     tc_fence_after();
                     const uint32_t s2 = stage(w);
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024),
-                               kmaj(sbase + OFF_TW + ks * 32), idMN, ks > 0 ? 1u : 0u);
-                    mma_commit(&bars[B_WF]);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024),
+                                   kmaj(sbase + OFF_TW + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                        mma_commit(&bars[B_WF]);
+                    }
+                    __syncwarp();
                     ++w;
                     prog = true;
                 }
                 if (u < kq && rdy(B_TUF + (u & 1), u >> 1) && (u == 0 || rdy(B_VTF, u - 1))) {
                     // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
                     tc_fence_after();
-                    if (!zero_values) {
-                        const uint32_t s2 = stage(u);
-#pragma unroll 1
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024),
-                                   kmaj(sbase + OFF_TU + (u & 1) * 8192 + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                    const uint32_t s2 = stage(u);
+                    if (elect_one()) {
+                        if (!zero_values) {
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024),
+                                       kmaj(sbase + OFF_TU + (u & 1) * 8192 + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars[B_TUE + (u & 1)]);
                     }
-                    mma_commit(&bars[B_TUE + (u & 1)]);
+                    __syncwarp();
                     ++u;
                     prog = true;
                 }
@@ -438,14 +473,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     t_last = globaltimer();
                 } else {
                     __nanosleep(20);  // polling competes with the other warps for the shared-memory pipe
-                    if ((++idle & 255u) == 0 && globaltimer() - t_last > kWaitNs) {
-                        atomicOr(status, kStatusTimeout);
+                    if ((++idle & 255u) == 0 &&
+                        __shfl_sync(0xffffffffu, (int)(globaltimer() - t_last > kWaitNs), 0)) {
+                        ok = false;
                         break;
                     }
                 }
             }
+            if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
             // every product issued so far has finished before the CTA frees its tensor memory
-            mma_commit(&bars[B_FIN]);
+            if (elect_one()) mma_commit(&bars[B_FIN]);
+            __syncwarp();
             mbar_wait(&bars[B_FIN], 0, status, kStatusTimeout, kWaitNs);
         }
     } else if (warp == 2 || warp == 3) {
@@ -708,10 +746,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 }
                 if (check_norm && bdiag > 2.0001f) atomicOr(status, kStatusNormBound);
             }
-            // X of the previous chunk has been turned into the operand tiles
-            if (i >= 1) ok = mbar_wait(&bars[B_XFREE], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
-            ok = bar_and(NB_PREP, 128, ok);
-            if (!ok) break;
+            bar_sync(NB_PREP, 128);
 
             // ---- A: the eight 8 x 8 diagonal blocks by forward substitution; 2 threads per (block, column)
             {
@@ -837,9 +872,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     sLX[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
                 }
             }
-            // X is complete once all four warps have arrived
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_XR]);
+            // ---- operand tiles: T_U = A_g diag(beta), T_W = A_g diag(beta gam) = diag(gam) X diag(beta),
+            //      A_g = Gam * X; thread = (row r, 32 columns); buffers free once U of chunk i - 2 and
+            //      W of chunk i - 1 have finished
+            {
+                const int b = i & 1;
+                bool k2 = true;
+                if (i >= 2) k2 = mbar_wait(&bars[B_TUE + b], ((i - 2) >> 1) & 1, status, kStatusTimeout, kWaitNs);
+                if (k2 && i >= 1) k2 = mbar_wait(&bars[B_WF], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
+                ok = bar_and(NB_PREP, 128, k2);  // also: X is complete
+                if (!ok) break;
+                const int r = pt >> 1, h = pt & 1;
+                const float gr = gt[GT_GAM + r], Gr = gt[GT_G + r];
+                uint8_t *tu = sm + OFF_TU + b * 8192, *tw = sm + OFF_TW;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const int j0 = 32 * h + 8 * q;
+                    float vu[8], vw[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int jj = j0 + u;
+                        const float x = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                        const float bx = gt[GT_BETA + jj] * x;
+                        vw[u] = gr * bx;
+                        vu[u] = jj <= r ? ex2(Gr - gt[GT_G + jj]) * bx : 0.f;
+                    }
+                    *(uint4 *)(tu + sw128(r, j0)) = pack8(vu);
+                    *(uint4 *)(tw + sw128(r, j0)) = pack8(vw);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[B_TUF + b]);
+                    mbar_arrive(&bars[B_TWF]);
+                }
+            }
         }
     } else {
         // ================================================================ output warps
@@ -847,44 +914,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
         bool ok = true;
         int e = 0;
-        // operand tiles of chunk j: T_U = A_g diag(beta), T_W = A_g diag(beta gam) = diag(gam) X diag(beta)
-        auto tiles = [&](int j) -> bool {
-            const int b = j & 1;
-            bool k2 = mbar_wait(&bars[B_XR], j & 1, status, kStatusTimeout, kWaitNs);
-            if (k2 && j >= 2) k2 = mbar_wait(&bars[B_TUE + b], ((j - 2) >> 1) & 1, status, kStatusTimeout, kWaitNs);
-            if (k2 && j >= 1) k2 = mbar_wait(&bars[B_WF], (j - 1) & 1, status, kStatusTimeout, kWaitNs);
-            k2 = __all_sync(0xffffffffu, k2);  // warps work on their own rows: no group barrier
-            if (!k2) return false;
-            const float *gt = gates(j);
-            const int r = et >> 1, h = et & 1;
-            const float gr = gt[GT_GAM + r], Gr = gt[GT_G + r];
-            uint8_t *tu = sm + OFF_TU + b * 8192, *tw = sm + OFF_TW;
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                const int j0 = 32 * h + 8 * q;
-                float vu[8], vw[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int jj = j0 + u;
-                    const float x = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                    const float bx = gt[GT_BETA + jj] * x;
-                    vw[u] = gr * bx;
-                    vu[u] = jj <= r ? ex2(Gr - gt[GT_G + jj]) * bx : 0.f;
-                }
-                *(uint4 *)(tu + sw128(r, j0)) = pack8(vu);
-                *(uint4 *)(tw + sw128(r, j0)) = pack8(vw);
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_XFREE]);
-                mbar_arrive(&bars[B_TUF + b]);
-                mbar_arrive(&bars[B_TWF]);
-            }
-            return true;
-        };
-        for (int it = -1; it <= nch && ok; ++it) {
-            if (it >= 0 && it < nch) {
+        for (int it = 0; it <= nch && ok; ++it) {
+            if (it < nch) {
                 // ---- -W^T of chunk it (lane = dk) -> shared memory, MN-major operand of V' = U - W S
                 ok = mbar_wait(&bars[B_WF], it & 1, status, kStatusTimeout, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
@@ -938,7 +969,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 }
                 ++e;
             }
-            if (it + 1 < nch) ok = tiles(it + 1);
         }
     }
 
