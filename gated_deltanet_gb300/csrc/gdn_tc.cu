@@ -57,7 +57,8 @@ constexpr uint32_t OFF_BAR = OFF_SCR + 4096;
 constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_RGAM = 256, GT_SGAM = 320;
+constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_BR = 256, GT_SGAM = 320;
+constexpr float kFactorFloor = -100.f;  // chunks with G_C >= this form Gam_ij as gam_i * 2^-G_j
 
 // ---- tensor memory columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_VP = 128, TM_O = 192, TM_W = 256, TM_SBF = 320, TM_VB = 384, TM_VTB = 416,
@@ -70,7 +71,7 @@ enum Bar {
     B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_TUF, B_TUF1, B_TUE, B_TUE1, B_TWF, B_WF,
     B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF, B_PF1, B_PE, B_PE1, B_OF, B_OE, B_FIN, B_COUNT
 };
-static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");
+static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");  // + TMEM slot, cs, c0, c1
 
 struct TcMaps {
     CUtensorMap q, k, v;
@@ -186,20 +187,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         len = a.T;
     }
     const int NT = (int)((len + kChunk - 1) / kChunk);
-    const int c0 = seg * a.seg_chunks;
-    if (seg > 0 && c0 >= NT) return;
-    const int c1 = min(c0 + a.seg_chunks, NT);
+    if (seg > 0 && seg * a.seg_chunks >= NT) return;
     const bool fwd = a.mode == kModeForward;
     const size_t sidx = ((size_t)n * HV + hv) * a.n_seg + seg;
     const bool zero_values = !fwd && vt == 1;   // pre-pass: the M columns carry no values
     const bool check_norm = fwd && (a.warm_start != nullptr || a.warm_in_kernel != 0);
 
     if (warp == 0) {
-        int cs = c0;
-        if (fwd && seg > 0) {
-            if (a.warm_in_kernel) {
-                cs = warm_start_of(a.g, bos, len, HV, hv, c0, a.warm_log2_eps);
-            } else if (a.warm_start) {
+        int c0 = seg * a.seg_chunks, c1 = min(c0 + a.seg_chunks, NT), cs = c0;
+        if (fwd && a.warm_in_kernel) {
+            // Warmup split with balanced segments: the boundary at nominal chunk c moves to
+            // c + w / 2, w = c - (warmup start of c), capped at half a segment, so that the segment
+            // after it (which also scans its warmup) and the one before do about equal work.
+            const int L = a.seg_chunks;
+            auto bnd = [&](int j) -> int {
+                const int cj = j * L;
+                if (j == 0) return 0;
+                if (cj >= NT) return NT;
+                const int w = cj - warm_start_of(a.g, bos, len, HV, hv, cj, a.warm_log2_eps);
+                return min(cj + min(w, L) / 2, NT);
+            };
+            c0 = bnd(seg);
+            c1 = bnd(seg + 1);
+            if (seg > 0) cs = warm_start_of(a.g, bos, len, HV, hv, c0, a.warm_log2_eps);
+        } else if (fwd && seg > 0) {
+            if (a.warm_start) {
                 cs = a.warm_start[sidx];
                 if (cs < 0 || cs > c0) {
                     if (lane == 0) atomicOr(a.status, kStatusPlan);
@@ -208,7 +220,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             }
         }
         if (lane == 0) {
-            *s_cs = cs;
+            s_cs[0] = cs;
+            s_cs[1] = c0;
+            s_cs[2] = c1;
             if (seg == a.n_seg - 1 && c1 < NT) atomicOr(a.status, kStatusPlan);
         }
     }
@@ -246,7 +260,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *tslot;
-    const int cs = *s_cs;
+    const int cs = s_cs[0], c0 = s_cs[1], c1 = s_cs[2];
     const int nch = c1 - cs;
     unsigned *status = a.status;
     float *sLX = (float *)(sm + OFF_LX);
@@ -307,7 +321,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             *(float2 *)(gt + GT_BETA + r0) = make_float2(b0, b1);
             *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
             *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
-            *(float2 *)(gt + GT_RGAM + r0) = make_float2(ex2(-G0), ex2(-G1));
+            *(float2 *)(gt + GT_BR + r0) = make_float2(b0 * ex2(-G0), b1 * ex2(-G1));  // beta / gam
             *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
             ok = mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -884,18 +898,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (!ok) break;
                 const int r = pt >> 1, h = pt & 1;
                 const float gr = gt[GT_GAM + r], Gr = gt[GT_G + r];
+                const bool factored = gt[GT_G + 63] >= kFactorFloor;
                 uint8_t *tu = sm + OFF_TU + b * 8192, *tw = sm + OFF_TW;
 #pragma unroll 1
                 for (int q = 0; q < 4; ++q) {
                     const int j0 = 32 * h + 8 * q;
-                    float vu[8], vw[8];
+                    const float4 b0 = *(const float4 *)(gt + GT_BETA + j0), b1 = *(const float4 *)(gt + GT_BETA + j0 + 4);
+                    const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    float xv[8], vu[8], vw[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int jj = j0 + u;
-                        const float x = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                        const float bx = gt[GT_BETA + jj] * x;
-                        vw[u] = gr * bx;
-                        vu[u] = jj <= r ? ex2(Gr - gt[GT_G + jj]) * bx : 0.f;
+                        xv[u] = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                        vw[u] = gr * bj[u] * xv[u];
+                    }
+                    if (factored) {
+                        // Gam_rj beta_j = gam_r (beta_j / gam_j); x = 0 above the diagonal
+                        const float4 c0 = *(const float4 *)(gt + GT_BR + j0), c1 = *(const float4 *)(gt + GT_BR + j0 + 4);
+                        const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) vu[u] = gr * cj[u] * xv[u];
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) vu[u] = j0 + u <= r ? ex2(Gr - gt[GT_G + j0 + u]) * bj[u] * xv[u] : 0.f;
                     }
                     *(uint4 *)(tu + sw128(r, j0)) = pack8(vu);
                     *(uint4 *)(tw + sw128(r, j0)) = pack8(vw);
