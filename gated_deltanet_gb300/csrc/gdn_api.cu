@@ -23,7 +23,7 @@ struct Plan {
     int seg_chunks, n_seg, value_tiles, kernels, max_nt;
     float log2_eps;
     // workspace layout
-    size_t off_warm, off_segout, off_seginit, bytes;
+    size_t off_warm, off_segout, off_seginit, off_tiles, tile_slots, bytes;
 };
 
 bool is_varlen(const gdn_shape *s, const int64_t *cu) { return cu != nullptr; }
@@ -106,7 +106,13 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     if (p->n_seg == 1 && cp != GDN_CP_OFF) { p->cp = GDN_CP_OFF; cp = GDN_CP_OFF; p->seg_chunks = std::max(max_nt, 1); }
 
     size_t off = kStatusBytes;
-    p->off_warm = p->off_segout = p->off_seginit = 0;
+    p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->tile_slots = 0;
+    if (p->engine == GDN_ENGINE_TC) {
+        // operand tiles of every chunk, written by the preparation kernel
+        p->tile_slots = (size_t)tile_slots((int64_t)s->B * s->T, N);
+        p->off_tiles = off;
+        off = align_up(off + p->tile_slots * s->HV * kTcTileBytesPerChunk, 256);
+    }
     const size_t nsegs = (size_t)N * s->HV * p->n_seg;
     if (cp == GDN_CP_WARMUP && p->engine == GDN_ENGINE_TC) {
         p->kernels = 1;  // each CTA of the scan finds its own warmup start
@@ -124,6 +130,7 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     } else {
         p->kernels = 1;
     }
+    if (p->engine == GDN_ENGINE_TC) p->kernels += 1;  // the chunk preparation
     p->bytes = off;
     return GDN_OK;
 }
@@ -183,6 +190,18 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
 
     cudaError_t e = cudaSuccess;
     const bool tc = p.engine == GDN_ENGINE_TC;
+    if (tc) {
+        PrepArgs pa{};
+        pa.k = k; pa.g = g; pa.beta = beta; pa.cu_seqlens = cu;
+        pa.tiles = wsb + p.off_tiles;
+        pa.T = s->T; pa.H = s->H; pa.HV = s->HV; pa.N = N; pa.slots = (int)p.tile_slots;
+        pa.check_norm = p.cp == GDN_CP_WARMUP;
+        pa.status = status;
+        e = launch_tc_prep(pa, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        a.tiles = pa.tiles;
+        a.tile_slots = pa.slots;
+    }
     auto scan = [&](const ScanArgs &sa) -> cudaError_t {
         if (tc) return launch_tc_scan(sa, sa.mode == kModePrepass ? 2 : 1, stream);
         return launch_simt_scan(sa, s->qkv_dtype, s->gate_kind, stream);

@@ -37,6 +37,8 @@ struct ScanArgs {
     const int *warm_start;  // [N*HV*n_seg] first chunk a segment processes (warmup), nullable
     int warm_in_kernel;     // tensor-core engine: each CTA finds its own warmup start from g
     float warm_log2_eps;    // threshold of that search (accumulated log2-decay)
+    const void *tiles;      // tensor-core engine: operand tiles of tc_prep_kernel (see tile_slot)
+    int tile_slots;         //   chunk slots of that buffer
     const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
     float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
     int mode;               // Mode
@@ -63,6 +65,17 @@ struct GateStatsArgs {
     int max_warm_chunks;   // walk at most this far back, else start from the sequence start
 };
 
+// Arguments of the tensor-core engine's chunk preparation (operand tiles of every chunk).
+struct PrepArgs {
+    const void *k;
+    const float *g, *beta;
+    const int64_t *cu_seqlens;  // nullable
+    void *tiles;                // bf16 [slot][HV][2][64][64]: T_U, T_W (slot: tile_slot)
+    int T, H, HV, N, slots;
+    int check_norm;             // flag beta ||k||^2 > 2 in the status word (warmup split)
+    unsigned *status;
+};
+
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_simt_scan(const ScanArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
 cudaError_t launch_cp_combine(const CombineArgs &a, cudaStream_t st);
@@ -74,6 +87,14 @@ size_t simt_smem_bytes(int K, gdn_gate_kind gate);
 bool tc_shape_ok(const gdn_shape *s);
 bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o);
 cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st);
+cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st);
+constexpr size_t kTcTileBytesPerChunk = 2 * 64 * 64 * 2;  // T_U and T_W, bf16
+
+// Chunk c of a sequence starting at token bos (sequence index n) has the operand-tile
+// slot floor(bos / 64) + n + c: consecutive sequences never overlap and a batch of
+// `tokens` tokens in `nseq` sequences needs at most tokens / 64 + nseq + 1 slots.
+__host__ __device__ inline int64_t tile_slot(int64_t bos, int n, int c) { return bos / kChunk + n + c; }
+__host__ __device__ inline int64_t tile_slots(int64_t tokens, int nseq) { return tokens / kChunk + nseq + 1; }
 size_t tc_smem_bytes();
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

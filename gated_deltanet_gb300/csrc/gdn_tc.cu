@@ -1,28 +1,26 @@
 // Tensor-core engine (sm_103a: tcgen05 + TMEM + TMA) of the chunked gated
-// delta rule for bf16 q/k/v, dk = dv = 128, scalar gate, C = 64.
+// delta rule for bf16 q/k/v, dk = dv = 128, scalar gate, C = 64: the serial scan.
 //
 // One CTA owns one (sequence, value head, segment) and walks its chunks
 // serially.  The state is kept transposed, S^T [dv x dk] fp32, in tensor
 // memory (lane = dv), so every product is an M = 128 tcgen05 MMA.  Per chunk
 // (G = chunk-local inclusive cumsum of the log-gate in base 2, gam = 2^G,
-// Gam_ij = 2^(G_i - G_j), gC = gam of the last row):
+// Gam_ij = 2^(G_i - G_j), gC = gam of the last row), with the operand tiles
+// T_U = A_g diag(beta) and T_W = A_g diag(beta gam) of tc_prep_kernel
+// (A_g = Gam * (I + StrictLower(diag(beta) K K^T))^-1, FlashQLA blog, step 1):
 //
-//   X    = (I + StrictLower(diag(beta) K K^T))^-1       gate-free inverse (FlashQLA
-//                                                       blog, "A balanced solution")
-//   A_g  = Gam * X                                       gated inverse (same page)
-//   U    = A_g diag(beta) V,  W = A_g diag(beta gam) K   WY form (FLA page, sec. 4)
+//   U    = T_U V,  W = T_W K                             WY form (FLA page, sec. 4)
 //   V'   = U - W S                                       the only state-dependent product
 //   O    = Q~ S + P V',  Q~ = diag(scale gam) Q,  P = scale Lower(Gam) * (Q K^T)
 //   S   <- gC S + K^T diag(gC / gam) V'
 //
-// Everything but V' = U - W S and the state update is independent of the
-// state, so the serial chain per chunk is: S -> bf16 copy, one MMA group
+// The serial chain per chunk is: S -> bf16 copy, one MMA group
 // (V'^T = U^T - S^T W^T), V' -> bf16, one MMA group (the state update).
 //
-// Warp roles (16 warps): 0 TMA producer + gate statistics (and the warmup
-// start), 1 MMA issuer (event driven), 2-3 aux (Q~ in place, P), 4-7 chain
-// (state copy, V'), 8-11 prep (L, blockwise inverse, U / W operand tiles), 12-15
-// output (W^T -> shared memory, O epilogue).
+// Warp roles (12 warps): 0 TMA producer (q, k, v boxes and the two tiles) + gate
+// statistics (and the warmup start), 1 MMA issuer (event driven), 2-3 aux (Q~ in
+// place, P), 4-7 chain (state copy, V'), 8-11 output (W^T -> shared memory, O
+// epilogue).
 // Every wait is bounded in wall time; a wait that runs out records a timeout
 // in the status word and the roles leave their loops, so the kernel always
 // ends, waits for its copies and products in flight and frees its tensor memory.
@@ -36,59 +34,44 @@ namespace gdn {
 namespace {
 using namespace ptx;
 
-constexpr int kThreadsTC = 512;
+constexpr int kThreadsTC = 384;
 constexpr int kStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kStageBytes = 49152;  // K0 | Q0 | K1 | Q1 | V0 | V1, 8 KB each (64 rows x 64 bf16)
-constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, sV1 = 40960;
+// stage: K0 | Q0 | K1 | Q1 | V0 | V1 | T_U | T_W, 8 KB each (64 rows x 64 bf16, 128-byte swizzle)
+constexpr uint32_t kStageBytes = 65536;
+constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, sV1 = 40960, sTU = 49152,
+                   sTW = 57344;
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_TU = OFF_STAGE + kStages * kStageBytes;  // A_g diag(beta) [64 x 64] bf16, x2
-constexpr uint32_t OFF_TW = OFF_TU + 2 * 8192;                  // A_g diag(beta gam) [64 x 64] bf16
-constexpr uint32_t OFF_P = OFF_TW + 8192;                       // P [64 x 64] bf16, x2
-constexpr uint32_t OFF_WS = OFF_P + 2 * 8192;                      // -W^T [128 (dk) x 64] bf16, MN-major
-constexpr int kLdX = 68;                                        // row pitch (floats) of the L / X tile
-constexpr uint32_t OFF_LX = OFF_WS + 16384;                     // L (lower) and X^T (upper), fp32 [64][68]
-constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each
-constexpr uint32_t OFF_GATE = OFF_LX + 64 * kLdX * 4;
-constexpr uint32_t OFF_SCR = OFF_GATE + kStages * kGateBytes;  // merge scratch, 4 warps x 32 x 8 fp32
-constexpr uint32_t OFF_BAR = OFF_SCR + 4096;
+constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16
+constexpr uint32_t OFF_WS = OFF_P + 8192;                       // -W^T [128 (dk) x 64] bf16, MN-major
+constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), (unused), scale*gam  [64] f32 each
+constexpr uint32_t OFF_GATE = OFF_WS + 16384;
+constexpr uint32_t OFF_BAR = OFF_GATE + kStages * kGateBytes;
 constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_BR = 256, GT_SGAM = 320;
-constexpr float kFactorFloor = -100.f;  // chunks with G_C >= this form Gam_ij as gam_i * 2^-G_j
+constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_SGAM = 320;
 
 // ---- tensor memory columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_VP = 128, TM_O = 192, TM_W = 256, TM_SBF = 320, TM_VB = 384, TM_VTB = 416,
                    TM_KQ = 448;
 
 // ---- named barriers (0 is __syncthreads)
-constexpr int NB_PREP = 1;
 
 enum Bar {
-    B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_TUF, B_TUF1, B_TUE, B_TUE1, B_TWF, B_WF,
-    B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF, B_PF1, B_PE, B_PE1, B_OF, B_OE, B_FIN, B_COUNT
+    B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_WF, B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF,
+    B_OF, B_OE, B_FIN, B_COUNT
 };
 static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");  // + TMEM slot, cs, c0, c1
 
 struct TcMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, tiles;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
-
-__device__ __forceinline__ bool bar_and(int id, int count, bool pred)
-{
-    uint32_t r;
-    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-                 : "=r"(r)
-                 : "r"((uint32_t)pred), "r"(id), "r"(count)
-                 : "memory");
-    return r != 0;
-}
 
 __device__ __forceinline__ int rows_in(int64_t len, int c)
 {
@@ -106,26 +89,6 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
-// d += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation (one warp; the merges of the
-// blockwise inverse, whose result is rounded to bf16 for the MMA operands afterwards).  The fp32
-// operands go in as they are: the tensor core reads their top 19 bits (tf32 by truncation).
-__device__ __forceinline__ void mma_tf32(float *d, float a0, float a1, float a2, float a3, float b0, float b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(f2u(a0)), "r"(f2u(a1)), "r"(f2u(a2)), "r"(f2u(a3)), "r"(f2u(b0)), "r"(f2u(b1)));
-}
-
-__device__ __forceinline__ uint4 pack8(const float *v)
-{
-    uint4 pk;
-    pk.x = pack_bf16(v[0], v[1]);
-    pk.y = pack_bf16(v[2], v[3]);
-    pk.z = pack_bf16(v[4], v[5]);
-    pk.w = pack_bf16(v[6], v[7]);
-    return pk;
-}
 
 // Warmup start of a segment beginning at chunk c0: walk back over whole chunks,
 // adding their log2-decays, until the window has decayed to log2_eps or below;
@@ -191,7 +154,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const bool fwd = a.mode == kModeForward;
     const size_t sidx = ((size_t)n * HV + hv) * a.n_seg + seg;
     const bool zero_values = !fwd && vt == 1;   // pre-pass: the M columns carry no values
-    const bool check_norm = fwd && (a.warm_start != nullptr || a.warm_in_kernel != 0);
 
     if (warp == 0) {
         int c0 = seg * a.seg_chunks, c1 = min(c0 + a.seg_chunks, NT), cs = c0;
@@ -234,12 +196,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             mbar_init(&bars[B_QS + j], 2);
         }
         mbar_init(&bars[B_KQF], 1);
-        mbar_init(&bars[B_KQE], 4);
-        mbar_init(&bars[B_TUF], 4);
-        mbar_init(&bars[B_TUF1], 4);
-        mbar_init(&bars[B_TUE], 1);
-        mbar_init(&bars[B_TUE1], 1);
-        mbar_init(&bars[B_TWF], 4);
+        mbar_init(&bars[B_KQE], 2);
         mbar_init(&bars[B_WF], 1);
         mbar_init(&bars[B_WC], 4);
         mbar_init(&bars[B_SBF], 4);
@@ -247,9 +204,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         mbar_init(&bars[B_VTF], 4);
         mbar_init(&bars[B_SF], 1);
         mbar_init(&bars[B_PF], 2);
-        mbar_init(&bars[B_PF1], 2);
-        mbar_init(&bars[B_PE], 1);
-        mbar_init(&bars[B_PE1], 1);
         mbar_init(&bars[B_OF], 1);
         mbar_init(&bars[B_OE], 4);
         mbar_init(&bars[B_FIN], 1);
@@ -263,7 +217,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const int cs = s_cs[0], c0 = s_cs[1], c1 = s_cs[2];
     const int nch = c1 - cs;
     unsigned *status = a.status;
-    float *sLX = (float *)(sm + OFF_LX);
     auto gates = [&](int i) { return (float *)(sm + OFF_GATE + (i % kStages) * kGateBytes); };
     auto emit_of = [&](int i) { return fwd && cs + i >= c0; };
 
@@ -281,7 +234,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             const bool emit = emit_of(i);
             uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
             if (lane == 0) {
-                const uint32_t bytes = 16384u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
+                const uint32_t bytes = 32768u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
                 mbar_arrive_expect_tx(&bars[B_TMA + s], bytes);
                 const int tt = (int)t0;
                 tma_load_3d(st + sK0, &m.k, 0, hq, tt, &bars[B_TMA + s]);
@@ -294,6 +247,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     tma_load_3d(st + sV0, &m.v, 0, hv, tt, &bars[B_TMA + s]);
                     tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
                 }
+                // operand tiles of the chunk: rows (slot * HV + hv) * 128 + {0, 64}
+                const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 128);
+                tma_load_2d(st + sTU, &m.tiles, 0, trow, &bars[B_TMA + s]);
+                tma_load_2d(st + sTW, &m.tiles, 0, trow + 64, &bars[B_TMA + s]);
             }
             ++issued;
             // gate statistics while the tiles land: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
@@ -321,7 +278,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             *(float2 *)(gt + GT_BETA + r0) = make_float2(b0, b1);
             *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
             *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
-            *(float2 *)(gt + GT_BR + r0) = make_float2(b0 * ex2(-G0), b1 * ex2(-G1));  // beta / gam
             *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
             ok = mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -412,15 +368,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     cst = em ? 3 : 4;
                     prog = true;
                 }
-                if (cst == 3 && rdy(B_PF + (e & 1), e >> 1)) {
+                if (cst == 3 && rdy(B_PF, e)) {
                     // O^T += V'^T P^T
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + (e & 1) * 8192 + ks * 32), idO, 1u);
+                            mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + ks * 32), idO, 1u);
                         mma_commit(&bars[B_OF]);
-                        mma_commit(&bars[B_PE + (e & 1)]);
                     }
                     __syncwarp();
                     ++e;
@@ -450,7 +405,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     ++kq;
                     prog = true;
                 }
-                if (w < kq && rdy(B_TWF, w) && (w == 0 || rdy(B_WC, w - 1))) {
+                if (w < kq && (w == 0 || rdy(B_WC, w - 1))) {   // the tiles came with the stage (KQ waited for it)
                     // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
                     tc_fence_after();
                     const uint32_t s2 = stage(w);
@@ -458,14 +413,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
                             mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024),
-                                   kmaj(sbase + OFF_TW + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                                   kmaj(s2 + sTW + ks * 32), idMN, ks > 0 ? 1u : 0u);
                         mma_commit(&bars[B_WF]);
                     }
                     __syncwarp();
                     ++w;
                     prog = true;
                 }
-                if (u < kq && rdy(B_TUF + (u & 1), u >> 1) && (u == 0 || rdy(B_VTF, u - 1))) {
+                if (u < kq && (u == 0 || rdy(B_VTF, u - 1))) {
                     // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
                     tc_fence_after();
                     const uint32_t s2 = stage(u);
@@ -474,9 +429,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
                                 mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024),
-                                       kmaj(sbase + OFF_TU + (u & 1) * 8192 + ks * 32), idMN, ks > 0 ? 1u : 0u);
+                                       kmaj(s2 + sTU + ks * 32), idMN, ks > 0 ? 1u : 0u);
                         }
-                        mma_commit(&bars[B_TUE + (u & 1)]);
                     }
                     __syncwarp();
                     ++u;
@@ -515,30 +469,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (!ok) break;
             tc_fence_after();
             const float *gt = gates(i);
-            // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j] -> bf16 into buffer e & 1, once O2 of
-            // the chunk that used it before has finished
+            // Q K^T row r into registers: the K K^T / Q K^T region is released at once
+            uint32_t kq[64];
             if (emit) {
-                if (e >= 2) ok = mbar_wait(&bars[B_PE + (e & 1)], ((e >> 1) - 1) & 1, status, kStatusTimeout, kWaitNs);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const float Gr = gt[GT_G + r], sc = a.scale;
-                uint8_t *prow = sm + OFF_P + (e & 1) * 8192;
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t kq[32];
-                    tmem_ld32(tl + TM_KQ + 32 * hf, kq);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float v[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int j = 32 * hf + 8 * q + u;
-                            v[u] = (j <= r) ? sc * ex2(Gr - gt[GT_G + j]) * u2f(kq[8 * q + u]) : 0.f;
-                        }
-                        *(uint4 *)(prow + sw128(r, 32 * hf + 8 * q)) = pack8(v);
-                    }
-                }
+                tmem_ld32(tl + TM_KQ, kq);
+                tmem_ld32(tl + TM_KQ + 32, kq + 32);
+                tmem_ld_wait();
             }
             tc_fence_before();
             __syncwarp();
@@ -569,8 +505,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_QS + s]);
             if (!emit) continue;
+            if (e > 0) ok = mbar_wait(&bars[B_OF], (e - 1) & 1, status, kStatusTimeout, kWaitNs);  // P free
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            {
+                // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j] -> bf16, 128-byte swizzled
+                const float Gr = gt[GT_G + r], sc = a.scale;
+                uint8_t *prow = sm + OFF_P;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = 8 * q + u;
+                        v[u] = (j <= r) ? sc * ex2(Gr - gt[GT_G + j]) * u2f(kq[j]) : 0.f;
+                    }
+                    *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
+                }
+            }
+            fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_PF + (e & 1)]);
+            if (lane == 0) mbar_arrive(&bars[B_PF]);
             ++e;
         }
     } else if (warp >= 4 && warp < 8) {
@@ -710,232 +665,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 }
             }
         }
-    } else if (warp >= 8 && warp < 12) {
-        // ================================================================ prep: L and the blockwise inverse
-        // sLX holds L = diag(beta) StrictLower(K K^T) in its lower triangle and X = (I + L)^-1
-        // transposed in its upper triangle: X(r, j), j < r, at sLX[j * kLdX + r]; X(r, r) = 1.
-        // Blocks are merged exactly: [[A, 0], [C, D]]^-1 = [[A^-1, 0], [-D^-1 C A^-1, D^-1]].
-        const int pt = tid - 256, pw = warp - 8;
-        const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
-        float *scr = (float *)(sm + OFF_SCR);
-        auto Lx = [&](int r, int j) -> float { return sLX[r * kLdX + j]; };
-        auto Xt = [&](int r, int j) -> float { return sLX[j * kLdX + r]; };  // X(r, j), j < r
-        auto Xm = [&](int r, int j) -> float { return r > j ? sLX[j * kLdX + r] : (r == j ? 1.f : 0.f); };  // X(r, j)
-        bool ok = true;
-        for (int i = 0; i < nch && ok; ++i) {
-            const int s = i % kStages;
-            ok = mbar_wait(&bars[B_FULL + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
-            if (ok) ok = mbar_wait(&bars[B_KQF], i & 1, status, kStatusTimeout, kWaitNs);
-            ok = bar_and(NB_PREP, 128, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const float *gt = gates(i);
-            if (pt < 64) {
-                // L row r = beta_r * (K K^T)[r, j < r]   (lower triangle only: X of the previous chunk
-                // in the upper triangle may still be read by the output warps)
-                const int r = pt;
-                const float br = gt[GT_BETA + r];
-                uint32_t kq[64];
-                tmem_ld32(tl + TM_KQ, kq);
-                tmem_ld32(tl + TM_KQ + 32, kq + 32);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_KQE]);
-                float bdiag = 0.f;  // beta_r ||k_r||^2 (<= 2 keeps every transition non-expansive)
-#pragma unroll
-                for (int j4 = 0; j4 < 16; ++j4) {
-                    const int j = 4 * j4;
-                    const float4 w4 = make_float4(br * u2f(kq[j]), br * u2f(kq[j + 1]), br * u2f(kq[j + 2]),
-                                                  br * u2f(kq[j + 3]));
-                    if (j + 3 < r) {
-                        *(float4 *)(sLX + r * kLdX + j) = w4;
-                    } else if (j <= r) {
-                        // the quad holding the diagonal: strictly lower part stored, diagonal kept
-                        if (j < r) sLX[r * kLdX + j] = w4.x;
-                        if (j + 1 < r) sLX[r * kLdX + j + 1] = w4.y;
-                        if (j + 2 < r) sLX[r * kLdX + j + 2] = w4.z;
-                        bdiag = (r & 1) ? ((r & 2) ? w4.w : w4.y) : ((r & 2) ? w4.z : w4.x);
-                    }
-                }
-                if (check_norm && bdiag > 2.0001f) atomicOr(status, kStatusNormBound);
-            }
-            bar_sync(NB_PREP, 128);
-
-            // ---- A: the eight 8 x 8 diagonal blocks by forward substitution; 2 threads per (block, column)
-            {
-                const int task = pt >> 1, hh = pt & 1;
-                const int base = 8 * (task >> 3), cc = task & 7;
-                float x[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int r = 1; r < 8; ++r) {
-                    float part = 0.f;
-#pragma unroll
-                    for (int j = 0; j < r; ++j)
-                        if ((j & 1) == hh) part = fmaf(Lx(base + r, base + j), x[j], part);
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    if (r > cc) x[r] = -part;
-                }
-                if (hh == 0) {
-#pragma unroll
-                    for (int r = 1; r < 8; ++r)
-                        if (r > cc) sLX[(base + cc) * kLdX + base + r] = x[r];
-                }
-            }
-            bar_sync(NB_PREP, 128);
-            // ---- B: 8 -> 16, one warp per merge:  X(B, A) = -X(B, B) (L(B, A) X(A, A))
-            {
-                const int A = 16 * pw, Bb = A + 8;
-                const int r = lane >> 2, cp = (lane & 3) * 2;
-                float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float l = Lx(Bb + r, A + k);
-                    const float x0 = k > cp ? Xt(A + k, A + cp) : (k == cp ? 1.f : 0.f);
-                    const float x1 = k > cp + 1 ? Xt(A + k, A + cp + 1) : (k == cp + 1 ? 1.f : 0.f);
-                    t0 = fmaf(l, x0, t0);
-                    t1 = fmaf(l, x1, t1);
-                }
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float tk0 = __shfl_sync(0xffffffffu, t0, 4 * k + (lane & 3));
-                    const float tk1 = __shfl_sync(0xffffffffu, t1, 4 * k + (lane & 3));
-                    const float xb = k < r ? Xt(Bb + r, Bb + k) : (k == r ? 1.f : 0.f);
-                    a0 = fmaf(xb, tk0, a0);
-                    a1 = fmaf(xb, tk1, a1);
-                }
-                sLX[(A + cp) * kLdX + Bb + r] = -a0;
-                sLX[(A + cp + 1) * kLdX + Bb + r] = -a1;
-            }
-            bar_sync(NB_PREP, 128);
-            // ---- C: 16 -> 32 on the tensor cores (tf32 m16n8k8); warp = (merge, 8-column tile):
-            //      T = L(B, A) X(A, A)[:, tile], then X(B, A)[:, tile] = -X(B, B) T
-            {
-                const int g = lane >> 2, t = lane & 3;
-                const int A = 32 * (pw >> 1), Bb = A + 16, n0 = 8 * (pw & 1);
-                float *T = scr + pw * 128;  // T[m][n], 16 x 8, private to the warp
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int k0 = 8 * ks;
-                    mma_tf32(d, Lx(Bb + g, A + k0 + t), Lx(Bb + g + 8, A + k0 + t), Lx(Bb + g, A + k0 + t + 4),
-                             Lx(Bb + g + 8, A + k0 + t + 4), Xm(A + k0 + t, A + n0 + g), Xm(A + k0 + t + 4, A + n0 + g));
-                }
-                *(float2 *)(T + g * 8 + 2 * t) = make_float2(d[0], d[1]);
-                *(float2 *)(T + (g + 8) * 8 + 2 * t) = make_float2(d[2], d[3]);
-                __syncwarp();
-                float u[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int k0 = 8 * ks;
-                    mma_tf32(u, Xm(Bb + g, Bb + k0 + t), Xm(Bb + g + 8, Bb + k0 + t), Xm(Bb + g, Bb + k0 + t + 4),
-                             Xm(Bb + g + 8, Bb + k0 + t + 4), T[(k0 + t) * 8 + g], T[(k0 + t + 4) * 8 + g]);
-                }
-                sLX[(A + n0 + 2 * t) * kLdX + Bb + g] = -u[0];
-                sLX[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = -u[1];
-                sLX[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = -u[2];
-                sLX[(A + n0 + 2 * t + 1) * kLdX + Bb + g + 8] = -u[3];
-            }
-            bar_sync(NB_PREP, 128);
-            // ---- D: 32 -> 64 on the tensor cores; warp = 8-column tile of the lower-left 32 x 32 block:
-            //      T = L(32:64, 0:32) X(0:32, tile), then X(32:64, tile) = -X(32:64, 32:64) T
-            {
-                const int g = lane >> 2, t = lane & 3, n0 = 8 * pw;
-                float *T = scr + pw * 256;  // T[m][n], 32 x 8, private to the warp
-                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    if (ks < pw) continue;  // X(k, n) = 0 for k < n
-                    const int k0 = 8 * ks;
-                    const float b0 = Xm(k0 + t, n0 + g), b1 = Xm(k0 + t + 4, n0 + g);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        const int m0 = 32 + 16 * mt;
-                        mma_tf32(d[mt], Lx(m0 + g, k0 + t), Lx(m0 + g + 8, k0 + t), Lx(m0 + g, k0 + t + 4),
-                                 Lx(m0 + g + 8, k0 + t + 4), b0, b1);
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    *(float2 *)(T + (16 * mt + g) * 8 + 2 * t) = make_float2(d[mt][0], d[mt][1]);
-                    *(float2 *)(T + (16 * mt + g + 8) * 8 + 2 * t) = make_float2(d[mt][2], d[mt][3]);
-                }
-                __syncwarp();
-                float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const int k0 = 8 * ks;
-                    const float b0 = T[(k0 + t) * 8 + g], b1 = T[(k0 + t + 4) * 8 + g];
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        if (k0 > 16 * mt + 15) continue;  // X(32 + m, 32 + k) = 0 for k > m
-                        const int m0 = 32 + 16 * mt;
-                        mma_tf32(u[mt], Xm(m0 + g, 32 + k0 + t), Xm(m0 + g + 8, 32 + k0 + t), Xm(m0 + g, 32 + k0 + t + 4),
-                                 Xm(m0 + g + 8, 32 + k0 + t + 4), b0, b1);
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int m0 = 32 + 16 * mt;
-                    sLX[(n0 + 2 * t) * kLdX + m0 + g] = -u[mt][0];
-                    sLX[(n0 + 2 * t + 1) * kLdX + m0 + g] = -u[mt][1];
-                    sLX[(n0 + 2 * t) * kLdX + m0 + g + 8] = -u[mt][2];
-                    sLX[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
-                }
-            }
-            // ---- operand tiles: T_U = A_g diag(beta), T_W = A_g diag(beta gam) = diag(gam) X diag(beta),
-            //      A_g = Gam * X; thread = (row r, 32 columns); buffers free once U of chunk i - 2 and
-            //      W of chunk i - 1 have finished
-            {
-                const int b = i & 1;
-                bool k2 = true;
-                if (i >= 2) k2 = mbar_wait(&bars[B_TUE + b], ((i - 2) >> 1) & 1, status, kStatusTimeout, kWaitNs);
-                if (k2 && i >= 1) k2 = mbar_wait(&bars[B_WF], (i - 1) & 1, status, kStatusTimeout, kWaitNs);
-                ok = bar_and(NB_PREP, 128, k2);  // also: X is complete
-                if (!ok) break;
-                const int r = pt >> 1, h = pt & 1;
-                const float gr = gt[GT_GAM + r], Gr = gt[GT_G + r];
-                const bool factored = gt[GT_G + 63] >= kFactorFloor;
-                uint8_t *tu = sm + OFF_TU + b * 8192, *tw = sm + OFF_TW;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    const int j0 = 32 * h + 8 * q;
-                    const float4 b0 = *(const float4 *)(gt + GT_BETA + j0), b1 = *(const float4 *)(gt + GT_BETA + j0 + 4);
-                    const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                    float xv[8], vu[8], vw[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int jj = j0 + u;
-                        xv[u] = jj < r ? sLX[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                        vw[u] = gr * bj[u] * xv[u];
-                    }
-                    if (factored) {
-                        // Gam_rj beta_j = gam_r (beta_j / gam_j); x = 0 above the diagonal
-                        const float4 c0 = *(const float4 *)(gt + GT_BR + j0), c1 = *(const float4 *)(gt + GT_BR + j0 + 4);
-                        const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) vu[u] = gr * cj[u] * xv[u];
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) vu[u] = j0 + u <= r ? ex2(Gr - gt[GT_G + j0 + u]) * bj[u] * xv[u] : 0.f;
-                    }
-                    *(uint4 *)(tu + sw128(r, j0)) = pack8(vu);
-                    *(uint4 *)(tw + sw128(r, j0)) = pack8(vw);
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[B_TUF + b]);
-                    mbar_arrive(&bars[B_TWF]);
-                }
-            }
-        }
     } else {
         // ================================================================ output warps
-        const int et = tid - 384;
+        const int et = tid - 256;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
         bool ok = true;
         int e = 0;
@@ -1037,6 +769,21 @@ bool make_map(CUtensorMap *map, const void *base, int heads, int64_t rows)
     return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the operand tiles, bf16 [rows][64], box = 64 x 64, 128-byte swizzle.
+bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows)
+{
+    auto enc = get_encoder();
+    if (!enc || !base) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {64 * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t tc_smem_bytes() { return kSmemTC; }
@@ -1063,7 +810,8 @@ cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st)
     const int64_t rows = (int64_t)a.B * a.T;
     if (rows > 0) {
         if (!make_map(&maps.q, a.q, a.H, rows) || !make_map(&maps.k, a.k, a.H, rows) ||
-            !make_map(&maps.v, a.v, a.HV, rows))
+            !make_map(&maps.v, a.v, a.HV, rows) ||
+            !make_tiles_map(&maps.tiles, a.tiles, (int64_t)a.tile_slots * a.HV * 128))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTC);

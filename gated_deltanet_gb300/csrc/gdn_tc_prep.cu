@@ -1,0 +1,315 @@
+// Chunk preparation for the tensor-core engine: for every chunk of every
+// (sequence, value head), the two bf16 operand tiles of the WY form
+//
+//   L    = diag(beta) StrictLower(K K^T)                    (FlashQLA blog, step 1)
+//   X    = (I + L)^-1                                      (FLA page, sec. 4: exact blocked inverse)
+//   A_g  = Gam * X,   Gam_ij = 2^(G_i - G_j)               (gated inverse, FlashQLA blog)
+//   T_U  = A_g diag(beta),   T_W = A_g diag(beta gam) = diag(gam) X diag(beta)
+//
+// (G = chunk-local inclusive cumsum of the log-gate in base 2, gam = 2^G).  None of
+// this depends on the state, so all chunks are prepared at once, one CTA per chunk,
+// several CTAs per SM; the scan kernel loads the tiles with TMA (U = T_U V and
+// W = T_W K are then single tensor-core products on its side).
+//
+// Tiles: bf16 [slot][HV][2][64][64] row-major (T_U then T_W), slot = tile_slot(bos, n, c).
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace {
+using namespace ptx;
+
+constexpr int kThreadsPrep = 128;
+constexpr int kLdK = 136;  // bf16 row pitch of the K tile (272 B: conflict-free fragment loads)
+constexpr int kLdX = 68;   // fp32 row pitch of the L / X tile
+constexpr float kFactorFloor = -100.f;  // G_C >= this: Gam_ij = gam_i * 2^-G_j without overflow
+
+struct PrepSmem {
+    union {
+        __nv_bfloat16 k[64 * kLdK];  // the chunk's K rows, until K K^T is formed
+        float lx[64 * kLdX];         // then L in the lower triangle, X^T in the upper:
+                                     // X(r, j), j < r, at lx[j * kLdX + r]
+    };
+    float G[64], beta[64], gam[64], br[64];  // br = beta / gam
+};
+
+__device__ __forceinline__ int rows_in(int64_t len, int c)
+{
+    const int64_t r = len - (int64_t)c * kChunk;
+    return r < kChunk ? (int)r : kChunk;
+}
+
+__global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a)
+{
+    __shared__ __align__(16) PrepSmem sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = blockIdx.x, hv = blockIdx.y;
+    const int HV = a.HV, hq = hv / (HV / a.H);
+    auto seq_start = [&](int m) -> int64_t { return a.cu_seqlens ? a.cu_seqlens[m] : (int64_t)m * a.T; };
+    // the sequence owning this slot: the last n with tile_slot(bos_n, n, 0) <= slot
+    int lo = 0, hi = a.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_slot(seq_start(mid), mid, 0) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int n = lo;
+    const int64_t bos = seq_start(n), len = seq_start(n + 1) - bos;
+    const int c = (int)(slot - tile_slot(bos, n, 0));
+    const int NT = (int)((len + kChunk - 1) / kChunk);
+    if (c < 0 || c >= NT) return;  // an unused slot
+    const int rows = rows_in(len, c);
+    const int64_t t0 = bos + (int64_t)c * kChunk;
+    float *lx = sh.lx;
+
+    // ---- K rows (rows past the end of the sequence are zero), gates
+    {
+        const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows) v = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
+            *(uint4 *)(sh.k + r * kLdK + ch * 8) = v;
+        }
+    }
+    if (warp == 0) {
+        const int r0 = 2 * lane, r1 = r0 + 1;
+        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+        if (r0 < rows) {
+            g0 = a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2;
+            b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
+        }
+        if (r1 < rows) {
+            g1 = a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2;
+            b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
+        }
+        float sp = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sp, off);
+            if (lane >= off) sp += y;
+        }
+        const float G0 = sp - g1, G1 = sp;
+        sh.G[r0] = G0;
+        sh.G[r1] = G1;
+        sh.beta[r0] = b0;
+        sh.beta[r1] = b1;
+        sh.gam[r0] = ex2(G0);
+        sh.gam[r1] = ex2(G1);
+        sh.br[r0] = b0 * ex2(-G0);  // used only when G_C >= kFactorFloor
+        sh.br[r1] = b1 * ex2(-G1);
+    }
+    __syncthreads();
+
+    // ---- L = beta_i (K K^T)[i, j < i] on the tensor cores (bf16 m16n8k16); warp = 16 rows
+    {
+        const int g = lane >> 2, t = lane & 3, m0 = 16 * warp;
+        const uint32_t *kw = (const uint32_t *)sh.k;  // packed bf16 pairs
+        const int ldw = kLdK / 2;
+        float acc[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int kw0 = 8 * ks + t;  // word index of columns 16 ks + 2t, +1
+            const uint32_t a0 = kw[(m0 + g) * ldw + kw0], a1 = kw[(m0 + g + 8) * ldw + kw0];
+            const uint32_t a2 = kw[(m0 + g) * ldw + kw0 + 4], a3 = kw[(m0 + g + 8) * ldw + kw0 + 4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                if (nt > 2 * warp + 1) continue;  // only columns j <= i are needed
+                const uint32_t b0 = kw[(8 * nt + g) * ldw + kw0], b1 = kw[(8 * nt + g) * ldw + kw0 + 4];
+                mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        __syncthreads();  // every warp has read K: its buffer becomes the L / X tile
+        float bdiag = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            if (nt > 2 * warp + 1) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = m0 + g + 8 * (q >> 1), j = 8 * nt + 2 * t + (q & 1);
+                const float v = sh.beta[i] * acc[nt][q];
+                if (j < i) lx[i * kLdX + j] = v;
+                if (j == i) bdiag = fmaxf(bdiag, v);
+            }
+        }
+        // beta ||k||^2 <= 2 keeps every transition non-expansive (warmup split)
+        if (a.check_norm && bdiag > 2.0001f) atomicOr(a.status, kStatusNormBound);
+    }
+    __syncthreads();
+
+    auto Lx = [&](int r, int j) -> float { return lx[r * kLdX + j]; };
+    auto Xt = [&](int r, int j) -> float { return lx[j * kLdX + r]; };  // X(r, j), j < r
+    auto Xm = [&](int r, int j) -> float { return r > j ? lx[j * kLdX + r] : (r == j ? 1.f : 0.f); };
+    const int pw = warp;
+    // ---- A: the eight 8 x 8 diagonal blocks by forward substitution; 2 threads per (block, column)
+    {
+        const int task = tid >> 1, hh = tid & 1;
+        const int base = 8 * (task >> 3), cc = task & 7;
+        float x[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 8; ++r) {
+            float part = 0.f;
+#pragma unroll
+            for (int j = 0; j < r; ++j)
+                if ((j & 1) == hh) part = fmaf(Lx(base + r, base + j), x[j], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            if (r > cc) x[r] = -part;
+        }
+        if (hh == 0) {
+#pragma unroll
+            for (int r = 1; r < 8; ++r)
+                if (r > cc) lx[(base + cc) * kLdX + base + r] = x[r];
+        }
+    }
+    __syncthreads();
+    // ---- B: 8 -> 16, one warp per merge:  X(B, A) = -X(B, B) (L(B, A) X(A, A))
+    {
+        const int A = 16 * pw, Bb = A + 8;
+        const int r = lane >> 2, cp = (lane & 3) * 2;
+        float t0v = 0.f, t1v = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float l = Lx(Bb + r, A + k);
+            const float x0 = k > cp ? Xt(A + k, A + cp) : (k == cp ? 1.f : 0.f);
+            const float x1 = k > cp + 1 ? Xt(A + k, A + cp + 1) : (k == cp + 1 ? 1.f : 0.f);
+            t0v = fmaf(l, x0, t0v);
+            t1v = fmaf(l, x1, t1v);
+        }
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float tk0 = __shfl_sync(0xffffffffu, t0v, 4 * k + (lane & 3));
+            const float tk1 = __shfl_sync(0xffffffffu, t1v, 4 * k + (lane & 3));
+            const float xb = k < r ? Xt(Bb + r, Bb + k) : (k == r ? 1.f : 0.f);
+            a0 = fmaf(xb, tk0, a0);
+            a1 = fmaf(xb, tk1, a1);
+        }
+        lx[(A + cp) * kLdX + Bb + r] = -a0;
+        lx[(A + cp + 1) * kLdX + Bb + r] = -a1;
+    }
+    __syncthreads();
+    // ---- C: 16 -> 32 (tf32 m16n8k8); warp = (merge, 8-column tile):
+    //      T = L(B, A) X(A, A)[:, tile] (kept in place of L(B, A)), then X(B, A)[:, tile] = -X(B, B) T
+    {
+        const int g = lane >> 2, t = lane & 3;
+        const int A = 32 * (pw >> 1), Bb = A + 16, n0 = 8 * (pw & 1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = 8 * ks;
+            mma_tf32(d, Lx(Bb + g, A + k0 + t), Lx(Bb + g + 8, A + k0 + t), Lx(Bb + g, A + k0 + t + 4),
+                     Lx(Bb + g + 8, A + k0 + t + 4), Xm(A + k0 + t, A + n0 + g), Xm(A + k0 + t + 4, A + n0 + g));
+        }
+        __syncthreads();  // every warp has read L(B, A)
+        *(float2 *)(lx + (Bb + g) * kLdX + A + n0 + 2 * t) = make_float2(d[0], d[1]);
+        *(float2 *)(lx + (Bb + g + 8) * kLdX + A + n0 + 2 * t) = make_float2(d[2], d[3]);
+        __syncwarp();
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = 8 * ks;
+            mma_tf32(u, Xm(Bb + g, Bb + k0 + t), Xm(Bb + g + 8, Bb + k0 + t), Xm(Bb + g, Bb + k0 + t + 4),
+                     Xm(Bb + g + 8, Bb + k0 + t + 4), Lx(Bb + k0 + t, A + n0 + g), Lx(Bb + k0 + t + 4, A + n0 + g));
+        }
+        lx[(A + n0 + 2 * t) * kLdX + Bb + g] = -u[0];
+        lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = -u[1];
+        lx[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = -u[2];
+        lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g + 8] = -u[3];
+    }
+    __syncthreads();
+    // ---- D: 32 -> 64; warp = 8-column tile of the lower-left 32 x 32 block:
+    //      T = L(32:64, 0:32) X(0:32, tile) (kept in place of L), then X(32:64, tile) = -X(32:64, 32:64) T
+    {
+        const int g = lane >> 2, t = lane & 3, n0 = 8 * pw;
+        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            if (ks < pw) continue;  // X(k, n) = 0 for k < n
+            const int k0 = 8 * ks;
+            const float b0 = Xm(k0 + t, n0 + g), b1 = Xm(k0 + t + 4, n0 + g);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int m0 = 32 + 16 * mt;
+                mma_tf32(d[mt], Lx(m0 + g, k0 + t), Lx(m0 + g + 8, k0 + t), Lx(m0 + g, k0 + t + 4),
+                         Lx(m0 + g + 8, k0 + t + 4), b0, b1);
+            }
+        }
+        __syncthreads();  // every warp has read L(32:64, 0:32)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            *(float2 *)(lx + (32 + 16 * mt + g) * kLdX + n0 + 2 * t) = make_float2(d[mt][0], d[mt][1]);
+            *(float2 *)(lx + (32 + 16 * mt + g + 8) * kLdX + n0 + 2 * t) = make_float2(d[mt][2], d[mt][3]);
+        }
+        __syncwarp();
+        float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int k0 = 8 * ks;
+            const float b0 = Lx(32 + k0 + t, n0 + g), b1 = Lx(32 + k0 + t + 4, n0 + g);  // T(k, n)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                if (k0 > 16 * mt + 15) continue;  // X(32 + m, 32 + k) = 0 for k > m
+                const int m0 = 32 + 16 * mt;
+                mma_tf32(u[mt], Xm(m0 + g, 32 + k0 + t), Xm(m0 + g + 8, 32 + k0 + t), Xm(m0 + g, 32 + k0 + t + 4),
+                         Xm(m0 + g + 8, 32 + k0 + t + 4), b0, b1);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const int m0 = 32 + 16 * mt;
+            lx[(n0 + 2 * t) * kLdX + m0 + g] = -u[mt][0];
+            lx[(n0 + 2 * t + 1) * kLdX + m0 + g] = -u[mt][1];
+            lx[(n0 + 2 * t) * kLdX + m0 + g + 8] = -u[mt][2];
+            lx[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
+        }
+    }
+    __syncthreads();
+
+    // ---- operand tiles; thread = (row r, 32 columns), two 16-byte pieces per tile and step
+    {
+        const int r = tid >> 1, h = tid & 1;
+        const float gr = sh.gam[r], Gr = sh.G[r];
+        const bool factored = sh.G[63] >= kFactorFloor;
+        __nv_bfloat16 *tu = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 2 * 4096 + r * 64 + 32 * h;
+        __nv_bfloat16 *tw = tu + 4096;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            const int j0 = 32 * h + 8 * q;
+            float xv[8], vu[8], vw[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int jj = j0 + u;
+                xv[u] = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                vw[u] = gr * sh.beta[jj] * xv[u];
+            }
+            if (factored) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) vu[u] = gr * sh.br[j0 + u] * xv[u];  // x = 0 above the diagonal
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    vu[u] = j0 + u <= r ? ex2(Gr - sh.G[j0 + u]) * sh.beta[j0 + u] * xv[u] : 0.f;
+            }
+            *(uint4 *)(tu + 8 * q) = pack8(vu);
+            *(uint4 *)(tw + 8 * q) = pack8(vw);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
+{
+    if (a.N * a.HV == 0 || a.slots == 0) return cudaSuccess;
+    dim3 grid(a.slots, a.HV);
+    tc_prep_kernel<<<grid, kThreadsPrep, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

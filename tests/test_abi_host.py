@@ -69,7 +69,7 @@ def test_plans(gdn):
     # bf16, dk = dv = 128, scalar gate: tensor-core engine, one CTA per (sequence, head)
     p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152)
     assert p.engine == 2 and p.value_tiles == 1
-    assert p.cp_mode == 1 and p.segments == 1 and p.kernels == 1
+    assert p.cp_mode == 1 and p.segments == 1 and p.kernels == 2  # chunk preparation + scan
     # 64 pairs leave half the SMs idle: with unit-norm keys asserted, the warmup split
     p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152, keys_unit_norm=True)
     assert p.cp_mode == 3 and p.segments == 2
@@ -80,9 +80,9 @@ def test_plans(gdn):
     assert p.engine == 1
     # few pairs and a long sequence: the split is planned
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152)
-    assert p.cp_mode == 2 and p.segments > 1 and p.kernels == 3
+    assert p.cp_mode == 2 and p.segments > 1 and p.kernels == 4
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, keys_unit_norm=True)
-    assert p.cp_mode == 3 and p.kernels == 1  # the tensor-core scan finds its own warmup starts
+    assert p.cp_mode == 3 and p.kernels == 2  # the tensor-core scan finds its own warmup starts
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="off")
     assert p.cp_mode == 1 and p.segments == 1
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152, cp_mode="exact", segment_chunks=64)
