@@ -272,6 +272,15 @@ __device__ __forceinline__ void mma_bf16_16816(float *d, uint32_t a0, uint32_t a
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// four 8 x 8 b16 matrices from shared memory (lanes 8i..8i+7 address the rows of matrix i)
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 // byte offset of (row r, element k) inside a 128-byte-swizzled tile with 64
 // bf16 per row (what TMA writes for a box of 64 x 128 B with SWIZZLE_128B)
 __device__ __forceinline__ uint32_t sw128(int r, int k)

@@ -14,13 +14,23 @@
 //   O    = Q~ S + P V',  Q~ = diag(scale gam) Q,  P = scale Lower(Gam) * (Q K^T)
 //   S   <- gC S + K^T diag(gC / gam) V'
 //
+// With Gam_ij = gam_i / gam_j the output factors as
+//   O = diag(scale gam) (Q S + (Lower(Q K^T) / gC) (diag(gC / gam) V'))
+// so the products take the raw Q, an unscaled causal mask of Q K^T and the
+// same gC/gam-scaled V' as the state update, and the O epilogue applies the row
+// factors.  2^-G_C must then be finite: a chunk whose decay passes 2^-100
+// takes the direct form (Q~ in place, P with its per-entry powers, unscaled V').
+//
 // The serial chain per chunk is: S -> bf16 copy, one MMA group
 // (V'^T = U^T - S^T W^T), V' -> bf16, one MMA group (the state update).
 //
-// Warp roles (12 warps): 0 TMA producer (q, k, v boxes and the two tiles) + gate
-// statistics (and the warmup start), 1 MMA issuer (event driven), 2-3 aux (Q~ in
-// place, P), 4-7 chain (state copy, V'), 8-11 output (W^T -> shared memory, O
-// epilogue).
+// Warp roles (16 warps): 0 TMA producer (q, k, v boxes and the two tiles) + gate
+// statistics (and the warmup start), 1 MMA issuer (a fixed program per chunk),
+// 2-3 aux (P; Q~ in place for steep chunks), 4-11 chain (state copy, V'; two warps per 32-lane
+// slice of tensor memory, each converting half of the columns), 12-15 output
+// (W^T -> shared memory, O epilogue).  Every role batches its shared-memory
+// loads ahead of the arithmetic: with one or two warps of a role per scheduler,
+// a role's speed is its dependency latency, not its instruction count.
 // Every wait is bounded in wall time; a wait that runs out records a timeout
 // in the status word and the roles leave their loops, so the kernel always
 // ends, waits for its copies and products in flight and frees its tensor memory.
@@ -34,7 +44,7 @@ namespace gdn {
 namespace {
 using namespace ptx;
 
-constexpr int kThreadsTC = 384;
+constexpr int kThreadsTC = 512;
 constexpr int kStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 
@@ -46,19 +56,22 @@ constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, s
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16
 constexpr uint32_t OFF_WS = OFF_P + 8192;                       // -W^T [128 (dk) x 64] bf16, MN-major
-constexpr uint32_t kGateBytes = 1536;  // per stage: G, beta, gam, 2^(G_C-G), (unused), scale*gam  [64] f32 each
+// gate statistics per chunk: G, (unused), gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each.  A ring of
+// four: the O epilogue of chunk c still reads its row factors while chunk c + 3 is loaded
+constexpr int kGateStages = 4;
+constexpr uint32_t kGateBytes = 1536;
 constexpr uint32_t OFF_GATE = OFF_WS + 16384;
-constexpr uint32_t OFF_BAR = OFF_GATE + kStages * kGateBytes;
+constexpr uint32_t OFF_BAR = OFF_GATE + kGateStages * kGateBytes;
 constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_BETA = 64, GT_GAM = 128, GT_RDEC = 192, GT_SGAM = 320;
+constexpr int GT_G = 0, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320;
+// G_C >= this: Gam_ij = gam_i * 2^-G_j with every factor inside the fp32 range
+constexpr float kFactorFloor = -100.f;
 
 // ---- tensor memory columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_VP = 128, TM_O = 192, TM_W = 256, TM_SBF = 320, TM_VB = 384, TM_VTB = 416,
                    TM_KQ = 448;
-
-// ---- named barriers (0 is __syncthreads)
 
 enum Bar {
     B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_WF, B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF,
@@ -199,9 +212,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         mbar_init(&bars[B_KQE], 2);
         mbar_init(&bars[B_WF], 1);
         mbar_init(&bars[B_WC], 4);
-        mbar_init(&bars[B_SBF], 4);
+        mbar_init(&bars[B_SBF], 8);
         mbar_init(&bars[B_VPF], 1);
-        mbar_init(&bars[B_VTF], 4);
+        mbar_init(&bars[B_VTF], 8);
         mbar_init(&bars[B_SF], 1);
         mbar_init(&bars[B_PF], 2);
         mbar_init(&bars[B_OF], 1);
@@ -217,7 +230,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const int cs = s_cs[0], c0 = s_cs[1], c1 = s_cs[2];
     const int nch = c1 - cs;
     unsigned *status = a.status;
-    auto gates = [&](int i) { return (float *)(sm + OFF_GATE + (i % kStages) * kGateBytes); };
+    auto gates = [&](int i) { return (float *)(sm + OFF_GATE + (i % kGateStages) * kGateBytes); };
+    // factored output form (see the header): the chunk's decay 2^-G_C is finite
+    auto factored = [&](int i) { return gates(i)[GT_G + 63] >= kFactorFloor; };
     auto emit_of = [&](int i) { return fwd && cs + i >= c0; };
 
     if (warp == 0) {
@@ -255,15 +270,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             ++issued;
             // gate statistics while the tiles land: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
             const int r0 = 2 * lane, r1 = r0 + 1;
-            float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-            if (r0 < rows) {
-                g0 = a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2;
-                b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
-            }
-            if (r1 < rows) {
-                g1 = a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2;
-                b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
-            }
+            const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2 : 0.f;
+            const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2 : 0.f;
             float sp = g0 + g1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -275,9 +283,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             float *gt = gates(i);
             const float gm0 = ex2(G0), gm1 = ex2(G1);
             *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
-            *(float2 *)(gt + GT_BETA + r0) = make_float2(b0, b1);
             *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
             *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
+            *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
             *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
             ok = mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -304,45 +312,112 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         for (int i = landed; i < issued; ++i)
             mbar_wait(&bars[B_TMA + i % kStages], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
     } else if (warp == 1) {
-        // ================================================================ MMA issuer (event driven)
-        // The whole warp runs the loop with warp-uniform decisions and one elected lane issues:
-        // the operands of tcgen05.mma are then warp-uniform values and unrolled groups issue at
-        // the tensor core's rate (a divergent single-thread issuer is several times slower).
+        // ================================================================ MMA issuer
+        // A fixed program per chunk, ordered around the serial chain: each chain product is
+        // issued as soon as its operands are ready, and the state-independent products are
+        // queued behind it so that the tensor pipe stays busy while the chain warps convert.
+        // The whole warp follows the program (warp-uniform waits) and one elected lane issues:
+        // the operands of tcgen05.mma are then warp-uniform values.
         if (nch > 0) {
             const uint32_t idKQ = idesc_bf16_f32(128, 64, 0, 0);   // K-major A and B
             const uint32_t idMN = idesc_bf16_f32(128, 64, 1, 0);   // MN-major A (V^T, K^T), K-major B
             const uint32_t idV1 = idesc_bf16_f32(128, 64, 0, 1);   // A in TMEM, MN-major B (-W^T)
             const uint32_t idO = idesc_bf16_f32(128, 64, 0, 0);    // A in TMEM, K-major B (Q~, P)
             const uint32_t idS = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, MN-major B (K), N = dk
-            // readiness as seen by lane 0, shared by the warp
-            auto rdy = [&](int b, int ph) {
+            auto stage = [&](int i) { return sbase + OFF_STAGE + (i % kStages) * kStageBytes; };
+            bool ok = true;
+            auto wait = [&](int b, int ph) {
+                if (ok) ok = mbar_wait(&bars[b], (uint32_t)ph & 1u, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                return ok;
+            };
+            auto ready = [&](int b, int ph) {
                 return __shfl_sync(0xffffffffu, (int)mbar_test_wait(&bars[b], (uint32_t)ph & 1u), 0) != 0;
             };
-            auto stage = [&](int i) { return sbase + OFF_STAGE + (i % kStages) * kStageBytes; };
-            int kq = 0, u = 0, w = 0, c = 0, e = 0, cst = 0;
-            uint64_t t_last = globaltimer();
-            uint32_t idle = 0;
-            bool ok = true;
-            while (c < nch) {
-                bool prog = false;
+            // Q K^T (lanes 64-127 of [K; Q] K^T) of emitted chunks only; its phases count emitted chunks
+            const int ce0 = fwd ? min(max(c0 - cs, 0), nch) : nch;
+            int kq = ce0;
+            auto issue_kq = [&]() {
+                const uint32_t s2 = stage(kq);
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars[B_KQF]);
+                }
+                __syncwarp();
+                ++kq;
+            };
+            // up to chunk lim: blocking (the program needs it now) or only what is ready
+            auto kq_upto = [&](int lim, bool block) {
+                while (ok && kq < nch && kq <= lim) {
+                    const int fs = B_FULL + kq % kStages, fp = kq / kStages;
+                    if (block) {
+                        if (!wait(fs, fp) || (kq > ce0 && !wait(B_KQE, kq - 1 - ce0))) break;
+                    } else if (!ready(fs, fp) || (kq > ce0 && !ready(B_KQE, kq - 1 - ce0))) {
+                        break;
+                    }
+                    issue_kq();
+                }
+            };
+            auto issue_w = [&](int i) {
+                // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
+                const uint32_t s2 = stage(i);
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024), kmaj(s2 + sTW + ks * 32),
+                               idMN, ks > 0 ? 1u : 0u);
+                    mma_commit(&bars[B_WF]);
+                }
+                __syncwarp();
+            };
+            auto issue_u = [&](int i) {
+                // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
+                if (zero_values) return;
+                const uint32_t s2 = stage(i);
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024), kmaj(s2 + sTU + ks * 32),
+                               idMN, ks > 0 ? 1u : 0u);
+                }
+                __syncwarp();
+            };
+            // prologue: the first chunk's W and U, Q K^T of the first emitted chunks
+            if (wait(B_FULL, 0)) {
+                issue_w(0);
+                issue_u(0);
+            }
+            kq_upto(1, false);
+            int e = 0;
+            for (int c = 0; c < nch && ok; ++c) {
                 const bool em = emit_of(c);
                 const uint32_t st = stage(c);
-                if (cst == 0 && u > c && rdy(B_SBF, c) && rdy(B_WC, c)) {
-                    // V'^T (holding U^T) -= S^T W^T
-                    tc_fence_after();
-                    if (elect_one()) {
+                // ---- V'^T (holding U^T, issued before) -= S^T W^T
+                if (!wait(B_SBF, c) || !wait(B_WC, c)) break;
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
-                                   idV1, (ks > 0 || !zero_values) ? 1u : 0u);
-                        mma_commit(&bars[B_VPF]);
-                    }
-                    __syncwarp();
-                    cst = em ? 1 : 2;
-                    prog = true;
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
+                               idV1, (ks > 0 || !zero_values) ? 1u : 0u);
+                    mma_commit(&bars[B_VPF]);
                 }
-                if (cst == 1 && rdy(B_QS + c % kStages, c / kStages) && (e == 0 || rdy(B_OE, e - 1))) {
-                    // O^T = S^T Q~^T
+                __syncwarp();
+                kq_upto(c + 1, false);
+                if (em) {
+                    // ---- O^T = S^T Q^T, or S^T Q~^T for a steep chunk (S^T is read before the chain
+                    //      overwrites it: SF commits after it); the raw Q of a factored chunk is ready
+                    //      with the stage, a steep chunk waits for Q~
+                    kq_upto(c, true);
+                    if ((!factored(c) && !wait(B_QS + c % kStages, c / kStages)) || (e > 0 && !wait(B_OE, e - 1)))
+                        break;
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
@@ -352,101 +427,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                         }
                     }
                     __syncwarp();
-                    cst = 2;
-                    prog = true;
                 }
-                if (cst == 2 && rdy(B_VTF, c)) {
-                    // S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
+                // ---- S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
+                if (!wait(B_VTF, c)) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                    mma_commit(&bars[B_SF]);
+                }
+                __syncwarp();
+                // ---- the next chunk's W (its conversion then overlaps the state copy)
+                if (c + 1 < nch) {
+                    if (!wait(B_FULL + (c + 1) % kStages, (c + 1) / kStages)) break;
+                    issue_w(c + 1);
+                }
+                if (em) {
+                    // ---- O^T += V'^T P^T, or (V'^T diag(gC/gam)) (Lower(Q K^T) / gC)^T in the factored
+                    //      form (before the next V' product: the chain's V' commit covers it)
+                    if (!wait(B_PF, e)) break;
+                    const uint32_t va = tb + (factored(c) ? TM_VTB : TM_VB);
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
-                        mma_commit(&bars[B_SF]);
-                    }
-                    __syncwarp();
-                    cst = em ? 3 : 4;
-                    prog = true;
-                }
-                if (cst == 3 && rdy(B_PF, e)) {
-                    // O^T += V'^T P^T
-                    tc_fence_after();
-                    if (elect_one()) {
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(sbase + OFF_P + ks * 32), idO, 1u);
+                            mma_ts(tb + TM_O, va + ks * 8, kmaj(sbase + OFF_P + ks * 32), idO, 1u);
                         mma_commit(&bars[B_OF]);
                     }
                     __syncwarp();
                     ++e;
-                    cst = 4;
-                    prog = true;
                 }
-                if (cst == 4) {
-                    if (elect_one()) mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
-                    __syncwarp();
-                    ++c;
-                    cst = 0;
-                }
-                // ---- state-independent products, issued as soon as their inputs are ready
-                if (kq < nch && rdy(B_FULL + kq % kStages, kq / kStages) && (kq == 0 || rdy(B_KQE, kq - 1))) {
-                    // [K; Q] K^T: K K^T in lanes 0-63, Q K^T in lanes 64-127
-                    tc_fence_after();
-                    const uint32_t s2 = stage(kq);
-                    if (elect_one()) {
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars[B_KQF]);
-                    }
-                    __syncwarp();
-                    ++kq;
-                    prog = true;
-                }
-                if (w < kq && (w == 0 || rdy(B_WC, w - 1))) {   // the tiles came with the stage (KQ waited for it)
-                    // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
-                    tc_fence_after();
-                    const uint32_t s2 = stage(w);
-                    if (elect_one()) {
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024),
-                                   kmaj(s2 + sTW + ks * 32), idMN, ks > 0 ? 1u : 0u);
-                        mma_commit(&bars[B_WF]);
-                    }
-                    __syncwarp();
-                    ++w;
-                    prog = true;
-                }
-                if (u < kq && (u == 0 || rdy(B_VTF, u - 1))) {
-                    // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
-                    tc_fence_after();
-                    const uint32_t s2 = stage(u);
-                    if (elect_one()) {
-                        if (!zero_values) {
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)
-                                mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024),
-                                       kmaj(s2 + sTU + ks * 32), idMN, ks > 0 ? 1u : 0u);
-                        }
-                    }
-                    __syncwarp();
-                    ++u;
-                    prog = true;
-                }
-                if (prog) {
-                    idle = 0;
-                    t_last = globaltimer();
-                } else {
-                    __nanosleep(20);  // polling competes with the other warps for the shared-memory pipe
-                    if ((++idle & 255u) == 0 &&
-                        __shfl_sync(0xffffffffu, (int)(globaltimer() - t_last > kWaitNs), 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
+                if (c + 1 < nch) issue_u(c + 1);  // V'(c) has been read (VTF)
+                kq_upto(c + 2, false);
+                if (elect_one()) mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                __syncwarp();
             }
             if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
             // every product issued so far has finished before the CTA frees its tensor memory
@@ -462,65 +477,89 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         int e = 0;
         for (int i = 0; i < nch && ok; ++i) {
             const int s = i % kStages;
-            const bool emit = emit_of(i);
+            if (!emit_of(i)) {
+                // warmup chunk: nothing reads its Q~; the arrival keeps the stage barrier's phase count
+                if (lane == 0) mbar_arrive(&bars[B_QS + s]);
+                continue;
+            }
             ok = mbar_wait(&bars[B_FULL + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
-            if (ok) ok = mbar_wait(&bars[B_KQF], i & 1, status, kStatusTimeout, kWaitNs);
+            if (ok) ok = mbar_wait(&bars[B_KQF], e & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const float *gt = gates(i);
             // Q K^T row r into registers: the K K^T / Q K^T region is released at once
             uint32_t kq[64];
-            if (emit) {
-                tmem_ld32(tl + TM_KQ, kq);
-                tmem_ld32(tl + TM_KQ + 32, kq + 32);
-                tmem_ld_wait();
-            }
+            tmem_ld32(tl + TM_KQ, kq);
+            tmem_ld32(tl + TM_KQ + 32, kq + 32);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_KQE]);
-            if (emit) {
-                // Q~ row r = scale * gam_r * q_r, in place (the K K^T / Q K^T product has read Q);
-                // the 16-byte pieces are visited in a row-rotated order to spread the banks
+            const bool fac = gt[GT_G + 63] >= kFactorFloor;
+            if (!fac) {
+                // steep chunk: Q~ row r = scale * gam_r * q_r, in place (the Q K^T product has read Q);
+                // the 16-byte pieces go in a row-rotated order to spread the banks, all loads first
                 uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
                 const float f = gt[GT_SGAM + r];
 #pragma unroll 1
                 for (int bx = 0; bx < 2; ++bx) {
+                    uint8_t *row = st + (bx ? sQ1 : sQ0) + r * 128;
+                    uint4 x[8];
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) x[c8] = *(const uint4 *)(row + ((c8 + r) & 7) * 16);
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {
-                        const int ch = (c8 + r) & 7;
-                        uint4 *ptr = (uint4 *)(st + (bx ? sQ1 : sQ0) + r * 128 + ch * 16);
-                        uint4 x = *ptr;
-                        __nv_bfloat162 *h2 = (__nv_bfloat162 *)&x;
+                        __nv_bfloat162 *h2 = (__nv_bfloat162 *)&x[c8];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float2 fv = __bfloat1622float2(h2[q]);
                             h2[q] = __floats2bfloat162_rn(fv.x * f, fv.y * f);
                         }
-                        *ptr = x;
                     }
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) *(uint4 *)(row + ((c8 + r) & 7) * 16) = x[c8];
                 }
                 fence_proxy_async();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_QS + s]);
-            if (!emit) continue;
             if (e > 0) ok = mbar_wait(&bars[B_OF], (e - 1) & 1, status, kStatusTimeout, kWaitNs);  // P free
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             {
-                // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j] -> bf16, 128-byte swizzled
-                const float Gr = gt[GT_G + r], sc = a.scale;
+                // row r of the intra-chunk operand -> bf16, 128-byte swizzled
                 uint8_t *prow = sm + OFF_P;
+                if (fac) {
+                    // Lower(Q K^T)[r, j] / gC (the gate factors sit in V' and in the O epilogue)
+                    const float rg = gt[GT_GINV + 63];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float v[8];
+                    for (int q = 0; q < 8; ++q) {
+                        float v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int j = 8 * q + u;
-                        v[u] = (j <= r) ? sc * ex2(Gr - gt[GT_G + j]) * u2f(kq[j]) : 0.f;
+                        for (int u = 0; u < 8; ++u) v[u] = (8 * q + u <= r) ? u2f(kq[8 * q + u]) * rg : 0.f;
+                        *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
                     }
-                    *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
+                } else {
+                    // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j]
+                    // steep decay: 2^-G_j may overflow, so each entry takes its own power
+                    const float Gr = gt[GT_G + r], sc = a.scale;
+#pragma unroll 1
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 g0 = *(const float4 *)(gt + GT_G + 8 * q);
+                        const float4 g1 = *(const float4 *)(gt + GT_G + 8 * q + 4);
+                        const float gj[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                        float v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            uint32_t x = kq[0];
+#pragma unroll
+                            for (int qq = 0; qq < 8; ++qq)
+                                if (qq == q) x = kq[8 * qq + u];
+                            v[u] = (8 * q + u <= r) ? sc * ex2(Gr - gj[u]) * u2f(x) : 0.f;
+                        }
+                        *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
+                    }
                 }
             }
             fence_proxy_async();
@@ -528,9 +567,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (lane == 0) mbar_arrive(&bars[B_PF]);
             ++e;
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ================================================================ chain (lane = dv)
-        const int dv = tid - 128;
+    } else if (warp >= 4 && warp < 12) {
+        // ================================================================ chain (lane = dv; half hh of the columns)
+        const int dv = 32 * (warp & 3) + lane;
+        const int hh = (warp - 4) >> 2;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
         const float *init = nullptr;
         bool identity = false;
@@ -544,9 +584,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         }
         bool ok = true;
         if (nch > 0) {
-            // the segment's initial state into the state accumulator (no product touches it yet)
+            // the segment's initial state (dk columns 64 hh .. 64 hh + 63) into the state accumulator
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
                 uint32_t r[32];
                 if (init) {
                     const float *src = init + (size_t)(32 * q4) * V + dv;
@@ -569,62 +609,64 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             tc_fence_after();
             const float *gt = gates(i);
             const float dec = gt[GT_GAM + 63];  // gC = 2^G_C
-            // ---- S_i -> bf16 copy (MMA operand) and gC * S_i (accumulator of this chunk's update)
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            {
+                // ---- S_i -> bf16 copy (MMA operand) and gC * S_i (accumulator of this chunk's update)
                 uint32_t r[64];
-                tmem_ld32(tl + TM_S + 64 * h, r);
-                tmem_ld32(tl + TM_S + 64 * h + 32, r + 32);
+                tmem_ld32(tl + TM_S + 64 * hh, r);
+                tmem_ld32(tl + TM_S + 64 * hh + 32, r + 32);
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) p[j] = pack_bf16(u2f(r[32 * q + 2 * j]), u2f(r[32 * q + 2 * j + 1]));
-                    tmem_st16(tl + TM_SBF + 32 * h + 16 * q, p);
+                    tmem_st16(tl + TM_SBF + 32 * hh + 16 * q, p);
                 }
 #pragma unroll
                 for (int j = 0; j < 64; ++j) r[j] = f2u(u2f(r[j]) * dec);
-                tmem_st32(tl + TM_S + 64 * h, r);
-                tmem_st32(tl + TM_S + 64 * h + 32, r + 32);
+                tmem_st32(tl + TM_S + 64 * hh, r);
+                tmem_st32(tl + TM_S + 64 * hh + 32, r + 32);
+                tmem_st_wait();
             }
-            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_SBF]);
 
-            // ---- V'^T -> bf16: as the output operand (TMEM) and scaled by gC/gam as the update operand
+            // ---- V'^T (tokens 32 hh .. 32 hh + 31) -> bf16: as the output operand and scaled by
+            //      gC/gam as the update operand; the scale factors are loaded while the product runs
+            float rd[32];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 x = *(const float4 *)(gt + GT_RDEC + 32 * hh + 4 * j4);
+                rd[4 * j4] = x.x;
+                rd[4 * j4 + 1] = x.y;
+                rd[4 * j4 + 2] = x.z;
+                rd[4 * j4 + 3] = x.w;
+            }
             ok = mbar_wait(&bars[B_VPF], i & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             {
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t r[32];
-                    tmem_ld32(tl + TM_VP + 32 * h, r);
-                    tmem_ld_wait();
-                    uint32_t vb[16], vtb[16];
+                uint32_t r[32];
+                tmem_ld32(tl + TM_VP + 32 * hh, r);
+                tmem_ld_wait();
+                uint32_t vb[16], vtb[16];
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 rd = *(const float4 *)(gt + GT_RDEC + 32 * h + 4 * j4);
-                        const float x0 = u2f(r[4 * j4 + 0]), x1 = u2f(r[4 * j4 + 1]);
-                        const float x2 = u2f(r[4 * j4 + 2]), x3 = u2f(r[4 * j4 + 3]);
-                        vb[2 * j4] = pack_bf16(x0, x1);
-                        vb[2 * j4 + 1] = pack_bf16(x2, x3);
-                        vtb[2 * j4] = pack_bf16(x0 * rd.x, x1 * rd.y);
-                        vtb[2 * j4 + 1] = pack_bf16(x2 * rd.z, x3 * rd.w);
-                    }
-                    tmem_st16(tl + TM_VTB + 16 * h, vtb);
-                    tmem_st16(tl + TM_VB + 16 * h, vb);
+                for (int j = 0; j < 16; ++j) {
+                    const float x0 = u2f(r[2 * j]), x1 = u2f(r[2 * j + 1]);
+                    vb[j] = pack_bf16(x0, x1);
+                    vtb[j] = pack_bf16(x0 * rd[2 * j], x1 * rd[2 * j + 1]);
                 }
+                tmem_st16(tl + TM_VTB + 16 * hh, vtb);
+                tmem_st16(tl + TM_VB + 16 * hh, vb);
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_VTF]);
         }
-        // ---- final state of the segment
+        // ---- final state of the segment (dk rows 64 hh .. 64 hh + 63)
         const bool write_ht = fwd && c1 == NT && a.ht != nullptr;
         const bool write_seg = !fwd;
         if (write_ht || write_seg) {
@@ -639,7 +681,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             }
             if (nch == 0) {
 #pragma unroll 1
-                for (int d = 0; d < 128; ++d) {
+                for (int d = 64 * hh; d < 64 * hh + 64; ++d) {
                     float x = 0.f;
                     if (init) x = init[(size_t)d * V + dv];
                     else if (identity) x = (d == dv) ? 1.f : 0.f;
@@ -651,7 +693,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (ok) {
                     tc_fence_after();
 #pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
+                    for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
                         uint32_t r[32];
                         tmem_ld32(tl + TM_S + 32 * q4, r);
                         tmem_ld_wait();
@@ -667,7 +709,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         }
     } else {
         // ================================================================ output warps
-        const int et = tid - 256;
+        const int et = tid - 384;
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
         bool ok = true;
         int e = 0;
@@ -711,9 +753,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld32(tl + TM_O, r);
                 tmem_ld32(tl + TM_O + 32, r + 32);
                 tmem_ld_wait();
+                const float *gt = gates(it - 1);
+                if (factored(it - 1)) {
+                    // the row factors scale * gam_t of the factored form
+#pragma unroll
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        const float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
+                        r[4 * j4] = f2u(u2f(r[4 * j4]) * f.x);
+                        r[4 * j4 + 1] = f2u(u2f(r[4 * j4 + 1]) * f.y);
+                        r[4 * j4 + 2] = f2u(u2f(r[4 * j4 + 2]) * f.z);
+                        r[4 * j4 + 3] = f2u(u2f(r[4 * j4 + 3]) * f.w);
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_OE]);  // O region drained
+                // O region drained and the chunk's gate block read (the producer reuses it after the
+                // next chunk's S^T Q^T product, which waits for this)
+                if (lane == 0) mbar_arrive(&bars[B_OE]);
                 __nv_bfloat16 *og = (__nv_bfloat16 *)a.o + ((size_t)t0 * HV + hv) * V + et;
                 const size_t ostride = (size_t)HV * V;
                 {

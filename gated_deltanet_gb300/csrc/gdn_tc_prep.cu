@@ -30,7 +30,7 @@ struct PrepSmem {
         float lx[64 * kLdX];         // then L in the lower triangle, X^T in the upper:
                                      // X(r, j), j < r, at lx[j * kLdX + r]
     };
-    float G[64], beta[64], gam[64], br[64];  // br = beta / gam
+    __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
 };
 
 __device__ __forceinline__ int rows_in(int64_t len, int c)
@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     // ---- L = beta_i (K K^T)[i, j < i] on the tensor cores (bf16 m16n8k16); warp = 16 rows
     {
         const int g = lane >> 2, t = lane & 3, m0 = 16 * warp;
-        const uint32_t *kw = (const uint32_t *)sh.k;  // packed bf16 pairs
-        const int ldw = kLdK / 2;
+        const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: this lane addresses row ri of matrix mi
+        const uint32_t kbase = smem_u32(sh.k);
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -113,14 +113,17 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const int kw0 = 8 * ks + t;  // word index of columns 16 ks + 2t, +1
-            const uint32_t a0 = kw[(m0 + g) * ldw + kw0], a1 = kw[(m0 + g + 8) * ldw + kw0];
-            const uint32_t a2 = kw[(m0 + g) * ldw + kw0 + 4], a3 = kw[(m0 + g + 8) * ldw + kw0 + 4];
+            // A fragment of rows m0..m0+15, columns 16 ks..16 ks+15: matrices (rows +0/+8) x (columns +0/+8)
+            uint32_t af[4];
+            ldsm_x4(af, kbase + ((m0 + (mi & 1) * 8 + ri) * kLdK + 16 * ks + (mi >> 1) * 8) * 2);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                if (nt > 2 * warp + 1) continue;  // only columns j <= i are needed
-                const uint32_t b0 = kw[(8 * nt + g) * ldw + kw0], b1 = kw[(8 * nt + g) * ldw + kw0 + 4];
-                mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+            for (int np = 0; np < 4; ++np) {
+                if (2 * np > 2 * warp + 1) continue;  // only columns j <= i are needed
+                // B fragments of key rows 16 np..16 np+15 (two 8-column tiles): (rows +0/+8) x (columns +0/+8)
+                uint32_t bf[4];
+                ldsm_x4(bf, kbase + ((16 * np + (mi >> 1) * 8 + ri) * kLdK + 16 * ks + (mi & 1) * 8) * 2);
+                mma_bf16_16816(acc[2 * np], af[0], af[1], af[2], af[3], bf[0], bf[1]);
+                mma_bf16_16816(acc[2 * np + 1], af[0], af[1], af[2], af[3], bf[2], bf[3]);
             }
         }
         __syncthreads();  // every warp has read K: its buffer becomes the L / X tile
@@ -281,16 +284,20 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             const int j0 = 32 * h + 8 * q;
+            const float4 b0 = *(const float4 *)(sh.beta + j0), b1 = *(const float4 *)(sh.beta + j0 + 4);
+            const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
             float xv[8], vu[8], vw[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int jj = j0 + u;
                 xv[u] = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                vw[u] = gr * sh.beta[jj] * xv[u];
+                vw[u] = gr * bj[u] * xv[u];
             }
             if (factored) {
+                const float4 c0 = *(const float4 *)(sh.br + j0), c1 = *(const float4 *)(sh.br + j0 + 4);
+                const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int u = 0; u < 8; ++u) vu[u] = gr * sh.br[j0 + u] * xv[u];  // x = 0 above the diagonal
+                for (int u = 0; u < 8; ++u) vu[u] = gr * cj[u] * xv[u];  // x = 0 above the diagonal
             } else {
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
