@@ -56,7 +56,7 @@ constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, s
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16
 constexpr uint32_t OFF_WS = OFF_P + 8192;                       // -W^T [128 (dk) x 64] bf16, MN-major
-// gate statistics per chunk: G, (unused), gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each.  A ring of
+// gate statistics per chunk: G, raw log-gate, gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each.  A ring of
 // four: the O epilogue of chunk c still reads its row factors while chunk c + 3 is loaded
 constexpr int kGateStages = 4;
 constexpr uint32_t kGateBytes = 1536;
@@ -65,7 +65,7 @@ constexpr uint32_t OFF_BAR = OFF_GATE + kGateStages * kGateBytes;
 constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320;
+constexpr int GT_G = 0, GT_GRAW = 64, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320;
 // G_C >= this: Gam_ij = gam_i * 2^-G_j with every factor inside the fp32 range
 constexpr float kFactorFloor = -100.f;
 
@@ -237,80 +237,121 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
 
     if (warp == 0) {
         // ================================================================ producer
+        // Keeps up to kStages chunks of loads in flight: a chunk's TMA boxes, and its raw log-gates
+        // by cp.async, are issued as soon as its stage is free; chunks are then landed in order
+        // (gate statistics, inert tail rows, FULL) as their loads complete.  Waiting for each
+        // chunk's loads before issuing the next would leave one chunk of HBM traffic in flight.
         bool ok = true;
-        int issued = 0, landed = 0;
-        for (int i = 0; i < nch && ok; ++i) {
-            const int c = cs + i, s = i % kStages;
-            if (i >= kStages) ok = mbar_wait(&bars[B_EMPTY + s], ((i / kStages) - 1) & 1, status, kStatusTimeout, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const int64_t t0 = bos + (int64_t)c * kChunk;
-            const int rows = rows_in(len, c);
-            const bool emit = emit_of(i);
-            uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-            if (lane == 0) {
-                const uint32_t bytes = 32768u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
-                mbar_arrive_expect_tx(&bars[B_TMA + s], bytes);
-                const int tt = (int)t0;
-                tma_load_3d(st + sK0, &m.k, 0, hq, tt, &bars[B_TMA + s]);
-                tma_load_3d(st + sK1, &m.k, 64, hq, tt, &bars[B_TMA + s]);
-                if (emit) {
-                    tma_load_3d(st + sQ0, &m.q, 0, hq, tt, &bars[B_TMA + s]);
-                    tma_load_3d(st + sQ1, &m.q, 64, hq, tt, &bars[B_TMA + s]);
+        int ni = 0, nl = 0;  // next chunk to issue, next chunk to land
+        uint64_t t_last = globaltimer();
+        uint32_t idle = 0;
+        auto rdy = [&](int b, int ph) {
+            return __shfl_sync(0xffffffffu, (int)mbar_test_wait(&bars[b], (uint32_t)ph & 1u), 0) != 0;
+        };
+        while (nl < nch) {
+            bool prog = false;
+            if (ni < nch && (ni < kStages || rdy(B_EMPTY + ni % kStages, ni / kStages - 1))) {
+                // ---- issue chunk ni (its stage and gate-ring entry are free: chunk ni - 3 is done)
+                const int c = cs + ni, s = ni % kStages;
+                const int64_t t0 = bos + (int64_t)c * kChunk;
+                const int rows = rows_in(len, c);
+                const bool emit = emit_of(ni);
+                uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
+                if (lane == 0) {
+                    const uint32_t bytes = 32768u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
+                    mbar_arrive_expect_tx(&bars[B_TMA + s], bytes);
+                    const int tt = (int)t0;
+                    tma_load_3d(st + sK0, &m.k, 0, hq, tt, &bars[B_TMA + s]);
+                    tma_load_3d(st + sK1, &m.k, 64, hq, tt, &bars[B_TMA + s]);
+                    if (emit) {
+                        tma_load_3d(st + sQ0, &m.q, 0, hq, tt, &bars[B_TMA + s]);
+                        tma_load_3d(st + sQ1, &m.q, 64, hq, tt, &bars[B_TMA + s]);
+                    }
+                    if (!zero_values) {
+                        tma_load_3d(st + sV0, &m.v, 0, hv, tt, &bars[B_TMA + s]);
+                        tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
+                    }
+                    // operand tiles of the chunk: rows (slot * HV + hv) * 128 + {0, 64}
+                    const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 128);
+                    tma_load_2d(st + sTU, &m.tiles, 0, trow, &bars[B_TMA + s]);
+                    tma_load_2d(st + sTW, &m.tiles, 0, trow + 64, &bars[B_TMA + s]);
                 }
-                if (!zero_values) {
-                    tma_load_3d(st + sV0, &m.v, 0, hv, tt, &bars[B_TMA + s]);
-                    tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
-                }
-                // operand tiles of the chunk: rows (slot * HV + hv) * 128 + {0, 64}
-                const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 128);
-                tma_load_2d(st + sTU, &m.tiles, 0, trow, &bars[B_TMA + s]);
-                tma_load_2d(st + sTW, &m.tiles, 0, trow + 64, &bars[B_TMA + s]);
-            }
-            ++issued;
-            // gate statistics while the tiles land: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
-            const int r0 = 2 * lane, r1 = r0 + 1;
-            const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2 : 0.f;
-            const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2 : 0.f;
-            float sp = g0 + g1;
+                // raw log-gates of rows 2l, 2l+1 into the chunk's gate block (zeros past the end)
+                float *graw = gates(ni) + GT_GRAW;
+                const float *gsrc = a.g + (size_t)t0 * HV + hv;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, sp, off);
-                if (lane >= off) sp += y;
-            }
-            const float G0 = sp - g1, G1 = sp;
-            const float GC = __shfl_sync(0xffffffffu, sp, 31);
-            float *gt = gates(i);
-            const float gm0 = ex2(G0), gm1 = ex2(G1);
-            *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
-            *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
-            *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
-            *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
-            *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
-            ok = mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ++landed;
-            if (rows < kChunk) {
-                // rows past the end of the sequence belong to the next one: make them inert zeros
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                const int nz = (kChunk - rows) * 8;  // 16-byte pieces per box
-#pragma unroll
-                for (int bx = 0; bx < 6; ++bx) {
-                    if ((bx == 2 || bx == 3) && !emit) continue;
-                    if (bx >= 4 && zero_values) continue;
-                    const uint32_t boff = bx == 0 ? sK0 : bx == 1 ? sK1 : bx == 2 ? sQ0 : bx == 3 ? sQ1 : bx == 4 ? sV0 : sV1;
-                    uint4 *p = (uint4 *)(st + boff + rows * 128);
-                    for (int e = lane; e < nz; e += 32) p[e] = z;
+                for (int u = 0; u < 2; ++u) {
+                    const int r = 2 * lane + u;
+                    cp_async4(graw + r, gsrc + (size_t)(r < rows ? r : 0) * HV, r < rows ? 4u : 0u);
                 }
-                fence_proxy_async();
+                cp_async_commit();
+                ++ni;
+                prog = true;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_FULL + s]);
+            if (nl < ni && rdy(B_TMA + nl % kStages, nl / kStages)) {
+                // ---- land chunk nl: its raw gates are in once at most ni - nl - 1 younger groups are pending
+                const int younger = ni - nl - 1;
+                if (younger >= 2) cp_async_wait<2>();
+                else if (younger == 1) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                const int c = cs + nl, s = nl % kStages;
+                const int rows = rows_in(len, c);
+                float *gt = gates(nl);
+                // gate statistics: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
+                const int r0 = 2 * lane, r1 = r0 + 1;
+                const float2 gr = *(const float2 *)(gt + GT_GRAW + r0);
+                const float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
+                float sp = g0 + g1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, sp, off);
+                    if (lane >= off) sp += y;
+                }
+                const float G0 = sp - g1, G1 = sp;
+                const float GC = __shfl_sync(0xffffffffu, sp, 31);
+                const float gm0 = ex2(G0), gm1 = ex2(G1);
+                *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
+                *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
+                *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
+                *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
+                *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
+                if (rows < kChunk) {
+                    // rows past the end of the sequence belong to the next one: make them inert zeros
+                    uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
+                    const bool emit = emit_of(nl);
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    const int nz = (kChunk - rows) * 8;  // 16-byte pieces per box
+#pragma unroll 1
+                    for (int bx = 0; bx < 6; ++bx) {
+                        if ((bx == 2 || bx == 3) && !emit) continue;
+                        if (bx >= 4 && zero_values) continue;
+                        const uint32_t boff = bx == 0 ? sK0 : bx == 1 ? sK1 : bx == 2 ? sQ0 : bx == 3 ? sQ1 : bx == 4 ? sV0 : sV1;
+                        uint4 *p = (uint4 *)(st + boff + rows * 128);
+                        for (int e = lane; e < nz; e += 32) p[e] = z;
+                    }
+                    fence_proxy_async();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_FULL + s]);
+                ++nl;
+                prog = true;
+            }
+            if (prog) {
+                idle = 0;
+                t_last = globaltimer();
+            } else {
+                __nanosleep(32);
+                if ((++idle & 255u) == 0 && __shfl_sync(0xffffffffu, (int)(globaltimer() - t_last > kWaitNs), 0)) {
+                    ok = false;
+                    break;
+                }
+            }
         }
+        if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
         // copies still in flight after a failure land before the CTA releases its shared memory
-        for (int i = landed; i < issued; ++i)
+        for (int i = nl; i < ni; ++i)
             mbar_wait(&bars[B_TMA + i % kStages], (i / kStages) & 1, status, kStatusTimeout, kWaitNs);
+        cp_async_wait<0>();
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         // A fixed program per chunk, ordered around the serial chain: each chain product is
@@ -410,7 +451,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     mma_commit(&bars[B_VPF]);
                 }
                 __syncwarp();
-                kq_upto(c + 1, false);
                 if (em) {
                     // ---- O^T = S^T Q^T, or S^T Q~^T for a steep chunk (S^T is read before the chain
                     //      overwrites it: SF commits after it); the raw Q of a factored chunk is ready

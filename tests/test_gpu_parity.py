@@ -84,6 +84,10 @@ SMALL = {
     "bf16_strong_decay": Workload("bf16_strong_decay", B=1, T=300, H=2, K=128, V=128, g_mu=-2.0, h0=True,
                                   seed=17),
     "bf16_no_decay": Workload("bf16_no_decay", B=1, T=700, H=2, K=128, V=128, g_mu=30.0, h0=True, seed=18),
+    # chunk decays on both sides of 2^-100 (7 of 26 chunks above it): the tensor-core scan's factored
+    # output form and its direct form for steep chunks alternate within one sequence
+    "bf16_mixed_decay": Workload("bf16_mixed_decay", B=1, T=64 * 12 + 5, H=2, K=128, V=128, g_mu=-0.6,
+                                 g_sigma=1.0, h0=True, seed=20),
 }
 
 
