@@ -80,7 +80,7 @@ enum Bar {
 static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");  // + TMEM slot, cs, c0, c1
 
 struct TcMaps {
-    CUtensorMap q, k, v, tiles;
+    CUtensorMap q, k, v, o, tiles;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -172,15 +172,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         int c0 = seg * a.seg_chunks, c1 = min(c0 + a.seg_chunks, NT), cs = c0;
         if (fwd && a.warm_in_kernel) {
             // Warmup split with balanced segments: the boundary at nominal chunk c moves to
-            // c + w / 2, w = c - (warmup start of c), capped at half a segment, so that the segment
-            // after it (which also scans its warmup) and the one before do about equal work.
+            // c + w / 4, w = c - (warmup start of c) capped at a segment, so that the segment after
+            // it (which also scans its warmup) and the one before do about equal work: a warmup chunk
+            // costs about half an emitted one (no q, no output products, no P, no O epilogue).
             const int L = a.seg_chunks;
             auto bnd = [&](int j) -> int {
                 const int cj = j * L;
                 if (j == 0) return 0;
                 if (cj >= NT) return NT;
                 const int w = cj - warm_start_of(a.g, bos, len, HV, hv, cj, a.warm_log2_eps);
-                return min(cj + min(w, L) / 2, NT);
+                return min(cj + (min(w, L) + 2) / 4, NT);
             };
             c0 = bnd(seg);
             c1 = bnd(seg + 1);
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         for (int j = 0; j < kStages; ++j) {
             mbar_init(&bars[B_TMA + j], 1);
             mbar_init(&bars[B_FULL + j], 1);
-            mbar_init(&bars[B_EMPTY + j], 1);
+            mbar_init(&bars[B_EMPTY + j], 2);  // the issuer's commit and the output warps' O store
             mbar_init(&bars[B_QS + j], 2);
         }
         mbar_init(&bars[B_KQF], 1);
@@ -780,9 +781,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_WC]);
             }
-            if (it >= 1 && emit_of(it - 1)) {
+            if (it >= 1 && !emit_of(it - 1)) {
+                if (et == 0) mbar_arrive(&bars[B_EMPTY + (it - 1) % kStages]);  // nothing to store
+            } else if (it >= 1) {
                 // ---- O of chunk it - 1 (lane = dv)
-                const int c = cs + it - 1;
+                const int ci = it - 1, c = cs + ci;
                 const int64_t t0 = bos + (int64_t)c * kChunk;
                 const int rows = rows_in(len, c);
                 ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
@@ -793,8 +796,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld32(tl + TM_O, r);
                 tmem_ld32(tl + TM_O + 32, r + 32);
                 tmem_ld_wait();
-                const float *gt = gates(it - 1);
-                if (factored(it - 1)) {
+                const float *gt = gates(ci);
+                if (factored(ci)) {
                     // the row factors scale * gam_t of the factored form
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
@@ -810,15 +813,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 // O region drained and the chunk's gate block read (the producer reuses it after the
                 // next chunk's S^T Q^T product, which waits for this)
                 if (lane == 0) mbar_arrive(&bars[B_OE]);
-                __nv_bfloat16 *og = (__nv_bfloat16 *)a.o + ((size_t)t0 * HV + hv) * V + et;
-                const size_t ostride = (size_t)HV * V;
-                {
-                    __nv_bfloat16 *p = og;  // (incremented pointer: keeps the unrolled stores compact)
+                if (rows == kChunk) {
+                    // the O tile goes out by TMA from the chunk's Q boxes, which are dead now (both
+                    // products reading them have completed): bf16, 128-byte swizzled rows of 64 dv
+                    uint8_t *ob = sm + OFF_STAGE + (ci % kStages) * kStageBytes + (et >= 64 ? sQ1 : sQ0);
+                    const int cd = et & 63;
+                    uint32_t off[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) off[jj] = ((((uint32_t)cd >> 3) ^ (uint32_t)jj) << 4) + ((uint32_t)(cd & 7) << 1);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        *(__nv_bfloat16 *)(ob + j * 128 + off[j & 7]) = __float2bfloat16_rn(u2f(r[j]));
+                    fence_proxy_async();
+                    bar_sync(1, 128);  // the four output warps
+                    if (et == 0) {
+                        uint8_t *st = sm + OFF_STAGE + (ci % kStages) * kStageBytes;
+                        tma_store_3d(&m.o, st + sQ0, 0, hv, (int)t0);
+                        tma_store_3d(&m.o, st + sQ1, 64, hv, (int)t0);
+                        tma_store_commit();
+                        tma_store_wait_read0();  // the stage may be reloaded once the copy has read it
+                        mbar_arrive(&bars[B_EMPTY + ci % kStages]);
+                    }
+                } else {
+                    // ragged tail chunk: only the sequence's own rows are written
+                    __nv_bfloat16 *p = (__nv_bfloat16 *)a.o + ((size_t)t0 * HV + hv) * V + et;
+                    const size_t ostride = (size_t)HV * V;
 #pragma unroll
                     for (int j = 0; j < 64; ++j) {
                         if (j < rows) *p = __float2bfloat16_rn(u2f(r[j]));
                         p += ostride;
                     }
+                    if (et == 0) mbar_arrive(&bars[B_EMPTY + ci % kStages]);
                 }
                 ++e;
             }
@@ -906,7 +931,7 @@ cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st)
     const int64_t rows = (int64_t)a.B * a.T;
     if (rows > 0) {
         if (!make_map(&maps.q, a.q, a.H, rows) || !make_map(&maps.k, a.k, a.H, rows) ||
-            !make_map(&maps.v, a.v, a.HV, rows) ||
+            !make_map(&maps.v, a.v, a.HV, rows) || !make_map(&maps.o, a.o, a.HV, rows) ||
             !make_tiles_map(&maps.tiles, a.tiles, (int64_t)a.tile_slots * a.HV * 128))
             return cudaErrorInvalidValue;
     }
