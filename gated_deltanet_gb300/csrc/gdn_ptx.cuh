@@ -133,6 +133,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
                  : "memory");
 }
+// true on one lane of a converged warp
+__device__ __forceinline__ bool elect_one_sync()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
 // 4-byte asynchronous global -> shared copy; src_bytes = 0 writes a zero and reads nothing
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem, uint32_t src_bytes)
 {

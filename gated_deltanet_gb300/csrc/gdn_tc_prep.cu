@@ -20,17 +20,20 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreadsPrep = 128;
-constexpr int kLdK = 136;  // bf16 row pitch of the K tile (272 B: conflict-free fragment loads)
 constexpr int kLdX = 68;   // fp32 row pitch of the L / X tile
+constexpr uint32_t kTmemCols = 64;  // the K K^T accumulator; eight CTAs per SM fill the 512 columns
 constexpr float kFactorFloor = -100.f;  // G_C >= this: Gam_ij = gam_i * 2^-G_j without overflow
 
 struct PrepSmem {
     union {
-        __nv_bfloat16 k[64 * kLdK];  // the chunk's K rows, until K K^T is formed
-        float lx[64 * kLdX];         // then L in the lower triangle, X^T in the upper:
-                                     // X(r, j), j < r, at lx[j * kLdX + r]
+        // the chunk's K rows, 128-byte swizzled boxes of 64 rows x 64 dk (dk 0-63, then 64-127), until
+        // K K^T is formed; the 128-row operand of the product reads one box past the second (24 KB)
+        __align__(1024) uint8_t k[24576];
+        float lx[64 * kLdX];  // then L in the lower triangle, X^T in the upper: X(r, j), j < r, at lx[j * kLdX + r]
     };
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
+    uint64_t bar;
+    uint32_t tslot;
 };
 
 __device__ __forceinline__ int rows_in(int64_t len, int c)
@@ -41,7 +44,7 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 
 __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a)
 {
-    __shared__ __align__(16) PrepSmem sh;
+    __shared__ __align__(1024) PrepSmem sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slot = blockIdx.x, hv = blockIdx.y;
     const int HV = a.HV, hq = hv / (HV / a.H);
@@ -61,7 +64,12 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     const int64_t t0 = bos + (int64_t)c * kChunk;
     float *lx = sh.lx;
 
-    // ---- K rows (rows past the end of the sequence are zero), gates
+    if (warp == 0) tmem_alloc(&sh.tslot, kTmemCols);
+    if (tid == 32) {
+        mbar_init(&sh.bar, 1);
+        fence_mbar_init();
+    }
+    // ---- K rows into the swizzled boxes (rows past the end of the sequence are zero), gates
     {
         const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k;
 #pragma unroll
@@ -69,8 +77,9 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (r < rows) v = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
-            *(uint4 *)(sh.k + r * kLdK + ch * 8) = v;
+            *(uint4 *)(sh.k + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
         }
+        fence_proxy_async();  // the tensor core reads them
     }
     if (warp == 0) {
         const int r0 = 2 * lane, r1 = r0 + 1;
@@ -101,48 +110,61 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     }
     __syncthreads();
 
-    // ---- L = beta_i (K K^T)[i, j < i] on the tensor cores (bf16 m16n8k16); warp = 16 rows
-    {
-        const int g = lane >> 2, t = lane & 3, m0 = 16 * warp;
-        const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: this lane addresses row ri of matrix mi
-        const uint32_t kbase = smem_u32(sh.k);
-        float acc[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            // A fragment of rows m0..m0+15, columns 16 ks..16 ks+15: matrices (rows +0/+8) x (columns +0/+8)
-            uint32_t af[4];
-            ldsm_x4(af, kbase + ((m0 + (mi & 1) * 8 + ri) * kLdK + 16 * ks + (mi >> 1) * 8) * 2);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                if (2 * np > 2 * warp + 1) continue;  // only columns j <= i are needed
-                // B fragments of key rows 16 np..16 np+15 (two 8-column tiles): (rows +0/+8) x (columns +0/+8)
-                uint32_t bf[4];
-                ldsm_x4(bf, kbase + ((16 * np + (mi >> 1) * 8 + ri) * kLdK + 16 * ks + (mi & 1) * 8) * 2);
-                mma_bf16_16816(acc[2 * np], af[0], af[1], af[2], af[3], bf[0], bf[1]);
-                mma_bf16_16816(acc[2 * np + 1], af[0], af[1], af[2], af[3], bf[2], bf[3]);
-            }
-        }
-        __syncthreads();  // every warp has read K: its buffer becomes the L / X tile
-        float bdiag = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            if (nt > 2 * warp + 1) continue;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = m0 + g + 8 * (q >> 1), j = 8 * nt + 2 * t + (q & 1);
-                const float v = sh.beta[i] * acc[nt][q];
-                if (j < i) lx[i * kLdX + j] = v;
-                if (j == i) bdiag = fmaxf(bdiag, v);
-            }
-        }
-        // beta ||k||^2 <= 2 keeps every transition non-expansive (warmup split)
-        if (a.check_norm && bdiag > 2.0001f) atomicOr(a.status, kStatusNormBound);
-    }
+    // ---- K K^T on the tensor core: one M = 128 product ([K; next box] K^T, lanes 0-63 hold K K^T);
+    //      L row r = beta_r (K K^T)[r, :] straight from tensor memory (the upper triangle is
+    //      overwritten by X^T later and never read before)
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = sh.tslot;
+    if (warp == 0) {
+        const uint32_t kb = smem_u32(sh.k);
+        const uint32_t idKK = idesc_bf16_f32(128, 64, 0, 0);
+        if (elect_one_sync()) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t d = sdesc_sw128(kb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+                mma_ss(tb, d, d, idKK, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&sh.bar);
+        }
+        __syncwarp();
+    }
+    if (warp < 2) {
+        const bool ok = mbar_wait(&sh.bar, 0, a.status, kStatusTimeout, 2000000000ull);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc_fence_after();
+            const int r = 32 * warp + lane;
+            const float br_ = sh.beta[r];
+            float *lr = lx + r * kLdX;
+            float diag = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t d[32];
+                tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32 * h, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float4 v;
+                    v.x = br_ * __uint_as_float(d[4 * j4]);
+                    v.y = br_ * __uint_as_float(d[4 * j4 + 1]);
+                    v.z = br_ * __uint_as_float(d[4 * j4 + 2]);
+                    v.w = br_ * __uint_as_float(d[4 * j4 + 3]);
+                    if (32 * h + 4 * j4 == (r & ~3))
+                        diag = (r & 3) == 0 ? v.x : (r & 3) == 1 ? v.y : (r & 3) == 2 ? v.z : v.w;
+                    *(float4 *)(lr + 32 * h + 4 * j4) = v;
+                }
+            }
+            // beta ||k||^2 <= 2 keeps every transition non-expansive (warmup split)
+            if (a.check_norm && diag > 2.0001f) atomicOr(a.status, kStatusNormBound);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, kTmemCols);
+    }
 
     auto Lx = [&](int r, int j) -> float { return lx[r * kLdX + j]; };
     auto Xt = [&](int r, int j) -> float { return lx[j * kLdX + r]; };  // X(r, j), j < r
