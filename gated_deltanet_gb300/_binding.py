@@ -32,7 +32,8 @@ class GdnShape(ctypes.Structure):
 class GdnOptions(ctypes.Structure):
     _fields_ = [("cp_mode", ctypes.c_int), ("segment_chunks", ctypes.c_int), ("engine", ctypes.c_int),
                 ("keys_unit_norm", ctypes.c_int), ("warmup_log2_eps", ctypes.c_float),
-                ("max_seq_len", ctypes.c_int)]
+                ("max_seq_len", ctypes.c_int), ("launch_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("n_launch_events", ctypes.c_int)]
 
 
 class GdnPlanInfo(ctypes.Structure):
@@ -98,9 +99,17 @@ def _dtype_code(t: torch.dtype) -> int:
 
 
 def make_options(cp_mode="auto", engine="auto", keys_unit_norm=False, segment_chunks=0,
-                 warmup_log2_eps=0.0, max_seq_len=0) -> GdnOptions:
-    return GdnOptions(CP_MODES[cp_mode], int(segment_chunks), ENGINES[engine], int(bool(keys_unit_norm)),
-                      float(warmup_log2_eps), int(max_seq_len))
+                 warmup_log2_eps=0.0, max_seq_len=0, launch_events=None) -> GdnOptions:
+    """``launch_events``: optional sequence of raw CUDA event handles (ints) to be recorded
+    around each kernel launch (see ``gdn_options.launch_events`` in ``include/gdn.h``)."""
+    opt = GdnOptions(CP_MODES[cp_mode], int(segment_chunks), ENGINES[engine], int(bool(keys_unit_norm)),
+                     float(warmup_log2_eps), int(max_seq_len), None, 0)
+    if launch_events:
+        arr = (ctypes.c_void_p * len(launch_events))(*[int(h) for h in launch_events])
+        opt._events_keepalive = arr  # the array lives as long as the options
+        opt.launch_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        opt.n_launch_events = len(launch_events)
+    return opt
 
 
 def make_shape(q, v, g, cu_seqlens, B=None) -> GdnShape:
@@ -123,7 +132,7 @@ def _check(code: int, what: str):
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
                            cu_seqlens=None, chunk_size=64, *, cp_mode="auto", engine="auto",
                            keys_unit_norm=False, segment_chunks=0, warmup_log2_eps=0.0, max_seq_len=0,
-                           workspace=None, out=None, final_state=None):
+                           workspace=None, out=None, final_state=None, launch_events=None):
     """Gated delta-rule chunked-prefill forward on the GPU.
 
     q, k [B,T,H,K]; v [B,T,HV,V] (float32 or bfloat16, same dtype); g [B,T,HV]
@@ -154,7 +163,8 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     if output_final_state:
         ht = final_state if final_state is not None else torch.empty(
             s.num_seqs, s.HV, s.K, s.V, dtype=torch.float32, device=q.device)
-    opt = make_options(cp_mode, engine, keys_unit_norm, segment_chunks, warmup_log2_eps, max_seq_len)
+    opt = make_options(cp_mode, engine, keys_unit_norm, segment_chunks, warmup_log2_eps, max_seq_len,
+                       launch_events)
     L = lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
     with torch.cuda.device(q.device):

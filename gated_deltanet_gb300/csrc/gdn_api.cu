@@ -189,6 +189,13 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     a.mode = kModeForward; a.vext = s->V; a.status = status;
 
     cudaError_t e = cudaSuccess;
+    // optional per-kernel timing marks on the caller's events
+    int n_marks = 0;
+    auto mark = [&]() {
+        if (opt.launch_events && n_marks < opt.n_launch_events && opt.launch_events[n_marks])
+            cudaEventRecord((cudaEvent_t)opt.launch_events[n_marks], stream);
+        ++n_marks;
+    };
     const bool tc = p.engine == GDN_ENGINE_TC;
     if (tc) {
         PrepArgs pa{};
@@ -197,6 +204,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         pa.T = s->T; pa.H = s->H; pa.HV = s->HV; pa.N = N; pa.slots = (int)p.tile_slots;
         pa.check_norm = p.cp == GDN_CP_WARMUP;
         pa.status = status;
+        mark();
         e = launch_tc_prep(pa, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         a.tiles = pa.tiles;
@@ -218,6 +226,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         gs.channel = s->gate_kind == GDN_GATE_CHANNEL;
         gs.log2_eps = p.log2_eps;
         gs.max_warm_chunks = 1 << 30;
+        mark();
         e = launch_gate_stats(gs, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         a.warm_start = gs.warm_start;
@@ -226,6 +235,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         pre.mode = kModePrepass;
         pre.vext = s->V + s->K;
         pre.seg_out = (float *)(wsb + p.off_segout);
+        mark();
         e = scan_prepass(pre, tc, s, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         CombineArgs cb{};
@@ -233,12 +243,15 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         cb.seg_init = (float *)(wsb + p.off_seginit);
         cb.T = s->T; cb.HV = s->HV; cb.K = s->K; cb.V = s->V; cb.N = N;
         cb.seg_chunks = p.seg_chunks; cb.n_seg = p.n_seg; cb.status = status;
+        mark();
         e = launch_cp_combine(cb, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         a.seg_init = cb.seg_init;
     }
+    mark();
     e = scan(a);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
+    mark();
     return GDN_OK;
 }
 

@@ -102,6 +102,12 @@ typedef struct {
     float warmup_log2_eps; /* warmup stops once the window's decay <= 2^this (0 = -24) */
     int max_seq_len;       /* packed input: bound on one sequence's length, used to
                               size the split grid (0 = T)                             */
+    void *const *launch_events; /* optional, caller-owned CUDA events (cudaEvent_t):
+                              event i is recorded on the stream right before the
+                              call's i-th kernel launch and event `kernels` (see
+                              gdn_plan) right after the last one, so consecutive
+                              events time each kernel.  NULL: nothing recorded.   */
+    int n_launch_events;   /* length of launch_events; extra marks are skipped      */
 } gdn_options;
 
 /* Fill `opt` with the defaults (AUTO everywhere, no assertions). */
