@@ -206,7 +206,7 @@ def run_ours(args):
         gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
                                    x["cu_seqlens"], out=o, final_state=ht,
                                    max_seq_len=(w.T if w.varlen else 0),
-                                   launch_events=[ev.cuda_event for ev in evs] if evs else None, **opts)
+                                   launch_events=evs, **opts)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -217,8 +217,10 @@ def run_ours(args):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    # per-kernel marks: the library records them on this stream around each of its launches
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(info.kernels + 1)] for _ in range(args.steps)]
+    # per-kernel marks: the library records them on this stream between its launches (the
+    # step's own start and end events bound the first and the last launch)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(max(info.kernels - 1, 0))]
+           for _ in range(args.steps)]
     for evs in kev:
         for ev in evs:
             ev.record(stream)  # creates the event; the library re-records it inside each timed step
@@ -232,7 +234,7 @@ def run_ours(args):
     for i in range(args.steps):
         flush.zero_()                      # L2 flushed between timed steps (not timed)
         starts[i].record(stream)
-        step(kev[i])
+        step([0] + [ev.cuda_event for ev in kev[i]] + [0])
         ends[i].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -240,7 +242,8 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
-    kernel_ms = [sum(kev[i][j].elapsed_time(kev[i][j + 1]) for i in range(args.steps)) / args.steps
+    marks = [[starts[i]] + kev[i] + [ends[i]] for i in range(args.steps)]
+    kernel_ms = [sum(marks[i][j].elapsed_time(marks[i][j + 1]) for i in range(args.steps)) / args.steps
                  for j in range(info.kernels)]
     dev_ms = max_over_ranks(sum(per_step), dev)
     status = gdn.read_device_status()
