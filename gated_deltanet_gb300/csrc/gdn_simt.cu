@@ -23,9 +23,11 @@
 // k = q = v = 0, g = 0, beta = 0, which makes them inert, so the decay to the
 // chunk end uses the last valid token (same walkthrough, last_idx).
 #include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
 
 namespace gdn {
 namespace {
+using ptx::ex2;  // the MUFU base-2 exponential (a handful of ulp; inputs are log-gate sums)
 
 constexpr int kBV = 32;
 constexpr int kThreads = 256;
@@ -192,10 +194,10 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
                         const float gr = sG[j0 * KP + d];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const float fi = exp2f(sG[(i0 + u) * KP + d] - gr);
+                            const float fi = ex2(sG[(i0 + u) * KP + d] - gr);
                             ki[u] = sK[(i0 + u) * KP + d] * fi;
                             qi[u] = sQ[(i0 + u) * KP + d] * fi;
-                            kj[u] = sK[(j0 + u) * KP + d] * exp2f(gr - sG[(j0 + u) * KP + d]);
+                            kj[u] = sK[(j0 + u) * KP + d] * ex2(gr - sG[(j0 + u) * KP + d]);
                         }
                     } else {
 #pragma unroll
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
                         const int i = i0 + u, j = j0 + w;
                         float lv = 0.f, pv = 0.f;
                         if (j <= i) {
-                            const float gf = CHANNEL ? 1.f : exp2f(sG[i] - sG[j]);
+                            const float gf = CHANNEL ? 1.f : ex2(sG[i] - sG[j]);
                             if (j < i) lv = sB[i] * gf * ak[u][w];
                             pv = gf * aq[u][w];
                         }
@@ -244,9 +246,9 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
             for (int e = tid; e < 64 * K; e += kThreads) {
                 const int r = e / K, d = e % K;
                 const float G = sG[r * KP + d], kv = sK[r * KP + d];
-                sG[r * KP + d] = kv * exp2f(sGC[d] - G);  // k * 2^(G_C - G): state write
-                sK[r * KP + d] = kv * exp2f(G);           // k * 2^G: read-out of the old state
-                if (emit) sQ[r * KP + d] *= exp2f(G);     // q * 2^G: inter-chunk output
+                sG[r * KP + d] = kv * ex2(sGC[d] - G);  // k * 2^(G_C - G): state write
+                sK[r * KP + d] = kv * ex2(G);           // k * 2^G: read-out of the old state
+                if (emit) sQ[r * KP + d] *= ex2(G);     // q * 2^G: inter-chunk output
             }
         }
 
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = r0 + u;
-                const float ks = CHANNEL ? acc[u] : exp2f(sG[i]) * acc[u];
+                const float ks = CHANNEL ? acc[u] : ex2(sG[i]) * acc[u];
                 sV[i * kBV + cc] = sB[i] * (sV[i * kBV + cc] - ks);
             }
         }
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
                 for (int u = 0; u < 8; ++u) {
                     const int i = r0 + u;
                     if (i < nrow) {
-                        const float inter = CHANNEL ? acc[u] : exp2f(sG[i]) * acc[u];
+                        const float inter = CHANNEL ? acc[u] : ex2(sG[i]) * acc[u];
                         from_f(o + ((size_t)(t0 + i) * a.HV + hv) * V + col, a.scale * (inter + acc2[u]));
                     }
                 }
@@ -343,12 +345,12 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
 #pragma unroll
             for (int m = 0; m < DPT; ++m) {
                 const int d = dr + 8 * m;
-                const float decay = exp2f(CHANNEL ? sGC[d] : sGC[0]);
+                const float decay = ex2(CHANNEL ? sGC[d] : sGC[0]);
                 acc[m] = decay * sS[d * kBV + cc];
             }
             for (int j = 0; j < 64; ++j) {
                 const float vp = sVp[j * kBV + cc];
-                const float rowf = CHANNEL ? 1.f : exp2f(sGC[0] - sG[j]);
+                const float rowf = CHANNEL ? 1.f : ex2(sGC[0] - sG[j]);
 #pragma unroll
                 for (int m = 0; m < DPT; ++m) {
                     const int d = dr + 8 * m;
