@@ -97,7 +97,7 @@ def test_small_cases(gdn, name):
 
 
 @pytest.mark.parametrize("engine", ["simt", "tc"])
-@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_T65"])
+@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_T65", "bf16_gva"])
 def test_engines_match_oracle(gdn, engine, name):
     check(gdn, SMALL[name], engine=engine)
 
