@@ -23,7 +23,8 @@ struct Plan {
     int seg_chunks, n_seg, value_tiles, kernels, max_nt;
     float log2_eps;
     // workspace layout
-    size_t off_warm, off_segout, off_seginit, off_tiles, tile_slots, bytes;
+    size_t off_warm, off_segout, off_seginit, off_tiles, off_gc, tile_slots, bytes;
+    bool kda;  // tensor-core engine with per-channel gates
 };
 
 bool is_varlen(const gdn_shape *s, const int64_t *cu) { return cu != nullptr; }
@@ -65,9 +66,12 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     const int max_nt = ceil_div(maxlen, kChunk);
 
     *p = Plan{};
-    const bool tc_ok = tc_shape_ok(s);
+    const bool channel = s->gate_kind == GDN_GATE_CHANNEL;
+    // per-channel gates on the tensor-core engine run without the chunk-parallel split
+    const bool tc_ok = tc_shape_ok(s) && !(channel && (opt.cp_mode == GDN_CP_EXACT || opt.cp_mode == GDN_CP_WARMUP));
     if (opt.engine == GDN_ENGINE_TC && !tc_ok) return GDN_ERR_UNSUPPORTED;
     p->engine = (opt.engine != GDN_ENGINE_SIMT && tc_ok) ? GDN_ENGINE_TC : GDN_ENGINE_SIMT;
+    p->kda = p->engine == GDN_ENGINE_TC && channel;
     p->value_tiles = p->engine == GDN_ENGINE_TC ? 1 : ceil_div(s->V, 32);
     p->max_nt = max_nt;
     p->log2_eps = opt.warmup_log2_eps < 0.f ? opt.warmup_log2_eps : -24.f;
@@ -84,7 +88,7 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         if (pairs > 0 && opt.keys_unit_norm && base * 2 <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
         else if (pairs > 0 && base * 4 <= num_sms && max_nt >= 16) cp = GDN_CP_EXACT;
     }
-    if (max_nt <= 1) cp = GDN_CP_OFF;
+    if (max_nt <= 1 || p->kda) cp = GDN_CP_OFF;
     int L;
     if (cp == GDN_CP_OFF) {
         L = std::max(max_nt, 1);
@@ -106,12 +110,18 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     if (p->n_seg == 1 && cp != GDN_CP_OFF) { p->cp = GDN_CP_OFF; cp = GDN_CP_OFF; p->seg_chunks = std::max(max_nt, 1); }
 
     size_t off = kStatusBytes;
-    p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->tile_slots = 0;
+    p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->off_gc = p->tile_slots = 0;
     if (p->engine == GDN_ENGINE_TC) {
         // operand tiles of every chunk, written by the preparation kernel
         p->tile_slots = (size_t)tile_slots((int64_t)s->B * s->T, N);
         p->off_tiles = off;
-        off = align_up(off + p->tile_slots * s->HV * kTcTileBytesPerChunk, 256);
+        if (p->kda) {
+            off = align_up(off + p->tile_slots * s->HV * (kKdaTileBytesPerChunk - 512), 256);
+            p->off_gc = off;
+            off = align_up(off + p->tile_slots * s->HV * 512, 256);
+        } else {
+            off = align_up(off + p->tile_slots * s->HV * kTcTileBytesPerChunk, 256);
+        }
     }
     const size_t nsegs = (size_t)N * s->HV * p->n_seg;
     if (cp == GDN_CP_WARMUP && p->engine == GDN_ENGINE_TC) {
@@ -153,7 +163,7 @@ gdn_status check_ptrs(const gdn_shape *s, const void *q, const void *k, const vo
 
 cudaError_t scan_prepass(const ScanArgs &pre, bool tc, const gdn_shape *s, cudaStream_t stream)
 {
-    if (tc) return launch_tc_scan(pre, 2, stream);
+    if (tc) return launch_tc_scan(pre, 2, false, stream);
     return launch_simt_scan(pre, s->qkv_dtype, s->gate_kind, stream);
 }
 
@@ -197,7 +207,19 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         ++n_marks;
     };
     const bool tc = p.engine == GDN_ENGINE_TC;
-    if (tc) {
+    if (tc && p.kda) {
+        KdaPrepArgs ka{};
+        ka.q = q; ka.k = k; ka.v = v; ka.gk = g; ka.beta = beta; ka.scale = scale; ka.cu_seqlens = cu;
+        ka.tiles = wsb + p.off_tiles;
+        ka.gc = (float *)(wsb + p.off_gc);
+        ka.T = s->T; ka.H = s->H; ka.HV = s->HV; ka.N = N; ka.slots = (int)p.tile_slots;
+        mark();
+        e = launch_kda_prep(ka, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        a.tiles = ka.tiles;
+        a.tile_slots = ka.slots;
+        a.kda_gc = ka.gc;
+    } else if (tc) {
         PrepArgs pa{};
         pa.k = k; pa.g = g; pa.beta = beta; pa.cu_seqlens = cu;
         pa.tiles = wsb + p.off_tiles;
@@ -211,7 +233,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         a.tile_slots = pa.slots;
     }
     auto scan = [&](const ScanArgs &sa) -> cudaError_t {
-        if (tc) return launch_tc_scan(sa, sa.mode == kModePrepass ? 2 : 1, stream);
+        if (tc) return launch_tc_scan(sa, sa.mode == kModePrepass ? 2 : 1, p.kda, stream);
         return launch_simt_scan(sa, s->qkv_dtype, s->gate_kind, stream);
     };
     if (p.cp == GDN_CP_WARMUP && tc) {

@@ -37,7 +37,8 @@ struct ScanArgs {
     const int *warm_start;  // [N*HV*n_seg] first chunk a segment processes (warmup), nullable
     int warm_in_kernel;     // tensor-core engine: each CTA finds its own warmup start from g
     float warm_log2_eps;    // threshold of that search (accumulated log2-decay)
-    const void *tiles;      // tensor-core engine: operand tiles of tc_prep_kernel (see tile_slot)
+    const void *tiles;      // tensor-core engine: operand tiles of tc_prep_kernel / kda_prep_kernel (see tile_slot)
+    const float *kda_gc;    // per-channel gates: 2^G_C per (slot, value head, channel)
     int tile_slots;         //   chunk slots of that buffer
     const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
     float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
@@ -86,7 +87,20 @@ size_t simt_smem_bytes(int K, gdn_gate_kind gate);
 // the forward pass and 2 for the exact split's pre-pass (S* and M columns).
 bool tc_shape_ok(const gdn_shape *s);
 bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o);
-cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st);
+// Per-key-channel gates on the tensor-core engine: the chunk preparation (gdn_tc_kda.cu).
+struct KdaPrepArgs {
+    const void *q, *k, *v;
+    const float *gk, *beta;     // gk [B*T][HV][128]
+    float scale;
+    const int64_t *cu_seqlens;  // nullable
+    void *tiles;                // bf16 [slot][HV][9][64][64] (see gdn_tc_kda.cu)
+    float *gc;                  // [slot][HV][128] per-channel chunk decay 2^G_C
+    int T, H, HV, N, slots;
+};
+cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st);
+constexpr size_t kKdaTileBytesPerChunk = 9 * 64 * 64 * 2 + 128 * 4;  // nine bf16 boxes and gC
+
+cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st);
 cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st);
 constexpr size_t kTcTileBytesPerChunk = 2 * 64 * 64 * 2;  // T_U and T_W, bf16
 

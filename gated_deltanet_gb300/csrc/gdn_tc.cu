@@ -49,20 +49,26 @@ constexpr int kStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-// stage: K0 | Q0 | K1 | Q1 | V0 | V1 | T_U | T_W, 8 KB each (64 rows x 64 bf16, 128-byte swizzle)
-constexpr uint32_t kStageBytes = 65536;
+// stage: K0 | Q0 | K1 | Q1 | V0 | V1 | T_U | T_W, 8 KB each (64 rows x 64 bf16, 128-byte swizzle).
+// Per-channel gates (KDA): K^0 | Q~0 | K^1 | Q~1 | U0 | U1 | -W0 | -W1 | P, the preparation's boxes
+// in the same places (and P after them).
 constexpr uint32_t sK0 = 0, sQ0 = 8192, sK1 = 16384, sQ1 = 24576, sV0 = 32768, sV1 = 40960, sTU = 49152,
-                   sTW = 57344;
+                   sTW = 57344, sKdaP = 65536;
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16
-constexpr uint32_t OFF_WS = OFF_P + 8192;                       // -W^T [128 (dk) x 64] bf16, MN-major
-// gate statistics per chunk: G, raw log-gate, gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each.  A ring of
-// four: the O epilogue of chunk c still reads its row factors while chunk c + 3 is loaded
+// gate statistics per chunk: G, raw log-gate, gam, 2^(G_C-G), 2^-G, scale*gam  [64] f32 each (KDA:
+// 2^G_C of the 128 channels).  A ring of four: the O epilogue of chunk c still reads its row
+// factors while chunk c + 3 is loaded
 constexpr int kGateStages = 4;
 constexpr uint32_t kGateBytes = 1536;
-constexpr uint32_t OFF_GATE = OFF_WS + 16384;
-constexpr uint32_t OFF_BAR = OFF_GATE + kGateStages * kGateBytes;
-constexpr uint32_t kSmemTC = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
+template <bool KDA>
+struct TcLayout {
+    static constexpr uint32_t kStageBytes = KDA ? 73728u : 65536u;
+    static constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16 (scalar gate)
+    static constexpr uint32_t OFF_WS = OFF_P + (KDA ? 0u : 8192u);         // -W^T [128 (dk) x 64] bf16, MN-major
+    static constexpr uint32_t OFF_GATE = OFF_WS + (KDA ? 0u : 16384u);
+    static constexpr uint32_t OFF_BAR = OFF_GATE + kGateStages * kGateBytes;
+    static constexpr uint32_t kSmem = OFF_BAR + 512 + 1024;  // + slack for the 1024-byte alignment
+};
 
 // gate arrays inside a stage's gate block
 constexpr int GT_G = 0, GT_GRAW = 64, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320;
@@ -139,8 +145,12 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
     return 0;
 }
 
+template <bool KDA>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a, const __grid_constant__ TcMaps m)
 {
+    using Lay = TcLayout<KDA>;
+    constexpr uint32_t kStageBytes = Lay::kStageBytes, OFF_P = Lay::OFF_P, OFF_WS = Lay::OFF_WS,
+                       OFF_GATE = Lay::OFF_GATE, OFF_BAR = Lay::OFF_BAR;
     extern __shared__ __align__(1024) uint8_t smraw[];
     // 1024-byte aligned base (128-byte swizzle atoms); pointer arithmetic on the
     // __shared__ array keeps every derived access in the shared state space
@@ -258,32 +268,49 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const int rows = rows_in(len, c);
                 const bool emit = emit_of(ni);
                 uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-                if (lane == 0) {
-                    const uint32_t bytes = 32768u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
-                    mbar_arrive_expect_tx(&bars[B_TMA + s], bytes);
-                    const int tt = (int)t0;
-                    tma_load_3d(st + sK0, &m.k, 0, hq, tt, &bars[B_TMA + s]);
-                    tma_load_3d(st + sK1, &m.k, 64, hq, tt, &bars[B_TMA + s]);
-                    if (emit) {
-                        tma_load_3d(st + sQ0, &m.q, 0, hq, tt, &bars[B_TMA + s]);
-                        tma_load_3d(st + sQ1, &m.q, 64, hq, tt, &bars[B_TMA + s]);
-                    }
-                    if (!zero_values) {
-                        tma_load_3d(st + sV0, &m.v, 0, hv, tt, &bars[B_TMA + s]);
-                        tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
-                    }
-                    // operand tiles of the chunk: rows (slot * HV + hv) * 128 + {0, 64}
-                    const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 128);
-                    tma_load_2d(st + sTU, &m.tiles, 0, trow, &bars[B_TMA + s]);
-                    tma_load_2d(st + sTW, &m.tiles, 0, trow + 64, &bars[B_TMA + s]);
-                }
-                // raw log-gates of rows 2l, 2l+1 into the chunk's gate block (zeros past the end)
-                float *graw = gates(ni) + GT_GRAW;
-                const float *gsrc = a.g + (size_t)t0 * HV + hv;
+                if constexpr (KDA) {
+                    // the preparation's nine boxes of the chunk (three TMA copies of 192 rows), its 2^G_C
+                    (void)rows;
+                    (void)emit;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars[B_TMA + s], 73728u);
+                        const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 576);
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int r = 2 * lane + u;
-                    cp_async4(graw + r, gsrc + (size_t)(r < rows ? r : 0) * HV, r < rows ? 4u : 0u);
+                        for (int b3 = 0; b3 < 3; ++b3)
+                            tma_load_2d(st + 24576 * b3, &m.tiles, 0, trow + 192 * b3, &bars[B_TMA + s]);
+                    }
+                    float *gcd = gates(ni);
+                    const float *gsrc = a.kda_gc + ((size_t)tile_slot(bos, n, c) * HV + hv) * 128;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) cp_async4(gcd + 4 * lane + u, gsrc + 4 * lane + u, 4u);
+                } else {
+                    if (lane == 0) {
+                        const uint32_t bytes = 32768u + (emit ? 16384u : 0u) + (zero_values ? 0u : 16384u);
+                        mbar_arrive_expect_tx(&bars[B_TMA + s], bytes);
+                        const int tt = (int)t0;
+                        tma_load_3d(st + sK0, &m.k, 0, hq, tt, &bars[B_TMA + s]);
+                        tma_load_3d(st + sK1, &m.k, 64, hq, tt, &bars[B_TMA + s]);
+                        if (emit) {
+                            tma_load_3d(st + sQ0, &m.q, 0, hq, tt, &bars[B_TMA + s]);
+                            tma_load_3d(st + sQ1, &m.q, 64, hq, tt, &bars[B_TMA + s]);
+                        }
+                        if (!zero_values) {
+                            tma_load_3d(st + sV0, &m.v, 0, hv, tt, &bars[B_TMA + s]);
+                            tma_load_3d(st + sV1, &m.v, 64, hv, tt, &bars[B_TMA + s]);
+                        }
+                        // operand tiles of the chunk: rows (slot * HV + hv) * 128 + {0, 64}
+                        const int trow = (int)((tile_slot(bos, n, c) * HV + hv) * 128);
+                        tma_load_2d(st + sTU, &m.tiles, 0, trow, &bars[B_TMA + s]);
+                        tma_load_2d(st + sTW, &m.tiles, 0, trow + 64, &bars[B_TMA + s]);
+                    }
+                    // raw log-gates of rows 2l, 2l+1 into the chunk's gate block (zeros past the end)
+                    float *graw = gates(ni) + GT_GRAW;
+                    const float *gsrc = a.g + (size_t)t0 * HV + hv;
+    #pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int r = 2 * lane + u;
+                        cp_async4(graw + r, gsrc + (size_t)(r < rows ? r : 0) * HV, r < rows ? 4u : 0u);
+                    }
                 }
                 cp_async_commit();
                 ++ni;
@@ -297,40 +324,44 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 else cp_async_wait<0>();
                 const int c = cs + nl, s = nl % kStages;
                 const int rows = rows_in(len, c);
-                float *gt = gates(nl);
-                // gate statistics: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
-                const int r0 = 2 * lane, r1 = r0 + 1;
-                const float2 gr = *(const float2 *)(gt + GT_GRAW + r0);
-                const float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
-                float sp = g0 + g1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, sp, off);
-                    if (lane >= off) sp += y;
-                }
-                const float G0 = sp - g1, G1 = sp;
-                const float GC = __shfl_sync(0xffffffffu, sp, 31);
-                const float gm0 = ex2(G0), gm1 = ex2(G1);
-                *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
-                *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
-                *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
-                *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
-                *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
-                if (rows < kChunk) {
-                    // rows past the end of the sequence belong to the next one: make them inert zeros
-                    uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-                    const bool emit = emit_of(nl);
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    const int nz = (kChunk - rows) * 8;  // 16-byte pieces per box
-#pragma unroll 1
-                    for (int bx = 0; bx < 6; ++bx) {
-                        if ((bx == 2 || bx == 3) && !emit) continue;
-                        if (bx >= 4 && zero_values) continue;
-                        const uint32_t boff = bx == 0 ? sK0 : bx == 1 ? sK1 : bx == 2 ? sQ0 : bx == 3 ? sQ1 : bx == 4 ? sV0 : sV1;
-                        uint4 *p = (uint4 *)(st + boff + rows * 128);
-                        for (int e = lane; e < nz; e += 32) p[e] = z;
+                if constexpr (!KDA) {
+                    float *gt = gates(nl);
+                    // gate statistics: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
+                    const int r0 = 2 * lane, r1 = r0 + 1;
+                    const float2 gr = *(const float2 *)(gt + GT_GRAW + r0);
+                    const float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
+                    float sp = g0 + g1;
+    #pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, sp, off);
+                        if (lane >= off) sp += y;
                     }
-                    fence_proxy_async();
+                    const float G0 = sp - g1, G1 = sp;
+                    const float GC = __shfl_sync(0xffffffffu, sp, 31);
+                    const float gm0 = ex2(G0), gm1 = ex2(G1);
+                    *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
+                    *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
+                    *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
+                    *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
+                    *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
+                    if (rows < kChunk) {
+                        // rows past the end of the sequence belong to the next one: make them inert zeros
+                        uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
+                        const bool emit = emit_of(nl);
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+                        const int nz = (kChunk - rows) * 8;  // 16-byte pieces per box
+    #pragma unroll 1
+                        for (int bx = 0; bx < 6; ++bx) {
+                            if ((bx == 2 || bx == 3) && !emit) continue;
+                            if (bx >= 4 && zero_values) continue;
+                            const uint32_t boff = bx == 0 ? sK0 : bx == 1 ? sK1 : bx == 2 ? sQ0 : bx == 3 ? sQ1 : bx == 4 ? sV0 : sV1;
+                            uint4 *p = (uint4 *)(st + boff + rows * 128);
+                            for (int e = lane; e < nz; e += 32) p[e] = z;
+                        }
+                        fence_proxy_async();
+                    }
+                } else {
+                    (void)rows;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_FULL + s]);
@@ -360,7 +391,71 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         // queued behind it so that the tensor pipe stays busy while the chain warps convert.
         // The whole warp follows the program (warp-uniform waits) and one elected lane issues:
         // the operands of tcgen05.mma are then warp-uniform values.
-        if (nch > 0) {
+        if (KDA && nch > 0) {
+            // per-channel gates: U, -W, K^, Q~ and P come with the stage; the program holds only the chain
+            // products and the output products
+            const uint32_t idV1K = idesc_bf16_f32(128, 64, 0, 0);  // A in TMEM, K-major B (-W, Q~, P)
+            const uint32_t idS = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, MN-major B (K^), N = dk
+            bool ok = true;
+            auto wait = [&](int b, int ph) {
+                if (ok) ok = mbar_wait(&bars[b], (uint32_t)ph & 1u, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                return ok;
+            };
+            int e = 0;
+            for (int c = 0; c < nch && ok; ++c) {
+                const uint32_t st = sbase + OFF_STAGE + (c % kStages) * kStageBytes;
+                // ---- -(W S)^T = S^T (-W)^T: -W as K-major B (rows = tokens), fresh accumulator
+                if (!wait(B_SBF, c)) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, kmaj(st + sTU + (ks >> 2) * 8192 + (ks & 3) * 32),
+                               idV1K, ks > 0 ? 1u : 0u);
+                    mma_commit(&bars[B_VPF]);
+                }
+                __syncwarp();
+                // ---- O^T = S^T Q~^T
+                if (e > 0 && !wait(B_OE, e - 1)) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idV1K, ks > 0 ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+                // ---- S^T += V'^T K^  (B = K^, MN-major: dk atoms 16 KB apart; the per-channel decay is applied
+                //      to S^T by the chain)
+                if (!wait(B_VTF, c)) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tb + TM_S, tb + TM_VB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                    mma_commit(&bars[B_SF]);
+                }
+                __syncwarp();
+                // ---- O^T += V'^T P^T
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(st + sKdaP + ks * 32), idV1K, 1u);
+                    mma_commit(&bars[B_OF]);
+                }
+                __syncwarp();
+                ++e;
+                if (elect_one()) mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                __syncwarp();
+            }
+            if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
+            if (elect_one()) mma_commit(&bars[B_FIN]);
+            __syncwarp();
+            mbar_wait(&bars[B_FIN], 0, status, kStatusTimeout, kWaitNs);
+        } else if (!KDA && nch > 0) {
             const uint32_t idKQ = idesc_bf16_f32(128, 64, 0, 0);   // K-major A and B
             const uint32_t idMN = idesc_bf16_f32(128, 64, 1, 0);   // MN-major A (V^T, K^T), K-major B
             const uint32_t idV1 = idesc_bf16_f32(128, 64, 0, 1);   // A in TMEM, MN-major B (-W^T)
@@ -511,6 +606,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             mbar_wait(&bars[B_FIN], 0, status, kStatusTimeout, kWaitNs);
         }
     } else if (warp == 2 || warp == 3) {
+        if constexpr (!KDA) {
         // ================================================================ aux: Q~ in place, P (lane = row of Q K^T)
         const int r = tid - 64;  // 0..63; TMEM lanes 64..127
         const uint32_t tl = tb + ((uint32_t)((warp & 3) * 32) << 16);
@@ -608,6 +704,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (lane == 0) mbar_arrive(&bars[B_PF]);
             ++e;
         }
+        }
     } else if (warp >= 4 && warp < 12) {
         // ================================================================ chain (lane = dv; half hh of the columns)
         const int dv = 32 * (warp & 3) + lane;
@@ -649,7 +746,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (!ok) break;
             tc_fence_after();
             const float *gt = gates(i);
-            const float dec = gt[GT_GAM + 63];  // gC = 2^G_C
+            const float dec = KDA ? 1.f : gt[GT_GAM + 63];  // gC = 2^G_C (per channel with KDA: below)
             {
                 // ---- S_i -> bf16 copy (MMA operand) and gC * S_i (accumulator of this chunk's update)
                 uint32_t r[64];
@@ -663,8 +760,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     for (int j = 0; j < 16; ++j) p[j] = pack_bf16(u2f(r[32 * q + 2 * j]), u2f(r[32 * q + 2 * j + 1]));
                     tmem_st16(tl + TM_SBF + 32 * hh + 16 * q, p);
                 }
+                if constexpr (KDA) {
+                    // S^T column dk decays by 2^G_C,dk
 #pragma unroll
-                for (int j = 0; j < 64; ++j) r[j] = f2u(u2f(r[j]) * dec);
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        const float4 f = *(const float4 *)(gt + 64 * hh + 4 * j4);
+                        r[4 * j4] = f2u(u2f(r[4 * j4]) * f.x);
+                        r[4 * j4 + 1] = f2u(u2f(r[4 * j4 + 1]) * f.y);
+                        r[4 * j4 + 2] = f2u(u2f(r[4 * j4 + 2]) * f.z);
+                        r[4 * j4 + 3] = f2u(u2f(r[4 * j4 + 3]) * f.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) r[j] = f2u(u2f(r[j]) * dec);
+                }
                 tmem_st32(tl + TM_S + 64 * hh, r);
                 tmem_st32(tl + TM_S + 64 * hh + 32, r + 32);
                 tmem_st_wait();
@@ -675,14 +784,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
 
             // ---- V'^T (tokens 32 hh .. 32 hh + 31) -> bf16: as the output operand and scaled by
             //      gC/gam as the update operand; the scale factors are loaded while the product runs
-            float rd[32];
+            float rd[32];  // GDN: the update operand's factors gC/gam; KDA: U of this thread's column
+            if constexpr (KDA) {
+                // U[t][dv] for the tokens t of this half, from the chunk's U boxes (128-byte swizzled rows)
+                const uint8_t *ub = sm + OFF_STAGE + s * kStageBytes + (dv >= 64 ? sV1 : sV0);
+                const int cd = dv & 63;
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 x = *(const float4 *)(gt + GT_RDEC + 32 * hh + 4 * j4);
-                rd[4 * j4] = x.x;
-                rd[4 * j4 + 1] = x.y;
-                rd[4 * j4 + 2] = x.z;
-                rd[4 * j4 + 3] = x.w;
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hh + j;
+                    rd[j] = __bfloat162float(*(const __nv_bfloat16 *)(ub + t * 128 + ((((cd >> 3) ^ (t & 7)) << 4) | ((cd & 7) << 1))));
+                }
+            } else {
+    #pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 x = *(const float4 *)(gt + GT_RDEC + 32 * hh + 4 * j4);
+                    rd[4 * j4] = x.x;
+                    rd[4 * j4 + 1] = x.y;
+                    rd[4 * j4 + 2] = x.z;
+                    rd[4 * j4 + 3] = x.w;
+                }
             }
             ok = mbar_wait(&bars[B_VPF], i & 1, status, kStatusTimeout, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -693,13 +813,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld32(tl + TM_VP + 32 * hh, r);
                 tmem_ld_wait();
                 uint32_t vb[16], vtb[16];
+                if constexpr (KDA) {
+                    // V' = U - W S (the product holds -W S)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float x0 = u2f(r[2 * j]), x1 = u2f(r[2 * j + 1]);
-                    vb[j] = pack_bf16(x0, x1);
-                    vtb[j] = pack_bf16(x0 * rd[2 * j], x1 * rd[2 * j + 1]);
+                    for (int j = 0; j < 16; ++j) vb[j] = pack_bf16(u2f(r[2 * j]) + rd[2 * j], u2f(r[2 * j + 1]) + rd[2 * j + 1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float x0 = u2f(r[2 * j]), x1 = u2f(r[2 * j + 1]);
+                        vb[j] = pack_bf16(x0, x1);
+                        vtb[j] = pack_bf16(x0 * rd[2 * j], x1 * rd[2 * j + 1]);
+                    }
+                    tmem_st16(tl + TM_VTB + 16 * hh, vtb);
                 }
-                tmem_st16(tl + TM_VTB + 16 * hh, vtb);
                 tmem_st16(tl + TM_VB + 16 * hh, vb);
                 tmem_st_wait();
             }
@@ -755,7 +881,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         bool ok = true;
         int e = 0;
         for (int it = 0; it <= nch && ok; ++it) {
-            if (it < nch) {
+            if (!KDA && it < nch) {
                 // ---- -W^T of chunk it (lane = dk) -> shared memory, MN-major operand of V' = U - W S
                 ok = mbar_wait(&bars[B_WF], it & 1, status, kStatusTimeout, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
@@ -797,8 +923,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld32(tl + TM_O + 32, r + 32);
                 tmem_ld_wait();
                 const float *gt = gates(ci);
-                if (factored(ci)) {
-                    // the row factors scale * gam_t of the factored form
+                if (!KDA && factored(ci)) {
+                    // the row factors scale * gam_t of the factored form (per-channel gates: inside Q~ and P)
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         const float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
@@ -890,14 +1016,14 @@ bool make_map(CUtensorMap *map, const void *base, int heads, int64_t rows)
     return r == CUDA_SUCCESS;
 }
 
-// 2-D map over the operand tiles, bf16 [rows][64], box = 64 x 64, 128-byte swizzle.
-bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows)
+// 2-D map over the operand tiles, bf16 [rows][64], box = 64 x box_rows, 128-byte swizzle.
+bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t box_rows = 64)
 {
     auto enc = get_encoder();
     if (!enc || !base) return false;
     cuuint64_t dims[2] = {64, (cuuint64_t)rows};
     cuuint64_t strides[1] = {64 * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -907,12 +1033,12 @@ bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows)
 
 }  // namespace
 
-size_t tc_smem_bytes() { return kSmemTC; }
+size_t tc_smem_bytes() { return TcLayout<false>::kSmem; }
 
 bool tc_shape_ok(const gdn_shape *s)
 {
-    return s->qkv_dtype == GDN_BF16 && s->gate_kind == GDN_GATE_SCALAR && s->K == 128 && s->V == 128 &&
-           (size_t)s->B * s->T < (1ull << 31);
+    // scalar gates, or per-channel gates (their own chunk preparation; no chunk-parallel split)
+    return s->qkv_dtype == GDN_BF16 && s->K == 128 && s->V == 128 && (size_t)s->B * s->T < (1ull << 31);
 }
 
 bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o)
@@ -922,23 +1048,38 @@ bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *
     return al(q) && al(k) && al(v) && al(o) && get_encoder() != nullptr;
 }
 
-cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, cudaStream_t st)
+cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st)
 {
-    static_assert(kSmemTC <= 227 * 1024, "shared memory budget");
+    static_assert(TcLayout<false>::kSmem <= 227 * 1024 && TcLayout<true>::kSmem <= 227 * 1024,
+                  "shared memory budget");
     if (a.N * a.HV == 0) return cudaSuccess;
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
     const int64_t rows = (int64_t)a.B * a.T;
     if (rows > 0) {
-        if (!make_map(&maps.q, a.q, a.H, rows) || !make_map(&maps.k, a.k, a.H, rows) ||
-            !make_map(&maps.v, a.v, a.HV, rows) || !make_map(&maps.o, a.o, a.HV, rows) ||
-            !make_tiles_map(&maps.tiles, a.tiles, (int64_t)a.tile_slots * a.HV * 128))
+        if (!make_map(&maps.o, a.o, a.HV, rows)) return cudaErrorInvalidValue;
+        if (kda) {
+            // the preparation's boxes: nine of 64 rows per (slot, value head), copied three at a time
+            if (!make_tiles_map(&maps.tiles, a.tiles, (int64_t)a.tile_slots * a.HV * 576, 192))
+                return cudaErrorInvalidValue;
+        } else if (!make_map(&maps.q, a.q, a.H, rows) || !make_map(&maps.k, a.k, a.H, rows) ||
+                   !make_map(&maps.v, a.v, a.HV, rows) ||
+                   !make_tiles_map(&maps.tiles, a.tiles, (int64_t)a.tile_slots * a.HV * 128)) {
             return cudaErrorInvalidValue;
+        }
     }
-    cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTC);
-    if (e != cudaSuccess) return e;
     dim3 grid(value_tiles, a.n_seg, a.N * a.HV);
-    tc_scan_kernel<<<grid, kThreadsTC, kSmemTC, st>>>(a, maps);
+    if (kda) {
+        constexpr uint32_t smem = TcLayout<true>::kSmem;
+        cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        tc_scan_kernel<true><<<grid, kThreadsTC, smem, st>>>(a, maps);
+    } else {
+        constexpr uint32_t smem = TcLayout<false>::kSmem;
+        cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        tc_scan_kernel<false><<<grid, kThreadsTC, smem, st>>>(a, maps);
+    }
     return cudaGetLastError();
 }
 

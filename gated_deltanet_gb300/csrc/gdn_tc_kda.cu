@@ -1,0 +1,257 @@
+// Chunk preparation for the tensor-core engine with per-key-channel gates (the
+// "KDA source walkthrough" chunk form): for every chunk of every (sequence, value
+// head), everything of the chunk that does not depend on the state, as bf16 tiles
+// the scan loads with TMA.  With G = chunk-local inclusive cumsum of the log-gate
+// per channel (base 2), G_C = G of the last row:
+//
+//   Akk_ij = beta_i sum_d k_id k_jd 2^(G_id - G_jd)   (j < i)     gated K K^T
+//   Aqk_ij =        sum_d q_id k_jd 2^(G_id - G_jd)   (j <= i)    gated Q K^T
+//   X      = (I + Akk)^-1
+//   U      = X diag(beta) V,   W = X diag(beta) (K * 2^G)         WY form: V' = U - W S
+//   K^     = K * 2^(G_C - G),  Q~ = scale Q * 2^G,  P = scale Aqk
+//   gC_d   = 2^(G_C,d)                                            per-channel state decay
+//
+// so that the scan computes V' = U - W S, O = Q~ S + P V', S <- diag(gC) S + K^T V'.
+// Both gated products take each 2^(G_i - G_j) as 2^(G_i - G_r) 2^(G_r - G_j) with r
+// the first row of j's group of four, so no factor overflows.
+//
+// Tiles: bf16 [slot][HV][9][64][64] (boxes: K^ dk 0-63, Q~ dk 0-63, K^ dk 64-127, Q~ dk 64-127,
+// U dv 0-63, U dv 64-127, -W dk 0-63, -W dk 64-127, P), rows of 64 elements; gC fp32
+// [slot][HV][128].  One CTA of 256 threads per (slot, value head).
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace {
+using ptx::ex2;
+
+constexpr int kThreadsKda = 256;
+constexpr int KP = 129;  // fp32 row pitch of the 64 x 128 tiles
+constexpr int kLd = 65;  // fp32 row pitch of the 64 x 64 tiles
+
+struct KdaSmem {
+    float k[64 * KP];   // k, then k * 2^G
+    float q[64 * KP];   // q, then v
+    float g[64 * KP];   // G
+    float l[64 * kLd];  // beta_i Akk_ij (j < i)
+    float x[64 * kLd];  // X = (I + L)^-1, then X diag(beta)
+    float p[64 * kLd];  // Aqk (j <= i)
+    float beta[64];
+    float gc[128];
+};
+
+__device__ __forceinline__ int rows_in(int64_t len, int c)
+{
+    const int64_t r = len - (int64_t)c * kChunk;
+    return r < kChunk ? (int)r : kChunk;
+}
+
+// element (row r, column col) of a 64 x 128 matrix stored as two [64][64] boxes b0, b0 + 1
+__device__ __forceinline__ size_t box_index(int b0, int r, int col) { return (size_t)((b0 + (col >> 6)) * 64 + r) * 64 + (col & 63); }
+
+__global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepArgs a)
+{
+    extern __shared__ __align__(16) uint8_t kda_raw[];
+    KdaSmem &sh = *(KdaSmem *)kda_raw;
+    const int tid = threadIdx.x;
+    const int slot = blockIdx.x, hv = blockIdx.y;
+    const int HV = a.HV, hq = hv / (HV / a.H);
+    auto seq_start = [&](int m) -> int64_t { return a.cu_seqlens ? a.cu_seqlens[m] : (int64_t)m * a.T; };
+    // the sequence owning this slot: the last n with tile_slot(bos_n, n, 0) <= slot
+    int lo = 0, hi = a.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_slot(seq_start(mid), mid, 0) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int n = lo;
+    const int64_t bos = seq_start(n), len = seq_start(n + 1) - bos;
+    const int c = (int)(slot - tile_slot(bos, n, 0));
+    const int NT = (int)((len + kChunk - 1) / kChunk);
+    if (c < 0 || c >= NT) return;  // an unused slot
+    const int rows = rows_in(len, c);
+    const int64_t t0 = bos + (int64_t)c * kChunk;
+    const __nv_bfloat16 *qg = (const __nv_bfloat16 *)a.q, *kg = (const __nv_bfloat16 *)a.k;
+    const __nv_bfloat16 *vg = (const __nv_bfloat16 *)a.v;
+    __nv_bfloat16 *tile = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 9 * 4096;
+
+    // ---- k, q, log-gates (rows past the end of the sequence are inert zeros), beta
+    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
+        const int r = e >> 7, d = e & 127;
+        float kv = 0.f, qv = 0.f, gv = 0.f;
+        if (r < rows) {
+            const size_t off = ((size_t)(t0 + r) * a.H + hq) * 128 + d;
+            kv = __bfloat162float(kg[off]);
+            qv = __bfloat162float(qg[off]);
+            gv = a.gk[((size_t)(t0 + r) * HV + hv) * 128 + d] * kRcpLn2;
+        }
+        sh.k[r * KP + d] = kv;
+        sh.q[r * KP + d] = qv;
+        sh.g[r * KP + d] = gv;
+    }
+    if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
+    __syncthreads();
+    // ---- per-channel inclusive cumsum (one thread per channel)
+    if (tid < 128) {
+        float acc = 0.f;
+        for (int r = 0; r < 64; ++r) {
+            acc += sh.g[r * KP + tid];
+            sh.g[r * KP + tid] = acc;
+        }
+        sh.gc[tid] = acc;
+    }
+    __syncthreads();
+
+    // ---- gated K K^T (times beta_i, strictly lower) and Q K^T (lower with the diagonal); 4 x 4 blocks
+    {
+        const int bi = tid >> 4, bj = tid & 15;
+        const int i0 = 4 * bi, j0 = 4 * bj;
+        if (bj <= bi) {
+            float ak[4][4], aq[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) ak[u][w] = aq[u][w] = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < 128; ++d) {
+                // reference row j0: 2^(G_i - G_j) = 2^(G_i - G_j0) 2^(G_j0 - G_j), both factors bounded
+                const float gr = sh.g[j0 * KP + d];
+                float ki[4], qi[4], kj[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float fi = ex2(sh.g[(i0 + u) * KP + d] - gr);
+                    ki[u] = sh.k[(i0 + u) * KP + d] * fi;
+                    qi[u] = sh.q[(i0 + u) * KP + d] * fi;
+                    kj[u] = sh.k[(j0 + u) * KP + d] * ex2(gr - sh.g[(j0 + u) * KP + d]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        ak[u][w] = fmaf(ki[u], kj[w], ak[u][w]);
+                        aq[u][w] = fmaf(qi[u], kj[w], aq[u][w]);
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int i = i0 + u, j = j0 + w;
+                    sh.l[i * kLd + j] = j < i ? sh.beta[i] * ak[u][w] : 0.f;
+                    sh.p[i * kLd + j] = j <= i ? aq[u][w] : 0.f;
+                }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    sh.l[(i0 + u) * kLd + j0 + w] = 0.f;
+                    sh.p[(i0 + u) * kLd + j0 + w] = 0.f;
+                }
+        }
+    }
+    __syncthreads();
+
+    // ---- K^ = k 2^(G_C - G) and Q~ = scale q 2^G to the tiles (bf16, 8 per 16-byte store); k -> k 2^G
+    for (int e = tid; e < 64 * 16; e += kThreadsKda) {
+        const int r = e >> 4, c8 = (e & 15) * 8;
+        float kh[8], qt[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int d = c8 + u;
+            const float G = sh.g[r * KP + d], kv = sh.k[r * KP + d];
+            kh[u] = kv * ex2(sh.gc[d] - G);
+            qt[u] = a.scale * sh.q[r * KP + d] * ex2(G);
+            sh.k[r * KP + d] = kv * ex2(G);
+        }
+        *(uint4 *)(tile + box_index(0, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(kh);  // K^: boxes 0, 2
+        *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
+    }
+    if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
+
+    // ---- X = (I + L)^-1: each column by 4 lanes, forward substitution
+    {
+        const int col = tid >> 2, r4 = tid & 3;
+        for (int j = r4; j < 64; j += 4) sh.x[j * kLd + col] = (j == col) ? 1.f : 0.f;
+        __syncwarp();
+        const int first = (tid >> 5) * 8 + 1;  // smallest column of this warp, plus one
+        for (int i = first; i < 64; ++i) {
+            float part = 0.f;
+            if (i > col)
+                for (int j = col + r4; j < i; j += 4) part = fmaf(sh.l[i * kLd + j], sh.x[j * kLd + col], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (r4 == 0 && i > col) sh.x[i * kLd + col] = -part;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // ---- X diag(beta) in place; v into the q buffer
+    for (int e = tid; e < 64 * 64; e += kThreadsKda) {
+        const int i = e >> 6, j = e & 63;
+        sh.x[i * kLd + j] *= sh.beta[j];
+    }
+    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
+        const int r = e >> 7, d = e & 127;
+        sh.q[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
+    }
+    __syncthreads();
+
+    // ---- U = (X diag(beta)) V and -W = -(X diag(beta)) (k 2^G): thread = 8 rows x 8 columns (16 apart)
+    //      of one of them; a half-warp reads 16 consecutive columns (no bank conflicts)
+    {
+        const int which = tid >> 7;  // 0: U from v, 1: -W from k 2^G
+        const int t = tid & 127, rb = (t >> 4) * 8, cl = t & 15;
+        const float *src = which ? sh.k : sh.q;
+        const float sgn = which ? -1.f : 1.f;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            const int r0 = rb + 4 * half;
+            float acc[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) acc[u][w] = 0.f;
+            for (int j = 0; j <= r0 + 3; ++j) {  // X is lower triangular
+                float s[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) s[w] = src[j * KP + cl + 16 * w];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float xv = sh.x[(r0 + u) * kLd + j];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) acc[u][w] = fmaf(xv, s[w], acc[u][w]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    tile[box_index(which ? 6 : 4, r0 + u, cl + 16 * w)] = __float2bfloat16_rn(sgn * acc[u][w]);
+        }
+    }
+    // ---- P = scale Aqk -> box 8
+    for (int e = tid; e < 64 * 8; e += kThreadsKda) {
+        const int r = e >> 3, c8 = (e & 7) * 8;
+        float o[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) o[w] = a.scale * sh.p[r * kLd + c8 + w];
+        *(uint4 *)(tile + (size_t)(8 * 64 + r) * 64 + c8) = ptx::pack8(o);
+    }
+}
+
+}  // namespace
+
+size_t kda_prep_smem_bytes() { return sizeof(KdaSmem); }
+
+cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st)
+{
+    if (a.N * a.HV == 0 || a.slots == 0) return cudaSuccess;
+    const int smem = (int)sizeof(KdaSmem);
+    cudaError_t e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.slots, a.HV);
+    kda_prep_kernel<<<grid, kThreadsKda, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

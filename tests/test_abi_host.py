@@ -76,7 +76,13 @@ def test_plans(gdn):
     # fp32 or other head dims: CUDA-core engine
     p = gdn.plan(4, 4096, 16, 16, 128, 128, dtype="f32", num_sms=152)
     assert p.engine == 1 and p.value_tiles == 4
-    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152)
+    # per-key-channel gates, bf16, dk = dv = 128: tensor-core engine with its own chunk preparation,
+    # never split; a requested split keeps them on the CUDA-core engine
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152, keys_unit_norm=True)
+    assert p.engine == 2 and p.cp_mode == 1 and p.segments == 1 and p.kernels == 2
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152, cp_mode="exact")
+    assert p.engine == 1
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", dtype="f32", num_sms=152)
     assert p.engine == 1
     # few pairs and a long sequence: the split is planned
     p = gdn.plan(1, 65536, 8, 8, 128, 128, num_sms=152)
