@@ -17,7 +17,8 @@
 //
 // Tiles: bf16 [slot][HV][9][64][64] (boxes: K^ dk 0-63, Q~ dk 0-63, K^ dk 64-127, Q~ dk 64-127,
 // U dv 0-63, U dv 64-127, -W dk 0-63, -W dk 64-127, P), rows of 64 elements; gC fp32
-// [slot][HV][128].  One CTA of 256 threads per (slot, value head).
+// [slot][HV][128].  One CTA of 256 threads per (slot, value head), two per SM (99 KB of shared
+// memory: four buffers that change roles as the chunk's data dies).
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -27,15 +28,17 @@ using ptx::ex2;
 
 constexpr int kThreadsKda = 256;
 constexpr int KP = 129;  // fp32 row pitch of the 64 x 128 tiles
+constexpr int QP = 136;  // bf16 row pitch of q
 constexpr int kLd = 65;  // fp32 row pitch of the 64 x 64 tiles
 
 struct KdaSmem {
-    float k[64 * KP];   // k, then k * 2^G
-    float q[64 * KP];   // q, then v
-    float g[64 * KP];   // G
+    float k[64 * KP];  // k, then k * 2^G
+    union {
+        __nv_bfloat16 q[64 * QP];  // q, until Q~ is written
+        float x[64 * kLd];         // then X = (I + L)^-1, then X diag(beta)
+    };
+    float g[64 * KP];   // G, then v
     float l[64 * kLd];  // beta_i Akk_ij (j < i)
-    float x[64 * kLd];  // X = (I + L)^-1, then X diag(beta)
-    float p[64 * kLd];  // Aqk (j <= i)
     float beta[64];
     float gc[128];
 };
@@ -49,7 +52,7 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 // element (row r, column col) of a 64 x 128 matrix stored as two [64][64] boxes b0, b0 + 1
 __device__ __forceinline__ size_t box_index(int b0, int r, int col) { return (size_t)((b0 + (col >> 6)) * 64 + r) * 64 + (col & 63); }
 
-__global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepArgs a)
+__global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepArgs a)
 {
     extern __shared__ __align__(16) uint8_t kda_raw[];
     KdaSmem &sh = *(KdaSmem *)kda_raw;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
             gv = a.gk[((size_t)(t0 + r) * HV + hv) * 128 + d] * kRcpLn2;
         }
         sh.k[r * KP + d] = kv;
-        sh.q[r * KP + d] = qv;
+        sh.q[r * QP + d] = __float2bfloat16_rn(qv);  // exact: q is bf16
         sh.g[r * KP + d] = gv;
     }
     if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
                 for (int u = 0; u < 4; ++u) {
                     const float fi = ex2(sh.g[(i0 + u) * KP + d] - gr);
                     ki[u] = sh.k[(i0 + u) * KP + d] * fi;
-                    qi[u] = sh.q[(i0 + u) * KP + d] * fi;
+                    qi[u] = __bfloat162float(sh.q[(i0 + u) * QP + d]) * fi;
                     kj[u] = sh.k[(j0 + u) * KP + d] * ex2(gr - sh.g[(j0 + u) * KP + d]);
                 }
 #pragma unroll
@@ -132,21 +135,26 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
                     }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                float pv[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const int i = i0 + u, j = j0 + w;
+                    const int j = j0 + w;
                     sh.l[i * kLd + j] = j < i ? sh.beta[i] * ak[u][w] : 0.f;
-                    sh.p[i * kLd + j] = j <= i ? aq[u][w] : 0.f;
+                    pv[w] = j <= i ? a.scale * aq[u][w] : 0.f;
                 }
+                // P = scale Aqk -> box 8, four columns per 8-byte store
+                *(uint2 *)(tile + (size_t)(8 * 64 + i) * 64 + j0) =
+                    make_uint2(ptx::pack_bf16(pv[0], pv[1]), ptx::pack_bf16(pv[2], pv[3]));
+            }
         } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 4; ++u) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    sh.l[(i0 + u) * kLd + j0 + w] = 0.f;
-                    sh.p[(i0 + u) * kLd + j0 + w] = 0.f;
-                }
+                for (int w = 0; w < 4; ++w) sh.l[(i0 + u) * kLd + j0 + w] = 0.f;
+                *(uint2 *)(tile + (size_t)(8 * 64 + i0 + u) * 64 + j0) = make_uint2(0u, 0u);
+            }
         }
     }
     __syncthreads();
@@ -160,13 +168,14 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
             const int d = c8 + u;
             const float G = sh.g[r * KP + d], kv = sh.k[r * KP + d];
             kh[u] = kv * ex2(sh.gc[d] - G);
-            qt[u] = a.scale * sh.q[r * KP + d] * ex2(G);
+            qt[u] = a.scale * __bfloat162float(sh.q[r * QP + d]) * ex2(G);
             sh.k[r * KP + d] = kv * ex2(G);
         }
         *(uint4 *)(tile + box_index(0, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(kh);  // K^: boxes 0, 2
         *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
     }
     if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
+    __syncthreads();  // q and G are dead: their buffers take X and v
 
     // ---- X = (I + L)^-1: each column by 4 lanes, forward substitution
     {
@@ -185,14 +194,14 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
         }
     }
     __syncthreads();
-    // ---- X diag(beta) in place; v into the q buffer
+    // ---- X diag(beta) in place; v into the G buffer
     for (int e = tid; e < 64 * 64; e += kThreadsKda) {
         const int i = e >> 6, j = e & 63;
         sh.x[i * kLd + j] *= sh.beta[j];
     }
     for (int e = tid; e < 64 * 128; e += kThreadsKda) {
         const int r = e >> 7, d = e & 127;
-        sh.q[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
+        sh.g[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
     }
     __syncthreads();
 
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
     {
         const int which = tid >> 7;  // 0: U from v, 1: -W from k 2^G
         const int t = tid & 127, rb = (t >> 4) * 8, cl = t & 15;
-        const float *src = which ? sh.k : sh.q;
+        const float *src = which ? sh.k : sh.g;
         const float sgn = which ? -1.f : 1.f;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -228,14 +237,6 @@ __global__ void __launch_bounds__(kThreadsKda, 1) kda_prep_kernel(const KdaPrepA
                 for (int w = 0; w < 8; ++w)
                     tile[box_index(which ? 6 : 4, r0 + u, cl + 16 * w)] = __float2bfloat16_rn(sgn * acc[u][w]);
         }
-    }
-    // ---- P = scale Aqk -> box 8
-    for (int e = tid; e < 64 * 8; e += kThreadsKda) {
-        const int r = e >> 3, c8 = (e & 7) * 8;
-        float o[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w) o[w] = a.scale * sh.p[r * kLd + c8 + w];
-        *(uint4 *)(tile + (size_t)(8 * 64 + r) * 64 + c8) = ptx::pack8(o);
     }
 }
 
