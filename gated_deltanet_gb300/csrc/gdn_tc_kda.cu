@@ -32,13 +32,14 @@ constexpr int QP = 136;  // bf16 row pitch of q
 constexpr int kLd = 65;  // fp32 row pitch of the 64 x 64 tiles
 
 struct KdaSmem {
-    float k[64 * KP];  // k, then k * 2^G
+    __nv_bfloat16 k[64 * QP];  // k (bf16 input, exact), then k * 2^G
     union {
         __nv_bfloat16 q[64 * QP];  // q, until Q~ is written
         float x[64 * kLd];         // then X = (I + L)^-1, then X diag(beta)
     };
-    float g[64 * KP];   // G, then v
-    float l[64 * kLd];  // beta_i Akk_ij (j < i)
+    float g[64 * KP];            // G, then v
+    float l[64 * kLd];           // beta_i Akk_ij (j < i)
+    __nv_bfloat16 kj[64 * QP];   // k_j 2^(G_r - G_j), r = first row of j's 16-row block
     float beta[64];
     float gc[128];
 };
@@ -87,8 +88,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             qv = __bfloat162float(qg[off]);
             gv = a.gk[((size_t)(t0 + r) * HV + hv) * 128 + d] * kRcpLn2;
         }
-        sh.k[r * KP + d] = kv;
-        sh.q[r * QP + d] = __float2bfloat16_rn(qv);  // exact: q is bf16
+        sh.k[r * QP + d] = __float2bfloat16_rn(kv);  // exact: k and q are bf16
+        sh.q[r * QP + d] = __float2bfloat16_rn(qv);
         sh.g[r * KP + d] = gv;
     }
     if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
@@ -104,8 +105,68 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     }
     __syncthreads();
 
-    // ---- gated K K^T (times beta_i, strictly lower) and Q K^T (lower with the diagonal); 4 x 4 blocks
-    {
+    // ---- gated K K^T (times beta_i, strictly lower) and Q K^T (lower with the diagonal).  On the tensor
+    //      cores: for the 16-row key block b with reference row r = 16 b, [K; Q]_i 2^(G_i - G_r) times
+    //      (k_j 2^(G_r - G_j))^T; the factors stay bounded while the decay inside a block is below 2^100
+    float emax = 0.f;
+    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
+        const int j = e >> 7, d = e & 127, r = j & ~15;
+        const float ex = sh.g[r * KP + d] - sh.g[j * KP + d];
+        emax = fmaxf(emax, ex);
+        sh.kj[j * QP + d] = __float2bfloat16_rn(__bfloat162float(sh.k[j * QP + d]) * ex2(ex));
+    }
+    if (!__syncthreads_or(emax > 100.f)) {
+        const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
+        // item = (key block b, 16-row tile mt >= b): ten of them over the eight warps
+        for (int item = warp; item < 10; item += 8) {
+            const int b = item < 4 ? 0 : item < 7 ? 1 : item < 9 ? 2 : 3;
+            const int mt = item < 4 ? item : item < 7 ? item - 3 : item < 9 ? item - 5 : 3;
+            const int r = 16 * b, i0 = 16 * mt, j0 = 16 * b;
+            float ak[2][4], aq[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ak[nt][c] = aq[nt][c] = 0.f;
+#pragma unroll 2
+            for (int ks = 0; ks < 8; ++ks) {
+                const int d0 = 16 * ks + 2 * t;
+                // A fragments (rows i0 + gq (+8), columns d0, d0 + 1 (+8)) with the factor 2^(G_i - G_r)
+                uint32_t fk[4], fq[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int i = i0 + gq + 8 * (h & 1), d = d0 + 8 * (h >> 1);
+                    const float f0 = ex2(sh.g[i * KP + d] - sh.g[r * KP + d]);
+                    const float f1 = ex2(sh.g[i * KP + d + 1] - sh.g[r * KP + d + 1]);
+                    const __nv_bfloat162 kk = *(const __nv_bfloat162 *)(sh.k + i * QP + d);
+                    const __nv_bfloat162 qq = *(const __nv_bfloat162 *)(sh.q + i * QP + d);
+                    fk[h] = ptx::pack_bf16(__low2float(kk) * f0, __high2float(kk) * f1);
+                    fq[h] = ptx::pack_bf16(__low2float(qq) * f0, __high2float(qq) * f1);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = j0 + 8 * nt + gq;
+                    const uint32_t b0 = *(const uint32_t *)(sh.kj + j * QP + d0);
+                    const uint32_t b1 = *(const uint32_t *)(sh.kj + j * QP + d0 + 8);
+                    ptx::mma_bf16_16816(ak[nt], fk[0], fk[1], fk[2], fk[3], b0, b1);
+                    ptx::mma_bf16_16816(aq[nt], fq[0], fq[1], fq[2], fq[3], b0, b1);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = i0 + gq + 8 * (c >> 1), j = j0 + 8 * nt + 2 * t + (c & 1);
+                    sh.l[i * kLd + j] = j < i ? sh.beta[i] * ak[nt][c] : 0.f;
+                    tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(j <= i ? a.scale * aq[nt][c] : 0.f);
+                }
+        }
+        // P is zero above the diagonal blocks (L there is never read)
+        for (int e = tid; e < 64 * 64; e += kThreadsKda) {
+            const int i = e >> 6, j = e & 63;
+            if ((j >> 4) > (i >> 4)) tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(0.f);
+        }
+    } else {
+        // steep chunk: per-element factors with a reference row per group of four (4 x 4 blocks)
         const int bi = tid >> 4, bj = tid & 15;
         const int i0 = 4 * bi, j0 = 4 * bj;
         if (bj <= bi) {
@@ -122,9 +183,9 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const float fi = ex2(sh.g[(i0 + u) * KP + d] - gr);
-                    ki[u] = sh.k[(i0 + u) * KP + d] * fi;
+                    ki[u] = __bfloat162float(sh.k[(i0 + u) * QP + d]) * fi;
                     qi[u] = __bfloat162float(sh.q[(i0 + u) * QP + d]) * fi;
-                    kj[u] = sh.k[(j0 + u) * KP + d] * ex2(gr - sh.g[(j0 + u) * KP + d]);
+                    kj[u] = __bfloat162float(sh.k[(j0 + u) * QP + d]) * ex2(gr - sh.g[(j0 + u) * KP + d]);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -166,10 +227,10 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int d = c8 + u;
-            const float G = sh.g[r * KP + d], kv = sh.k[r * KP + d];
+            const float G = sh.g[r * KP + d], kv = __bfloat162float(sh.k[r * QP + d]);
             kh[u] = kv * ex2(sh.gc[d] - G);
             qt[u] = a.scale * __bfloat162float(sh.q[r * QP + d]) * ex2(G);
-            sh.k[r * KP + d] = kv * ex2(G);
+            sh.k[r * QP + d] = __float2bfloat16_rn(kv * ex2(G));
         }
         *(uint4 *)(tile + box_index(0, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(kh);  // K^: boxes 0, 2
         *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
@@ -210,7 +271,6 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     {
         const int which = tid >> 7;  // 0: U from v, 1: -W from k 2^G
         const int t = tid & 127, rb = (t >> 4) * 8, cl = t & 15;
-        const float *src = which ? sh.k : sh.g;
         const float sgn = which ? -1.f : 1.f;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -223,7 +283,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             for (int j = 0; j <= r0 + 3; ++j) {  // X is lower triangular
                 float s[8];
 #pragma unroll
-                for (int w = 0; w < 8; ++w) s[w] = src[j * KP + cl + 16 * w];
+                for (int w = 0; w < 8; ++w)
+                    s[w] = which ? __bfloat162float(sh.k[j * QP + cl + 16 * w]) : sh.g[j * KP + cl + 16 * w];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const float xv = sh.x[(r0 + u) * kLd + j];

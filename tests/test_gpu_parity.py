@@ -76,6 +76,10 @@ SMALL = {
     "f32_channel": Workload("f32_channel", B=1, T=190, H=2, K=64, V=64, dtype="f32", gate="channel",
                             h0=True, seed=7),
     "bf16_channel": Workload("bf16_channel", B=2, T=140, H=2, K=128, V=128, gate="channel", seed=8),
+    # per-channel decay steep enough (about 2^-138 over 16 tokens) that the tensor-core engine's chunk
+    # preparation takes its per-element form
+    "bf16_channel_steep": Workload("bf16_channel_steep", B=1, T=150, H=2, K=128, V=128, gate="channel",
+                                   g_mu=-6.0, h0=True, seed=21),
     "f32_strong_decay": Workload("f32_strong_decay", B=1, T=256, H=2, K=64, V=64, dtype="f32", g_mu=-2.0,
                                  h0=True, seed=9),
     "bf16_T1": Workload("bf16_T1", B=2, T=1, H=2, K=128, V=128, h0=True, seed=14),
