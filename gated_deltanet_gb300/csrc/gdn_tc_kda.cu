@@ -24,21 +24,19 @@
 
 namespace gdn {
 namespace {
-using ptx::ex2;
+using namespace ptx;
 
 constexpr int kThreadsKda = 256;
 constexpr int KP = 129;  // fp32 row pitch of the 64 x 128 tiles
 constexpr int QP = 136;  // bf16 row pitch of q
-constexpr int kLd = 65;  // fp32 row pitch of the 64 x 64 tiles
+constexpr int kLdX = 68;  // fp32 row pitch of the L / X tile
 
 struct KdaSmem {
     __nv_bfloat16 k[64 * QP];  // k (bf16 input, exact), then k * 2^G
-    union {
-        __nv_bfloat16 q[64 * QP];  // q, until Q~ is written
-        float x[64 * kLd];         // then X = (I + L)^-1, then X diag(beta)
-    };
+    __nv_bfloat16 q[64 * QP];    // q, until Q~ is written
     float g[64 * KP];            // G, then v
-    float l[64 * kLd];           // beta_i Akk_ij (j < i)
+    float lx[64 * kLdX];         // L = beta_i Akk_ij in the lower triangle, then X^T in the upper:
+                                 // X(r, j), j < r, at lx[j * kLdX + r]
     __nv_bfloat16 kj[64 * QP];   // k_j 2^(G_r - G_j), r = first row of j's 16-row block
     float beta[64];
     float gc[128];
@@ -156,7 +154,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int i = i0 + gq + 8 * (c >> 1), j = j0 + 8 * nt + 2 * t + (c & 1);
-                    sh.l[i * kLd + j] = j < i ? sh.beta[i] * ak[nt][c] : 0.f;
+                    sh.lx[i * kLdX + j] = j < i ? sh.beta[i] * ak[nt][c] : 0.f;
                     tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(j <= i ? a.scale * aq[nt][c] : 0.f);
                 }
         }
@@ -202,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const int j = j0 + w;
-                    sh.l[i * kLd + j] = j < i ? sh.beta[i] * ak[u][w] : 0.f;
+                    sh.lx[i * kLdX + j] = j < i ? sh.beta[i] * ak[u][w] : 0.f;
                     pv[w] = j <= i ? a.scale * aq[u][w] : 0.f;
                 }
                 // P = scale Aqk -> box 8, four columns per 8-byte store
@@ -213,7 +211,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) sh.l[(i0 + u) * kLd + j0 + w] = 0.f;
+                for (int w = 0; w < 4; ++w) sh.lx[(i0 + u) * kLdX + j0 + w] = 0.f;
                 *(uint2 *)(tile + (size_t)(8 * 64 + i0 + u) * 64 + j0) = make_uint2(0u, 0u);
             }
         }
@@ -236,33 +234,146 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
     }
     if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
-    __syncthreads();  // q and G are dead: their buffers take X and v
+    __syncthreads();  // q and G are dead: the G buffer takes v
 
-    // ---- X = (I + L)^-1: each column by 4 lanes, forward substitution
-    {
-        const int col = tid >> 2, r4 = tid & 3;
-        for (int j = r4; j < 64; j += 4) sh.x[j * kLd + col] = (j == col) ? 1.f : 0.f;
-        __syncwarp();
-        const int first = (tid >> 5) * 8 + 1;  // smallest column of this warp, plus one
-        for (int i = first; i < 64; ++i) {
-            float part = 0.f;
-            if (i > col)
-                for (int j = col + r4; j < i; j += 4) part = fmaf(sh.l[i * kLd + j], sh.x[j * kLd + col], part);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            if (r4 == 0 && i > col) sh.x[i * kLd + col] = -part;
-            __syncwarp();
+    // ---- X = (I + L)^-1 by blocks (FLA page, sec. 4): 8 x 8 forward substitution, exact merges 8 -> 16
+    //      (FMA), 16 -> 32 and 32 -> 64 (tf32 m16n8k8) on warps 0-3; warps 4-7 load v meanwhile
+    if (tid < 128) {
+        const int warp = tid >> 5, lane = tid & 31;
+        float *lx = sh.lx;
+        auto Lx = [&](int r, int j) -> float { return lx[r * kLdX + j]; };
+        auto Xt = [&](int r, int j) -> float { return lx[j * kLdX + r]; };  // X(r, j), j < r
+        auto Xm = [&](int r, int j) -> float { return r > j ? lx[j * kLdX + r] : (r == j ? 1.f : 0.f); };
+        const int pw = warp;  // 0..3
+        // ---- A: the eight 8 x 8 diagonal blocks by forward substitution; 2 threads per (block, column)
+        {
+            const int task = tid >> 1, hh = tid & 1;
+            const int base = 8 * (task >> 3), cc = task & 7;
+            float x[8];
+    #pragma unroll
+            for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+    #pragma unroll
+            for (int r = 1; r < 8; ++r) {
+                float part = 0.f;
+    #pragma unroll
+                for (int j = 0; j < r; ++j)
+                    if ((j & 1) == hh) part = fmaf(Lx(base + r, base + j), x[j], part);
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                if (r > cc) x[r] = -part;
+            }
+            if (hh == 0) {
+    #pragma unroll
+                for (int r = 1; r < 8; ++r)
+                    if (r > cc) lx[(base + cc) * kLdX + base + r] = x[r];
+            }
         }
-    }
-    __syncthreads();
-    // ---- X diag(beta) in place; v into the G buffer
-    for (int e = tid; e < 64 * 64; e += kThreadsKda) {
-        const int i = e >> 6, j = e & 63;
-        sh.x[i * kLd + j] *= sh.beta[j];
-    }
-    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
-        const int r = e >> 7, d = e & 127;
-        sh.g[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
+        bar_sync(1, 128);
+        // ---- B: 8 -> 16, one warp per merge:  X(B, A) = -X(B, B) (L(B, A) X(A, A))
+        {
+            const int A = 16 * pw, Bb = A + 8;
+            const int r = lane >> 2, cp = (lane & 3) * 2;
+            float t0v = 0.f, t1v = 0.f;
+    #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float l = Lx(Bb + r, A + k);
+                const float x0 = k > cp ? Xt(A + k, A + cp) : (k == cp ? 1.f : 0.f);
+                const float x1 = k > cp + 1 ? Xt(A + k, A + cp + 1) : (k == cp + 1 ? 1.f : 0.f);
+                t0v = fmaf(l, x0, t0v);
+                t1v = fmaf(l, x1, t1v);
+            }
+            float a0 = 0.f, a1 = 0.f;
+    #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float tk0 = __shfl_sync(0xffffffffu, t0v, 4 * k + (lane & 3));
+                const float tk1 = __shfl_sync(0xffffffffu, t1v, 4 * k + (lane & 3));
+                const float xb = k < r ? Xt(Bb + r, Bb + k) : (k == r ? 1.f : 0.f);
+                a0 = fmaf(xb, tk0, a0);
+                a1 = fmaf(xb, tk1, a1);
+            }
+            lx[(A + cp) * kLdX + Bb + r] = -a0;
+            lx[(A + cp + 1) * kLdX + Bb + r] = -a1;
+        }
+        bar_sync(1, 128);
+        // ---- C: 16 -> 32 (tf32 m16n8k8); warp = (merge, 8-column tile):
+        //      T = L(B, A) X(A, A)[:, tile] (kept in place of L(B, A)), then X(B, A)[:, tile] = -X(B, B) T
+        {
+            const int g = lane >> 2, t = lane & 3;
+            const int A = 32 * (pw >> 1), Bb = A + 16, n0 = 8 * (pw & 1);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 8 * ks;
+                mma_tf32(d, Lx(Bb + g, A + k0 + t), Lx(Bb + g + 8, A + k0 + t), Lx(Bb + g, A + k0 + t + 4),
+                         Lx(Bb + g + 8, A + k0 + t + 4), Xm(A + k0 + t, A + n0 + g), Xm(A + k0 + t + 4, A + n0 + g));
+            }
+            bar_sync(1, 128);  // every warp has read L(B, A)
+            *(float2 *)(lx + (Bb + g) * kLdX + A + n0 + 2 * t) = make_float2(d[0], d[1]);
+            *(float2 *)(lx + (Bb + g + 8) * kLdX + A + n0 + 2 * t) = make_float2(d[2], d[3]);
+            __syncwarp();
+            float u[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 8 * ks;
+                mma_tf32(u, Xm(Bb + g, Bb + k0 + t), Xm(Bb + g + 8, Bb + k0 + t), Xm(Bb + g, Bb + k0 + t + 4),
+                         Xm(Bb + g + 8, Bb + k0 + t + 4), Lx(Bb + k0 + t, A + n0 + g), Lx(Bb + k0 + t + 4, A + n0 + g));
+            }
+            lx[(A + n0 + 2 * t) * kLdX + Bb + g] = -u[0];
+            lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = -u[1];
+            lx[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = -u[2];
+            lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g + 8] = -u[3];
+        }
+        bar_sync(1, 128);
+        // ---- D: 32 -> 64; warp = 8-column tile of the lower-left 32 x 32 block:
+        //      T = L(32:64, 0:32) X(0:32, tile) (kept in place of L), then X(32:64, tile) = -X(32:64, 32:64) T
+        {
+            const int g = lane >> 2, t = lane & 3, n0 = 8 * pw;
+            float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    #pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks < pw) continue;  // X(k, n) = 0 for k < n
+                const int k0 = 8 * ks;
+                const float b0 = Xm(k0 + t, n0 + g), b1 = Xm(k0 + t + 4, n0 + g);
+    #pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int m0 = 32 + 16 * mt;
+                    mma_tf32(d[mt], Lx(m0 + g, k0 + t), Lx(m0 + g + 8, k0 + t), Lx(m0 + g, k0 + t + 4),
+                             Lx(m0 + g + 8, k0 + t + 4), b0, b1);
+                }
+            }
+            bar_sync(1, 128);  // every warp has read L(32:64, 0:32)
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                *(float2 *)(lx + (32 + 16 * mt + g) * kLdX + n0 + 2 * t) = make_float2(d[mt][0], d[mt][1]);
+                *(float2 *)(lx + (32 + 16 * mt + g + 8) * kLdX + n0 + 2 * t) = make_float2(d[mt][2], d[mt][3]);
+            }
+            __syncwarp();
+            float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    #pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int k0 = 8 * ks;
+                const float b0 = Lx(32 + k0 + t, n0 + g), b1 = Lx(32 + k0 + t + 4, n0 + g);  // T(k, n)
+    #pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    if (k0 > 16 * mt + 15) continue;  // X(32 + m, 32 + k) = 0 for k > m
+                    const int m0 = 32 + 16 * mt;
+                    mma_tf32(u[mt], Xm(m0 + g, 32 + k0 + t), Xm(m0 + g + 8, 32 + k0 + t), Xm(m0 + g, 32 + k0 + t + 4),
+                             Xm(m0 + g + 8, 32 + k0 + t + 4), b0, b1);
+                }
+            }
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int m0 = 32 + 16 * mt;
+                lx[(n0 + 2 * t) * kLdX + m0 + g] = -u[mt][0];
+                lx[(n0 + 2 * t + 1) * kLdX + m0 + g] = -u[mt][1];
+                lx[(n0 + 2 * t) * kLdX + m0 + g + 8] = -u[mt][2];
+                lx[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
+            }
+        }
+    } else {
+        for (int e = tid - 128; e < 64 * 128; e += 128) {
+            const int r = e >> 7, d = e & 127;
+            sh.g[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
+        }
     }
     __syncthreads();
 
@@ -287,7 +398,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                     s[w] = which ? __bfloat162float(sh.k[j * QP + cl + 16 * w]) : sh.g[j * KP + cl + 16 * w];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float xv = sh.x[(r0 + u) * kLd + j];
+                    const int rr = r0 + u;
+                    const float xv = (j < rr ? sh.lx[j * kLdX + rr] : (j == rr ? 1.f : 0.f)) * sh.beta[j];
 #pragma unroll
                     for (int w = 0; w < 8; ++w) acc[u][w] = fmaf(xv, s[w], acc[u][w]);
                 }
