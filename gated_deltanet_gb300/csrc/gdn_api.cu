@@ -174,8 +174,8 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     Plan p;
     gdn_options opt;
     if (optp) opt = *optp; else gdn_default_options(&opt);
-    // the tensor-core engine needs 16-byte aligned q/k/v/o for its TMA maps
-    if (opt.engine != GDN_ENGINE_SIMT && tc_shape_ok(s) && !tc_supported(s, q, k, v, o)) {
+    // the tensor-core engine needs 16-byte aligned q/k/v/o for its TMA maps (and gk rows)
+    if (opt.engine != GDN_ENGINE_SIMT && tc_shape_ok(s) && !tc_supported(s, q, k, v, g, o)) {
         if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_INVALID;
         opt.engine = GDN_ENGINE_SIMT;
     }

@@ -86,7 +86,8 @@ size_t simt_smem_bytes(int K, gdn_gate_kind gate);
 // Tensor-core engine (bf16, K = V = 128, scalar gate).  `value_tiles` is 1 for
 // the forward pass and 2 for the exact split's pre-pass (S* and M columns).
 bool tc_shape_ok(const gdn_shape *s);
-bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o);
+bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                  const void *o);
 // Per-key-channel gates on the tensor-core engine: the chunk preparation (gdn_tc_kda.cu).
 struct KdaPrepArgs {
     const void *q, *k, *v;

@@ -1041,11 +1041,14 @@ bool tc_shape_ok(const gdn_shape *s)
     return s->qkv_dtype == GDN_BF16 && s->K == 128 && s->V == 128 && (size_t)s->B * s->T < (1ull << 31);
 }
 
-bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const void *o)
+bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                  const void *o)
 {
     if (!tc_shape_ok(s)) return false;
     auto al = [](const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; };
-    return al(q) && al(k) && al(v) && al(o) && get_encoder() != nullptr;
+    // per-channel gates are read as float4 rows by the KDA preparation
+    const bool g_ok = s->gate_kind != GDN_GATE_CHANNEL || al(g);
+    return al(q) && al(k) && al(v) && al(o) && g_ok && get_encoder() != nullptr;
 }
 
 cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st)

@@ -76,19 +76,42 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     const __nv_bfloat16 *vg = (const __nv_bfloat16 *)a.v;
     __nv_bfloat16 *tile = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 9 * 4096;
 
-    // ---- k, q, log-gates (rows past the end of the sequence are inert zeros), beta
-    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
-        const int r = e >> 7, d = e & 127;
-        float kv = 0.f, qv = 0.f, gv = 0.f;
-        if (r < rows) {
-            const size_t off = ((size_t)(t0 + r) * a.H + hq) * 128 + d;
-            kv = __bfloat162float(kg[off]);
-            qv = __bfloat162float(qg[off]);
-            gv = a.gk[((size_t)(t0 + r) * HV + hv) * 128 + d] * kRcpLn2;
+    // ---- k, q, log-gates (rows past the end of the sequence are inert zeros), beta: 16-byte loads,
+    //      all issued before the first store
+    {
+        uint4 kv[4], qv[4];
+        float4 gv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + kThreadsKda * i, r = e >> 4, c8 = (e & 15) * 8;
+            kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
+            if (r < rows) {
+                const size_t off = ((size_t)(t0 + r) * a.H + hq) * 128 + c8;
+                kv[i] = *(const uint4 *)(kg + off);
+                qv[i] = *(const uint4 *)(qg + off);
+            }
         }
-        sh.k[r * QP + d] = __float2bfloat16_rn(kv);  // exact: k and q are bf16
-        sh.q[r * QP + d] = __float2bfloat16_rn(qv);
-        sh.g[r * KP + d] = gv;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + kThreadsKda * i, r = e >> 5, c4 = (e & 31) * 4;
+            gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < rows) gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + kThreadsKda * i, r = e >> 4, c8 = (e & 15) * 8;
+            *(uint4 *)(sh.k + r * QP + c8) = kv[i];  // bf16 as given (exact)
+            *(uint4 *)(sh.q + r * QP + c8) = qv[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + kThreadsKda * i, r = e >> 5, c4 = (e & 31) * 4;
+            float *gd = sh.g + r * KP + c4;
+            gd[0] = gv[i].x * kRcpLn2;
+            gd[1] = gv[i].y * kRcpLn2;
+            gd[2] = gv[i].z * kRcpLn2;
+            gd[3] = gv[i].w * kRcpLn2;
+        }
     }
     if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
     __syncthreads();
@@ -370,9 +393,25 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             }
         }
     } else {
-        for (int e = tid - 128; e < 64 * 128; e += 128) {
-            const int r = e >> 7, d = e & 127;
-            sh.g[r * KP + d] = r < rows ? __bfloat162float(vg[((size_t)(t0 + r) * HV + hv) * 128 + d]) : 0.f;
+        // v as fp32 into the G buffer: 16-byte loads, all issued first
+        uint4 vv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid - 128 + 128 * i, r = e >> 4, c8 = (e & 15) * 8;
+            vv[i] = make_uint4(0, 0, 0, 0);
+            if (r < rows) vv[i] = *(const uint4 *)(vg + ((size_t)(t0 + r) * HV + hv) * 128 + c8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid - 128 + 128 * i, r = e >> 4, c8 = (e & 15) * 8;
+            const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&vv[i];
+            float *gd = sh.g + r * KP + c8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                gd[2 * u] = f.x;
+                gd[2 * u + 1] = f.y;
+            }
         }
     }
     __syncthreads();

@@ -89,7 +89,10 @@ typedef enum {
 typedef enum {
     GDN_ENGINE_AUTO = 0, /* tensor-core engine where supported, else SIMT            */
     GDN_ENGINE_SIMT = 1, /* fp32 CUDA-core engine (any supported shape, fp32 inputs) */
-    GDN_ENGINE_TC = 2    /* tcgen05/TMEM engine (bf16, K = V = 128, scalar gate)     */
+    GDN_ENGINE_TC = 2    /* tcgen05/TMEM engine: bf16, K = V = 128, scalar or
+                            per-channel gate, q/k/v/o (and gk) 16-byte aligned; a
+                            call that asks for it on other inputs gets
+                            GDN_ERR_INVALID                                       */
 } gdn_engine;
 
 typedef struct {
