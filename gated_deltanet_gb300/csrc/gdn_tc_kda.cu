@@ -33,8 +33,8 @@ constexpr int kLdX = 68;  // fp32 row pitch of the L / X tile
 
 struct KdaSmem {
     __nv_bfloat16 k[64 * QP];  // k (bf16 input, exact), then k * 2^G
-    __nv_bfloat16 q[64 * QP];    // q, until Q~ is written
-    float g[64 * KP];            // G, then v
+    __nv_bfloat16 q[64 * QP];    // q until Q~ is written, then v
+    float g[64 * KP];            // G (base 2, chunk-local cumsum per channel)
     float lx[64 * kLdX];         // L = beta_i Akk_ij in the lower triangle, then X^T in the upper:
                                  // X(r, j), j < r, at lx[j * kLdX + r]
     __nv_bfloat16 kj[64 * QP];   // k_j 2^(G_r - G_j), r = first row of j's 16-row block
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
     }
     if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
-    __syncthreads();  // q and G are dead: the G buffer takes v
+    __syncthreads();  // q and G are dead: the q buffer takes v
 
     // ---- X = (I + L)^-1 by blocks (FLA page, sec. 4): 8 x 8 forward substitution, exact merges 8 -> 16
     //      (FMA), 16 -> 32 and 32 -> 64 (tf32 m16n8k8) on warps 0-3; warps 4-7 load v meanwhile
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             }
         }
     } else {
-        // v as fp32 into the G buffer: 16-byte loads, all issued first
+        // v (bf16) into the q buffer: 16-byte loads, all issued first
         uint4 vv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -404,51 +404,61 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = tid - 128 + 128 * i, r = e >> 4, c8 = (e & 15) * 8;
-            const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&vv[i];
-            float *gd = sh.g + r * KP + c8;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h2[u]);
-                gd[2 * u] = f.x;
-                gd[2 * u + 1] = f.y;
-            }
+            *(uint4 *)(sh.q + r * QP + c8) = vv[i];
         }
     }
     __syncthreads();
 
-    // ---- U = (X diag(beta)) V and -W = -(X diag(beta)) (k 2^G): thread = 8 rows x 8 columns (16 apart)
-    //      of one of them; a half-warp reads 16 consecutive columns (no bank conflicts)
+    // ---- U = (X diag(beta)) V and -W = -(X diag(beta)) (k 2^G) on the tensor cores (tf32 m16n8k8; the bf16
+    //      operands are exact in tf32, X beta is rounded to it): warp = (U or W, 32 output columns) over all
+    //      64 rows, so every warp does the same work; a 16-row tile stops at its diagonal (X is lower
+    //      triangular)
     {
-        const int which = tid >> 7;  // 0: U from v, 1: -W from k 2^G
-        const int t = tid & 127, rb = (t >> 4) * 8, cl = t & 15;
-        const float sgn = which ? -1.f : 1.f;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-            const int r0 = rb + 4 * half;
-            float acc[4][8];
+        const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+        const int which = warp >> 2, n0 = (warp & 3) * 32;
+        const __nv_bfloat16 *src = which ? sh.k : sh.q;  // k 2^G or v, bf16 rows of pitch QP
+        auto bf = [](__nv_bfloat16 h) { return __uint_as_float((uint32_t)__bfloat16_as_ushort(h) << 16); };
+        auto xb = [&](int r, int j, float be) {  // X(r, j) beta_j, rounded to the nearest tf32
+            const float x = j < r ? sh.lx[j * kLdX + r] : (j == r ? 1.f : 0.f);
+            return __uint_as_float((__float_as_uint(x * be) + 0x1000u) & 0xffffe000u);
+        };
+        float acc[4][4][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-                for (int w = 0; w < 8; ++w) acc[u][w] = 0.f;
-            for (int j = 0; j <= r0 + 3; ++j) {  // X is lower triangular
-                float s[8];
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    s[w] = which ? __bfloat162float(sh.k[j * QP + cl + 16 * w]) : sh.g[j * KP + cl + 16 * w];
+                for (int c = 0; c < 4; ++c) acc[mt][nt][c] = 0.f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int rr = r0 + u;
-                    const float xv = (j < rr ? sh.lx[j * kLdX + rr] : (j == rr ? 1.f : 0.f)) * sh.beta[j];
+        for (int ks = 0; ks < 8; ++ks) {
+            const int k0 = 8 * ks;
+            float b[4][2];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) acc[u][w] = fmaf(xv, s[w], acc[u][w]);
-                }
+            for (int nt = 0; nt < 4; ++nt) {
+                b[nt][0] = bf(src[(k0 + t) * QP + n0 + 8 * nt + g]);
+                b[nt][1] = bf(src[(k0 + t + 4) * QP + n0 + 8 * nt + g]);
             }
+            const float be0 = sh.beta[k0 + t], be1 = sh.beta[k0 + t + 4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int mt = ks >> 1; mt < 4; ++mt) {
+                const int r = 16 * mt + g;
+                const float a0 = xb(r, k0 + t, be0), a1 = xb(r + 8, k0 + t, be0);
+                const float a2 = xb(r, k0 + t + 4, be1), a3 = xb(r + 8, k0 + t + 4, be1);
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    tile[box_index(which ? 6 : 4, r0 + u, cl + 16 * w)] = __float2bfloat16_rn(sgn * acc[u][w]);
+                for (int nt = 0; nt < 4; ++nt) mma_tf32(acc[mt][nt], a0, a1, a2, a3, b[nt][0], b[nt][1]);
+            }
         }
+        const float sgn = which ? -1.f : 1.f;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int r = 16 * mt + g, col = n0 + 8 * nt + 2 * t;
+                *(uint32_t *)(tile + box_index(which ? 6 : 4, r, col)) =
+                    ptx::pack_bf16(sgn * acc[mt][nt][0], sgn * acc[mt][nt][1]);
+                *(uint32_t *)(tile + box_index(which ? 6 : 4, r + 8, col)) =
+                    ptx::pack_bf16(sgn * acc[mt][nt][2], sgn * acc[mt][nt][3]);
+            }
     }
 }
 
@@ -461,6 +471,9 @@ cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st)
     if (a.N * a.HV == 0 || a.slots == 0) return cudaSuccess;
     const int smem = (int)sizeof(KdaSmem);
     cudaError_t e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // two CTAs per SM need the largest shared-memory carveout
+    e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     dim3 grid(a.slots, a.HV);
     kda_prep_kernel<<<grid, kThreadsKda, smem, st>>>(a);

@@ -336,6 +336,9 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
 {
     if (a.N * a.HV == 0 || a.slots == 0) return cudaSuccess;
+    // eight CTAs per SM need the largest shared-memory carveout
+    cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     dim3 grid(a.slots, a.HV);
     tc_prep_kernel<<<grid, kThreadsPrep, 0, st>>>(a);
     return cudaGetLastError();
