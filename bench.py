@@ -45,13 +45,13 @@ def algorithmic_work(w, N, total_tokens):
     return float(flop), float(qk_bytes + hv_bytes + state)
 
 
-def kernel_names(info):
+def kernel_names(info, channel=False):
     """Names of a call's launches in order (the plan's kernel count)."""
     eng = ["auto", "simt", "tc"][info.engine]
     cp = ["auto", "off", "exact", "warmup"][info.cp_mode]
     scan = "tc_scan_kernel" if eng == "tc" else "simt_scan_kernel"
     if eng == "tc":
-        seq = ["tc_prep_kernel"] + ([scan + " (pre-pass)", "cp_combine_kernel"] if cp == "exact" else []) + [scan]
+        seq = ["kda_prep_kernel" if channel else "tc_prep_kernel"] + ([scan + " (pre-pass)", "cp_combine_kernel"] if cp == "exact" else []) + [scan]
     else:
         seq = (["gate_stats_kernel"] if cp == "warmup" else []) + \
               ([scan + " (pre-pass)", "cp_combine_kernel"] if cp == "exact" else []) + [scan]
@@ -274,7 +274,7 @@ def run_ours(args):
     value = job_value(ws, tokens, args.steps, dev_ms)
     # dominant kernel: the longest launch of the step, timed by the library's own event marks.
     # Its algorithmic bytes are the step's (one launch covers every token-head of the call).
-    names = kernel_names(info)
+    names = kernel_names(info, channel=w.gate == "channel")
     dom = max(range(len(kernel_ms)), key=lambda j: kernel_ms[j])
     achieved = byts / (kernel_ms[dom] / 1e3) / 1e9
     step_achieved = byts / t_step / 1e9

@@ -17,7 +17,7 @@
 //
 // Tiles: bf16 [slot][HV][9][64][64] (boxes: K^ dk 0-63, Q~ dk 0-63, K^ dk 64-127, Q~ dk 64-127,
 // U dv 0-63, U dv 64-127, -W dk 0-63, -W dk 64-127, P), rows of 64 elements; gC fp32
-// [slot][HV][128].  One CTA of 256 threads per (slot, value head), two per SM (99 KB of shared
+// [slot][HV][128].  One CTA of 256 threads per (slot, value head), two per SM (102 KB of shared
 // memory: four buffers that change roles as the chunk's data dies).
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
@@ -27,7 +27,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreadsKda = 256;
-constexpr int KP = 129;  // fp32 row pitch of the 64 x 128 tiles
+constexpr int KP = 132;  // fp32 row pitch of G (rows 16-byte aligned)
 constexpr int QP = 136;  // bf16 row pitch of q
 constexpr int kLdX = 68;  // fp32 row pitch of the L / X tile
 
@@ -106,11 +106,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = tid + kThreadsKda * i, r = e >> 5, c4 = (e & 31) * 4;
-            float *gd = sh.g + r * KP + c4;
-            gd[0] = gv[i].x * kRcpLn2;
-            gd[1] = gv[i].y * kRcpLn2;
-            gd[2] = gv[i].z * kRcpLn2;
-            gd[3] = gv[i].w * kRcpLn2;
+            *(float4 *)(sh.g + r * KP + c4) =
+                make_float4(gv[i].x * kRcpLn2, gv[i].y * kRcpLn2, gv[i].z * kRcpLn2, gv[i].w * kRcpLn2);
         }
     }
     if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
@@ -130,11 +127,17 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     //      cores: for the 16-row key block b with reference row r = 16 b, [K; Q]_i 2^(G_i - G_r) times
     //      (k_j 2^(G_r - G_j))^T; the factors stay bounded while the decay inside a block is below 2^100
     float emax = 0.f;
-    for (int e = tid; e < 64 * 128; e += kThreadsKda) {
-        const int j = e >> 7, d = e & 127, r = j & ~15;
-        const float ex = sh.g[r * KP + d] - sh.g[j * KP + d];
-        emax = fmaxf(emax, ex);
-        sh.kj[j * QP + d] = __float2bfloat16_rn(__bfloat162float(sh.k[j * QP + d]) * ex2(ex));
+#pragma unroll 2
+    for (int e = tid; e < 64 * 32; e += kThreadsKda) {  // four channels per step
+        const int j = e >> 5, d = (e & 31) * 4, r = j & ~15;
+        const float4 gr = *(const float4 *)(sh.g + r * KP + d), gj = *(const float4 *)(sh.g + j * KP + d);
+        const uint2 kk = *(const uint2 *)(sh.k + j * QP + d);
+        const float2 k01 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.x);
+        const float2 k23 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.y);
+        const float e0 = gr.x - gj.x, e1 = gr.y - gj.y, e2 = gr.z - gj.z, e3 = gr.w - gj.w;
+        emax = fmaxf(emax, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
+        *(uint2 *)(sh.kj + j * QP + d) = make_uint2(ptx::pack_bf16(k01.x * ex2(e0), k01.y * ex2(e1)),
+                                                    ptx::pack_bf16(k23.x * ex2(e2), k23.y * ex2(e3)));
     }
     if (!__syncthreads_or(emax > 100.f)) {
         const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
@@ -156,8 +159,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int i = i0 + gq + 8 * (h & 1), d = d0 + 8 * (h >> 1);
-                    const float f0 = ex2(sh.g[i * KP + d] - sh.g[r * KP + d]);
-                    const float f1 = ex2(sh.g[i * KP + d + 1] - sh.g[r * KP + d + 1]);
+                    const float2 gi = *(const float2 *)(sh.g + i * KP + d), gr = *(const float2 *)(sh.g + r * KP + d);
+                    const float f0 = ex2(gi.x - gr.x), f1 = ex2(gi.y - gr.y);
                     const __nv_bfloat162 kk = *(const __nv_bfloat162 *)(sh.k + i * QP + d);
                     const __nv_bfloat162 qq = *(const __nv_bfloat162 *)(sh.q + i * QP + d);
                     fk[h] = ptx::pack_bf16(__low2float(kk) * f0, __high2float(kk) * f1);
@@ -197,8 +200,10 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
                 for (int w = 0; w < 4; ++w) ak[u][w] = aq[u][w] = 0.f;
 #pragma unroll 4
-            for (int d = 0; d < 128; ++d) {
-                // reference row j0: 2^(G_i - G_j) = 2^(G_i - G_j0) 2^(G_j0 - G_j), both factors bounded
+            for (int dd = 0; dd < 128; ++dd) {
+                // reference row j0: 2^(G_i - G_j) = 2^(G_i - G_j0) 2^(G_j0 - G_j), both factors bounded.
+                // Each thread starts at its own channel so that the sixteen j0 of a warp read distinct banks.
+                const int d = (dd + bj) & 127;
                 const float gr = sh.g[j0 * KP + d];
                 float ki[4], qi[4], kj[4];
 #pragma unroll
@@ -242,19 +247,24 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     __syncthreads();
 
     // ---- K^ = k 2^(G_C - G) and Q~ = scale q 2^G to the tiles (bf16, 8 per 16-byte store); k -> k 2^G
-    for (int e = tid; e < 64 * 16; e += kThreadsKda) {
-        const int r = e >> 4, c8 = (e & 15) * 8;
-        float kh[8], qt[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int d = c8 + u;
-            const float G = sh.g[r * KP + d], kv = __bfloat162float(sh.k[r * QP + d]);
-            kh[u] = kv * ex2(sh.gc[d] - G);
-            qt[u] = a.scale * __bfloat162float(sh.q[r * QP + d]) * ex2(G);
-            sh.k[r * QP + d] = __float2bfloat16_rn(kv * ex2(G));
-        }
-        *(uint4 *)(tile + box_index(0, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(kh);  // K^: boxes 0, 2
-        *(uint4 *)(tile + box_index(1, r, c8) + (c8 >= 64 ? 64 * 64 : 0)) = ptx::pack8(qt);  // Q~: boxes 1, 3
+#pragma unroll 2
+    for (int e = tid; e < 64 * 32; e += kThreadsKda) {  // four channels per step; a warp writes one row
+        const int r = e >> 5, c4 = (e & 31) * 4;
+        const float4 G4 = *(const float4 *)(sh.g + r * KP + c4), gc4 = *(const float4 *)(sh.gc + c4);
+        const uint2 kk = *(const uint2 *)(sh.k + r * QP + c4), qq = *(const uint2 *)(sh.q + r * QP + c4);
+        const float2 k01 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.x);
+        const float2 k23 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.y);
+        const float2 q01 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.x);
+        const float2 q23 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.y);
+        const float p0 = ex2(G4.x), p1 = ex2(G4.y), p2 = ex2(G4.z), p3 = ex2(G4.w);
+        const uint2 kh = make_uint2(ptx::pack_bf16(k01.x * ex2(gc4.x - G4.x), k01.y * ex2(gc4.y - G4.y)),
+                                    ptx::pack_bf16(k23.x * ex2(gc4.z - G4.z), k23.y * ex2(gc4.w - G4.w)));
+        const uint2 qt = make_uint2(ptx::pack_bf16(a.scale * q01.x * p0, a.scale * q01.y * p1),
+                                    ptx::pack_bf16(a.scale * q23.x * p2, a.scale * q23.y * p3));
+        *(uint2 *)(sh.k + r * QP + c4) =
+            make_uint2(ptx::pack_bf16(k01.x * p0, k01.y * p1), ptx::pack_bf16(k23.x * p2, k23.y * p3));
+        *(uint2 *)(tile + box_index(0, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = kh;  // K^: boxes 0, 2
+        *(uint2 *)(tile + box_index(1, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = qt;  // Q~: boxes 1, 3
     }
     if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
     __syncthreads();  // q and G are dead: the q buffer takes v
