@@ -271,6 +271,12 @@ __device__ __forceinline__ uint4 pack8(const float *v)
     return pk;
 }
 
+// bring [p, p + bytes) into L2 without waiting (bytes a multiple of 16, p 16-byte aligned)
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // d += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation (one warp).  The fp32 operands
 // go in as they are: the tensor core reads their top 19 bits (tf32 by truncation).
 __device__ __forceinline__ void mma_tf32(float *d, float a0, float a1, float a2, float a3, float b0, float b1)

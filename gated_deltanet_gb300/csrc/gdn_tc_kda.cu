@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     const __nv_bfloat16 *vg = (const __nv_bfloat16 *)a.v;
     __nv_bfloat16 *tile = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 9 * 4096;
 
+    // v is read only after the inverse: start bringing its rows into L2 now
+    if (tid < rows) prefetch_l2(vg + ((size_t)(t0 + tid) * HV + hv) * 128, 256);
     // ---- k, q, log-gates (rows past the end of the sequence are inert zeros), beta: 16-byte loads,
     //      all issued before the first store
     {
