@@ -80,6 +80,18 @@ SMALL = {
     # preparation takes its per-element form
     "bf16_channel_steep": Workload("bf16_channel_steep", B=1, T=150, H=2, K=128, V=128, gate="channel",
                                    g_mu=-6.0, h0=True, seed=21),
+    "bf16_channel_varlen": Workload("bf16_channel_varlen", B=1, T=300, H=2, K=128, V=128, gate="channel",
+                                    h0=True, varlen=7, seed=22),
+    "bf16_channel_gva": Workload("bf16_channel_gva", B=1, T=150, H=2, HV=4, K=128, V=128, gate="channel",
+                                 h0=True, seed=23),
+    "bf16_channel_T1": Workload("bf16_channel_T1", B=2, T=1, H=2, K=128, V=128, gate="channel", h0=True,
+                                seed=24),
+    "bf16_channel_T65": Workload("bf16_channel_T65", B=1, T=65, H=2, K=128, V=128, gate="channel", h0=True,
+                                 seed=25),
+    # per-channel decay near the tensor-core preparation's 2^100-per-16-rows limit: some chunks of each
+    # sequence take the factored products, others the per-element form (checked below)
+    "bf16_channel_mixed": Workload("bf16_channel_mixed", B=2, T=64 * 8 + 9, H=2, K=128, V=128, gate="channel",
+                                   g_mu=-3.8, h0=True, seed=26),
     "f32_strong_decay": Workload("f32_strong_decay", B=1, T=256, H=2, K=64, V=64, dtype="f32", g_mu=-2.0,
                                  h0=True, seed=9),
     "bf16_T1": Workload("bf16_T1", B=2, T=1, H=2, K=128, V=128, h0=True, seed=14),
@@ -101,9 +113,35 @@ def test_small_cases(gdn, name):
 
 
 @pytest.mark.parametrize("engine", ["simt", "tc"])
-@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_T65", "bf16_gva"])
+@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_T65", "bf16_gva", "bf16_channel_varlen",
+                                  "bf16_channel_gva"])
 def test_engines_match_oracle(gdn, engine, name):
     check(gdn, SMALL[name], engine=engine)
+
+
+def steep_blocks(w: Workload):
+    """Per (sequence, head, chunk): whether some channel decays by more than 2^100 between the first
+    row of a 16-row block and a later row of it (fp64 from the inputs)."""
+    x = make_inputs(w)
+    G = to_f64(x["g"]) / np.log(2.0)  # [B, T, HV, K]
+    out = []
+    for b in range(G.shape[0]):
+        for c0 in range(0, G.shape[1], 64):
+            Gc = np.cumsum(G[b, c0:c0 + 64], axis=0)  # [rows, HV, K]
+            for h in range(G.shape[2]):
+                worst = 0.0
+                for r in range(0, Gc.shape[0], 16):
+                    blk = Gc[r:r + 16, h]
+                    worst = max(worst, float((blk[0] - blk).max()))
+                out.append(worst > 100.0)
+    return out
+
+
+def test_channel_mixed_steepness(gdn):
+    w = SMALL["bf16_channel_mixed"]
+    st = steep_blocks(w)
+    assert any(st) and not all(st), "the case should mix steep and ordinary chunks"
+    check(gdn, w, engine="tc")
 
 
 @pytest.mark.parametrize("mode", ["exact", "warmup"])
@@ -124,6 +162,25 @@ def test_split_modes_varlen(gdn):
     w = Workload("split_varlen", B=1, T=900, H=2, K=64, V=64, dtype="f32", h0=True, varlen=5, seed=11)
     for mode in ("exact", "warmup"):
         check(gdn, w, cp_mode=mode, segment_chunks=2, keys_unit_norm=True, max_seq_len=900)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+def test_empty_and_single_token_sequences_tc(gdn, gate):
+    """The tensor-core engine (bf16, d = 128) on empty, one-token and exact-chunk sequences."""
+    cu = torch.tensor([0, 0, 1, 65, 65, 129, 130], dtype=torch.int64)
+    w = Workload("edge_varlen_tc", B=1, T=130, H=2, K=128, V=128, gate=gate, h0=True, seed=27)
+    x = make_inputs(w)
+    x["cu_seqlens"] = cu
+    x["h0"] = 0.1 * torch.randn(6, 2, 128, 128, generator=torch.Generator().manual_seed(4))
+    ro, rh = recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], cu, gate=x["gate"])
+    xd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    o, ht = gdn.chunk_gated_delta_rule(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], x["scale"], xd["h0"],
+                                       True, xd["cu_seqlens"], engine="tc")
+    torch.cuda.synchronize()
+    assert gdn.read_device_status() == 0
+    tol_check("edge tc o", to_f64(o), ro, "bf16")
+    tol_check("edge tc ht", to_f64(ht), rh, "bf16")
+    assert torch.equal(ht[0].cpu(), x["h0"][0]) and torch.equal(ht[3].cpu(), x["h0"][3])
 
 
 def test_empty_and_single_token_sequences(gdn):
