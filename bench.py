@@ -73,7 +73,9 @@ def read_peaks():
 KERNEL_SOURCES = {  # the files a kernel's code comes from (its own unit and the shared headers)
     "scan": ("gdn_tc.cu", "gdn_ptx.cuh", "gdn_internal.cuh"),
     "prep": ("gdn_tc_prep.cu", "gdn_ptx.cuh", "gdn_internal.cuh"),
+    "kda_prep": ("gdn_tc_kda.cu", "gdn_ptx.cuh", "gdn_internal.cuh"),
 }
+KERNEL_KEYS = {"tc_scan_kernel": "scan", "tc_prep_kernel": "prep", "kda_prep_kernel": "kda_prep"}
 
 
 def kernel_sources_sha(kernel="scan"):
@@ -302,7 +304,7 @@ def run_ours(args):
         "tflops": flop / t_step / 1e12,
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind,
-                     "traffic": ncu_traffic(w.name, "scan") if names[dom] == "tc_scan_kernel" else None,
+                     "traffic": ncu_traffic(w.name, KERNEL_KEYS[names[dom]]) if names[dom] in KERNEL_KEYS else None,
                      "kernel_ms": {names[j]: kernel_ms[j] for j in range(len(kernel_ms))},
                      "step": {"achieved": step_achieved, "frac": step_achieved / peaks["hbm_gbs"]},
                      "algorithmic_bytes": byts, "algorithmic_flop": flop,
