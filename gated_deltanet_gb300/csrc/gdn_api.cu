@@ -23,7 +23,8 @@ struct Plan {
     int seg_chunks, n_seg, value_tiles, kernels, max_nt;
     float log2_eps;
     // workspace layout
-    size_t off_warm, off_segout, off_seginit, off_tiles, off_gc, tile_slots, bytes;
+    size_t off_warm, off_segout, off_seginit, off_tiles, off_gc, off_order, tile_slots, bytes;
+    int n_buckets;
     bool kda;  // tensor-core engine with per-channel gates
 };
 
@@ -110,7 +111,8 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     if (p->n_seg == 1 && cp != GDN_CP_OFF) { p->cp = GDN_CP_OFF; cp = GDN_CP_OFF; p->seg_chunks = std::max(max_nt, 1); }
 
     size_t off = kStatusBytes;
-    p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->off_gc = p->tile_slots = 0;
+    p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->off_gc = p->off_order = p->tile_slots = 0;
+    p->n_buckets = 0;
     if (p->engine == GDN_ENGINE_TC) {
         // operand tiles of every chunk, written by the preparation kernel
         p->tile_slots = (size_t)tile_slots((int64_t)s->B * s->T, N);
@@ -121,6 +123,12 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
             off = align_up(off + p->tile_slots * s->HV * 512, 256);
         } else {
             off = align_up(off + p->tile_slots * s->HV * kTcTileBytesPerChunk, 256);
+        }
+        if (varlen && N > 1) {
+            // packed sequences of different lengths: the preparation sorts them longest first for the scan
+            p->off_order = off;
+            p->n_buckets = std::min(max_nt + 1, kOrderBuckets);
+            off = align_up(off + (size_t)N * sizeof(int), 256);
         }
     }
     const size_t nsegs = (size_t)N * s->HV * p->n_seg;
@@ -213,6 +221,8 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         ka.tiles = wsb + p.off_tiles;
         ka.gc = (float *)(wsb + p.off_gc);
         ka.T = s->T; ka.H = s->H; ka.HV = s->HV; ka.N = N; ka.slots = (int)p.tile_slots;
+        if (p.off_order) { ka.seq_order = (int *)(wsb + p.off_order); ka.n_buckets = p.n_buckets; }
+        a.seq_order = ka.seq_order;
         mark();
         e = launch_kda_prep(ka, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -225,6 +235,8 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         pa.tiles = wsb + p.off_tiles;
         pa.T = s->T; pa.H = s->H; pa.HV = s->HV; pa.N = N; pa.slots = (int)p.tile_slots;
         pa.check_norm = p.cp == GDN_CP_WARMUP;
+        if (p.off_order) { pa.seq_order = (int *)(wsb + p.off_order); pa.n_buckets = p.n_buckets; }
+        a.seq_order = pa.seq_order;
         pa.status = status;
         mark();
         e = launch_tc_prep(pa, stream);

@@ -45,6 +45,7 @@ struct ScanArgs {
     int mode;               // Mode
     int vext;               // value columns processed: V (forward) or V + K (prepass)
     unsigned *status;
+    const int *seq_order;   // [N] sequence of each grid.z group (longest first), nullable = natural order
 };
 
 struct CombineArgs {
@@ -75,6 +76,8 @@ struct PrepArgs {
     int T, H, HV, N, slots;
     int check_norm;             // flag beta ||k||^2 > 2 in the status word (warmup split)
     unsigned *status;
+    int *seq_order;             // nullable: block (0, 0) writes the longest-first sequence order here
+    int n_buckets;              //   chunk-count buckets of that sort (<= kOrderBuckets)
 };
 
 // Launchers (return cudaGetLastError() of the launch).
@@ -97,6 +100,8 @@ struct KdaPrepArgs {
     void *tiles;                // bf16 [slot][HV][9][64][64] (see gdn_tc_kda.cu)
     float *gc;                  // [slot][HV][128] per-channel chunk decay 2^G_C
     int T, H, HV, N, slots;
+    int *seq_order;             // as PrepArgs
+    int n_buckets;
 };
 cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st);
 constexpr size_t kKdaTileBytesPerChunk = 9 * 64 * 64 * 2 + 128 * 4;  // nine bf16 boxes and gC
@@ -109,6 +114,48 @@ constexpr size_t kTcTileBytesPerChunk = 2 * 64 * 64 * 2;  // T_U and T_W, bf16
 // slot floor(bos / 64) + n + c: consecutive sequences never overlap and a batch of
 // `tokens` tokens in `nseq` sequences needs at most tokens / 64 + nseq + 1 slots.
 __host__ __device__ inline int64_t tile_slot(int64_t bos, int n, int c) { return bos / kChunk + n + c; }
+
+// Longest-first order of the sequences of a packed batch.  The scan's CTAs are dispatched in grid
+// order, so with this order the longest chains start first and the short ones fill in behind them
+// (longest-processing-time-first scheduling).  One CTA, every thread: a counting sort on the chunk
+// count (counts above n_buckets - 1 share the top bucket), descending; equal counts in any order.
+// `hist` is shared-memory scratch of n_buckets + 32 ints.
+constexpr int kOrderBuckets = 4096;
+__device__ inline void order_longest_first(const int64_t *cu, int N, int n_buckets, int *hist, int *order)
+{
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    int *wsum = hist + n_buckets;
+    auto key = [&](int m) -> int {
+        const long long nc = (cu[m + 1] - cu[m] + kChunk - 1) / kChunk;
+        return n_buckets - 1 - (int)(nc < 0 ? 0 : nc > n_buckets - 1 ? n_buckets - 1 : nc);
+    };
+    for (int i = tid; i < n_buckets; i += nt) hist[i] = 0;
+    __syncthreads();
+    for (int m = tid; m < N; m += nt) atomicAdd(&hist[key(m)], 1);
+    __syncthreads();
+    // exclusive prefix sum over the buckets: a contiguous run per thread, then across threads
+    const int per = (n_buckets + nt - 1) / nt;
+    const int b0 = min(tid * per, n_buckets), b1 = min(b0 + per, n_buckets);
+    int s = 0;
+    for (int b = b0; b < b1; ++b) s += hist[b];
+    int incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - s;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int b = b0; b < b1; ++b) {
+        const int c = hist[b];
+        hist[b] = run;
+        run += c;
+    }
+    __syncthreads();
+    for (int m = tid; m < N; m += nt) order[atomicAdd(&hist[key(m)], 1)] = m;
+}
 __host__ __device__ inline int64_t tile_slots(int64_t tokens, int nseq) { return tokens / kChunk + nseq + 1; }
 size_t tc_smem_bytes();
 

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int vt = blockIdx.x, seg = blockIdx.y, pair = blockIdx.z;
     const int HV = a.HV, V = a.V;
-    const int n = pair / HV, hv = pair % HV, hq = hv / (HV / a.H);
+    const int n = a.seq_order ? a.seq_order[pair / HV] : pair / HV, hv = pair % HV, hq = hv / (HV / a.H);
     int64_t bos, len;
     if (a.cu_seqlens) {
         bos = a.cu_seqlens[n];

@@ -56,6 +56,10 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     extern __shared__ __align__(16) uint8_t kda_raw[];
     KdaSmem &sh = *(KdaSmem *)kda_raw;
     const int tid = threadIdx.x;
+    if (a.seq_order && blockIdx.x == 0 && blockIdx.y == 0) {  // the scan's CTA order (G's buffer as scratch)
+        order_longest_first(a.cu_seqlens, a.N, a.n_buckets, (int *)sh.g, a.seq_order);
+        __syncthreads();
+    }
     const int slot = blockIdx.x, hv = blockIdx.y;
     const int HV = a.HV, hq = hv / (HV / a.H);
     auto seq_start = [&](int m) -> int64_t { return a.cu_seqlens ? a.cu_seqlens[m] : (int64_t)m * a.T; };

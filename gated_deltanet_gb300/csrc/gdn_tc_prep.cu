@@ -46,6 +46,10 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 {
     __shared__ __align__(1024) PrepSmem sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.seq_order && blockIdx.x == 0 && blockIdx.y == 0) {  // the scan's CTA order (K's buffer as scratch)
+        order_longest_first(a.cu_seqlens, a.N, a.n_buckets, (int *)sh.k, a.seq_order);
+        __syncthreads();
+    }
     const int slot = blockIdx.x, hv = blockIdx.y;
     const int HV = a.HV, hq = hv / (HV / a.H);
     auto seq_start = [&](int m) -> int64_t { return a.cu_seqlens ? a.cu_seqlens[m] : (int64_t)m * a.T; };
