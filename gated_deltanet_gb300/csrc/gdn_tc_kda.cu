@@ -145,6 +145,26 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         *(uint2 *)(sh.kj + j * QP + d) = make_uint2(ptx::pack_bf16(k01.x * ex2(e0), k01.y * ex2(e1)),
                                                     ptx::pack_bf16(k23.x * ex2(e2), k23.y * ex2(e3)));
     }
+    // K^ = k 2^(G_C - G) and Q~ = scale q 2^G to the tiles (four channels per step, a warp writes one row);
+    // k, q and G are only read here, so this runs beside the gated products
+    auto khat_qtilde_out = [&](int first, int stride) {
+#pragma unroll 2
+        for (int e = first; e < 64 * 32; e += stride) {
+            const int r = e >> 5, c4 = (e & 31) * 4;
+            const float4 G4 = *(const float4 *)(sh.g + r * KP + c4), gc4 = *(const float4 *)(sh.gc + c4);
+            const uint2 kk = *(const uint2 *)(sh.k + r * QP + c4), qq = *(const uint2 *)(sh.q + r * QP + c4);
+            const float2 k01 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.x);
+            const float2 k23 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.y);
+            const float2 q01 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.x);
+            const float2 q23 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.y);
+            const uint2 kh = make_uint2(ptx::pack_bf16(k01.x * ex2(gc4.x - G4.x), k01.y * ex2(gc4.y - G4.y)),
+                                        ptx::pack_bf16(k23.x * ex2(gc4.z - G4.z), k23.y * ex2(gc4.w - G4.w)));
+            const uint2 qt = make_uint2(ptx::pack_bf16(a.scale * q01.x * ex2(G4.x), a.scale * q01.y * ex2(G4.y)),
+                                        ptx::pack_bf16(a.scale * q23.x * ex2(G4.z), a.scale * q23.y * ex2(G4.w)));
+            *(uint2 *)(tile + box_index(0, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = kh;  // K^: boxes 0, 2
+            *(uint2 *)(tile + box_index(1, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = qt;  // Q~: boxes 1, 3
+        }
+    };
     if (!__syncthreads_or(emax > 100.f)) {
         const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
         // item = (key block b, 16-row tile mt >= b): ten of them over the eight warps
@@ -157,7 +177,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ak[nt][c] = aq[nt][c] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
             for (int ks = 0; ks < 8; ++ks) {
                 const int d0 = 16 * ks + 2 * t;
                 // A fragments (rows i0 + gq (+8), columns d0, d0 + 1 (+8)) with the factor 2^(G_i - G_r)
@@ -190,10 +210,14 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                     tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(j <= i ? a.scale * aq[nt][c] : 0.f);
                 }
         }
-        // P is zero above the diagonal blocks (L there is never read)
-        for (int e = tid; e < 64 * 64; e += kThreadsKda) {
-            const int i = e >> 6, j = e & 63;
-            if ((j >> 4) > (i >> 4)) tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(0.f);
+        // warps 2-7 have one item, warps 0 and 1 two: the others write K^, Q~ and the zero blocks of P
+        // (above the diagonal blocks; L there is never read) meanwhile
+        if (warp >= 2) {
+            khat_qtilde_out(tid - 64, kThreadsKda - 64);
+            for (int e = tid - 64; e < 64 * 64; e += kThreadsKda - 64) {
+                const int i = e >> 6, j = e & 63;
+                if ((j >> 4) > (i >> 4)) tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(0.f);
+            }
         }
     } else {
         // steep chunk: per-element factors with a reference row per group of four (4 x 4 blocks)
@@ -249,34 +273,13 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                 *(uint2 *)(tile + (size_t)(8 * 64 + i0 + u) * 64 + j0) = make_uint2(0u, 0u);
             }
         }
+        khat_qtilde_out(tid, kThreadsKda);
     }
-    __syncthreads();
-
-    // ---- K^ = k 2^(G_C - G) and Q~ = scale q 2^G to the tiles (bf16, 8 per 16-byte store); k -> k 2^G
-#pragma unroll 2
-    for (int e = tid; e < 64 * 32; e += kThreadsKda) {  // four channels per step; a warp writes one row
-        const int r = e >> 5, c4 = (e & 31) * 4;
-        const float4 G4 = *(const float4 *)(sh.g + r * KP + c4), gc4 = *(const float4 *)(sh.gc + c4);
-        const uint2 kk = *(const uint2 *)(sh.k + r * QP + c4), qq = *(const uint2 *)(sh.q + r * QP + c4);
-        const float2 k01 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.x);
-        const float2 k23 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.y);
-        const float2 q01 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.x);
-        const float2 q23 = __bfloat1622float2(*(const __nv_bfloat162 *)&qq.y);
-        const float p0 = ex2(G4.x), p1 = ex2(G4.y), p2 = ex2(G4.z), p3 = ex2(G4.w);
-        const uint2 kh = make_uint2(ptx::pack_bf16(k01.x * ex2(gc4.x - G4.x), k01.y * ex2(gc4.y - G4.y)),
-                                    ptx::pack_bf16(k23.x * ex2(gc4.z - G4.z), k23.y * ex2(gc4.w - G4.w)));
-        const uint2 qt = make_uint2(ptx::pack_bf16(a.scale * q01.x * p0, a.scale * q01.y * p1),
-                                    ptx::pack_bf16(a.scale * q23.x * p2, a.scale * q23.y * p3));
-        *(uint2 *)(sh.k + r * QP + c4) =
-            make_uint2(ptx::pack_bf16(k01.x * p0, k01.y * p1), ptx::pack_bf16(k23.x * p2, k23.y * p3));
-        *(uint2 *)(tile + box_index(0, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = kh;  // K^: boxes 0, 2
-        *(uint2 *)(tile + box_index(1, r, c4) + (c4 >= 64 ? 64 * 64 : 0)) = qt;  // Q~: boxes 1, 3
-    }
-    if (tid < 128) a.gc[((size_t)slot * HV + hv) * 128 + tid] = ex2(sh.gc[tid]);
-    __syncthreads();  // q and G are dead: the q buffer takes v
+    __syncthreads();  // q is dead: its buffer takes v
 
     // ---- X = (I + L)^-1 by blocks (FLA page, sec. 4): 8 x 8 forward substitution, exact merges 8 -> 16
-    //      (FMA), 16 -> 32 and 32 -> 64 (tf32 m16n8k8) on warps 0-3; warps 4-7 load v meanwhile
+    //      (FMA), 16 -> 32 and 32 -> 64 (tf32 m16n8k8) on warps 0-3; warps 4-7 load v, scale k by 2^G and
+    //      write g_C meanwhile
     if (tid < 128) {
         const int warp = tid >> 5, lane = tid & 31;
         float *lx = sh.lx;
@@ -409,13 +412,25 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             }
         }
     } else {
-        // v (bf16) into the q buffer: 16-byte loads, all issued first
+        // v (bf16) into the q buffer: 16-byte loads, all issued first; meanwhile k -> k 2^G in place (the
+        // last use of k and G) and the per-channel chunk decay
         uint4 vv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = tid - 128 + 128 * i, r = e >> 4, c8 = (e & 15) * 8;
             vv[i] = make_uint4(0, 0, 0, 0);
             if (r < rows) vv[i] = *(const uint4 *)(vg + ((size_t)(t0 + r) * HV + hv) * 128 + c8);
+        }
+        a.gc[((size_t)slot * HV + hv) * 128 + tid - 128] = ex2(sh.gc[tid - 128]);
+#pragma unroll 4
+        for (int e = tid - 128; e < 64 * 32; e += 128) {
+            const int r = e >> 5, c4 = (e & 31) * 4;
+            const float4 G4 = *(const float4 *)(sh.g + r * KP + c4);
+            const uint2 kk = *(const uint2 *)(sh.k + r * QP + c4);
+            const float2 k01 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.x);
+            const float2 k23 = __bfloat1622float2(*(const __nv_bfloat162 *)&kk.y);
+            *(uint2 *)(sh.k + r * QP + c4) = make_uint2(ptx::pack_bf16(k01.x * ex2(G4.x), k01.y * ex2(G4.y)),
+                                                        ptx::pack_bf16(k23.x * ex2(G4.z), k23.y * ex2(G4.w)));
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
