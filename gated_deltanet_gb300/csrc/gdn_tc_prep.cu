@@ -300,9 +300,11 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     }
     __syncthreads();
 
-    // ---- operand tiles; thread = (row r, 32 columns), two 16-byte pieces per tile and step
+    // ---- operand tiles; thread = (row r, 32 columns), two 16-byte pieces per tile and step.  The two
+    //      threads of a row read X^T 32 rows apart (the same bank): the second takes each group of eight
+    //      columns upper half first, so the pair always reads banks 16 apart
     {
-        const int r = tid >> 1, h = tid & 1;
+        const int r = tid >> 1, h = tid & 1, rot = 4 * h;
         const float gr = sh.gam[r], Gr = sh.G[r];
         const bool factored = sh.G[63] >= kFactorFloor;
         __nv_bfloat16 *tu = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 2 * 4096 + r * 64 + 32 * h;
@@ -310,27 +312,31 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             const int j0 = 32 * h + 8 * q;
-            const float4 b0 = *(const float4 *)(sh.beta + j0), b1 = *(const float4 *)(sh.beta + j0 + 4);
+            // step u covers column j0 + ((u + rot) & 7)
+            const float4 b0 = *(const float4 *)(sh.beta + j0 + rot), b1 = *(const float4 *)(sh.beta + j0 + 4 - rot);
             const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
             float xv[8], vu[8], vw[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int jj = j0 + u;
+                const int jj = j0 + ((u + rot) & 7);
                 xv[u] = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
                 vw[u] = gr * bj[u] * xv[u];
             }
             if (factored) {
-                const float4 c0 = *(const float4 *)(sh.br + j0), c1 = *(const float4 *)(sh.br + j0 + 4);
+                const float4 c0 = *(const float4 *)(sh.br + j0 + rot), c1 = *(const float4 *)(sh.br + j0 + 4 - rot);
                 const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                 for (int u = 0; u < 8; ++u) vu[u] = gr * cj[u] * xv[u];  // x = 0 above the diagonal
             } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    vu[u] = j0 + u <= r ? ex2(Gr - sh.G[j0 + u]) * sh.beta[j0 + u] * xv[u] : 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = j0 + ((u + rot) & 7);
+                    vu[u] = jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv[u] : 0.f;
+                }
             }
-            *(uint4 *)(tu + 8 * q) = pack8(vu);
-            *(uint4 *)(tw + 8 * q) = pack8(vw);
+            const uint4 pu = pack8(vu), pw = pack8(vw);
+            *(uint4 *)(tu + 8 * q) = h ? make_uint4(pu.z, pu.w, pu.x, pu.y) : pu;
+            *(uint4 *)(tw + 8 * q) = h ? make_uint4(pw.z, pw.w, pw.x, pw.y) : pw;
         }
     }
 }
