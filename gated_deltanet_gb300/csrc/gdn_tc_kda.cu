@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         }
         bar_sync(1, 128);
         // ---- C: 16 -> 32 (tf32 m16n8k8); warp = (merge, 8-column tile):
-        //      T = L(B, A) X(A, A)[:, tile] (kept in place of L(B, A)), then X(B, A)[:, tile] = -X(B, B) T
+        //      T = L(B, A) X(A, A)[:, tile] (kept transposed where the result goes), then
+        //      X(B, A)[:, tile] = -X(B, B) T
         {
             const int g = lane >> 2, t = lane & 3;
             const int A = 32 * (pw >> 1), Bb = A + 16, n0 = 8 * (pw & 1);
@@ -348,17 +349,22 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                 mma_tf32(d, Lx(Bb + g, A + k0 + t), Lx(Bb + g + 8, A + k0 + t), Lx(Bb + g, A + k0 + t + 4),
                          Lx(Bb + g + 8, A + k0 + t + 4), Xm(A + k0 + t, A + n0 + g), Xm(A + k0 + t + 4, A + n0 + g));
             }
-            bar_sync(1, 128);  // every warp has read L(B, A)
-            *(float2 *)(lx + (Bb + g) * kLdX + A + n0 + 2 * t) = make_float2(d[0], d[1]);
-            *(float2 *)(lx + (Bb + g + 8) * kLdX + A + n0 + 2 * t) = make_float2(d[2], d[3]);
+            // T^T into this warp's own part of the upper triangle (where X(B, A)[:, tile]^T goes): no other
+            // warp reads there, and the B fragments below read it without bank conflicts
+            lx[(A + n0 + 2 * t) * kLdX + Bb + g] = d[0];
+            lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = d[1];
+            lx[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = d[2];
+            lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g + 8] = d[3];
             __syncwarp();
             float u[4] = {0.f, 0.f, 0.f, 0.f};
     #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = 8 * ks;
                 mma_tf32(u, Xm(Bb + g, Bb + k0 + t), Xm(Bb + g + 8, Bb + k0 + t), Xm(Bb + g, Bb + k0 + t + 4),
-                         Xm(Bb + g + 8, Bb + k0 + t + 4), Lx(Bb + k0 + t, A + n0 + g), Lx(Bb + k0 + t + 4, A + n0 + g));
+                         Xm(Bb + g + 8, Bb + k0 + t + 4), lx[(A + n0 + g) * kLdX + Bb + k0 + t],
+                         lx[(A + n0 + g) * kLdX + Bb + k0 + t + 4]);
             }
+            __syncwarp();  // every lane has read T^T
             lx[(A + n0 + 2 * t) * kLdX + Bb + g] = -u[0];
             lx[(A + n0 + 2 * t + 1) * kLdX + Bb + g] = -u[1];
             lx[(A + n0 + 2 * t) * kLdX + Bb + g + 8] = -u[2];
@@ -366,7 +372,8 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         }
         bar_sync(1, 128);
         // ---- D: 32 -> 64; warp = 8-column tile of the lower-left 32 x 32 block:
-        //      T = L(32:64, 0:32) X(0:32, tile) (kept in place of L), then X(32:64, tile) = -X(32:64, 32:64) T
+        //      T = L(32:64, 0:32) X(0:32, tile) (kept transposed where the result goes), then
+        //      X(32:64, tile) = -X(32:64, 32:64) T
         {
             const int g = lane >> 2, t = lane & 3, n0 = 8 * pw;
             float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -382,18 +389,22 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                              Lx(m0 + g + 8, k0 + t + 4), b0, b1);
                 }
             }
-            bar_sync(1, 128);  // every warp has read L(32:64, 0:32)
+            // T^T into this warp's own rows of the upper-right block (where X(32:64, tile)^T goes): no other
+            // warp reads there, and the B fragments below read it without bank conflicts
     #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                *(float2 *)(lx + (32 + 16 * mt + g) * kLdX + n0 + 2 * t) = make_float2(d[mt][0], d[mt][1]);
-                *(float2 *)(lx + (32 + 16 * mt + g + 8) * kLdX + n0 + 2 * t) = make_float2(d[mt][2], d[mt][3]);
+                const int m0 = 32 + 16 * mt;
+                lx[(n0 + 2 * t) * kLdX + m0 + g] = d[mt][0];
+                lx[(n0 + 2 * t + 1) * kLdX + m0 + g] = d[mt][1];
+                lx[(n0 + 2 * t) * kLdX + m0 + g + 8] = d[mt][2];
+                lx[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = d[mt][3];
             }
             __syncwarp();
             float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const int k0 = 8 * ks;
-                const float b0 = Lx(32 + k0 + t, n0 + g), b1 = Lx(32 + k0 + t + 4, n0 + g);  // T(k, n)
+                const float b0 = lx[(n0 + g) * kLdX + 32 + k0 + t], b1 = lx[(n0 + g) * kLdX + 32 + k0 + t + 4];  // T(k, n)
     #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     if (k0 > 16 * mt + 15) continue;  // X(32 + m, 32 + k) = 0 for k > m
@@ -402,6 +413,7 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                              Xm(m0 + g + 8, 32 + k0 + t + 4), b0, b1);
                 }
             }
+            __syncwarp();  // every lane has read T^T
     #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 const int m0 = 32 + 16 * mt;
