@@ -2,6 +2,7 @@
 // C-ABI layer.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -107,6 +108,8 @@ cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st);
 constexpr size_t kKdaTileBytesPerChunk = 9 * 64 * 64 * 2 + 128 * 4;  // nine bf16 boxes and gC
 
 cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st);
+// 2-D TMA map over the operand tiles, bf16 rows of 64, box 64 x box_rows, 128-byte swizzle
+bool encode_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t box_rows);
 cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st);
 constexpr size_t kTcTileBytesPerChunk = 2 * 64 * 64 * 2;  // T_U and T_W, bf16
 

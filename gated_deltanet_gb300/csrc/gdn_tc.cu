@@ -1033,12 +1033,21 @@ bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t b
 
 }  // namespace
 
+bool encode_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t box_rows)
+{
+    return make_tiles_map(map, base, rows, box_rows);
+}
+
 size_t tc_smem_bytes() { return TcLayout<false>::kSmem; }
 
 bool tc_shape_ok(const gdn_shape *s)
 {
-    // scalar gates, or per-channel gates (their own chunk preparation; no chunk-parallel split)
-    return s->qkv_dtype == GDN_BF16 && s->K == 128 && s->V == 128 && (size_t)s->B * s->T < (1ull << 31);
+    // scalar gates, or per-channel gates (their own chunk preparation; no chunk-parallel split).  The
+    // operand tiles are addressed by 32-bit TMA row coordinates (576 rows per chunk-head at most).
+    if (!(s->qkv_dtype == GDN_BF16 && s->K == 128 && s->V == 128 && (size_t)s->B * s->T < (1ull << 31)))
+        return false;
+    const int64_t rows = tile_slots((int64_t)s->B * s->T, s->num_seqs) * (int64_t)s->HV * 576;
+    return rows < (int64_t)1 << 31;
 }
 
 bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,

@@ -25,12 +25,11 @@ constexpr uint32_t kTmemCols = 64;  // the K K^T accumulator; eight CTAs per SM 
 constexpr float kFactorFloor = -100.f;  // G_C >= this: Gam_ij = gam_i * 2^-G_j without overflow
 
 struct PrepSmem {
-    union {
-        // the chunk's K rows, 128-byte swizzled boxes of 64 rows x 64 dk (dk 0-63, then 64-127), until
-        // K K^T is formed; the 128-row operand of the product reads one box past the second (24 KB)
-        __align__(1024) uint8_t k[24576];
-        float lx[64 * kLdX];  // then L in the lower triangle, X^T in the upper: X(r, j), j < r, at lx[j * kLdX + r]
-    };
+    // bytes 0-24575: the chunk's K rows, 128-byte swizzled boxes of 64 rows x 64 dk (dk 0-63, then
+    // 64-127), until K K^T is formed (the 128-row operand of the product reads one box past the second).
+    // Then bytes 0-8191: the T_W tile, 128-byte swizzled, for its TMA store; from byte 8192 the fp32 L / X
+    // tile: L in the lower triangle, X^T in the upper (X(r, j), j < r, at lx[j * kLdX + r]).
+    __align__(1024) uint8_t buf[8192 + 64 * kLdX * 4];
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
     uint64_t bar;
     uint32_t tslot;
@@ -42,12 +41,12 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
     return r < kChunk ? (int)r : kChunk;
 }
 
-__global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a)
+__global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tmap)
 {
     __shared__ __align__(1024) PrepSmem sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (a.seq_order && blockIdx.x == 0 && blockIdx.y == 0) {  // the scan's CTA order (K's buffer as scratch)
-        order_longest_first(a.cu_seqlens, a.N, a.n_buckets, (int *)sh.k, a.seq_order);
+        order_longest_first(a.cu_seqlens, a.N, a.n_buckets, (int *)sh.buf, a.seq_order);
         __syncthreads();
     }
     const int slot = blockIdx.x, hv = blockIdx.y;
@@ -66,7 +65,7 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     if (c < 0 || c >= NT) return;  // an unused slot
     const int rows = rows_in(len, c);
     const int64_t t0 = bos + (int64_t)c * kChunk;
-    float *lx = sh.lx;
+    float *lx = (float *)(sh.buf + 8192);
 
     if (warp == 0) tmem_alloc(&sh.tslot, kTmemCols);
     if (tid == 32) {
@@ -81,7 +80,7 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (r < rows) v = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
-            *(uint4 *)(sh.k + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+            *(uint4 *)(sh.buf + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async();  // the tensor core reads them
     }
@@ -122,7 +121,7 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     tc_fence_after();
     const uint32_t tb = sh.tslot;
     if (warp == 0) {
-        const uint32_t kb = smem_u32(sh.k);
+        const uint32_t kb = smem_u32(sh.buf);
         const uint32_t idKK = idesc_bf16_f32(128, 64, 0, 0);
         if (elect_one_sync()) {
 #pragma unroll
@@ -320,7 +319,6 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         const float gr = sh.gam[r], Gr = sh.G[r];
         const bool factored = sh.G[63] >= kFactorFloor;
         __nv_bfloat16 *tu = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 2 * 4096 + r * 64 + 32 * h;
-        __nv_bfloat16 *tw = tu + 4096;
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             const int j0 = 32 * h + 8 * q;
@@ -348,8 +346,16 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             }
             const uint4 pu = pack8(vu), pw = pack8(vw);
             *(uint4 *)(tu + 8 * q) = h ? make_uint4(pu.z, pu.w, pu.x, pu.y) : pu;
-            *(uint4 *)(tw + 8 * q) = h ? make_uint4(pw.z, pw.w, pw.x, pw.y) : pw;
+            // T_W: 16-byte piece 4h + q of row r into the swizzled staging box (conflict-free)
+            *(uint4 *)(sh.buf + r * 128 + (((4 * h + q) ^ (r & 7)) << 4)) = h ? make_uint4(pw.z, pw.w, pw.x, pw.y) : pw;
         }
+    }
+    fence_proxy_async();  // the tensor-memory-access unit reads the staging box
+    __syncthreads();
+    if (tid == 0) {
+        tma_store_2d(&tmap, sh.buf, 0, (int)((((size_t)slot * HV + hv) * 2 + 1) * 64));
+        tma_store_commit();
+        tma_store_wait_read0();  // the box stays valid until the copy has read it
     }
 }
 
@@ -361,8 +367,11 @@ cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
     // eight CTAs per SM need the largest shared-memory carveout
     cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
+    // T_W leaves through a TMA store: the same tile map as the scan reads it with
+    alignas(64) CUtensorMap tmap;
+    if (!encode_tiles_map(&tmap, a.tiles, (int64_t)a.slots * a.HV * 128, 64)) return cudaErrorInvalidValue;
     dim3 grid(a.slots, a.HV);
-    tc_prep_kernel<<<grid, kThreadsPrep, 0, st>>>(a);
+    tc_prep_kernel<<<grid, kThreadsPrep, 0, st>>>(a, tmap);
     return cudaGetLastError();
 }
 
