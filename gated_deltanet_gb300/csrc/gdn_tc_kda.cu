@@ -41,6 +41,7 @@ struct KdaSmem {
     float beta[64];
     float gc[128];
 };
+static_assert(64 * KP * sizeof(float) >= 4 * 8192 + 1024, "the U / -W staging boxes fit the G buffer");
 
 __device__ __forceinline__ int rows_in(int64_t len, int c)
 {
@@ -51,7 +52,8 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 // element (row r, column col) of a 64 x 128 matrix stored as two [64][64] boxes b0, b0 + 1
 __device__ __forceinline__ size_t box_index(int b0, int r, int col) { return (size_t)((b0 + (col >> 6)) * 64 + r) * 64 + (col & 63); }
 
-__global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepArgs a)
+__global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepArgs a,
+                                                                  const __grid_constant__ CUtensorMap tmap)
 {
     extern __shared__ __align__(16) uint8_t kda_raw[];
     KdaSmem &sh = *(KdaSmem *)kda_raw;
@@ -204,10 +206,13 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int i = i0 + gq + 8 * (c >> 1), j = j0 + 8 * nt + 2 * t + (c & 1);
-                    sh.lx[i * kLdX + j] = j < i ? sh.beta[i] * ak[nt][c] : 0.f;
-                    tile[(size_t)(8 * 64 + i) * 64 + j] = __float2bfloat16_rn(j <= i ? a.scale * aq[nt][c] : 0.f);
+                for (int hr = 0; hr < 2; ++hr) {  // rows i0 + gq and i0 + gq + 8; columns j, j + 1
+                    const int i = i0 + gq + 8 * hr, j = j0 + 8 * nt + 2 * t;
+                    const float b = sh.beta[i];
+                    sh.lx[i * kLdX + j] = j < i ? b * ak[nt][2 * hr] : 0.f;
+                    sh.lx[i * kLdX + j + 1] = j + 1 < i ? b * ak[nt][2 * hr + 1] : 0.f;
+                    *(uint32_t *)(tile + (size_t)(8 * 64 + i) * 64 + j) =
+                        ptx::pack_bf16(j <= i ? a.scale * aq[nt][2 * hr] : 0.f, j + 1 <= i ? a.scale * aq[nt][2 * hr + 1] : 0.f);
                 }
         }
         // warps 2-7 have one item, warps 0 and 1 two: the others write K^, Q~ and the zero blocks of P
@@ -456,6 +461,9 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     //      operands are exact in tf32, X beta is rounded to it): warp = (U or W, 32 output columns) over all
     //      64 rows, so every warp does the same work; a 16-row tile stops at its diagonal (X is lower
     //      triangular)
+    // the four output boxes of U and -W are staged in the G buffer (dead now), rounded up to the 1024-byte
+    // alignment of the 128-byte swizzle; the buffer has the 1 KB of slack that takes
+    uint8_t *stage = (uint8_t *)sh.g + ((1024u - (smem_u32(sh.g) & 1023u)) & 1023u);
     {
         const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
         const int which = warp >> 2, n0 = (warp & 3) * 32;
@@ -491,17 +499,28 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                 for (int nt = 0; nt < 4; ++nt) mma_tf32(acc[mt][nt], a0, a1, a2, a3, b[nt][0], b[nt][1]);
             }
         }
+        // into four 128-byte-swizzled staging boxes (U dv 0-63, U dv 64-127, -W dk 0-63, -W dk 64-127) in
+        // the dead G buffer: a fragment store's eight rows hit eight different 16-byte columns (no conflicts)
         const float sgn = which ? -1.f : 1.f;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int r = 16 * mt + g, col = n0 + 8 * nt + 2 * t;
-                *(uint32_t *)(tile + box_index(which ? 6 : 4, r, col)) =
-                    ptx::pack_bf16(sgn * acc[mt][nt][0], sgn * acc[mt][nt][1]);
-                *(uint32_t *)(tile + box_index(which ? 6 : 4, r + 8, col)) =
-                    ptx::pack_bf16(sgn * acc[mt][nt][2], sgn * acc[mt][nt][3]);
+                uint8_t *bx = stage + (2 * which + (col >> 6)) * 8192 + (col & 7) * 2;
+                const uint32_t sw = (uint32_t)((((col & 63) >> 3) ^ (r & 7)) << 4);  // (r + 8) & 7 == r & 7
+                *(uint32_t *)(bx + r * 128 + sw) = ptx::pack_bf16(sgn * acc[mt][nt][0], sgn * acc[mt][nt][1]);
+                *(uint32_t *)(bx + (r + 8) * 128 + sw) = ptx::pack_bf16(sgn * acc[mt][nt][2], sgn * acc[mt][nt][3]);
             }
+    }
+    fence_proxy_async();  // the boxes leave through TMA stores
+    __syncthreads();
+    if (tid == 0) {
+        const int row0 = (int)((((size_t)slot * HV + hv) * 9 + 4) * 64);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_store_2d(&tmap, stage + b * 8192, 0, row0 + 64 * b);
+        tma_store_commit();
+        tma_store_wait_read0();  // the boxes stay valid until the copies have read them
     }
 }
 
@@ -519,7 +538,10 @@ cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st)
     e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     dim3 grid(a.slots, a.HV);
-    kda_prep_kernel<<<grid, kThreadsKda, smem, st>>>(a);
+    // U and -W leave through TMA stores (2-D map over the tiles, 64-row boxes)
+    alignas(64) CUtensorMap tmap;
+    if (!encode_tiles_map(&tmap, a.tiles, (int64_t)a.slots * a.HV * 576, 64)) return cudaErrorInvalidValue;
+    kda_prep_kernel<<<grid, kThreadsKda, smem, st>>>(a, tmap);
     return cudaGetLastError();
 }
 
