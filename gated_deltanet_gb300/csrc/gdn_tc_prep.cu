@@ -311,51 +311,48 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     }
     __syncthreads();
 
-    // ---- operand tiles; thread = (row r, 32 columns), two 16-byte pieces per tile and step.  The two
-    //      threads of a row read X^T 32 rows apart (the same bank): the second takes each group of eight
-    //      columns upper half first, so the pair always reads banks 16 apart
+    // ---- operand tiles, each staged in the dead K box (128-byte swizzle) and written by one TMA store:
+    //      T_W, then T_U once the first copy has read the box.  Thread = (row r, 32 columns), one 16-byte
+    //      piece per step.  The two threads of a row read X^T 32 rows apart (the same bank): the second
+    //      takes each group of eight columns upper half first, so the pair always reads banks 16 apart
     {
         const int r = tid >> 1, h = tid & 1, rot = 4 * h;
         const float gr = sh.gam[r], Gr = sh.G[r];
         const bool factored = sh.G[63] >= kFactorFloor;
-        __nv_bfloat16 *tu = (__nv_bfloat16 *)a.tiles + ((size_t)slot * HV + hv) * 2 * 4096 + r * 64 + 32 * h;
+        const int row0 = (int)(((size_t)slot * HV + hv) * 2 * 64);  // T_U rows; T_W follows
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            const int j0 = 32 * h + 8 * q;
-            // step u covers column j0 + ((u + rot) & 7)
-            const float4 b0 = *(const float4 *)(sh.beta + j0 + rot), b1 = *(const float4 *)(sh.beta + j0 + 4 - rot);
-            const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            float xv[8], vu[8], vw[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int jj = j0 + ((u + rot) & 7);
-                xv[u] = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                vw[u] = gr * bj[u] * xv[u];
+        for (int pass = 0; pass < 2; ++pass) {  // 0: T_W, 1: T_U
+            if (pass == 1) {
+                if (tid == 0) tma_store_wait_read0();
+                __syncthreads();
             }
-            if (factored) {
-                const float4 c0 = *(const float4 *)(sh.br + j0 + rot), c1 = *(const float4 *)(sh.br + j0 + 4 - rot);
-                const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int u = 0; u < 8; ++u) vu[u] = gr * cj[u] * xv[u];  // x = 0 above the diagonal
-            } else {
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                const int j0 = 32 * h + 8 * q;
+                // step u covers column j0 + ((u + rot) & 7)
+                const float *bsrc = pass == 0 || !factored ? sh.beta : sh.br;
+                const float4 b0 = *(const float4 *)(bsrc + j0 + rot), b1 = *(const float4 *)(bsrc + j0 + 4 - rot);
+                const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int jj = j0 + ((u + rot) & 7);
-                    vu[u] = jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv[u] : 0.f;
+                    const float xv = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                    // T_W = gam_r X beta_j; T_U = gam_r X beta_j / gam_j (factored: br = beta / gam; else the
+                    // power 2^(G_r - G_j) per element, zero above the diagonal)
+                    v[u] = pass == 0 || factored ? gr * bj[u] * xv : (jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv : 0.f);
                 }
+                const uint4 pk = pack8(v);
+                *(uint4 *)(sh.buf + r * 128 + (((4 * h + q) ^ (r & 7)) << 4)) = h ? make_uint4(pk.z, pk.w, pk.x, pk.y) : pk;
             }
-            const uint4 pu = pack8(vu), pw = pack8(vw);
-            *(uint4 *)(tu + 8 * q) = h ? make_uint4(pu.z, pu.w, pu.x, pu.y) : pu;
-            // T_W: 16-byte piece 4h + q of row r into the swizzled staging box (conflict-free)
-            *(uint4 *)(sh.buf + r * 128 + (((4 * h + q) ^ (r & 7)) << 4)) = h ? make_uint4(pw.z, pw.w, pw.x, pw.y) : pw;
+            fence_proxy_async();  // the tensor-memory-access unit reads the staging box
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_2d(&tmap, sh.buf, 0, row0 + (pass == 0 ? 64 : 0));
+                tma_store_commit();
+            }
         }
-    }
-    fence_proxy_async();  // the tensor-memory-access unit reads the staging box
-    __syncthreads();
-    if (tid == 0) {
-        tma_store_2d(&tmap, sh.buf, 0, (int)((((size_t)slot * HV + hv) * 2 + 1) * 64));
-        tma_store_commit();
-        tma_store_wait_read0();  // the box stays valid until the copy has read it
+        if (tid == 0) tma_store_wait_read0();  // the box stays valid until the copy has read it
     }
 }
 
