@@ -80,6 +80,9 @@ SMALL = {
     # preparation takes its per-element form
     "bf16_channel_steep": Workload("bf16_channel_steep", B=1, T=150, H=2, K=128, V=128, gate="channel",
                                    g_mu=-6.0, h0=True, seed=21),
+    # more packed sequences than the preparation CTA has threads: the longest-first sort takes several
+    # passes, many lengths share a chunk count
+    "bf16_varlen_many": Workload("bf16_varlen_many", B=1, T=200, H=2, K=128, V=128, h0=True, varlen=300, seed=28),
     "bf16_channel_varlen": Workload("bf16_channel_varlen", B=1, T=300, H=2, K=128, V=128, gate="channel",
                                     h0=True, varlen=7, seed=22),
     "bf16_channel_gva": Workload("bf16_channel_gva", B=1, T=150, H=2, HV=4, K=128, V=128, gate="channel",
