@@ -312,38 +312,56 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     __syncthreads();
 
     // ---- operand tiles, each staged in the dead K box (128-byte swizzle) and written by one TMA store:
-    //      T_W, then T_U once the first copy has read the box.  Thread = (row r, 32 columns), one 16-byte
-    //      piece per step.  The two threads of a row read X^T 32 rows apart (the same bank): the second
-    //      takes each group of eight columns upper half first, so the pair always reads banks 16 apart
+    //      T_W, then T_U once the first copy has read the box.  Warp = (32 rows, 32 columns), lane = row,
+    //      one 16-byte piece per step: a warp reads consecutive rows of X^T (no conflicts) and its
+    //      quadrant of the lower-triangular tiles is all zeros (rows 0-31, columns 32-63: written once,
+    //      both tiles share them), all below the diagonal (rows 32-63, columns 0-31: no masks) or a
+    //      diagonal block
     {
-        const int r = tid >> 1, h = tid & 1, rot = 4 * h;
+        const int r = 32 * (warp & 1) + lane, h = warp >> 1;
+        const bool zeros = warp == 2, below = warp == 1;  // warp-uniform
         const float gr = sh.gam[r], Gr = sh.G[r];
         const bool factored = sh.G[63] >= kFactorFloor;
         const int row0 = (int)(((size_t)slot * HV + hv) * 2 * 64);  // T_U rows; T_W follows
+        uint8_t *srow = sh.buf + r * 128;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {  // 0: T_W, 1: T_U
             if (pass == 1) {
                 if (tid == 0) tma_store_wait_read0();
                 __syncthreads();
             }
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                const int j0 = 32 * h + 8 * q;
-                // step u covers column j0 + ((u + rot) & 7)
-                const float *bsrc = pass == 0 || !factored ? sh.beta : sh.br;
-                const float4 b0 = *(const float4 *)(bsrc + j0 + rot), b1 = *(const float4 *)(bsrc + j0 + 4 - rot);
-                const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                float v[8];
+            if (zeros) {
+                if (pass == 0) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int jj = j0 + ((u + rot) & 7);
-                    const float xv = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                    // T_W = gam_r X beta_j; T_U = gam_r X beta_j / gam_j (factored: br = beta / gam; else the
-                    // power 2^(G_r - G_j) per element, zero above the diagonal)
-                    v[u] = pass == 0 || factored ? gr * bj[u] * xv : (jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv : 0.f);
+                    for (int q = 0; q < 4; ++q) *(uint4 *)(srow + (((4 + q) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                 }
-                const uint4 pk = pack8(v);
-                *(uint4 *)(sh.buf + r * 128 + (((4 * h + q) ^ (r & 7)) << 4)) = h ? make_uint4(pk.z, pk.w, pk.x, pk.y) : pk;
+            } else {
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const int j0 = 32 * h + 8 * q;
+                    const float *bsrc = pass == 0 || !factored ? sh.beta : sh.br;
+                    const float4 b0 = *(const float4 *)(bsrc + j0), b1 = *(const float4 *)(bsrc + j0 + 4);
+                    const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    float v[8];
+                    if (below) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const float xv = lx[(j0 + u) * kLdX + r];
+                            // T_W = gam_r X beta_j; T_U = gam_r X beta_j / gam_j (factored: br = beta / gam;
+                            // else the power 2^(G_r - G_j) per element)
+                            v[u] = pass == 0 || factored ? gr * bj[u] * xv : ex2(Gr - sh.G[j0 + u]) * bj[u] * xv;
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int jj = j0 + u;
+                            const float xv = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
+                            v[u] = pass == 0 || factored ? gr * bj[u] * xv
+                                                         : (jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv : 0.f);
+                        }
+                    }
+                    *(uint4 *)(srow + (((4 * h + q) ^ (r & 7)) << 4)) = pack8(v);
+                }
             }
             fence_proxy_async();  // the tensor-memory-access unit reads the staging box
             __syncthreads();
