@@ -72,21 +72,11 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         mbar_init(&sh.bar, 1);
         fence_mbar_init();
     }
-    // ---- K rows into the swizzled boxes (rows past the end of the sequence are zero), gates
-    {
-        const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < rows) v = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
-            *(uint4 *)(sh.buf + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async();  // the tensor core reads them
-    }
+    // ---- K rows into the swizzled boxes (rows past the end of the sequence are zero), gates; every global
+    //      load (warp 0's gates included) is issued before the first store waits for one
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp == 0) {
-        const int r0 = 2 * lane, r1 = r0 + 1;
-        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
         if (r0 < rows) {
             g0 = a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2;
             b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
@@ -95,6 +85,24 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             g1 = a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2;
             b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
         }
+    }
+    {
+        const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k;
+        uint4 kv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
+            kv[i] = make_uint4(0, 0, 0, 0);
+            if (r < rows) kv[i] = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
+            *(uint4 *)(sh.buf + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = kv[i];
+        }
+        fence_proxy_async();  // the tensor core reads them
+    }
+    if (warp == 0) {
         float sp = g0 + g1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
