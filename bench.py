@@ -347,10 +347,14 @@ def _calibrated_sample(w, seconds):
     T_full = int(x["q"].shape[1])
     T_s = min(T_full, 64)
     fn, ntok = _oracle_sample(w, x, T_s)
-    t0 = time.perf_counter()
-    fn()
-    dt = max(time.perf_counter() - t0, 1e-4)
-    if dt < seconds and T_s < T_full:
+    # grow the prefix by extrapolation until a run takes at least half the target (a short first run
+    # is dominated by thread start-up, so one extrapolation undershoots)
+    for _ in range(3):
+        t0 = time.perf_counter()
+        fn()
+        dt = max(time.perf_counter() - t0, 1e-4)
+        if dt >= 0.5 * seconds or T_s >= T_full:
+            break
         T_s = int(min(T_full, max(T_s + 1, T_s * seconds / dt)))
         fn, ntok = _oracle_sample(w, x, T_s)
     return x, fn, ntok, T_s
@@ -359,9 +363,11 @@ def _calibrated_sample(w, seconds):
 def _describe(w, x, ntok, T_s, dt):
     from oracle.recurrence import host_cores
     cores = min(host_cores(), x["N"] * w.hv)
+    T_full = int(x["q"].shape[1])
+    what = "the whole workload" if T_s >= T_full else f"the first {T_s} tokens of each sequence of the workload"
     return {"unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 C recurrence (pthreads over sequence x head) on the first {T_s} tokens of "
-                      f"the workload ({ntok} tokens x {w.hv} heads, {dt:.2f} s wall per run)"}
+            "sample": f"fp64 C recurrence (pthreads over sequence x head) on {what} "
+                      f"({ntok} tokens x {w.hv} heads, {dt:.2f} s wall per run, {dt * cores:.1f} core-s)"}
 
 
 def cpu_baseline(w, seconds):
