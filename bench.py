@@ -335,7 +335,7 @@ def _oracle_sample(w, x, T_s):
         e = int(cu[n])
         return (lambda: recurrence(x["q"][:, :e], x["k"][:, :e], x["v"][:, :e], x["g"][:, :e],
                                    x["beta"][:, :e], x["scale"], x["h0"][:n] if x["h0"] is not None else None,
-                                   x["cu_seqlens"][:n + 1])), e
+                                   x["cu_seqlens"][:n + 1], gate=x["gate"])), e
     return (lambda: recurrence(x["q"][:, sl], x["k"][:, sl], x["v"][:, sl], x["g"][:, sl], x["beta"][:, sl],
                                x["scale"], x["h0"], None, gate=x["gate"])), x["q"].shape[0] * min(T_s, x["q"].shape[1])
 
@@ -364,7 +364,12 @@ def _describe(w, x, ntok, T_s, dt):
     from oracle.recurrence import host_cores
     cores = min(host_cores(), x["N"] * w.hv)
     T_full = int(x["q"].shape[1])
-    what = "the whole workload" if T_s >= T_full else f"the first {T_s} tokens of each sequence of the workload"
+    if T_s >= T_full:
+        what = "the whole workload"
+    elif x["cu_seqlens"] is not None:
+        what = "the leading packed sequences of the workload"
+    else:
+        what = f"the first {T_s} tokens of each sequence of the workload"
     return {"unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 C recurrence (pthreads over sequence x head) on {what} "
                       f"({ntok} tokens x {w.hv} heads, {dt:.2f} s wall per run, {dt * cores:.1f} core-s)"}
