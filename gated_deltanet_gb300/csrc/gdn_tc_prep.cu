@@ -119,14 +119,14 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         sh.br[r0] = b0 * ex2(-G0);  // used only when G_C >= kFactorFloor
         sh.br[r1] = b1 * ex2(-G1);
     }
+    // one barrier publishes the K boxes, the gates and the tensor-memory allocation
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
     // ---- K K^T on the tensor core: one M = 128 product ([K; next box] K^T, lanes 0-63 hold K K^T);
     //      L row r = beta_r (K K^T)[r, :] straight from tensor memory (the upper triangle is
     //      overwritten by X^T later and never read before)
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tb = sh.tslot;
     if (warp == 0) {
         const uint32_t kb = smem_u32(sh.buf);
