@@ -98,3 +98,17 @@ def test_plans(gdn):
     # a one-chunk sequence never splits
     p = gdn.plan(1, 64, 1, 1, 64, 64, num_sms=152, cp_mode="exact")
     assert p.cp_mode == 1
+
+
+def test_packed_batches_reserve_the_sequence_order(gdn):
+    # a packed batch on the tensor-core engine keeps one int per sequence for the longest-first order
+    # (on top of the operand tiles, whose slot count also grows by one per sequence)
+    one = gdn.plan(1, 8192, 16, 16, 128, 128, num_seqs=1, num_sms=152, cp_mode="off")
+    many = gdn.plan(1, 8192, 16, 16, 128, 128, num_seqs=300, num_sms=152, cp_mode="off")
+    assert many.engine == 2 and one.engine == 2
+    tiles_per_slot = 16 * 2 * 64 * 64 * 2
+    assert many.workspace_bytes >= one.workspace_bytes + 299 * tiles_per_slot + 300 * 4
+    # the CUDA-core engine does not sort
+    f_one = gdn.plan(1, 8192, 16, 16, 128, 128, dtype="f32", num_seqs=1, num_sms=152, cp_mode="off")
+    f_many = gdn.plan(1, 8192, 16, 16, 128, 128, dtype="f32", num_seqs=300, num_sms=152, cp_mode="off")
+    assert f_many.workspace_bytes == f_one.workspace_bytes
