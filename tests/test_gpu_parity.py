@@ -273,3 +273,19 @@ def test_workload_varlen_bf16_sampled(gdn):
 
 def test_workload_channel_bf16(gdn):
     check(gdn, WORKLOADS["channel_bf16"])
+
+
+@pytest.mark.parametrize("name", ["bf16_varlen_many", "bf16_channel_varlen", "bf16_mixed_decay", "bf16_gva"])
+def test_repeat_runs_are_bitwise_identical(gdn, name):
+    """Every kernel is deterministic: no atomics in any sum, the longest-first order of packed sequences
+    (built with atomics) only changes which CTA runs when.  Two runs give the same bits."""
+    w = SMALL[name]
+    x = make_inputs(w, device="cuda")
+    outs = []
+    for _ in range(2):
+        o, ht = gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
+                                           x["cu_seqlens"])
+        torch.cuda.synchronize()
+        outs.append((o.clone(), ht.clone()))
+    assert gdn.read_device_status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
