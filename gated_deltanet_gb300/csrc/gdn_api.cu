@@ -455,7 +455,6 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, 
         total = align_up(total + sizes[i], 256);
     }
     void *arena = nullptr;
-    size_t arena_bytes = 0;
     {
         // the host path keeps its own arena per (device, stream), keyed apart from the workspaces
         int dev = 0;
@@ -475,9 +474,7 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, 
             w.bytes = bytes;
         }
         arena = w.ptr;
-        arena_bytes = w.bytes;
     }
-    (void)arena_bytes;
     char *A = (char *)arena;
     const void *src[7] = {q, k, v, g, beta, h0, cu};
     for (int i = 0; i < 7; ++i)
