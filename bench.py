@@ -178,6 +178,13 @@ def job_value(world_size, tokens_per_rank, steps, max_ms):
     return world_size * tokens_per_rank * steps / (max_ms / 1e3)
 
 
+def bench_options(w):
+    """The call options of the timed step (the GPU parity tests run the same plan).  The
+    workloads L2-normalise k and take beta = sigmoid(.), so the caller may assert unit-norm keys;
+    packed batches bound one sequence's length by the batch's T."""
+    return dict(keys_unit_norm=True, max_seq_len=(w.T if w.varlen else 0))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -195,10 +202,9 @@ def run_ours(args):
     x = make_inputs(w, device=dev)
     N = x["N"]
     tokens = int(x["q"].shape[0] * x["q"].shape[1])
-    opts = dict(keys_unit_norm=True)  # the workloads L2-normalise k and use beta = sigmoid(.)
+    opts = bench_options(w)
     info = gdn.plan(int(x["q"].shape[0]), int(x["q"].shape[1]), w.H, w.hv, w.K, w.V, w.dtype, w.gate,
-                    num_seqs=N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
-                    max_seq_len=(w.T if w.varlen else 0), **opts)
+                    num_seqs=N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count, **opts)
     o = torch.empty_like(x["v"])
     ht = torch.empty(N, w.hv, w.K, w.V, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -206,9 +212,7 @@ def run_ours(args):
 
     def step(evs=None):
         gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
-                                   x["cu_seqlens"], out=o, final_state=ht,
-                                   max_seq_len=(w.T if w.varlen else 0),
-                                   launch_events=evs, **opts)
+                                   x["cu_seqlens"], out=o, final_state=ht, launch_events=evs, **opts)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -257,8 +261,7 @@ def run_ours(args):
 
     def e2e_step():
         gdn.chunk_gated_delta_rule_host(xh["q"], xh["k"], xh["v"], xh["g"], xh["beta"], xh["scale"], xh["h0"],
-                                        True, xh["cu_seqlens"], out=oh, final_state=hh, device=dev,
-                                        max_seq_len=(w.T if w.varlen else 0), **opts)
+                                        True, xh["cu_seqlens"], out=oh, final_state=hh, device=dev, **opts)
     e2e_step()
     n_e2e = max(3, min(20, args.steps // 10))
     torch.cuda.synchronize()

@@ -33,7 +33,8 @@ class GdnOptions(ctypes.Structure):
     _fields_ = [("cp_mode", ctypes.c_int), ("segment_chunks", ctypes.c_int), ("engine", ctypes.c_int),
                 ("keys_unit_norm", ctypes.c_int), ("warmup_log2_eps", ctypes.c_float),
                 ("max_seq_len", ctypes.c_int), ("launch_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("n_launch_events", ctypes.c_int)]
+                ("n_launch_events", ctypes.c_int), ("wait_limit_us", ctypes.c_int),
+                ("test_withhold_first_arrival", ctypes.c_int)]
 
 
 class GdnPlanInfo(ctypes.Structure):
@@ -75,6 +76,8 @@ def load_library(path: str | None = None):
         lib.gdn_workspace_size.restype = ctypes.c_size_t
         lib.gdn_plan.argtypes = [SP, ctypes.c_int, OP, ctypes.c_int, ctypes.POINTER(GdnPlanInfo)]
         lib.gdn_plan.restype = ctypes.c_int
+        lib.gdn_read_noalloc_status.argtypes = [VP]
+        lib.gdn_read_noalloc_status.restype = ctypes.c_int
         lib.gdn_read_device_status.argtypes = [VP, VP]
         lib.gdn_read_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -99,11 +102,15 @@ def _dtype_code(t: torch.dtype) -> int:
 
 
 def make_options(cp_mode="auto", engine="auto", keys_unit_norm=False, segment_chunks=0,
-                 warmup_log2_eps=0.0, max_seq_len=0, launch_events=None) -> GdnOptions:
+                 warmup_log2_eps=0.0, max_seq_len=0, launch_events=None, wait_limit_us=0,
+                 test_withhold_first_arrival=False) -> GdnOptions:
     """``launch_events``: optional sequence of raw CUDA event handles (ints) to be recorded
-    around each kernel launch (see ``gdn_options.launch_events`` in ``include/gdn.h``)."""
+    around each kernel launch (see ``gdn_options.launch_events`` in ``include/gdn.h``).
+    ``wait_limit_us`` and ``test_withhold_first_arrival``: the device-side wait limit and the
+    timeout-path test switch of ``gdn_options``."""
     opt = GdnOptions(CP_MODES[cp_mode], int(segment_chunks), ENGINES[engine], int(bool(keys_unit_norm)),
-                     float(warmup_log2_eps), int(max_seq_len), None, 0)
+                     float(warmup_log2_eps), int(max_seq_len), None, 0, int(wait_limit_us),
+                     int(bool(test_withhold_first_arrival)))
     if launch_events:
         arr = (ctypes.c_void_p * len(launch_events))(*[int(h) for h in launch_events])
         opt._events_keepalive = arr  # the array lives as long as the options
@@ -132,7 +139,8 @@ def _check(code: int, what: str):
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
                            cu_seqlens=None, chunk_size=64, *, cp_mode="auto", engine="auto",
                            keys_unit_norm=False, segment_chunks=0, warmup_log2_eps=0.0, max_seq_len=0,
-                           workspace=None, out=None, final_state=None, launch_events=None):
+                           workspace=None, out=None, final_state=None, launch_events=None, wait_limit_us=0,
+                           test_withhold_first_arrival=False):
     """Gated delta-rule chunked-prefill forward on the GPU.
 
     q, k [B,T,H,K]; v [B,T,HV,V] (float32 or bfloat16, same dtype); g [B,T,HV]
@@ -164,7 +172,7 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
         ht = final_state if final_state is not None else torch.empty(
             s.num_seqs, s.HV, s.K, s.V, dtype=torch.float32, device=q.device)
     opt = make_options(cp_mode, engine, keys_unit_norm, segment_chunks, warmup_log2_eps, max_seq_len,
-                       launch_events)
+                       launch_events, wait_limit_us, test_withhold_first_arrival)
     L = lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
     with torch.cuda.device(q.device):

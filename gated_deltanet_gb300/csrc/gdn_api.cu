@@ -43,6 +43,7 @@ gdn_status validate_shape(const gdn_shape *s, int chunk_size, const gdn_options 
         if (opt->engine < GDN_ENGINE_AUTO || opt->engine > GDN_ENGINE_TC) return GDN_ERR_INVALID;
         if (opt->segment_chunks < 0 || opt->max_seq_len < 0) return GDN_ERR_INVALID;
         if (!(opt->warmup_log2_eps <= 0.f)) return GDN_ERR_INVALID;
+        if (opt->wait_limit_us < 0) return GDN_ERR_INVALID;
     }
     if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
     if (s->K != 32 && s->K != 64 && s->K != 128) return GDN_ERR_UNSUPPORTED;
@@ -175,22 +176,34 @@ cudaError_t scan_prepass(const ScanArgs &pre, bool tc, const gdn_shape *s, cudaS
     return launch_simt_scan(pre, s->qkv_dtype, s->gate_kind, stream);
 }
 
+// Every host-side check of a call, before anything is enqueued: the options (with the engine
+// resolved against the pointers' alignment), the plan and the arguments.
+gdn_status prepare(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                   const float *beta, float scale, const int64_t *cu, int chunk_size, const void *o,
+                   const gdn_options *optp, gdn_options *opt, Plan *p)
+{
+    if (!s) return GDN_ERR_INVALID;
+    if (optp) *opt = *optp; else gdn_default_options(opt);
+    // the tensor-core engine needs 16-byte aligned q/k/v/o for its TMA maps (and gk rows)
+    if (opt->engine != GDN_ENGINE_SIMT && tc_shape_ok(s) && !tc_supported(s, q, k, v, g, o)) {
+        if (opt->engine == GDN_ENGINE_TC) return GDN_ERR_INVALID;
+        opt->engine = GDN_ENGINE_SIMT;
+    }
+    gdn_status st = make_plan(s, is_varlen(s, cu), chunk_size, opt, current_sm_count(), p);
+    if (st != GDN_OK) return st;
+    if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
+    if (!std::isfinite(scale)) return GDN_ERR_INVALID;
+    return GDN_OK;
+}
+
 gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
                const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size, void *o,
                float *ht, const gdn_options *optp, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     Plan p;
     gdn_options opt;
-    if (optp) opt = *optp; else gdn_default_options(&opt);
-    // the tensor-core engine needs 16-byte aligned q/k/v/o for its TMA maps (and gk rows)
-    if (opt.engine != GDN_ENGINE_SIMT && tc_shape_ok(s) && !tc_supported(s, q, k, v, g, o)) {
-        if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_INVALID;
-        opt.engine = GDN_ENGINE_SIMT;
-    }
-    gdn_status st = make_plan(s, is_varlen(s, cu), chunk_size, &opt, current_sm_count(), &p);
+    gdn_status st = prepare(s, q, k, v, g, beta, scale, cu, chunk_size, o, optp, &opt, &p);
     if (st != GDN_OK) return st;
-    if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
-    if (!std::isfinite(scale)) return GDN_ERR_INVALID;
     if (!ws || ws_bytes < p.bytes) return GDN_ERR_WORKSPACE;
     if (((uintptr_t)ws & 255u) != 0) return GDN_ERR_INVALID;
 
@@ -205,6 +218,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     a.scale = scale;
     a.seg_chunks = p.seg_chunks; a.n_seg = p.n_seg;
     a.mode = kModeForward; a.vext = s->V; a.status = status;
+    a.wait_ns = opt.wait_limit_us > 0 ? 1000ull * (unsigned long long)opt.wait_limit_us : 2000000000ull;
 
     cudaError_t e = cudaSuccess;
     // optional per-kernel timing marks on the caller's events
@@ -238,6 +252,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         if (p.off_order) { pa.seq_order = (int *)(wsb + p.off_order); pa.n_buckets = p.n_buckets; }
         a.seq_order = pa.seq_order;
         pa.status = status;
+        pa.wait_ns = a.wait_ns;
         mark();
         e = launch_tc_prep(pa, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -283,6 +298,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         a.seg_init = cb.seg_init;
     }
     mark();
+    a.withhold_full0 = opt.test_withhold_first_arrival != 0;
     e = scan(a);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     mark();
@@ -321,6 +337,28 @@ gdn_status managed_ws(size_t need, cudaStream_t stream, void **out, size_t *out_
 }
 
 }  // namespace
+
+gdn_status gdn::check_call(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const int64_t *cu, int chunk_size, const void *o,
+                           const gdn_options *opt, size_t *ws_bytes)
+{
+    Plan p;
+    gdn_options o2;
+    const gdn_status st = prepare(s, q, k, v, g, beta, scale, cu, chunk_size, o, opt, &o2, &p);
+    if (st == GDN_OK && ws_bytes) *ws_bytes = p.bytes;
+    return st;
+}
+
+gdn_status gdn::read_status_word(void *ws, cudaStream_t st)
+{
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof(unsigned), st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word & kStatusTimeout) return GDN_ERR_TIMEOUT;
+    if (word & (kStatusPlan | kStatusNormBound)) return GDN_ERR_INVALID;
+    return GDN_OK;
+}
 
 extern "C" {
 
@@ -424,13 +462,7 @@ gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream)
         if (it == g_ws.end() || !it->second.ptr) return GDN_OK;
         ws = it->second.ptr;
     }
-    unsigned word = 0;
-    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GDN_ERR_CUDA;
-    if (cudaMemsetAsync(ws, 0, sizeof(unsigned), st) != cudaSuccess) return GDN_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
-    if (word & kStatusTimeout) return GDN_ERR_TIMEOUT;
-    if (word & (kStatusPlan | kStatusNormBound)) return GDN_ERR_INVALID;
-    return GDN_OK;
+    return gdn::read_status_word(ws, st);
 }
 
 gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,

@@ -47,6 +47,8 @@ struct ScanArgs {
     int vext;               // value columns processed: V (forward) or V + K (prepass)
     unsigned *status;
     const int *seq_order;   // [N] sequence of each grid.z group (longest first), nullable = natural order
+    unsigned long long wait_ns;  // wall-clock limit of every device-side wait (tensor-core engine)
+    int withhold_full0;     // timeout-path test: the load warp never signals its first chunk
 };
 
 struct CombineArgs {
@@ -79,6 +81,7 @@ struct PrepArgs {
     unsigned *status;
     int *seq_order;             // nullable: block (0, 0) writes the longest-first sequence order here
     int n_buckets;              //   chunk-count buckets of that sort (<= kOrderBuckets)
+    unsigned long long wait_ns; // wall-clock limit of the product-completion wait
 };
 
 // Launchers (return cudaGetLastError() of the launch).
@@ -161,6 +164,14 @@ __device__ inline void order_longest_first(const int64_t *cu, int N, int n_bucke
 }
 __host__ __device__ inline int64_t tile_slots(int64_t tokens, int nseq) { return tokens / kChunk + nseq + 1; }
 size_t tc_smem_bytes();
+
+// Host-side checks of one forward call, as the entry points run them before anything is
+// enqueued; on GDN_OK *ws_bytes (nullable) is the workspace the call needs.
+gdn_status check_call(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, float scale, const int64_t *cu, int chunk_size, const void *o,
+                      const gdn_options *opt, size_t *ws_bytes);
+// Synchronise `st`, return the device status recorded in the word at `ws` and clear it.
+gdn_status read_status_word(void *ws, cudaStream_t st);
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

@@ -48,15 +48,26 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_shape *s, const void *q, c
                                             const float *h0, const int64_t *cu_seqlens, int chunk_size,
                                             void *o, float *ht, const gdn_options *opt, gdn_stream_t stream)
 {
-    const size_t need = gdn_workspace_size(s, chunk_size, opt);
-    if (need == 0) return s ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID;
+    // Every host-side check first (the same codes as the other entry points), so a rejected call
+    // enqueues nothing and leaves the status word of an earlier call untouched.
+    size_t need = 0;
+    gdn_status st = gdn::check_call(s, q, k, v, g_or_gk, beta, scale, cu_seqlens, chunk_size, o, opt, &need);
+    if (st != GDN_OK) return st;
     if (need > kStaticScratchBytes) return GDN_ERR_WORKSPACE;  // plan needs more than the fixed array
     void *ws = nullptr;
-    gdn_status st = scratch_address(&ws);
+    st = scratch_address(&ws);
     if (st != GDN_OK) return st;
-    // The array keeps the previous call's contents; only the status word must start at zero
-    // (the split tables are written in full before they are read).  A memset node allocates nothing.
-    if (cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    // The array keeps the previous call's contents.  The split tables are written in full before
+    // they are read; the status word starts at zero (device memory of the module is zero-initialised)
+    // and, as a workspace's, collects the device errors of every call until gdn_read_noalloc_status.
     return gdn_chunk_fwd_ws(s, q, k, v, g_or_gk, beta, scale, h0, cu_seqlens, chunk_size, o, ht, opt, ws,
                             kStaticScratchBytes, stream);
+}
+
+extern "C" gdn_status gdn_read_noalloc_status(gdn_stream_t stream)
+{
+    void *ws = nullptr;
+    const gdn_status st = scratch_address(&ws);
+    if (st != GDN_OK) return st;
+    return gdn::read_status_word(ws, (cudaStream_t)stream);
 }

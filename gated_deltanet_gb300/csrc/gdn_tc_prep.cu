@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         __syncwarp();
     }
     if (warp < 2) {
-        const bool ok = mbar_wait(&sh.bar, 0, a.status, kStatusTimeout, 2000000000ull);
+        const bool ok = mbar_wait(&sh.bar, 0, a.status, kStatusTimeout, a.wait_ns);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             const int r = 32 * warp + lane;

@@ -111,26 +111,44 @@ typedef struct {
                               gdn_plan) right after the last one, so consecutive
                               events time each kernel.  NULL: nothing recorded.   */
     int n_launch_events;   /* length of launch_events; extra marks are skipped      */
+    int wait_limit_us;     /* wall-clock limit of every device-side wait of the
+                              tensor-core kernels, in microseconds (0 = 2 s).  A
+                              wait that runs out records GDN_ERR_TIMEOUT in the
+                              device status and the kernel ends early.            */
+    int test_withhold_first_arrival; /* testing the timeout path only: nonzero makes
+                              the tensor-core scan's load warp withhold its "chunk
+                              loaded" signal for the first chunk of every CTA, so
+                              every role's wait runs out (bounded by
+                              wait_limit_us), the device status reads
+                              GDN_ERR_TIMEOUT and o / ht are left undefined.  No
+                              effect on the SIMT engine.                          */
 } gdn_options;
 
-/* Fill `opt` with the defaults (AUTO everywhere, no assertions). */
+/* Fill `opt` with the defaults (AUTO everywhere, no assertions).  No
+ * counterpart in the pages (library infrastructure). */
 void gdn_default_options(gdn_options *opt);
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).  No
+ * counterpart in the pages. */
 const char *gdn_status_string(gdn_status st);
 
-/* Library version: major * 10000 + minor * 100 + patch. */
+/* Library version: major * 10000 + minor * 100 + patch.  No counterpart in
+ * the pages. */
 int gdn_version(void);
 
 /*
  * Bytes of device workspace gdn_chunk_fwd_ws needs for this problem and
  * options (at least 256: the first 256 bytes hold the device status word).
- * Returns 0 if the arguments are invalid or unsupported.
+ * Returns 0 if the arguments are invalid or unsupported.  No counterpart in
+ * the pages (the pages' kernels allocate their intermediates themselves).
  */
 size_t gdn_workspace_size(const gdn_shape *s, int chunk_size, const gdn_options *opt);
 
 /*
- * The forward pass with a caller-provided workspace (`workspace`, at least
+ * The forward pass of the problem statement (FlashQLA blog, "Usage":
+ * chunk_gated_delta_rule(q, k, v, g, beta, scale, initial_state,
+ * output_final_state, cu_seqlens) -> (o, final_state)) with a caller-provided
+ * workspace (`workspace`, at least
  * gdn_workspace_size bytes, 256-byte aligned, device memory).  The
  * workspace must not be used by another call that can run concurrently.
  * Returns GDN_OK once all work is enqueued on `stream`.
@@ -143,7 +161,10 @@ gdn_status gdn_chunk_fwd_ws(const gdn_shape *s,
                             void *workspace, size_t ws_bytes, gdn_stream_t stream);
 
 /*
- * The forward pass with default options and a library-managed workspace,
+ * The forward pass of the problem statement (FlashQLA blog, "Usage"; the
+ * GDN-in-FLA notes, forward signature; "KDA source walkthrough",
+ * chunk_kda_fwd for the per-channel gate) -- the plain entry point -- with
+ * default options and a library-managed workspace,
  * cached per (device, stream) and grown stream-ordered (cudaMallocAsync on
  * `stream`) when a call needs more.  Arguments as in gdn_chunk_fwd_ws.
  */
@@ -153,7 +174,9 @@ gdn_status gdn_chunk_fwd(const gdn_shape *s,
                          const float *h0, const int64_t *cu_seqlens, int chunk_size,
                          void *o, float *ht, gdn_stream_t stream);
 
-/* As gdn_chunk_fwd with explicit options (NULL = defaults). */
+/* As gdn_chunk_fwd with explicit options (NULL = defaults): the split mode
+ * and warmup threshold follow the FlashQLA blog, "A balanced solution" and
+ * "Further optimisation via gate decay". */
 gdn_status gdn_chunk_fwd_ex(const gdn_shape *s,
                             const void *q, const void *k, const void *v,
                             const float *g_or_gk, const float *beta, float scale,
@@ -161,7 +184,8 @@ gdn_status gdn_chunk_fwd_ex(const gdn_shape *s,
                             void *o, float *ht, const gdn_options *opt, gdn_stream_t stream);
 
 /*
- * End-to-end call on HOST buffers (pageable or pinned): copies the inputs to
+ * The forward pass of the problem statement (FlashQLA blog, "Usage") as an
+ * end-to-end call on HOST buffers (pageable or pinned): copies the inputs to
  * a library-owned device arena on `stream`, runs gdn_chunk_fwd_ex, copies o
  * (and ht when non-NULL) back, and synchronises `stream` before returning.
  * `cu_seqlens` is a host array here too.  Same shapes as above.
@@ -174,6 +198,7 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s,
                               gdn_stream_t stream);
 
 /*
+ * No counterpart in the pages (the bounded device waits are this library's).
  * Synchronise `stream`, return the status the device recorded in the
  * workspace since the last read, and clear it.  `workspace` is the buffer
  * given to gdn_chunk_fwd_ws, or NULL for the library-managed workspace of
@@ -200,10 +225,14 @@ gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream);
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress with that device current); make that first call
  * before any stream capture.  Every call uses the same array, which keeps
- * the previous call's contents (the status word is cleared at the start of
- * each call): calls that can overlap on the GPU -- on different streams, or
- * from different threads -- race on it and must be serialised by the caller.
- * No cudaMalloc, cudaFree or other allocating routine is called.
+ * the previous call's contents: calls that can overlap on the GPU -- on
+ * different streams, or from different threads -- race on it and must be
+ * serialised by the caller.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.  Argument errors return the same codes as
+ * gdn_chunk_fwd_ex and enqueue nothing.  Errors found on the device (a wait
+ * that ran out, a failed plan check, the warmup split's key-norm check) are
+ * collected in the array's status word until gdn_read_noalloc_status reads
+ * and clears it.
  */
 gdn_status gdn_chunk_fwd_noalloc(const gdn_shape *s,
                                  const void *q, const void *k, const void *v,
@@ -211,7 +240,17 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_shape *s,
                                  const float *h0, const int64_t *cu_seqlens, int chunk_size,
                                  void *o, float *ht, const gdn_options *opt, gdn_stream_t stream);
 
-/* Plan summary (host only, no GPU needed) -- what a call would launch. */
+/*
+ * The device status of gdn_chunk_fwd_noalloc calls on the current device (no
+ * counterpart in the paper): synchronises `stream`, returns the status word of
+ * the fixed array as gdn_read_device_status does for a workspace (GDN_OK,
+ * GDN_ERR_TIMEOUT or GDN_ERR_INVALID) and clears it.  Allocates nothing.
+ */
+gdn_status gdn_read_noalloc_status(gdn_stream_t stream);
+
+/* Plan summary (host only, no GPU needed) -- what a call would launch: the
+ * engine and the in-GPU split (FlashQLA blog, "A balanced solution", the CP
+ * enable rule, re-derived for this GPU's SM count). */
 typedef struct {
     gdn_engine engine;    /* engine the call would use                    */
     gdn_cp_mode cp_mode;  /* OFF, EXACT or WARMUP after AUTO is resolved   */

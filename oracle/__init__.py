@@ -10,8 +10,7 @@ package never imports it and shares no code with it.
 * :mod:`oracle.chunkwise` -- naive fp64 NumPy statements of the chunk forms
   the pages give (FLA 4-step form, FlashQLA restructured form, the
   per-channel-gate form, the blockwise triangular inverse, the S*/M
-  chunk-parallel split and the gate-driven warmup).  They pin the recurrence
-  (two independent formulations must agree) and are the references for the
-  per-step debug outputs of the CUDA path.
+  chunk-parallel split and the gate-driven warmup), and the chunk-local gate
+  cumsum.  They pin the recurrence: two independent formulations must agree.
 """
 from .recurrence import recurrence, build_oracle_lib  # noqa: F401

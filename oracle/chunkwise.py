@@ -25,17 +25,22 @@ __all__ = [
 ]
 
 
-def local_cumsum(g, C):
-    """Chunk-local inclusive cumsum of the log-gate (restarts every C tokens).
+def local_cumsum(g, C, cu_seqlens=None):
+    """Chunk-local inclusive cumsum of the log-gate.
 
     "Flash Linear Attention" page, sec. 3 (chunk_local_cumsum): inside a chunk
     g_t <- sum of g_s for s in the chunk, s <= t; nothing carries across chunks.
-    Works on the leading (token) axis, so it covers the per-channel gate too.
+    Packed input ("Flash Linear Attention" page, sec. 2, varlen): chunks are
+    counted from each sequence's first token, so the sum also restarts at every
+    sequence start ``cu_seqlens[n]``.  Works on the leading (token) axis, so it
+    covers the per-channel gate too.
     """
     g = np.asarray(g, dtype=np.float64)
     out = np.empty_like(g)
-    for s in range(0, g.shape[0], C):
-        out[s:s + C] = np.cumsum(g[s:s + C], axis=0)
+    bounds = [0, g.shape[0]] if cu_seqlens is None else [int(b) for b in cu_seqlens]
+    for bos, eos in zip(bounds[:-1], bounds[1:]):
+        for s in range(bos, eos, C):
+            out[s:min(s + C, eos)] = np.cumsum(g[s:min(s + C, eos)], axis=0)
     return out
 
 

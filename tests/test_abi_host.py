@@ -112,3 +112,25 @@ def test_packed_batches_reserve_the_sequence_order(gdn):
     f_one = gdn.plan(1, 8192, 16, 16, 128, 128, dtype="f32", num_seqs=1, num_sms=152, cp_mode="off")
     f_many = gdn.plan(1, 8192, 16, 16, 128, 128, dtype="f32", num_seqs=300, num_sms=152, cp_mode="off")
     assert f_many.workspace_bytes == f_one.workspace_bytes
+
+
+def test_noalloc_validates_like_the_regular_entry_point(gdn):
+    """The allocation-free entry point returns the regular entry point's codes for rejected
+    arguments, on the host (no GPU work, so this runs without a GPU)."""
+    L = gdn.lib()
+    null = None
+    dummy = ctypes.c_void_p(256)  # never dereferenced: every case is rejected on the host
+    cases = [
+        (_shape(), 64, null),                     # null data pointers: invalid
+        (_shape(), 32, dummy),                    # chunk size other than 64: unsupported
+        (_shape(K=96), 64, dummy),                # head dim not supported
+        (_shape(H=0), 64, dummy),                 # invalid shape
+        (_shape(), 64, "varlen"),                 # packed input with B != 1: invalid
+    ]
+    for s, cs, ptr in cases:
+        cu = dummy if ptr == "varlen" else null
+        p = dummy if ptr == "varlen" else ptr
+        args = (ctypes.byref(s), p, p, p, p, p, ctypes.c_float(0.1), null, cu, cs, p, null, None, None)
+        a = L.gdn_chunk_fwd_ex(*args)
+        b = L.gdn_chunk_fwd_noalloc(*args)
+        assert a == b and a in (-1, -2), (s.K, cs, a, b)

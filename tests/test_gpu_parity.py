@@ -244,8 +244,23 @@ def test_workload_tiny_f32(gdn):
     check(gdn, WORKLOADS["tiny_f32"])
 
 
-def test_workload_batched_bf16(gdn):
-    check(gdn, WORKLOADS["batched_bf16"])
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("plan", ["timed", "unsplit"])
+def test_workload_batched_bf16(gdn, plan):
+    """``timed``: the exact call bench.py times (its options, so the planner's chunk-parallel split on
+    this GPU's SM count); ``unsplit``: one serial scan per (sequence, head)."""
+    from bench import bench_options
+    w = WORKLOADS["batched_bf16"]
+    if plan == "timed":
+        opts = bench_options(w)
+        info = gdn.plan(w.B, w.T, w.H, w.hv, w.K, w.V, w.dtype, w.gate, num_sms=_sms(), **opts)
+        assert info.engine == 2 and info.cp_mode == 3 and info.segments >= 2, "the bench times the warmup split"
+    else:
+        opts = dict(cp_mode="off")
+    check(gdn, w, **opts)
 
 
 @pytest.mark.parametrize("mode", ["auto", "exact", "warmup", "off"])
@@ -253,22 +268,11 @@ def test_workload_long_bf16(gdn, mode):
     check(gdn, WORKLOADS["long_bf16"], cp_mode=mode, keys_unit_norm=True)
 
 
-def test_workload_varlen_bf16_sampled(gdn):
-    """All sequences on the GPU; the oracle recomputes a sample of them one by one
-    (the longest, the shortest and four more)."""
+def test_workload_varlen_bf16(gdn):
+    """All 32 packed sequences against the oracle, in the plan bench.py times."""
+    from bench import bench_options
     w = WORKLOADS["varlen_bf16"]
-    x = make_inputs(w)
-    go, gh = run_gpu(gdn, w)
-    cu = x["cu_seqlens"].numpy()
-    lens = np.diff(cu)
-    pick = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] +
-                      list(np.random.default_rng(0).choice(len(lens), 4, replace=False))))
-    for n in pick:
-        s, e = cu[n], cu[n + 1]
-        ro, rh = recurrence(x["q"][:, s:e], x["k"][:, s:e], x["v"][:, s:e], x["g"][:, s:e], x["beta"][:, s:e],
-                            x["scale"], x["h0"][n:n + 1])
-        tol_check(f"varlen seq {n} o", go[:, s:e], ro, "bf16")
-        tol_check(f"varlen seq {n} ht", gh[n:n + 1], rh, "bf16")
+    check(gdn, w, **bench_options(w))
 
 
 def test_workload_channel_bf16(gdn):
@@ -289,3 +293,41 @@ def test_repeat_runs_are_bitwise_identical(gdn, name):
         outs.append((o.clone(), ht.clone()))
     assert gdn.read_device_status() == 0
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("name", ["bf16_varlen", "f32_d64_ragged"])
+def test_plain_entry_point(gdn, name):
+    """``gdn_chunk_fwd`` itself -- the plain signature of the problem statement (default options, the
+    library-managed workspace) -- called through ctypes and compared with the oracle."""
+    import ctypes
+    from gated_deltanet_gb300._binding import _ptr, make_shape
+    w = SMALL[name]
+    x = make_inputs(w, device="cuda")
+    s = make_shape(x["q"], x["v"], x["g"], x["cu_seqlens"])
+    o = torch.empty_like(x["v"])
+    ht = torch.empty(x["N"], w.hv, w.K, w.V, dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    code = gdn.lib().gdn_chunk_fwd(ctypes.byref(s), _ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _ptr(x["g"]),
+                                   _ptr(x["beta"]), ctypes.c_float(x["scale"]), _ptr(x["h0"]),
+                                   _ptr(x["cu_seqlens"]), 64, _ptr(o), _ptr(ht), stream)
+    assert code == 0
+    torch.cuda.synchronize()
+    assert gdn.read_device_status() == 0
+    ro, rh = oracle_for(w)
+    tol_check(f"{name} o", to_f64(o), ro, w.dtype)
+    tol_check(f"{name} ht", to_f64(ht), rh, w.dtype)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+def test_timeout_is_reported_and_the_stream_recovers(gdn, gate):
+    """The bounded-wait path: with the host-set test switch the scan's load warp withholds the first
+    chunk's "loaded" signal, every role's wait runs out after 5 ms, the kernel ends, and the status
+    reads GDN_ERR_TIMEOUT.  A normal call on the same stream right after matches the oracle."""
+    w = SMALL["bf16_d128_ragged"] if gate == "scalar" else SMALL["bf16_channel"]
+    x = make_inputs(w, device="cuda")
+    gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
+                               x["cu_seqlens"], engine="tc", wait_limit_us=5000, test_withhold_first_arrival=True)
+    torch.cuda.synchronize()
+    assert gdn.read_device_status() == -4  # GDN_ERR_TIMEOUT
+    assert gdn.read_device_status() == 0   # read clears it
+    check(gdn, w, engine="tc")

@@ -329,3 +329,28 @@ def test_warmup_start_walk():
     assert cw.warmup_start(sums, 5, -6.5) == 1
     assert cw.warmup_start(sums, 5, -4.0) == 3
     assert cw.warmup_start(sums, 2, -100.0) == 0
+
+
+# ---------------------------------------------------------------- step a1: the chunk-local gate cumsum
+def test_local_cumsum_golden():
+    """Hand-worked cumsums ("Flash Linear Attention" page, sec. 3, chunk_local_cumsum; sec. 2 for
+    the restart at every packed sequence start): exact binary values, compared exactly."""
+    with open(os.path.join(GOLDEN, "gate_cumsum_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        got = cw.local_cumsum(np.array(c["g"]), c["C"], c["cu_seqlens"])
+        assert np.array_equal(got, np.array(c["expected"])), c["name"]
+
+
+def test_local_cumsum_restarts_match_per_sequence_runs():
+    """Packed input equals the sequences cumsummed one by one, and each chunk's sum ends at
+    the sum of the chunk's gates."""
+    rng = np.random.default_rng(5)
+    cu = np.array([0, 70, 70, 200, 201, 330])
+    g = -rng.random((330, 3))
+    got = cw.local_cumsum(g, 64, cu)
+    for s, e in zip(cu[:-1], cu[1:]):
+        assert np.array_equal(got[s:e], cw.local_cumsum(g[s:e], 64))
+        for c0 in range(s, e, 64):
+            c1 = min(c0 + 64, e)
+            assert np.allclose(got[c1 - 1], g[c0:c1].sum(axis=0), rtol=0, atol=1e-12)
