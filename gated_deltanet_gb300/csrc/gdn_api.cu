@@ -6,6 +6,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "gdn_internal.cuh"
 
@@ -473,26 +474,56 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, 
     gdn_status st = make_plan(s, cu != nullptr, chunk_size, opt, current_sm_count(), &p);
     if (st != GDN_OK) return st;
     if ((st = check_ptrs(s, q, k, v, g, beta, o)) != GDN_OK) return st;
+    const int N = s->num_seqs;
+    const int64_t tokens = (int64_t)s->B * s->T;
+    if (cu) {
+        // host offsets: checked here, since the groups below are cut along them
+        if (cu[0] != 0 || cu[N] != tokens) return GDN_ERR_INVALID;
+        for (int n = 0; n < N; ++n)
+            if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID;
+    }
     cudaStream_t cs = (cudaStream_t)stream;
     const size_t esz = s->qkv_dtype == GDN_BF16 ? 2 : 4;
-    const size_t tok = (size_t)s->B * s->T;
-    const size_t n_q = tok * s->H * s->K, n_v = tok * s->HV * s->V;
-    const size_t n_g = tok * s->HV * (s->gate_kind == GDN_GATE_CHANNEL ? s->K : 1);
-    const size_t n_b = tok * s->HV, n_h = (size_t)s->num_seqs * s->HV * s->K * s->V;
-    const size_t sizes[9] = {n_q * esz, n_q * esz, n_v * esz, n_g * 4, n_b * 4, h0 ? n_h * 4 : 0,
-                             cu ? (size_t)(s->num_seqs + 1) * 8 : 0, n_v * esz, ht ? n_h * 4 : 0};
-    size_t offs[9], total = 0;
-    for (int i = 0; i < 9; ++i) {
+    const size_t gch = s->gate_kind == GDN_GATE_CHANNEL ? (size_t)s->K : 1;
+    // bytes per token of each token-major tensor, per sequence of each state
+    const size_t tq = (size_t)s->H * s->K * esz, tv = (size_t)s->HV * s->V * esz, tg = (size_t)s->HV * gch * 4,
+                 tb = (size_t)s->HV * 4, sh = (size_t)s->HV * s->K * s->V * 4;
+    enum { E_Q, E_K, E_V, E_G, E_BETA, E_H0, E_CU, E_O, E_HT, E_N };
+    const size_t sizes[E_N] = {tokens * tq, tokens * tq, tokens * tv, tokens * tg, tokens * tb, h0 ? N * sh : 0,
+                              cu ? (size_t)(N + 4) * 8 * 4 : 0, tokens * tv, ht ? N * sh : 0};
+    size_t offs[E_N], total = 0;
+    for (int i = 0; i < E_N; ++i) {
         offs[i] = total;
         total = align_up(total + sizes[i], 256);
     }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+    // Library-owned per device: the arena (per caller stream) and two copy streams with a pool of
+    // events.  The call is split into up to four groups of whole sequences (contiguous token ranges
+    // in every tensor): the inputs of group i+1 are copied in while group i runs on the caller's
+    // stream and group i-1's outputs are copied out, each direction on its own stream.
+    constexpr int kGroups = 4;
+    struct HostRes {
+        cudaStream_t in = nullptr, out = nullptr;
+        cudaEvent_t ev[3 * kGroups + 1] = {};
+    };
+    static std::map<int, HostRes> res;
+    static std::map<std::pair<int, cudaStream_t>, WsEntry> arenas;
     void *arena = nullptr;
+    HostRes *r = nullptr;
     {
-        // the host path keeps its own arena per (device, stream), keyed apart from the workspaces
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-        static std::map<std::pair<int, cudaStream_t>, WsEntry> arenas;
         std::lock_guard<std::mutex> lock(g_mu);
+        HostRes &hr = res[dev];
+        if (!hr.in) {
+            if (cudaStreamCreateWithFlags(&hr.in, cudaStreamNonBlocking) != cudaSuccess ||
+                cudaStreamCreateWithFlags(&hr.out, cudaStreamNonBlocking) != cudaSuccess) {
+                cudaGetLastError();
+                return GDN_ERR_CUDA;
+            }
+            for (auto &e : hr.ev)
+                if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        r = &hr;
         WsEntry &w = arenas[{dev, cs}];
         if (w.bytes < total) {
             if (w.ptr) cudaFreeAsync(w.ptr, cs);
@@ -508,18 +539,74 @@ gdn_status gdn_chunk_fwd_host(const gdn_shape *s, const void *q, const void *k, 
         arena = w.ptr;
     }
     char *A = (char *)arena;
-    const void *src[7] = {q, k, v, g, beta, h0, cu};
-    for (int i = 0; i < 7; ++i)
-        if (sizes[i] && cudaMemcpyAsync(A + offs[i], src[i], sizes[i], cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    // groups of whole sequences with about equal token counts
+    const int G = std::max(1, std::min(N, kGroups));
+    int bound[kGroups + 1];
+    bound[0] = 0;
+    auto seq_start = [&](int n) -> int64_t { return cu ? cu[n] : (int64_t)n * s->T; };
+    for (int gi = 1; gi < G; ++gi) {
+        int n = bound[gi - 1] + 1;
+        while (n < N - (G - gi) && seq_start(n) < tokens * gi / G) ++n;
+        bound[gi] = n;
+    }
+    bound[G] = N;
+    // the arena (and the events) must not be in use by a previous call still in flight on the copy
+    // streams: each call synchronises the caller's stream, which waits for both, before returning
+    if (cudaEventRecord(r->ev[3 * kGroups], cs) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamWaitEvent(r->in, r->ev[3 * kGroups], 0) != cudaSuccess) return GDN_ERR_CUDA;
+    int64_t *cu_dev_base = cu ? (int64_t *)(A + offs[E_CU]) : nullptr;
+    std::vector<int64_t> cu_rebased;
+    if (cu) cu_rebased.resize((size_t)N + G);
+    size_t cu_pos = 0;
+    for (int gi = 0; gi < G; ++gi) {
+        const int n0 = bound[gi], n1 = bound[gi + 1], ng = n1 - n0;
+        const int64_t t0 = seq_start(n0), t1 = n1 < N ? seq_start(n1) : tokens, tg_n = t1 - t0;
+        auto in = [&](int which, const void *src, size_t off, size_t bytes) -> bool {
+            return bytes == 0 || cudaMemcpyAsync(A + offs[which] + off, (const char *)src + off, bytes,
+                                                 cudaMemcpyHostToDevice, r->in) == cudaSuccess;
+        };
+        if (!in(E_Q, q, t0 * tq, tg_n * tq) || !in(E_K, k, t0 * tq, tg_n * tq) || !in(E_V, v, t0 * tv, tg_n * tv) ||
+            !in(E_G, g, t0 * tg, tg_n * tg) || !in(E_BETA, beta, t0 * tb, tg_n * tb) ||
+            (h0 && !in(E_H0, h0, n0 * sh, (size_t)ng * sh)))
             return GDN_ERR_CUDA;
-    st = gdn_chunk_fwd_ex(s, A + offs[0], A + offs[1], A + offs[2], (const float *)(A + offs[3]),
-                          (const float *)(A + offs[4]), scale, h0 ? (const float *)(A + offs[5]) : nullptr,
-                          cu ? (const int64_t *)(A + offs[6]) : nullptr, chunk_size, A + offs[7],
-                          ht ? (float *)(A + offs[8]) : nullptr, opt, stream);
-    if (st != GDN_OK) return st;
-    if (sizes[7] && cudaMemcpyAsync(o, A + offs[7], sizes[7], cudaMemcpyDeviceToHost, cs) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (sizes[8] && cudaMemcpyAsync(ht, A + offs[8], sizes[8], cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        const int64_t *cu_g = nullptr;
+        if (cu) {
+            int64_t *hcu = cu_rebased.data() + cu_pos;
+            for (int i = 0; i <= ng; ++i) hcu[i] = cu[n0 + i] - t0;
+            // pageable source: staged by the runtime before the call returns
+            if (cudaMemcpyAsync(cu_dev_base + cu_pos, hcu, (size_t)(ng + 1) * 8, cudaMemcpyHostToDevice, r->in) !=
+                cudaSuccess)
+                return GDN_ERR_CUDA;
+            cu_g = cu_dev_base + cu_pos;
+            cu_pos += (size_t)ng + 1;
+        }
+        if (cudaEventRecord(r->ev[3 * gi], r->in) != cudaSuccess || cudaStreamWaitEvent(cs, r->ev[3 * gi], 0) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        gdn_shape sg = *s;
+        if (cu) {
+            sg.T = (int)tg_n;  // B == 1
+        } else {
+            sg.B = ng;
+        }
+        sg.num_seqs = ng;
+        st = gdn_chunk_fwd_ex(&sg, A + offs[E_Q] + t0 * tq, A + offs[E_K] + t0 * tq, A + offs[E_V] + t0 * tv,
+                              (const float *)(A + offs[E_G] + t0 * tg), (const float *)(A + offs[E_BETA] + t0 * tb), scale,
+                              h0 ? (const float *)(A + offs[E_H0] + n0 * sh) : nullptr, cu_g, chunk_size,
+                              A + offs[E_O] + t0 * tv, ht ? (float *)(A + offs[E_HT] + n0 * sh) : nullptr, opt, stream);
+        if (st != GDN_OK) return st;
+        if (cudaEventRecord(r->ev[3 * gi + 1], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(r->out, r->ev[3 * gi + 1], 0) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if (tg_n > 0 && cudaMemcpyAsync((char *)o + t0 * tv, A + offs[E_O] + t0 * tv, tg_n * tv, cudaMemcpyDeviceToHost,
+                                        r->out) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if (ht && ng > 0 &&
+            cudaMemcpyAsync((char *)ht + n0 * sh, A + offs[E_HT] + n0 * sh, (size_t)ng * sh, cudaMemcpyDeviceToHost,
+                            r->out) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
+    if (cudaEventRecord(r->ev[3 * kGroups - 1], r->out) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, r->ev[3 * kGroups - 1], 0) != cudaSuccess)
         return GDN_ERR_CUDA;
     if (cudaStreamSynchronize(cs) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;

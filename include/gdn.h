@@ -186,9 +186,14 @@ gdn_status gdn_chunk_fwd_ex(const gdn_shape *s,
 /*
  * The forward pass of the problem statement (FlashQLA blog, "Usage") as an
  * end-to-end call on HOST buffers (pageable or pinned): copies the inputs to
- * a library-owned device arena on `stream`, runs gdn_chunk_fwd_ex, copies o
- * (and ht when non-NULL) back, and synchronises `stream` before returning.
- * `cu_seqlens` is a host array here too.  Same shapes as above.
+ * a library-owned device arena, runs gdn_chunk_fwd_ex, copies o (and ht when
+ * non-NULL) back, and synchronises `stream` before returning.  The call is
+ * cut into up to four groups of whole sequences (contiguous token ranges of
+ * every tensor); group i runs on `stream` while group i+1's inputs are copied
+ * in and group i-1's outputs copied out, each direction on a library-owned
+ * stream of the current device.  `cu_seqlens` is a host array here too and is
+ * checked on the host (cu[0] == 0, nondecreasing, cu[N] == T).  Same shapes
+ * as above.
  */
 gdn_status gdn_chunk_fwd_host(const gdn_shape *s,
                               const void *q, const void *k, const void *v,

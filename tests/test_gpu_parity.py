@@ -331,3 +331,20 @@ def test_timeout_is_reported_and_the_stream_recovers(gdn, gate):
     assert gdn.read_device_status() == -4  # GDN_ERR_TIMEOUT
     assert gdn.read_device_status() == 0   # read clears it
     check(gdn, w, engine="tc")
+
+
+@pytest.mark.parametrize("name", ["bf16_d128_ragged", "bf16_varlen", "bf16_varlen_many", "f32_channel"])
+def test_host_variant_in_groups_matches_oracle(gdn, name):
+    """gdn_chunk_fwd_host cuts the call into groups of whole sequences and overlaps the copies in,
+    the compute and the copies out on three streams: every group's outputs land in place (pinned and
+    pageable host buffers)."""
+    w = SMALL[name]
+    x = make_inputs(w)
+    ro, rh = oracle_for(w)
+    for pin in (True, False):
+        xh = {k: (v.pin_memory() if pin and torch.is_tensor(v) else v) for k, v in x.items()}
+        o, ht = gdn.chunk_gated_delta_rule_host(xh["q"], xh["k"], xh["v"], xh["g"], xh["beta"], xh["scale"],
+                                                xh["h0"], True, xh["cu_seqlens"])
+        tol_check(f"{name} host o", to_f64(o), ro, w.dtype)
+        tol_check(f"{name} host ht", to_f64(ht), rh, w.dtype)
+    assert gdn.read_device_status() == 0
