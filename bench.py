@@ -28,15 +28,17 @@ METRIC = "GDN chunked-prefill fwd tokens/s and TFLOP/s (% of roofline), 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def algorithmic_work(w, N, total_tokens):
+def algorithmic_work(w, N, total_tokens, C=None):
     """FLOP and bytes per call, implementation-independent.
 
     Per token-head: FLOP = 4 C (dk + dv) + 6 dk dv (K K^T, Q K^T, A V-delta,
-    P V', K S, Q S, K^T V' as dense tiles); bytes = e (2 dk + 2 dv) + 8
-    (+ 4 dk for per-channel gates): read q, k, v, g, beta, write o.  Plus
-    4 dk dv per (sequence, head) for each of h0 (when given) and ht.
+    P V', K S, Q S, K^T V' as dense tiles; C = 1 for the token-by-token form);
+    bytes = e (2 dk + 2 dv) + 8 (+ 4 dk for per-channel gates): read q, k, v,
+    g, beta, write o.  Plus 4 dk dv per (sequence, head) for each of h0 (when
+    given) and ht.
     """
-    C, dk, dv, HV = w.chunk, w.K, w.V, w.hv
+    C = w.chunk if C is None else C
+    dk, dv, HV = w.K, w.V, w.hv
     e = 2 if w.dtype == "bf16" else 4
     flop = total_tokens * HV * (4 * C * (dk + dv) + 6 * dk * dv)
     qk_bytes = total_tokens * w.H * e * 2 * dk          # q, k (per query/key head)
@@ -45,12 +47,17 @@ def algorithmic_work(w, N, total_tokens):
     return float(flop), float(qk_bytes + hv_bytes + state)
 
 
+ENGINE_NAMES = ["auto", "simt", "tc", "recurrent"]
+
+
 def kernel_names(info, channel=False):
     """Names of a call's launches in order (the plan's kernel count)."""
-    eng = ["auto", "simt", "tc"][info.engine]
+    eng = ENGINE_NAMES[info.engine]
     cp = ["auto", "off", "exact", "warmup"][info.cp_mode]
     scan = "tc_scan_kernel" if eng == "tc" else "simt_scan_kernel"
-    if eng == "tc":
+    if eng == "recurrent":
+        seq = ["recurrent_kernel"]
+    elif eng == "tc":
         seq = ["kda_prep_kernel" if channel else "tc_prep_kernel"] + ([scan + " (pre-pass)", "cp_combine_kernel"] if cp == "exact" else []) + [scan]
     else:
         seq = (["gate_stats_kernel"] if cp == "warmup" else []) + \
@@ -273,7 +280,7 @@ def run_ours(args):
               if xh[k] is not None)
     d2h = int(oh.numel() * oh.element_size() + hh.numel() * hh.element_size())
 
-    flop, byts = algorithmic_work(w, N, tokens)
+    flop, byts = algorithmic_work(w, N, tokens, C=1 if ENGINE_NAMES[info.engine] == "recurrent" else None)
     peaks, peak_kind = read_peaks()
     t_step = dev_ms / 1e3 / args.steps
     value = job_value(ws, tokens, args.steps, dev_ms)
@@ -300,7 +307,7 @@ def run_ours(args):
         "config": {"workload": w.name, "B": int(x["q"].shape[0]), "T": int(x["q"].shape[1]), "H": w.H,
                    "HV": w.hv, "dk": w.K, "dv": w.V, "chunk": w.chunk, "gate": w.gate, "h0": w.h0,
                    "sequences": N, "l2": "flushed (512 MiB write) before every timed step",
-                   "plan": {"engine": ["auto", "simt", "tc"][info.engine],
+                   "plan": {"engine": ENGINE_NAMES[info.engine],
                             "cp": ["auto", "off", "exact", "warmup"][info.cp_mode],
                             "segments": info.segments, "kernels": info.kernels},
                    "parallelism": f"replicas x{ws}"},

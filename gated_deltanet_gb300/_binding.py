@@ -12,7 +12,7 @@ from .build import lib_path
 GDN_F32, GDN_BF16 = 0, 1
 GATE_SCALAR, GATE_CHANNEL = 0, 1
 CP_MODES = {"auto": 0, "off": 1, "exact": 2, "warmup": 3}
-ENGINES = {"auto": 0, "simt": 1, "tc": 2}
+ENGINES = {"auto": 0, "simt": 1, "tc": 2, "recurrent": 3}
 _STATUS = {0: "GDN_OK", -1: "GDN_ERR_INVALID", -2: "GDN_ERR_UNSUPPORTED", -3: "GDN_ERR_CUDA",
            -4: "GDN_ERR_TIMEOUT", -5: "GDN_ERR_NOMEM", -6: "GDN_ERR_WORKSPACE"}
 
@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         lib.gdn_chunk_fwd_ws.argtypes = fwd_args + [OP, VP, ctypes.c_size_t, VP]
         lib.gdn_chunk_fwd_host.argtypes = fwd_args + [OP, VP]
         lib.gdn_chunk_fwd_noalloc.argtypes = fwd_args + [OP, VP]
+        lib.gdn_recurrent_fwd.argtypes = [SP, VP, VP, VP, FP, FP, ctypes.c_float, FP, I64P, VP, FP, VP]
+        lib.gdn_recurrent_fwd.restype = ctypes.c_int
         for f in (lib.gdn_chunk_fwd, lib.gdn_chunk_fwd_ex, lib.gdn_chunk_fwd_ws, lib.gdn_chunk_fwd_host,
                   lib.gdn_chunk_fwd_noalloc):
             f.restype = ctypes.c_int
@@ -184,6 +186,39 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
         else:
             code = L.gdn_chunk_fwd_ex(*args, ctypes.byref(opt), stream)
     _check(code, "gdn_chunk_fwd")
+    return o, ht
+
+
+def fused_recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+                                     cu_seqlens=None, *, final_state=None, out=None):
+    """Token-by-token forward (decode; ``gdn_recurrent_fwd``): same arguments and result as
+    :func:`chunk_gated_delta_rule`.  ``final_state`` may be ``initial_state`` itself, which then
+    is updated in place (the decode state cache)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share a dtype")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("initial_state", initial_state),
+                    ("final_state", final_state)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    s = make_shape(q, v, g, cu_seqlens)
+    o = out if out is not None else torch.empty_like(v)
+    ht = None
+    if output_final_state:
+        ht = final_state if final_state is not None else torch.empty(
+            s.num_seqs, s.HV, s.K, s.V, dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
+        code = lib().gdn_recurrent_fwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                       ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(o),
+                                       _ptr(ht), stream)
+    _check(code, "gdn_recurrent_fwd")
     return o, ht
 
 

@@ -41,7 +41,7 @@ gdn_status validate_shape(const gdn_shape *s, int chunk_size, const gdn_options 
     if (s->gate_kind != GDN_GATE_SCALAR && s->gate_kind != GDN_GATE_CHANNEL) return GDN_ERR_INVALID;
     if (opt) {
         if (opt->cp_mode < GDN_CP_AUTO || opt->cp_mode > GDN_CP_WARMUP) return GDN_ERR_INVALID;
-        if (opt->engine < GDN_ENGINE_AUTO || opt->engine > GDN_ENGINE_TC) return GDN_ERR_INVALID;
+        if (opt->engine < GDN_ENGINE_AUTO || opt->engine > GDN_ENGINE_RECURRENT) return GDN_ERR_INVALID;
         if (opt->segment_chunks < 0 || opt->max_seq_len < 0) return GDN_ERR_INVALID;
         if (!(opt->warmup_log2_eps <= 0.f)) return GDN_ERR_INVALID;
         if (opt->wait_limit_us < 0) return GDN_ERR_INVALID;
@@ -70,6 +70,22 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
 
     *p = Plan{};
     const bool channel = s->gate_kind == GDN_GATE_CHANNEL;
+    // Token by token ("Flash Linear Attention" page, sec. 8: the layer runs fused_recurrent for short
+    // queries): asked for, or AUTO with no sequence longer than kAutoRecurrentTokens.  No split, no
+    // workspace beyond the status word.
+    if (opt.engine == GDN_ENGINE_RECURRENT ||
+        (opt.engine == GDN_ENGINE_AUTO && opt.cp_mode == GDN_CP_AUTO && maxlen <= kAutoRecurrentTokens)) {
+        if (opt.cp_mode == GDN_CP_EXACT || opt.cp_mode == GDN_CP_WARMUP) return GDN_ERR_UNSUPPORTED;
+        p->engine = GDN_ENGINE_RECURRENT;
+        p->cp = GDN_CP_OFF;
+        p->value_tiles = ceil_div(s->V, 32);
+        p->seg_chunks = std::max(max_nt, 1);
+        p->n_seg = 1;
+        p->max_nt = max_nt;
+        p->kernels = 1;
+        p->bytes = kStatusBytes;
+        return GDN_OK;
+    }
     // per-channel gates on the tensor-core engine run without the chunk-parallel split
     const bool tc_ok = tc_shape_ok(s) && !(channel && (opt.cp_mode == GDN_CP_EXACT || opt.cp_mode == GDN_CP_WARMUP));
     if (opt.engine == GDN_ENGINE_TC && !tc_ok) return GDN_ERR_UNSUPPORTED;
@@ -222,6 +238,19 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     a.wait_ns = opt.wait_limit_us > 0 ? 1000ull * (unsigned long long)opt.wait_limit_us : 2000000000ull;
 
     cudaError_t e = cudaSuccess;
+    if (p.engine == GDN_ENGINE_RECURRENT) {
+        RecArgs ra{};
+        ra.q = q; ra.k = k; ra.v = v; ra.g = g; ra.beta = beta; ra.h0 = h0; ra.cu_seqlens = cu;
+        ra.o = o; ra.ht = ht;
+        ra.T = s->T; ra.H = s->H; ra.HV = s->HV; ra.K = s->K; ra.V = s->V; ra.N = N; ra.scale = scale;
+        if (opt.launch_events && opt.n_launch_events > 0 && opt.launch_events[0])
+            cudaEventRecord((cudaEvent_t)opt.launch_events[0], stream);
+        e = launch_recurrent(ra, s->qkv_dtype, s->gate_kind, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        if (opt.launch_events && opt.n_launch_events > 1 && opt.launch_events[1])
+            cudaEventRecord((cudaEvent_t)opt.launch_events[1], stream);
+        return GDN_OK;
+    }
     // optional per-kernel timing marks on the caller's events
     int n_marks = 0;
     auto mark = [&]() {
@@ -449,6 +478,16 @@ gdn_status gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const
                          void *o, float *ht, gdn_stream_t stream)
 {
     return gdn_chunk_fwd_ex(s, q, k, v, g, beta, scale, h0, cu, chunk_size, o, ht, nullptr, stream);
+}
+
+gdn_status gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float scale, const float *h0, const int64_t *cu, void *o, float *ht,
+                             gdn_stream_t stream)
+{
+    gdn_options opt;
+    gdn_default_options(&opt);
+    opt.engine = GDN_ENGINE_RECURRENT;
+    return gdn_chunk_fwd_ex(s, q, k, v, g, beta, scale, h0, cu, kChunk, o, ht, &opt, stream);
 }
 
 gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream)

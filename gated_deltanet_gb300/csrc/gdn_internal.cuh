@@ -165,6 +165,22 @@ __device__ inline void order_longest_first(const int64_t *cu, int N, int n_bucke
 __host__ __device__ inline int64_t tile_slots(int64_t tokens, int nseq) { return tokens / kChunk + nseq + 1; }
 size_t tc_smem_bytes();
 
+// Token-by-token engine (gdn_recurrent.cu): decode and short continuations.  h0 and ht may be the
+// same buffer (the state cache updated in place).
+struct RecArgs {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    const int64_t *cu_seqlens;  // nullable
+    void *o;
+    float *ht;                  // nullable
+    int T, H, HV, K, V, N;
+    float scale;
+};
+cudaError_t launch_recurrent(const RecArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
+// AUTO engine choice: packed or batched sequences of at most this many tokens go to the token-by-token
+// engine (decode, speculative continuations)
+constexpr int kAutoRecurrentTokens = 16;
+
 // Host-side checks of one forward call, as the entry points run them before anything is
 // enqueued; on GDN_OK *ws_bytes (nullable) is the workspace the call needs.
 gdn_status check_call(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,

@@ -68,6 +68,9 @@ WORKLOADS = {
                             h0=True, varlen=32, seed=1003),
     "channel_bf16": Workload("channel_bf16", B=2, T=8192, H=32, K=128, V=128,
                              gate="channel", seed=1004),
+    # one decode step of 64 sequences continuing from a state cache (the token-by-token engine)
+    "decode_bf16": Workload("decode_bf16", B=64, T=1, H=16, K=128, V=128,
+                            h0=True, seed=1005),
 }
 
 

@@ -89,10 +89,15 @@ typedef enum {
 typedef enum {
     GDN_ENGINE_AUTO = 0, /* tensor-core engine where supported, else SIMT            */
     GDN_ENGINE_SIMT = 1, /* fp32 CUDA-core engine (any supported shape, fp32 inputs) */
-    GDN_ENGINE_TC = 2    /* tcgen05/TMEM engine: bf16, K = V = 128, scalar or
+    GDN_ENGINE_TC = 2,   /* tcgen05/TMEM engine: bf16, K = V = 128, scalar or
                             per-channel gate, q/k/v/o (and gk) 16-byte aligned; a
                             call that asks for it on other inputs gets
                             GDN_ERR_INVALID                                       */
+    GDN_ENGINE_RECURRENT = 3 /* token by token, no chunks ("Flash Linear Attention"
+                            page, sec. 8, fused_recurrent, C = 1): for decode and
+                            short continuations; any supported shape; no split.
+                            AUTO selects it when no sequence is longer than 16
+                            tokens (T, or max_seq_len for packed input).          */
 } gdn_engine;
 
 typedef struct {
@@ -252,6 +257,21 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_shape *s,
  * GDN_ERR_TIMEOUT or GDN_ERR_INVALID) and clears it.  Allocates nothing.
  */
 gdn_status gdn_read_noalloc_status(gdn_stream_t stream);
+
+/*
+ * Decode / continuation of the problem statement ("Flash Linear Attention"
+ * page, sec. 8: fused_recurrent, the C = 1 form the layer selects for short
+ * queries): the same operation and arguments as gdn_chunk_fwd (no chunk
+ * size), evaluated token by token on the recurrent engine.  `ht` may be the
+ * same buffer as `h0`: the state cache is then updated in place.  Suited to
+ * a few tokens per sequence (decode steps continuing from a prefill's final
+ * state); longer sequences are faster on gdn_chunk_fwd.
+ */
+gdn_status gdn_recurrent_fwd(const gdn_shape *s,
+                             const void *q, const void *k, const void *v,
+                             const float *g_or_gk, const float *beta, float scale,
+                             const float *h0, const int64_t *cu_seqlens,
+                             void *o, float *ht, gdn_stream_t stream);
 
 /* Plan summary (host only, no GPU needed) -- what a call would launch: the
  * engine and the in-GPU split (FlashQLA blog, "A balanced solution", the CP
