@@ -69,6 +69,10 @@ def load_library(path: str | None = None):
         lib.gdn_chunk_fwd_ws.argtypes = fwd_args + [OP, VP, ctypes.c_size_t, VP]
         lib.gdn_chunk_fwd_host.argtypes = fwd_args + [OP, VP]
         lib.gdn_chunk_fwd_noalloc.argtypes = fwd_args + [OP, VP]
+        lib.gdn_chunk_summary.argtypes = [SP, VP, VP, FP, FP, I64P, ctypes.c_int, FP, OP, VP]
+        lib.gdn_chunk_summary.restype = ctypes.c_int
+        lib.gdn_chain_states.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, FP, FP, FP, VP]
+        lib.gdn_chain_states.restype = ctypes.c_int
         lib.gdn_recurrent_fwd.argtypes = [SP, VP, VP, VP, FP, FP, ctypes.c_float, FP, I64P, VP, FP, VP]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
         for f in (lib.gdn_chunk_fwd, lib.gdn_chunk_fwd_ex, lib.gdn_chunk_fwd_ws, lib.gdn_chunk_fwd_host,
@@ -220,6 +224,40 @@ def fused_recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state
                                        _ptr(ht), stream)
     _check(code, "gdn_recurrent_fwd")
     return o, ht
+
+
+def chunk_summary(k, v, g, beta, cu_seqlens=None, chunk_size=64, **opts):
+    """(S*, M) of every sequence of this input as one piece of a longer sequence (``gdn_chunk_summary``):
+    a float32 tensor [N, HV, K, V + K] (row d: S*[d, :V], then M[d, :K]), S_end = S* + M S_start."""
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    s = make_shape(k, v, g, cu_seqlens)
+    out = torch.empty(s.num_seqs, s.HV, s.K, s.V + s.K, dtype=torch.float32, device=k.device)
+    opt = make_options(**opts)
+    with torch.cuda.device(k.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(k.device).cuda_stream)
+        code = lib().gdn_chunk_summary(ctypes.byref(s), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                       int(chunk_size), _ptr(out), ctypes.byref(opt), stream)
+    _check(code, "gdn_chunk_summary")
+    return out
+
+
+def chain_states(summaries, h0=None):
+    """Start states of consecutive pieces (``gdn_chain_states``): ``summaries`` [R, N, HV, K, V + K] (piece r
+    of every (sequence, head)), ``h0`` [N, HV, K, V] or None; returns [R, N, HV, K, V] with
+    starts[0] = h0 and starts[r + 1] = S*_r + M_r starts[r]."""
+    R, N, HV, K, VE = summaries.shape
+    V = VE - K
+    summaries = summaries.contiguous()
+    if h0 is not None:
+        h0 = h0.contiguous()
+    starts = torch.empty(R, N, HV, K, V, dtype=torch.float32, device=summaries.device)
+    with torch.cuda.device(summaries.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(summaries.device).cuda_stream)
+        code = lib().gdn_chain_states(R, N * HV, K, V, _ptr(summaries), _ptr(h0), _ptr(starts), stream)
+    _check(code, "gdn_chain_states")
+    return starts
 
 
 def chunk_gated_delta_rule_host(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,

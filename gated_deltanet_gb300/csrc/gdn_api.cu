@@ -480,6 +480,73 @@ gdn_status gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const
     return gdn_chunk_fwd_ex(s, q, k, v, g, beta, scale, h0, cu, chunk_size, o, ht, nullptr, stream);
 }
 
+gdn_status gdn_chunk_summary(const gdn_shape *s, const void *k, const void *v, const float *g, const float *beta,
+                             const int64_t *cu, int chunk_size, float *summary, const gdn_options *optp,
+                             gdn_stream_t stream)
+{
+    if (!s || !summary) return GDN_ERR_INVALID;
+    gdn_options opt;
+    if (optp) opt = *optp; else gdn_default_options(&opt);
+    if (opt.engine == GDN_ENGINE_RECURRENT) return GDN_ERR_UNSUPPORTED;
+    // one segment per sequence: no split; per-channel gates take the CUDA-core engine's pre-pass
+    opt.cp_mode = GDN_CP_OFF;
+    if (s->gate_kind == GDN_GATE_CHANNEL) {
+        if (opt.engine == GDN_ENGINE_TC) return GDN_ERR_UNSUPPORTED;
+        opt.engine = GDN_ENGINE_SIMT;
+    }
+    Plan p;
+    gdn_options o2;
+    // q is not read by the pre-pass and o is not written: k and v stand in for their shapes
+    gdn_status st = prepare(s, k, k, v, g, beta, 1.f, cu, chunk_size, v, &opt, &o2, &p);
+    if (st != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    if ((st = managed_ws(p.bytes, cs, &ws, &ws_bytes)) != GDN_OK) return st;
+    char *wsb = (char *)ws;
+    const bool tc = p.engine == GDN_ENGINE_TC;
+    ScanArgs a{};
+    a.q = k; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = nullptr; a.cu_seqlens = cu;
+    a.o = const_cast<void *>(v); a.ht = nullptr;
+    a.B = s->B; a.T = s->T; a.H = s->H; a.HV = s->HV; a.K = s->K; a.V = s->V; a.N = s->num_seqs;
+    a.scale = 1.f;
+    a.seg_chunks = std::max(p.max_nt, 1);
+    a.n_seg = 1;
+    a.mode = kModePrepass;
+    a.vext = s->V + s->K;
+    a.seg_out = summary;
+    a.status = (unsigned *)wsb;
+    a.wait_ns = opt.wait_limit_us > 0 ? 1000ull * (unsigned long long)opt.wait_limit_us : 2000000000ull;
+    cudaError_t e;
+    if (tc) {
+        PrepArgs pa{};
+        pa.k = k; pa.g = g; pa.beta = beta; pa.cu_seqlens = cu;
+        pa.tiles = wsb + p.off_tiles;
+        pa.T = s->T; pa.H = s->H; pa.HV = s->HV; pa.N = s->num_seqs; pa.slots = (int)p.tile_slots;
+        if (p.off_order) { pa.seq_order = (int *)(wsb + p.off_order); pa.n_buckets = p.n_buckets; }
+        pa.status = a.status;
+        pa.wait_ns = a.wait_ns;
+        if ((e = launch_tc_prep(pa, cs)) != cudaSuccess) return GDN_ERR_CUDA;
+        a.tiles = pa.tiles;
+        a.tile_slots = pa.slots;
+        a.seq_order = pa.seq_order;
+        e = launch_tc_scan(a, 2, false, cs);
+    } else {
+        e = launch_simt_scan(a, s->qkv_dtype, s->gate_kind, cs);
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_chain_states(int ranks, int pairs, int K, int V, const float *summaries, const float *h0,
+                            float *starts, gdn_stream_t stream)
+{
+    if (ranks < 1 || pairs < 0 || V <= 0 || !starts || (ranks > 1 && !summaries)) return GDN_ERR_INVALID;
+    if (K != 32 && K != 64 && K != 128) return GDN_ERR_UNSUPPORTED;
+    if (pairs > 65535) return GDN_ERR_UNSUPPORTED;
+    ChainArgs a{summaries, h0, starts, ranks, pairs, K, V};
+    return launch_chain_states(a, (cudaStream_t)stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
                              const float *beta, float scale, const float *h0, const int64_t *cu, void *o, float *ht,
                              gdn_stream_t stream)

@@ -84,6 +84,15 @@ struct PrepArgs {
     unsigned long long wait_ns; // wall-clock limit of the product-completion wait
 };
 
+// Start states of consecutive pieces of sequences from their (S*, M) summaries (context parallel).
+struct ChainArgs {
+    const float *summaries;  // [ranks][pairs][K][V + K]
+    const float *h0;         // [pairs][K][V], nullable (zero)
+    float *starts;           // [ranks][pairs][K][V]
+    int ranks, pairs, K, V;
+};
+cudaError_t launch_chain_states(const ChainArgs &a, cudaStream_t st);
+
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_simt_scan(const ScanArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
 cudaError_t launch_cp_combine(const CombineArgs &a, cudaStream_t st);

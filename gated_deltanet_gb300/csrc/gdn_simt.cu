@@ -424,6 +424,47 @@ __global__ void __launch_bounds__(kThreads) cp_combine_kernel(const CombineArgs 
     }
 }
 
+// Start states of consecutive pieces of one sequence from their summaries (the context-parallel
+// exchange across ranks: FlashQLA blog, "Key problems", the S* / M pre-process, applied to the pieces
+// held by successive ranks): starts[0] = h0, starts[r + 1] = S*_r + M_r starts[r].  Summaries are
+// [ranks][pairs][K][V + K] (S* in the first V columns of each row, M in the last K), starts
+// [ranks][pairs][K][V].  One CTA per (32-column value tile, pair), serial over the ranks.
+template <int K>
+__global__ void __launch_bounds__(kThreads) chain_states_kernel(const ChainArgs a)
+{
+    extern __shared__ float smem[];
+    float *sS = smem, *sT = smem + K * kBV;
+    const int tid = threadIdx.x, pair = blockIdx.y, col0 = blockIdx.x * kBV;
+    const int V = a.V, VE = a.V + K;
+    const size_t pairs = (size_t)a.pairs;
+    for (int e = tid; e < K * kBV; e += kThreads) {
+        const int d = e / kBV, col = col0 + e % kBV;
+        const float x = (a.h0 && col < V) ? a.h0[((size_t)pair * K + d) * V + col] : 0.f;
+        sS[e] = x;
+        if (col < V) a.starts[((size_t)pair * K + d) * V + col] = x;
+    }
+    __syncthreads();
+    for (int r = 0; r + 1 < a.ranks; ++r) {
+        const float *so = a.summaries + ((size_t)r * pairs + pair) * K * VE;
+        for (int e = tid; e < K * kBV; e += kThreads) {
+            const int d = e / kBV, cc = e % kBV, col = col0 + cc;
+            float acc = col < V ? so[(size_t)d * VE + col] : 0.f;
+            const float *Mrow = so + (size_t)d * VE + V;
+#pragma unroll 8
+            for (int m = 0; m < K; ++m) acc = fmaf(Mrow[m], sS[m * kBV + cc], acc);
+            sT[e] = acc;
+        }
+        __syncthreads();
+        float *dst = a.starts + ((size_t)(r + 1) * pairs + pair) * K * V;
+        for (int e = tid; e < K * kBV; e += kThreads) {
+            const int d = e / kBV, col = col0 + e % kBV;
+            sS[e] = sT[e];
+            if (col < V) dst[(size_t)d * V + col] = sT[e];
+        }
+        __syncthreads();
+    }
+}
+
 // Gate statistics for the warmup split (FlashQLA blog, "Further optimisation
 // via gate decay": the warmup length of each segment comes from a separate
 // gate-statistics kernel).  Per chunk the base-2 log of an upper bound on the
@@ -545,6 +586,20 @@ cudaError_t launch_cp_combine(const CombineArgs &a, cudaStream_t st)
     case 32: cp_combine_kernel<32><<<grid, kThreads, smem, st>>>(a); break;
     case 64: cp_combine_kernel<64><<<grid, kThreads, smem, st>>>(a); break;
     case 128: cp_combine_kernel<128><<<grid, kThreads, smem, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chain_states(const ChainArgs &a, cudaStream_t st)
+{
+    if (a.ranks <= 0 || a.pairs <= 0 || a.V <= 0) return cudaSuccess;
+    const dim3 grid(ceil_div(a.V, kBV), a.pairs);
+    const size_t smem = 2 * sizeof(float) * (size_t)a.K * kBV;
+    switch (a.K) {
+    case 32: chain_states_kernel<32><<<grid, kThreads, smem, st>>>(a); break;
+    case 64: chain_states_kernel<64><<<grid, kThreads, smem, st>>>(a); break;
+    case 128: chain_states_kernel<128><<<grid, kThreads, smem, st>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

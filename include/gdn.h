@@ -273,6 +273,35 @@ gdn_status gdn_recurrent_fwd(const gdn_shape *s,
                              const float *h0, const int64_t *cu_seqlens,
                              void *o, float *ht, gdn_stream_t stream);
 
+/*
+ * Context parallel across devices, step 1 (FlashQLA blog, "Key problems in
+ * FLA's GDN chunked prefill": the S* / M pre-process; "KDA source
+ * walkthrough", the cp_context pre-process of chunk_kda_fwd): the summary of
+ * every sequence of this (local) input as one piece of a longer sequence.
+ * For sequence n and value head h, with S_end the state after the piece from
+ * a start state S_0:  S_end = S*[n,h] + M[n,h] S_0.  Written as
+ * summary[N, HV, K, V + K] fp32: row d holds S*[d, 0..V-1] then M[d, 0..K-1].
+ * q is not needed.  Arguments otherwise as gdn_chunk_fwd_ex (no h0, no
+ * outputs); the split options are ignored (one piece per sequence).
+ */
+gdn_status gdn_chunk_summary(const gdn_shape *s,
+                             const void *k, const void *v,
+                             const float *g_or_gk, const float *beta,
+                             const int64_t *cu_seqlens, int chunk_size,
+                             float *summary, const gdn_options *opt, gdn_stream_t stream);
+
+/*
+ * Context parallel, step 2 (same passages): the start state of every piece
+ * from the summaries of the pieces before it.  summaries [ranks][pairs][K][V+K]
+ * (as gdn_chunk_summary writes them, piece r of each of `pairs` (sequence,
+ * head) pairs, gathered in piece order), h0 [pairs][K][V] (nullable: zero),
+ * starts [ranks][pairs][K][V]:  starts[0] = h0,
+ * starts[r+1] = S*_r + M_r starts[r].  K in {32, 64, 128}; pairs <= 65535.
+ * Device pointers; asynchronous on `stream`.
+ */
+gdn_status gdn_chain_states(int ranks, int pairs, int K, int V, const float *summaries,
+                            const float *h0, float *starts, gdn_stream_t stream);
+
 /* Plan summary (host only, no GPU needed) -- what a call would launch: the
  * engine and the in-GPU split (FlashQLA blog, "A balanced solution", the CP
  * enable rule, re-derived for this GPU's SM count). */
