@@ -34,7 +34,9 @@ class GdnOptions(ctypes.Structure):
                 ("keys_unit_norm", ctypes.c_int), ("warmup_log2_eps", ctypes.c_float),
                 ("max_seq_len", ctypes.c_int), ("launch_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("n_launch_events", ctypes.c_int), ("wait_limit_us", ctypes.c_int),
-                ("test_withhold_first_arrival", ctypes.c_int)]
+                ("test_withhold_first_arrival", ctypes.c_int), ("gate_A_log", ctypes.c_void_p),
+                ("gate_dt_bias", ctypes.c_void_p), ("gate_lower_bound", ctypes.c_float),
+                ("beta_logits", ctypes.c_int), ("qk_l2norm", ctypes.c_int), ("state_v_first", ctypes.c_int)]
 
 
 class GdnPlanInfo(ctypes.Structure):
@@ -109,14 +111,22 @@ def _dtype_code(t: torch.dtype) -> int:
 
 def make_options(cp_mode="auto", engine="auto", keys_unit_norm=False, segment_chunks=0,
                  warmup_log2_eps=0.0, max_seq_len=0, launch_events=None, wait_limit_us=0,
-                 test_withhold_first_arrival=False) -> GdnOptions:
+                 test_withhold_first_arrival=False, gate_A_log=None, gate_dt_bias=None, gate_lower_bound=0.0,
+                 beta_logits=False, qk_l2norm=False, state_v_first=False) -> GdnOptions:
     """``launch_events``: optional sequence of raw CUDA event handles (ints) to be recorded
     around each kernel launch (see ``gdn_options.launch_events`` in ``include/gdn.h``).
     ``wait_limit_us`` and ``test_withhold_first_arrival``: the device-side wait limit and the
     timeout-path test switch of ``gdn_options``."""
     opt = GdnOptions(CP_MODES[cp_mode], int(segment_chunks), ENGINES[engine], int(bool(keys_unit_norm)),
                      float(warmup_log2_eps), int(max_seq_len), None, 0, int(wait_limit_us),
-                     int(bool(test_withhold_first_arrival)))
+                     int(bool(test_withhold_first_arrival)), None, None, float(gate_lower_bound),
+                     int(bool(beta_logits)), int(bool(qk_l2norm)), int(bool(state_v_first)))
+    for name, t in (("gate_A_log", gate_A_log), ("gate_dt_bias", gate_dt_bias)):
+        if t is not None:
+            if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+            setattr(opt, name, t.data_ptr())
+            setattr(opt, "_keep_" + name, t)
     if launch_events:
         arr = (ctypes.c_void_p * len(launch_events))(*[int(h) for h in launch_events])
         opt._events_keepalive = arr  # the array lives as long as the options
@@ -146,7 +156,7 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
                            cu_seqlens=None, chunk_size=64, *, cp_mode="auto", engine="auto",
                            keys_unit_norm=False, segment_chunks=0, warmup_log2_eps=0.0, max_seq_len=0,
                            workspace=None, out=None, final_state=None, launch_events=None, wait_limit_us=0,
-                           test_withhold_first_arrival=False):
+                           test_withhold_first_arrival=False, **activations):
     """Gated delta-rule chunked-prefill forward on the GPU.
 
     q, k [B,T,H,K]; v [B,T,HV,V] (float32 or bfloat16, same dtype); g [B,T,HV]
@@ -154,6 +164,9 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     [B,T,HV] float32; initial_state [N,HV,K,V] float32 or None; cu_seqlens
     [N+1] int64 on the device for packed input (B == 1).  Returns
     ``(o, final_state)``; ``final_state`` is None unless requested.
+    ``activations``: the in-kernel input activations of ``gdn_options`` (``gate_A_log``,
+    ``gate_dt_bias``, ``gate_lower_bound``, ``beta_logits``, ``qk_l2norm``, ``state_v_first``;
+    with ``state_v_first`` the states are [N,HV,V,K]).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         if not t.is_cuda:
@@ -175,10 +188,10 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     o = out if out is not None else torch.empty_like(v)
     ht = None
     if output_final_state:
-        ht = final_state if final_state is not None else torch.empty(
-            s.num_seqs, s.HV, s.K, s.V, dtype=torch.float32, device=q.device)
+        shp = (s.num_seqs, s.HV, s.V, s.K) if activations.get("state_v_first") else (s.num_seqs, s.HV, s.K, s.V)
+        ht = final_state if final_state is not None else torch.empty(*shp, dtype=torch.float32, device=q.device)
     opt = make_options(cp_mode, engine, keys_unit_norm, segment_chunks, warmup_log2_eps, max_seq_len,
-                       launch_events, wait_limit_us, test_withhold_first_arrival)
+                       launch_events, wait_limit_us, test_withhold_first_arrival, **activations)
     L = lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
     with torch.cuda.device(q.device):

@@ -25,6 +25,7 @@ struct Plan {
     float log2_eps;
     // workspace layout
     size_t off_warm, off_segout, off_seginit, off_tiles, off_gc, off_order, tile_slots, bytes;
+    size_t off_h0t, off_htt, off_rk;  // transposed-state copies; 1 / ||k|| per row (in-kernel L2 norm)
     int n_buckets;
     bool kda;  // tensor-core engine with per-channel gates
 };
@@ -45,6 +46,8 @@ gdn_status validate_shape(const gdn_shape *s, int chunk_size, const gdn_options 
         if (opt->segment_chunks < 0 || opt->max_seq_len < 0) return GDN_ERR_INVALID;
         if (!(opt->warmup_log2_eps <= 0.f)) return GDN_ERR_INVALID;
         if (opt->wait_limit_us < 0) return GDN_ERR_INVALID;
+        if (!(opt->gate_lower_bound <= 0.f)) return GDN_ERR_INVALID;
+        if (opt->gate_dt_bias && !opt->gate_A_log) return GDN_ERR_INVALID;
     }
     if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
     if (s->K != 32 && s->K != 64 && s->K != 128) return GDN_ERR_UNSUPPORTED;
@@ -84,6 +87,12 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         p->max_nt = max_nt;
         p->kernels = 1;
         p->bytes = kStatusBytes;
+        if (opt.state_v_first) {
+            const size_t sb = (size_t)s->num_seqs * s->HV * s->K * s->V * sizeof(float);
+            p->off_h0t = p->bytes;
+            p->off_htt = align_up(p->off_h0t + sb, 256);
+            p->bytes = align_up(p->off_htt + sb, 256);
+        }
         return GDN_OK;
     }
     // per-channel gates on the tensor-core engine run without the chunk-parallel split
@@ -167,6 +176,17 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         p->kernels = 1;
     }
     if (p->engine == GDN_ENGINE_TC) p->kernels += 1;  // the chunk preparation
+    if (opt.qk_l2norm && p->engine == GDN_ENGINE_TC && !p->kda) {
+        // 1 / ||k_t|| of every row, from the chunk preparation to the scan
+        p->off_rk = off;
+        off = align_up(off + p->tile_slots * s->HV * 64 * sizeof(float), 256);
+    }
+    if (opt.state_v_first) {
+        const size_t sb = (size_t)N * s->HV * s->K * s->V * sizeof(float);
+        p->off_h0t = off;
+        p->off_htt = align_up(off + sb, 256);
+        off = align_up(p->off_htt + sb, 256);
+    }
     p->bytes = off;
     return GDN_OK;
 }
@@ -227,10 +247,27 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     char *wsb = (char *)ws;
     unsigned *status = (unsigned *)wsb;
     const int N = s->num_seqs;
+    const Act act{opt.gate_A_log, opt.gate_dt_bias, opt.gate_lower_bound, opt.beta_logits, opt.qk_l2norm};
+    // the transposed state layout: the engines run on canonical [K][V] copies in the workspace
+    const float *h0u = h0;
+    float *htu = ht;
+    if (opt.state_v_first) {
+        if (h0) {
+            h0u = (const float *)(wsb + p.off_h0t);
+            if (launch_transpose(h0, (float *)h0u, N * s->HV, s->V, s->K, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        if (ht) htu = (float *)(wsb + p.off_htt);
+    }
+    auto finish = [&]() -> gdn_status {
+        if (opt.state_v_first && ht && launch_transpose(htu, ht, N * s->HV, s->K, s->V, stream) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        return GDN_OK;
+    };
 
     ScanArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu_seqlens = cu;
-    a.o = o; a.ht = ht;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0u; a.cu_seqlens = cu;
+    a.o = o; a.ht = htu;
+    a.act = act;
     a.B = s->B; a.T = s->T; a.H = s->H; a.HV = s->HV; a.K = s->K; a.V = s->V; a.N = N;
     a.scale = scale;
     a.seg_chunks = p.seg_chunks; a.n_seg = p.n_seg;
@@ -240,8 +277,9 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     cudaError_t e = cudaSuccess;
     if (p.engine == GDN_ENGINE_RECURRENT) {
         RecArgs ra{};
-        ra.q = q; ra.k = k; ra.v = v; ra.g = g; ra.beta = beta; ra.h0 = h0; ra.cu_seqlens = cu;
-        ra.o = o; ra.ht = ht;
+        ra.q = q; ra.k = k; ra.v = v; ra.g = g; ra.beta = beta; ra.h0 = h0u; ra.cu_seqlens = cu;
+        ra.o = o; ra.ht = htu;
+        ra.act = act;
         ra.T = s->T; ra.H = s->H; ra.HV = s->HV; ra.K = s->K; ra.V = s->V; ra.N = N; ra.scale = scale;
         if (opt.launch_events && opt.n_launch_events > 0 && opt.launch_events[0])
             cudaEventRecord((cudaEvent_t)opt.launch_events[0], stream);
@@ -249,7 +287,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         if (opt.launch_events && opt.n_launch_events > 1 && opt.launch_events[1])
             cudaEventRecord((cudaEvent_t)opt.launch_events[1], stream);
-        return GDN_OK;
+        return finish();
     }
     // optional per-kernel timing marks on the caller's events
     int n_marks = 0;
@@ -266,6 +304,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         ka.gc = (float *)(wsb + p.off_gc);
         ka.T = s->T; ka.H = s->H; ka.HV = s->HV; ka.N = N; ka.slots = (int)p.tile_slots;
         if (p.off_order) { ka.seq_order = (int *)(wsb + p.off_order); ka.n_buckets = p.n_buckets; }
+        ka.act = act;
         a.seq_order = ka.seq_order;
         mark();
         e = launch_kda_prep(ka, stream);
@@ -283,6 +322,9 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         a.seq_order = pa.seq_order;
         pa.status = status;
         pa.wait_ns = a.wait_ns;
+        pa.act = act;
+        if (p.off_rk) pa.rk = (float *)(wsb + p.off_rk);
+        a.rk = pa.rk;
         mark();
         e = launch_tc_prep(pa, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -304,6 +346,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         gs.seg_chunks = p.seg_chunks; gs.n_seg = p.n_seg;
         gs.channel = s->gate_kind == GDN_GATE_CHANNEL;
         gs.log2_eps = p.log2_eps;
+        gs.act = act;
         gs.max_warm_chunks = 1 << 30;
         mark();
         e = launch_gate_stats(gs, stream);
@@ -318,7 +361,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         e = scan_prepass(pre, tc, s, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         CombineArgs cb{};
-        cb.h0 = h0; cb.cu_seqlens = cu; cb.seg_out = pre.seg_out;
+        cb.h0 = h0u; cb.cu_seqlens = cu; cb.seg_out = pre.seg_out;
         cb.seg_init = (float *)(wsb + p.off_seginit);
         cb.T = s->T; cb.HV = s->HV; cb.K = s->K; cb.V = s->V; cb.N = N;
         cb.seg_chunks = p.seg_chunks; cb.n_seg = p.n_seg; cb.status = status;
@@ -332,7 +375,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     e = scan(a);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     mark();
-    return GDN_OK;
+    return finish();
 }
 
 // ---------------------------------------------------------------- library-managed workspaces
@@ -516,6 +559,7 @@ gdn_status gdn_chunk_summary(const gdn_shape *s, const void *k, const void *v, c
     a.vext = s->V + s->K;
     a.seg_out = summary;
     a.status = (unsigned *)wsb;
+    a.act = Act{opt.gate_A_log, opt.gate_dt_bias, opt.gate_lower_bound, opt.beta_logits, opt.qk_l2norm};
     a.wait_ns = opt.wait_limit_us > 0 ? 1000ull * (unsigned long long)opt.wait_limit_us : 2000000000ull;
     cudaError_t e;
     if (tc) {
@@ -526,6 +570,9 @@ gdn_status gdn_chunk_summary(const gdn_shape *s, const void *k, const void *v, c
         if (p.off_order) { pa.seq_order = (int *)(wsb + p.off_order); pa.n_buckets = p.n_buckets; }
         pa.status = a.status;
         pa.wait_ns = a.wait_ns;
+        pa.act = a.act;
+        if (p.off_rk) pa.rk = (float *)(wsb + p.off_rk);
+        a.rk = pa.rk;
         if ((e = launch_tc_prep(pa, cs)) != cudaSuccess) return GDN_ERR_CUDA;
         a.tiles = pa.tiles;
         a.tile_slots = pa.slots;

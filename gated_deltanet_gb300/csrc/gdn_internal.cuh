@@ -23,6 +23,29 @@ enum : unsigned {
 
 enum Mode : int { kModeForward = 0, kModePrepass = 1 };
 
+// Input activations applied where the kernels load their inputs ("Flash Linear Attention" page,
+// sec. 10, the in-kernel gate / L2-norm / sigma(beta) of the KDA inference backend; "KDA source
+// walkthrough", kda_gate_chunk_cumsum for the gate).  All fields zero: inputs are used as given.
+struct Act {
+    const float *A_log;    // [HV]: the gate input is activated (nullable = g is already the log-decay)
+    const float *dt_bias;  // [HV] (scalar gate) or [HV][K] (per-channel gate), nullable
+    float lower_bound;     // < 0: g = lower_bound * sigmoid(exp(A_log) (x + bias));
+                           // 0: g = -exp(A_log) * softplus(x + bias)
+    int beta_logits;       // beta = sigmoid(input)
+    int qk_l2norm;         // q, k scaled to unit L2 norm per (token, head) (x / max(||x||, 1e-12))
+};
+// the log-decay of gate input x for value head hv (channel d, or d < 0 for a scalar gate)
+__device__ __forceinline__ float act_gate(const Act &a, float x, int hv, int d, int K)
+{
+    if (!a.A_log) return x;
+    const float z = x + (a.dt_bias ? a.dt_bias[d < 0 ? hv : hv * K + d] : 0.f);
+    const float ea = expf(a.A_log[hv]);
+    if (a.lower_bound < 0.f) return a.lower_bound / (1.f + expf(-ea * z));
+    return -ea * (z > 20.f ? z : log1pf(expf(z)));  // softplus, linear past 20 like the usual threshold
+}
+__device__ __forceinline__ float act_beta(const Act &a, float x) { return a.beta_logits ? 1.f / (1.f + expf(-x)) : x; }
+constexpr float kNormEps = 1e-12f;
+
 // Arguments of one scan launch (one engine pass over segments).
 struct ScanArgs {
     const void *q, *k, *v;
@@ -49,6 +72,8 @@ struct ScanArgs {
     const int *seq_order;   // [N] sequence of each grid.z group (longest first), nullable = natural order
     unsigned long long wait_ns;  // wall-clock limit of every device-side wait (tensor-core engine)
     int withhold_full0;     // timeout-path test: the load warp never signals its first chunk
+    Act act;
+    const float *rk;        // tensor-core engine, in-kernel L2 norm: 1 / ||k_t|| per (slot, value head, row)
 };
 
 struct CombineArgs {
@@ -68,6 +93,7 @@ struct GateStatsArgs {
     int T, HV, K, N, seg_chunks, n_seg, channel;
     float log2_eps;        // threshold on the window's accumulated log2-decay
     int max_warm_chunks;   // walk at most this far back, else start from the sequence start
+    Act act;
 };
 
 // Arguments of the tensor-core engine's chunk preparation (operand tiles of every chunk).
@@ -82,6 +108,8 @@ struct PrepArgs {
     int *seq_order;             // nullable: block (0, 0) writes the longest-first sequence order here
     int n_buckets;              //   chunk-count buckets of that sort (<= kOrderBuckets)
     unsigned long long wait_ns; // wall-clock limit of the product-completion wait
+    Act act;
+    float *rk;                  // qk_l2norm: 1 / ||k_t|| per (slot, value head, row), written for the scan
 };
 
 // Start states of consecutive pieces of sequences from their (S*, M) summaries (context parallel).
@@ -92,6 +120,8 @@ struct ChainArgs {
     int ranks, pairs, K, V;
 };
 cudaError_t launch_chain_states(const ChainArgs &a, cudaStream_t st);
+// dst[p][b][a] = src[p][a][b] for p < P (fp32), the state layouts [K][V] <-> [V][K]
+cudaError_t launch_transpose(const float *src, float *dst, int P, int A, int B, cudaStream_t st);
 
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_simt_scan(const ScanArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
@@ -115,6 +145,7 @@ struct KdaPrepArgs {
     int T, H, HV, N, slots;
     int *seq_order;             // as PrepArgs
     int n_buckets;
+    Act act;
 };
 cudaError_t launch_kda_prep(const KdaPrepArgs &a, cudaStream_t st);
 constexpr size_t kKdaTileBytesPerChunk = 9 * 64 * 64 * 2 + 128 * 4;  // nine bf16 boxes and gC
@@ -184,6 +215,7 @@ struct RecArgs {
     float *ht;                  // nullable
     int T, H, HV, K, V, N;
     float scale;
+    Act act;
 };
 cudaError_t launch_recurrent(const RecArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
 // AUTO engine choice: packed or batched sequences of at most this many tokens go to the token-by-token

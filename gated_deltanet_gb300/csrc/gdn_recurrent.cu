@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_kernel(const RecArgs a)
     __shared__ float s_gk[2][CHANNEL ? KD : 1];
     __shared__ float s_red[2][4][kRecBV];  // [u, o][warp][column]
     __shared__ float s_gb[2][2];           // [token parity][alpha, beta]
+    __shared__ float s_nrm[2][2][4];       // [token parity][k, q][warp]: partial sums of squares
 
     const size_t sbase = ((size_t)n * HV + hv) * KD * V;
     float s[RPW];
@@ -72,14 +73,32 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_kernel(const RecArgs a)
     auto stage = [&](int64_t t) {
         const int b = (int)(t & 1);
         const size_t tok = (size_t)(bos + t);
-        for (int i = threadIdx.x; i < KD; i += kRecThreads) {
-            s_kq[b][0][i] = ldf(k + (tok * a.H + hq) * KD + i);
-            s_kq[b][1][i] = a.scale * ldf(q + (tok * a.H + hq) * KD + i);
-            if constexpr (CHANNEL) s_gk[b][i] = expf(a.g[(tok * HV + hv) * KD + i]);
+        // KD <= kRecThreads: at most one key-dimension element per thread
+        float kx = 0.f, qx = 0.f;
+        if (threadIdx.x < KD) {
+            const int i = threadIdx.x;
+            kx = ldf(k + (tok * a.H + hq) * KD + i);
+            qx = ldf(q + (tok * a.H + hq) * KD + i);
+            s_kq[b][0][i] = kx;
+            s_kq[b][1][i] = a.scale * qx;
+            if constexpr (CHANNEL) s_gk[b][i] = expf(act_gate(a.act, a.g[(tok * HV + hv) * KD + i], hv, i, KD));
+        }
+        if (a.act.qk_l2norm) {
+            // in-kernel L2 norm: per-warp sums of squares, combined by the readers
+            float sk = kx * kx, sq = qx * qx;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            }
+            if (lane == 0) {
+                s_nrm[b][0][warp] = sk;
+                s_nrm[b][1][warp] = sq;
+            }
         }
         if (threadIdx.x == 0) {
-            if constexpr (!CHANNEL) s_gb[b][0] = expf(a.g[tok * HV + hv]);
-            s_gb[b][1] = a.beta[tok * HV + hv];
+            if constexpr (!CHANNEL) s_gb[b][0] = expf(act_gate(a.act, a.g[tok * HV + hv], hv, -1, KD));
+            s_gb[b][1] = act_beta(a.act, a.beta[tok * HV + hv]);
         }
     };
     if (len > 0) stage(0);
@@ -88,6 +107,12 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_kernel(const RecArgs a)
         const size_t tok = (size_t)(bos + t);
         const float vval = vok ? ldf(vv + (tok * HV + hv) * V + v) : 0.f;
         __syncthreads();  // token t staged; the reductions of token t - 1 are read
+        // 1 / ||k_t||, 1 / ||q_t|| of the in-kernel L2 norm (1 otherwise)
+        float rk = 1.f, rq = 1.f;
+        if (a.act.qk_l2norm) {
+            rk = 1.f / fmaxf(sqrtf(s_nrm[b][0][0] + s_nrm[b][0][1] + s_nrm[b][0][2] + s_nrm[b][0][3]), kNormEps);
+            rq = 1.f / fmaxf(sqrtf(s_nrm[b][1][0] + s_nrm[b][1][1] + s_nrm[b][1][2] + s_nrm[b][1][3]), kNormEps);
+        }
         if (t + 1 < len) stage(t + 1);
         // decay, then the read-out of the decayed state
         float u = 0.f;
@@ -99,8 +124,8 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_kernel(const RecArgs a)
         }
         s_red[0][warp][lane] = u;
         __syncthreads();
-        u = s_red[0][0][lane] + s_red[0][1][lane] + s_red[0][2][lane] + s_red[0][3][lane];
-        const float delta = s_gb[b][1] * (vval - u);
+        u = rk * (s_red[0][0][lane] + s_red[0][1][lane] + s_red[0][2][lane] + s_red[0][3][lane]);
+        const float delta = rk * s_gb[b][1] * (vval - u);  // the write uses k / ||k|| too
         float ov = 0.f;
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
@@ -111,7 +136,8 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_kernel(const RecArgs a)
         s_red[1][warp][lane] = ov;
         __syncthreads();
         if (warp == 0 && vok)
-            stf(o + (tok * HV + hv) * V + v, s_red[1][0][lane] + s_red[1][1][lane] + s_red[1][2][lane] + s_red[1][3][lane]);
+            stf(o + (tok * HV + hv) * V + v,
+                rq * (s_red[1][0][lane] + s_red[1][1][lane] + s_red[1][2][lane] + s_red[1][3][lane]));
     }
     if (a.ht && vok) {
 #pragma unroll

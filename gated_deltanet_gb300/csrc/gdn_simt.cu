@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
                 const size_t off = ((size_t)(t0 + r) * a.H + hq) * K + d;
                 kv = to_f(k[off]);
                 if (emit) qv = to_f(q[off]);
-                if (CHANNEL) gv = a.g[((size_t)(t0 + r) * a.HV + hv) * K + d] * kRcpLn2;
+                if (CHANNEL) gv = act_gate(a.act, a.g[((size_t)(t0 + r) * a.HV + hv) * K + d], hv, d, K) * kRcpLn2;
             }
             sK[r * KP + d] = kv;
             sQ[r * KP + d] = qv;
@@ -145,10 +145,21 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
         }
         if (tid < 64) {
             const bool ok = tid < nrow;
-            sB[tid] = ok ? a.beta[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-            if (!CHANNEL) sG[tid] = ok ? a.g[(size_t)(t0 + tid) * a.HV + hv] * kRcpLn2 : 0.f;
+            sB[tid] = ok ? act_beta(a.act, a.beta[(size_t)(t0 + tid) * a.HV + hv]) : 0.f;
+            if (!CHANNEL) sG[tid] = ok ? act_gate(a.act, a.g[(size_t)(t0 + tid) * a.HV + hv], hv, -1, K) * kRcpLn2 : 0.f;
         }
         __syncthreads();
+        if (a.act.qk_l2norm) {
+            // in-kernel L2 norm: every row of k (and of q when the chunk is emitted) to unit length
+            if (tid < 128 && (tid < 64 || emit)) {
+                float *row = (tid < 64 ? sK : sQ) + (tid & 63) * KP;
+                float ss = 0.f;
+                for (int d = 0; d < K; ++d) ss = fmaf(row[d], row[d], ss);
+                const float rn = 1.f / fmaxf(sqrtf(ss), kNormEps);
+                for (int d = 0; d < K; ++d) row[d] *= rn;
+            }
+            __syncthreads();
+        }
 
         // ---- gate cumsum inside the chunk (inclusive)
         if (CHANNEL) {
@@ -496,11 +507,11 @@ __global__ void __launch_bounds__(kThreads) gate_stats_kernel(const GateStatsArg
             const size_t t = (size_t)(bos + (int64_t)c * kChunk + r);
             if (a.channel) {
                 const float *gt = a.g + (t * a.HV + hv) * a.K;
-                float mx = gt[0];
-                for (int d = 1; d < a.K; ++d) mx = fmaxf(mx, gt[d]);
+                float mx = act_gate(a.act, gt[0], hv, 0, a.K);
+                for (int d = 1; d < a.K; ++d) mx = fmaxf(mx, act_gate(a.act, gt[d], hv, d, a.K));
                 part += mx;
             } else {
-                part += a.g[t * a.HV + hv];
+                part += act_gate(a.act, a.g[t * a.HV + hv], hv, -1, a.K);
             }
         }
 #pragma unroll
@@ -602,6 +613,29 @@ cudaError_t launch_chain_states(const ChainArgs &a, cudaStream_t st)
     case 128: chain_states_kernel<128><<<grid, kThreads, smem, st>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
+}
+
+// Batched fp32 transpose through 32 x 33 shared tiles (coalesced reads and writes).
+__global__ void __launch_bounds__(256) transpose_kernel(const float *src, float *dst, int A, int B)
+{
+    __shared__ float t[32][33];
+    const size_t p = blockIdx.z;
+    const int a0 = blockIdx.y * 32, b0 = blockIdx.x * 32, tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const float *s = src + p * (size_t)A * B;
+    float *d = dst + p * (size_t)A * B;
+    for (int i = ty; i < 32; i += 8)
+        if (a0 + i < A && b0 + tx < B) t[i][tx] = s[(size_t)(a0 + i) * B + b0 + tx];
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8)
+        if (b0 + i < B && a0 + tx < A) d[(size_t)(b0 + i) * A + a0 + tx] = t[tx][i];
+}
+
+cudaError_t launch_transpose(const float *src, float *dst, int P, int A, int B, cudaStream_t st)
+{
+    if (P == 0 || A == 0 || B == 0) return cudaSuccess;
+    if (P > 65535) return cudaErrorInvalidValue;
+    transpose_kernel<<<dim3(ceil_div(B, 32), ceil_div(A, 32), P), 256, 0, st>>>(src, dst, A, B);
     return cudaGetLastError();
 }
 

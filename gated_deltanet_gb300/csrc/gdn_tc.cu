@@ -58,9 +58,11 @@ constexpr uint32_t OFF_STAGE = 0;
 // 2^G_C of the 128 channels).  A ring of four: the O epilogue of chunk c still reads its row
 // factors while chunk c + 3 is loaded
 constexpr int kGateStages = 4;
-constexpr uint32_t kGateBytes = 1536;
-template <bool KDA>
+template <bool ACT>
+constexpr uint32_t kGateBytesOf = ACT ? 2048u : 1536u;  // + 1/||k||, 1/||q|| with in-kernel activations
+template <bool KDA, bool ACT>
 struct TcLayout {
+    static constexpr uint32_t kGateBytes = kGateBytesOf<ACT>;
     static constexpr uint32_t kStageBytes = KDA ? 73728u : 65536u;
     static constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P [64 x 64] bf16 (scalar gate)
     static constexpr uint32_t OFF_WS = OFF_P + (KDA ? 0u : 8192u);         // -W^T [128 (dk) x 64] bf16, MN-major
@@ -70,7 +72,8 @@ struct TcLayout {
 };
 
 // gate arrays inside a stage's gate block
-constexpr int GT_G = 0, GT_GRAW = 64, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320;
+constexpr int GT_G = 0, GT_GRAW = 64, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320,
+              GT_RK = 384, GT_RQ = 448;  // in-kernel L2 norm: 1 / ||k_t|| (from the preparation), 1 / ||q_t||
 // G_C >= this: Gam_ij = gam_i * 2^-G_j with every factor inside the fp32 range
 constexpr float kFactorFloor = -100.f;
 
@@ -113,8 +116,9 @@ __device__ __forceinline__ bool elect_one()
 // the chunk where that happens is the start.  If the sequence start is reached
 // first, start there (the exact prefix).  One warp; lane l sums tokens l and
 // l + 32 of a chunk, eight chunks per round trip to memory.
+template <bool ACT>
 __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t len, int HV, int hv, int c0,
-                                          float log2_eps)
+                                          float log2_eps, const Act &act)
 {
     const int lane = threadIdx.x & 31;
     float acc = 0.f;
@@ -126,8 +130,13 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
             const int cc = c - 1 - b;
             const int rows = cc >= 0 ? rows_in(len, cc) : 0;
             const float *gp = g + ((size_t)(bos + (int64_t)(cc >= 0 ? cc : 0) * kChunk) + lane) * HV + hv;
-            v[2 * b] = lane < rows ? gp[0] : 0.f;
-            v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+            if constexpr (ACT) {
+                v[2 * b] = lane < rows ? act_gate(act, gp[0], hv, -1, 128) : 0.f;
+                v[2 * b + 1] = lane + 32 < rows ? act_gate(act, gp[(size_t)32 * HV], hv, -1, 128) : 0.f;
+            } else {
+                v[2 * b] = lane < rows ? gp[0] : 0.f;
+                v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+            }
         }
 #pragma unroll 1
         for (int b = 0; b < 8 && c - 1 - b >= 0; ++b) {
@@ -144,10 +153,15 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
     return 0;
 }
 
-template <bool KDA>
+template <bool KDA, bool ACT>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a, const __grid_constant__ TcMaps m)
 {
-    using Lay = TcLayout<KDA>;
+    // ACT: the in-kernel input activations (raw gate input, L2 norm of q and k); a separate instance, so
+    // that the plain one carries none of their code
+    using Lay = TcLayout<KDA, ACT>;
+    constexpr uint32_t kGateBytes = Lay::kGateBytes;
+    const float *const rkp = ACT ? a.rk : nullptr;
+    const bool nrm = ACT && a.act.qk_l2norm;
     constexpr uint32_t kStageBytes = Lay::kStageBytes, OFF_P = Lay::OFF_P, OFF_WS = Lay::OFF_WS,
                        OFF_GATE = Lay::OFF_GATE, OFF_BAR = Lay::OFF_BAR;
     extern __shared__ __align__(1024) uint8_t smraw[];
@@ -189,12 +203,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const int cj = j * L;
                 if (j == 0) return 0;
                 if (cj >= NT) return NT;
-                const int w = cj - warm_start_of(a.g, bos, len, HV, hv, cj, a.warm_log2_eps);
+                const int w = cj - warm_start_of<ACT>(a.g, bos, len, HV, hv, cj, a.warm_log2_eps, a.act);
                 return min(cj + (min(w, L) + 2) / 4, NT);
             };
             c0 = bnd(seg);
             c1 = bnd(seg + 1);
-            if (seg > 0) cs = warm_start_of(a.g, bos, len, HV, hv, c0, a.warm_log2_eps);
+            if (seg > 0) cs = warm_start_of<ACT>(a.g, bos, len, HV, hv, c0, a.warm_log2_eps, a.act);
         } else if (fwd && seg > 0) {
             if (a.warm_start) {
                 cs = a.warm_start[sidx];
@@ -311,6 +325,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                         const int r = 2 * lane + u;
                         cp_async4(graw + r, gsrc + (size_t)(r < rows ? r : 0) * HV, r < rows ? 4u : 0u);
                     }
+                    if (rkp) {
+                        const float *rsrc = rkp + ((size_t)tile_slot(bos, n, c) * HV + hv) * 64;
+                        cp_async4(gates(ni) + GT_RK + 2 * lane, rsrc + 2 * lane, 4u);
+                        cp_async4(gates(ni) + GT_RK + 2 * lane + 1, rsrc + 2 * lane + 1, 4u);
+                    }
                 }
                 cp_async_commit();
                 ++ni;
@@ -329,7 +348,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     // gate statistics: lane holds rows 2l, 2l+1; base-2 inclusive cumsum
                     const int r0 = 2 * lane, r1 = r0 + 1;
                     const float2 gr = *(const float2 *)(gt + GT_GRAW + r0);
-                    const float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
+                    // (activated in place when the gate input is raw; rows past the end stay exactly 0)
+                    float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
+                    if constexpr (ACT) {
+                        g0 = (r0 < rows ? act_gate(a.act, gr.x, hv, -1, 128) : 0.f) * kRcpLn2;
+                        g1 = (r1 < rows ? act_gate(a.act, gr.y, hv, -1, 128) : 0.f) * kRcpLn2;
+                    }
                     float sp = g0 + g1;
     #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
@@ -341,7 +365,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     const float gm0 = ex2(G0), gm1 = ex2(G1);
                     *(float2 *)(gt + GT_G + r0) = make_float2(G0, G1);
                     *(float2 *)(gt + GT_GAM + r0) = make_float2(gm0, gm1);
-                    *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0), ex2(GC - G1));
+                    // the update operand's row factors gC / gam (and 1 / ||k|| of the in-kernel L2 norm)
+                    float2 rk2 = make_float2(1.f, 1.f);
+                    if (rkp) rk2 = *(const float2 *)(gt + GT_RK + r0);
+                    *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0) * rk2.x, ex2(GC - G1) * rk2.y);
                     *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
                     *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
                     if (rows < kChunk) {
@@ -635,11 +662,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_KQE]);
             const bool fac = gt[GT_G + 63] >= kFactorFloor;
+            float rq = 1.f;
+            if (nrm) {
+                // in-kernel L2 norm: 1 / ||q_r|| from row r of the chunk's Q boxes (before a steep chunk's
+                // in-place Q~), for the O epilogue's row factor
+                const uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
+                float ss = 0.f;
+#pragma unroll 1
+                for (int bx = 0; bx < 2; ++bx) {
+                    const uint8_t *row = st + (bx ? sQ1 : sQ0) + r * 128;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 x = *(const uint4 *)(row + ((c8 + r) & 7) * 16);
+                        const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 fv = __bfloat1622float2(h2[q]);
+                            ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
+                        }
+                    }
+                }
+                rq = 1.f / fmaxf(sqrtf(ss), kNormEps);
+                ((float *)gt)[GT_RQ + r] = rq;
+            }
             if (!fac) {
                 // steep chunk: Q~ row r = scale * gam_r * q_r, in place (the Q K^T product has read Q);
                 // the 16-byte pieces go in a row-rotated order to spread the banks, all loads first
                 uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-                const float f = gt[GT_SGAM + r];
+                const float f = gt[GT_SGAM + r] * rq;
 #pragma unroll 1
                 for (int bx = 0; bx < 2; ++bx) {
                     uint8_t *row = st + (bx ? sQ1 : sQ0) + r * 128;
@@ -679,9 +729,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                         *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
                     }
                 } else {
-                    // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j]
+                    // P row r = scale * Gam[r, j <= r] * (Q K^T)[r, j]  (/ (||q_r|| ||k_j||) with the L2 norm)
                     // steep decay: 2^-G_j may overflow, so each entry takes its own power
-                    const float Gr = gt[GT_G + r], sc = a.scale;
+                    const float Gr = gt[GT_G + r], sc = a.scale * rq;
 #pragma unroll 1
                     for (int q = 0; q < 8; ++q) {
                         const float4 g0 = *(const float4 *)(gt + GT_G + 8 * q);
@@ -694,7 +744,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
 #pragma unroll
                             for (int qq = 0; qq < 8; ++qq)
                                 if (qq == q) x = kq[8 * qq + u];
-                            v[u] = (8 * q + u <= r) ? sc * ex2(Gr - gj[u]) * u2f(x) : 0.f;
+                            const float rkj = rkp ? gt[GT_RK + 8 * q + u] : 1.f;
+                            v[u] = (8 * q + u <= r) ? sc * rkj * ex2(Gr - gj[u]) * u2f(x) : 0.f;
                         }
                         *(uint4 *)(prow + sw128(r, 8 * q)) = pack8(v);
                     }
@@ -925,10 +976,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld_wait();
                 const float *gt = gates(ci);
                 if (!KDA && factored(ci)) {
-                    // the row factors scale * gam_t of the factored form (per-channel gates: inside Q~ and P)
+                    // the row factors scale * gam_t of the factored form (per-channel gates: inside Q~ and P),
+                    // with 1 / ||q_t|| of the in-kernel L2 norm
+                    const bool nq = nrm;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
-                        const float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
+                        float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
+                        if (nq) {
+                            const float4 rq4 = *(const float4 *)(gt + GT_RQ + 4 * j4);
+                            f.x *= rq4.x; f.y *= rq4.y; f.z *= rq4.z; f.w *= rq4.w;
+                        }
                         r[4 * j4] = f2u(u2f(r[4 * j4]) * f.x);
                         r[4 * j4 + 1] = f2u(u2f(r[4 * j4 + 1]) * f.y);
                         r[4 * j4 + 2] = f2u(u2f(r[4 * j4 + 2]) * f.z);
@@ -1039,7 +1096,7 @@ bool encode_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t
     return make_tiles_map(map, base, rows, box_rows);
 }
 
-size_t tc_smem_bytes() { return TcLayout<false>::kSmem; }
+size_t tc_smem_bytes() { return TcLayout<false, false>::kSmem; }
 
 bool tc_shape_ok(const gdn_shape *s)
 {
@@ -1063,7 +1120,8 @@ bool tc_supported(const gdn_shape *s, const void *q, const void *k, const void *
 
 cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st)
 {
-    static_assert(TcLayout<false>::kSmem <= 227 * 1024 && TcLayout<true>::kSmem <= 227 * 1024,
+    static_assert(TcLayout<false, false>::kSmem <= 227 * 1024 && TcLayout<false, true>::kSmem <= 227 * 1024 &&
+                      TcLayout<true, false>::kSmem <= 227 * 1024,
                   "shared memory budget");
     if (a.N * a.HV == 0) return cudaSuccess;
     TcMaps maps;
@@ -1082,17 +1140,19 @@ cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStr
         }
     }
     dim3 grid(value_tiles, a.n_seg, a.N * a.HV);
-    if (kda) {
-        constexpr uint32_t smem = TcLayout<true>::kSmem;
-        cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto go = [&](auto kern, uint32_t smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        tc_scan_kernel<true><<<grid, kThreadsTC, smem, st>>>(a, maps);
-    } else {
-        constexpr uint32_t smem = TcLayout<false>::kSmem;
-        cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        tc_scan_kernel<false><<<grid, kThreadsTC, smem, st>>>(a, maps);
-    }
+        kern<<<grid, kThreadsTC, smem, st>>>(a, maps);
+        return cudaSuccess;
+    };
+    // the per-channel engine's operands come prepared (activated, normalised) from its preparation
+    const bool act = !kda && (a.act.A_log != nullptr || a.act.qk_l2norm);
+    cudaError_t e;
+    if (kda) e = go(tc_scan_kernel<true, false>, TcLayout<true, false>::kSmem);
+    else if (act) e = go(tc_scan_kernel<false, true>, TcLayout<false, true>::kSmem);
+    else e = go(tc_scan_kernel<false, false>, TcLayout<false, false>::kSmem);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

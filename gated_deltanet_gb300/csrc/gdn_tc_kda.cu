@@ -103,7 +103,15 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         for (int i = 0; i < 8; ++i) {
             const int e = tid + kThreadsKda * i, r = e >> 5, c4 = (e & 31) * 4;
             gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < rows) gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
+            if (r < rows) {
+                gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
+                if (a.act.A_log) {  // raw gate input: the activation, per channel
+                    gv[i].x = act_gate(a.act, gv[i].x, hv, c4, 128);
+                    gv[i].y = act_gate(a.act, gv[i].y, hv, c4 + 1, 128);
+                    gv[i].z = act_gate(a.act, gv[i].z, hv, c4 + 2, 128);
+                    gv[i].w = act_gate(a.act, gv[i].w, hv, c4 + 3, 128);
+                }
+            }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -118,8 +126,25 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                 make_float4(gv[i].x * kRcpLn2, gv[i].y * kRcpLn2, gv[i].z * kRcpLn2, gv[i].w * kRcpLn2);
         }
     }
-    if (tid < 64) sh.beta[tid] = tid < rows ? a.beta[(size_t)(t0 + tid) * HV + hv] : 0.f;
+    if (tid < 64) sh.beta[tid] = tid < rows ? act_beta(a.act, a.beta[(size_t)(t0 + tid) * HV + hv]) : 0.f;
     __syncthreads();
+    if (a.act.qk_l2norm) {
+        // in-kernel L2 norm: the rows of k and q to unit length (fp32 arithmetic, one bf16 rounding, as
+        // every operand of the products below is bf16)
+        if (tid < 128) {
+            __nv_bfloat16 *row = (tid < 64 ? sh.k : sh.q) + (tid & 63) * QP;
+            float ss = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < 128; ++c) {
+                const float x = __bfloat162float(row[c]);
+                ss = fmaf(x, x, ss);
+            }
+            const float rn = 1.f / fmaxf(sqrtf(ss), kNormEps);
+#pragma unroll 4
+            for (int c = 0; c < 128; ++c) row[c] = __float2bfloat16_rn(__bfloat162float(row[c]) * rn);
+        }
+        __syncthreads();
+    }
     // ---- per-channel inclusive cumsum (one thread per channel)
     if (tid < 128) {
         float acc = 0.f;

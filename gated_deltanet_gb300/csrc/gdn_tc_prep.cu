@@ -31,6 +31,7 @@ struct PrepSmem {
     // tile: L in the lower triangle, X^T in the upper (X(r, j), j < r, at lx[j * kLdX + r]).
     __align__(1024) uint8_t buf[8192 + 64 * kLdX * 4];
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
+    __align__(16) float bw[64], rk[64];  // beta / ||k|| (T_W's column factor), 1 / ||k|| (in-kernel L2 norm)
     uint64_t bar;
     uint32_t tslot;
 };
@@ -41,8 +42,11 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
     return r < kChunk ? (int)r : kChunk;
 }
 
+template <bool ACT>
 __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tmap)
 {
+    // ACT: the in-kernel input activations (raw gate input, sigmoid(beta), L2 norm of k); a separate
+    // instance, so that the plain one carries none of their code
     __shared__ __align__(1024) PrepSmem sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (a.seq_order && blockIdx.x == 0 && blockIdx.y == 0) {  // the scan's CTA order (K's buffer as scratch)
@@ -78,12 +82,22 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp == 0) {
         if (r0 < rows) {
-            g0 = a.g[(size_t)(t0 + r0) * HV + hv] * kRcpLn2;
+            g0 = a.g[(size_t)(t0 + r0) * HV + hv];
             b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
+            if constexpr (ACT) {
+                g0 = act_gate(a.act, g0, hv, -1, 128);
+                b0 = act_beta(a.act, b0);
+            }
+            g0 *= kRcpLn2;
         }
         if (r1 < rows) {
-            g1 = a.g[(size_t)(t0 + r1) * HV + hv] * kRcpLn2;
+            g1 = a.g[(size_t)(t0 + r1) * HV + hv];
             b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
+            if constexpr (ACT) {
+                g1 = act_gate(a.act, g1, hv, -1, 128);
+                b1 = act_beta(a.act, b1);
+            }
+            g1 *= kRcpLn2;
         }
     }
     {
@@ -143,10 +157,33 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     }
     if (warp < 2) {
         const bool ok = mbar_wait(&sh.bar, 0, a.status, kStatusTimeout, a.wait_ns);
-        if (__all_sync(0xffffffffu, ok)) {
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        const int r = 32 * warp + lane;
+        // in-kernel L2 norm: ||k_r||^2 is the diagonal of K K^T (column r, in this warp's half); every
+        // entry of L takes beta_r / (||k_r|| ||k_j||) and T_W's columns 1 / ||k_j|| (W = T_W K^, K^ = diag(rk) K)
+        float rr = 1.f;
+        if (ACT && a.act.qk_l2norm) {
+            float dg = 0.f;
+            if (all_ok) {
+                uint32_t d[32];
+                tc_fence_after();
+                tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32 * warp, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j == lane) dg = __uint_as_float(d[j]);
+            }
+            rr = r < rows ? 1.f / fmaxf(sqrtf(fmaxf(dg, 0.f)), kNormEps) : 0.f;
+            if (a.rk) a.rk[((size_t)slot * HV + hv) * 64 + r] = rr;
+        }
+        if constexpr (ACT) {
+            sh.rk[r] = rr;
+            sh.bw[r] = sh.beta[r] * rr;
+            bar_sync(1, 64);  // both warps' 1 / ||k||
+        }
+        if (all_ok) {
             tc_fence_after();
-            const int r = 32 * warp + lane;
-            const float br_ = sh.beta[r];
+            const float br_ = sh.beta[r] * rr;
             float *lr = lx + r * kLdX;
             float diag = 0.f;
 #pragma unroll 1
@@ -156,11 +193,12 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
                 tmem_ld_wait();
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 c = ACT ? *(const float4 *)(sh.rk + 32 * h + 4 * j4) : make_float4(1.f, 1.f, 1.f, 1.f);
                     float4 v;
-                    v.x = br_ * __uint_as_float(d[4 * j4]);
-                    v.y = br_ * __uint_as_float(d[4 * j4 + 1]);
-                    v.z = br_ * __uint_as_float(d[4 * j4 + 2]);
-                    v.w = br_ * __uint_as_float(d[4 * j4 + 3]);
+                    v.x = br_ * c.x * __uint_as_float(d[4 * j4]);
+                    v.y = br_ * c.y * __uint_as_float(d[4 * j4 + 1]);
+                    v.z = br_ * c.z * __uint_as_float(d[4 * j4 + 2]);
+                    v.w = br_ * c.w * __uint_as_float(d[4 * j4 + 3]);
                     if (32 * h + 4 * j4 == (r & ~3))
                         diag = (r & 3) == 0 ? v.x : (r & 3) == 1 ? v.y : (r & 3) == 2 ? v.z : v.w;
                     *(float4 *)(lr + 32 * h + 4 * j4) = v;
@@ -347,7 +385,7 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 #pragma unroll 1
                 for (int q = 0; q < 4; ++q) {
                     const int j0 = 32 * h + 8 * q;
-                    const float *bsrc = pass == 0 || !factored ? sh.beta : sh.br;
+                    const float *bsrc = pass == 0 ? (ACT ? sh.bw : sh.beta) : !factored ? sh.beta : sh.br;
                     const float4 b0 = *(const float4 *)(bsrc + j0), b1 = *(const float4 *)(bsrc + j0 + 4);
                     const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                     float v[8];
@@ -388,13 +426,15 @@ cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
 {
     if (a.N * a.HV == 0 || a.slots == 0) return cudaSuccess;
     // eight CTAs per SM need the largest shared-memory carveout
-    cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(tc_prep_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     // T_W leaves through a TMA store: the same tile map as the scan reads it with
     alignas(64) CUtensorMap tmap;
     if (!encode_tiles_map(&tmap, a.tiles, (int64_t)a.slots * a.HV * 128, 64)) return cudaErrorInvalidValue;
     dim3 grid(a.slots, a.HV);
-    tc_prep_kernel<<<grid, kThreadsPrep, 0, st>>>(a, tmap);
+    if (a.act.A_log || a.act.beta_logits || a.act.qk_l2norm) tc_prep_kernel<true><<<grid, kThreadsPrep, 0, st>>>(a, tmap);
+    else tc_prep_kernel<false><<<grid, kThreadsPrep, 0, st>>>(a, tmap);
     return cudaGetLastError();
 }
 

@@ -127,6 +127,24 @@ typedef struct {
                               wait_limit_us), the device status reads
                               GDN_ERR_TIMEOUT and o / ht are left undefined.  No
                               effect on the SIMT engine.                          */
+    /* Input activations done inside the kernels ("Flash Linear Attention" page,
+     * sec. 10: the KDA inference backend takes raw tensors and fuses the gate,
+     * the L2 norm and sigma(beta); "KDA source walkthrough",
+     * kda_gate_chunk_cumsum, for the gate).  All zero: inputs used as given.   */
+    const float *gate_A_log;   /* [HV], device; non-NULL: g_or_gk holds the raw
+                              gate input x and the log-decay is
+                              -exp(A_log[h]) * softplus(x + dt_bias), or with
+                              gate_lower_bound < 0:
+                              gate_lower_bound * sigmoid(exp(A_log[h]) (x + dt_bias)) */
+    const float *gate_dt_bias; /* [HV] (scalar gate) or [HV][K] (per-channel), device,
+                              nullable (zero)                                       */
+    float gate_lower_bound;    /* < 0 selects the bounded form above; 0: softplus form */
+    int beta_logits;           /* beta holds logits: the kernels use sigmoid(beta)     */
+    int qk_l2norm;             /* q and k are scaled to unit L2 norm per (token, head)
+                              inside the kernels: x / max(||x||_2, 1e-12)            */
+    int state_v_first;         /* h0 and ht are [N, HV, V, K] instead of [N, HV, K, V]
+                              (the transposed state layout; the library transposes
+                              them around the call through its workspace)           */
 } gdn_options;
 
 /* Fill `opt` with the defaults (AUTO everywhere, no assertions).  No

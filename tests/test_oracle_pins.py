@@ -354,3 +354,30 @@ def test_local_cumsum_restarts_match_per_sequence_runs():
         for c0 in range(s, e, 64):
             c1 = min(c0 + 64, e)
             assert np.allclose(got[c1 - 1], g[c0:c1].sum(axis=0), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- input activations (f3)
+def test_activation_closed_forms():
+    """softplus, sigmoid, the two gate forms and the L2 norm against values they must take."""
+    from oracle import activations as act
+    assert act.softplus(0.0) == pytest.approx(math.log(2.0), abs=1e-15)
+    assert act.sigmoid(0.0) == 0.5
+    z = np.linspace(-50, 50, 101)
+    assert np.allclose(act.softplus(z) - act.softplus(-z), z, atol=1e-12)       # softplus(z) - softplus(-z) = z
+    assert np.allclose(act.sigmoid(z) + act.sigmoid(-z), 1.0, atol=1e-15)
+    assert act.softplus(800.0) == 800.0 and act.softplus(-800.0) == 0.0            # no overflow
+    # gate without a lower bound: -exp(A) * ln 2 at x + bias = 0; with one: lb / 2 there, lb and 0 at the ends
+    A_log = np.array([0.0, math.log(3.0)])
+    x = np.zeros((1, 1, 2))
+    assert np.allclose(act.gate(x, A_log), [[[-math.log(2.0), -3 * math.log(2.0)]]], atol=1e-15)
+    assert np.allclose(act.gate(x, A_log, lower_bound=-5.0), -2.5)
+    assert np.allclose(act.gate(np.full((1, 1, 2), 1e3), A_log, lower_bound=-5.0), -5.0)
+    assert np.allclose(act.gate(np.full((1, 1, 2), -1e3), A_log, lower_bound=-5.0), 0.0)
+    # per-channel bias: the bias of channel d shifts channel d only
+    xb = np.zeros((1, 1, 1, 3))
+    bias = np.array([[0.0, 1.0, -1.0]])
+    g = act.gate(xb, np.array([0.0]), bias)
+    assert np.allclose(g[0, 0, 0], -np.logaddexp(0.0, bias[0]), atol=1e-15)
+    # L2 norm: unit length, same direction; the zero vector stays zero
+    v = np.array([[3.0, 4.0], [0.0, 0.0]])
+    assert np.allclose(act.l2norm(v), [[0.6, 0.8], [0.0, 0.0]])
