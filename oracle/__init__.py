@@ -12,5 +12,8 @@ package never imports it and shares no code with it.
   per-channel-gate form, the blockwise triangular inverse, the S*/M
   chunk-parallel split and the gate-driven warmup), and the chunk-local gate
   cumsum.  They pin the recurrence: two independent formulations must agree.
+* :func:`recurrence_backward` -- the gradients of that recurrence with respect to q, k, v,
+  beta, g and h0 (plain C, fp64, the chain rule token by token in reverse order).
 """
 from .recurrence import recurrence, build_oracle_lib  # noqa: F401
+from .backward import recurrence_backward  # noqa: F401

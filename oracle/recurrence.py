@@ -12,7 +12,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_SRCS = [os.path.join(_HERE, "gdn_oracle.c"), os.path.join(_HERE, "gdn_oracle_bwd.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -20,13 +20,14 @@ _lib = None
 
 
 def build_oracle_lib(force: bool = False) -> str:
-    """Compile ``gdn_oracle.c`` with gcc (plain C, -O2, pthreads)."""
+    """Compile ``gdn_oracle.c`` (forward) and ``gdn_oracle_bwd.c`` (gradients) with gcc (plain C,
+    -O2, pthreads) into one library."""
     os.makedirs(_BUILD, exist_ok=True)
-    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    stale = (not os.path.exists(_LIB)) or any(os.path.getmtime(_LIB) < os.path.getmtime(s) for s in _SRCS)
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
-               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+               "-fno-fast-math", "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
