@@ -77,6 +77,9 @@ def load_library(path: str | None = None):
         lib.gdn_chain_states.restype = ctypes.c_int
         lib.gdn_recurrent_fwd.argtypes = [SP, VP, VP, VP, FP, FP, ctypes.c_float, FP, I64P, VP, FP, VP]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
+        lib.gdn_chunk_bwd.argtypes = [SP, VP, VP, VP, FP, FP, ctypes.c_float, FP, VP, FP, I64P, ctypes.c_int,
+                                      FP, FP, FP, FP, FP, FP, VP]
+        lib.gdn_chunk_bwd.restype = ctypes.c_int
         for f in (lib.gdn_chunk_fwd, lib.gdn_chunk_fwd_ex, lib.gdn_chunk_fwd_ws, lib.gdn_chunk_fwd_host,
                   lib.gdn_chunk_fwd_noalloc):
             f.restype = ctypes.c_int
@@ -237,6 +240,42 @@ def fused_recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state
                                        _ptr(ht), stream)
     _check(code, "gdn_recurrent_fwd")
     return o, ht
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, scale=None, initial_state=None, dht=None, cu_seqlens=None,
+                               chunk_size=64):
+    """Gradients of :func:`chunk_gated_delta_rule` (scalar gate; ``gdn_chunk_bwd``): ``do`` is the
+    gradient with respect to o (dtype of v), ``dht`` [N, HV, K, V] float32 (or None) with respect to the
+    final state.  Returns float32 ``(dq, dk, dv, dbeta, dg, dh0)`` shaped like q, k, v, beta, g and
+    [N, HV, K, V] (dh0 None when there is no initial state)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("do", do)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    for name, t in (("initial_state", initial_state), ("dht", dht)):
+        if t is not None and (not t.is_contiguous() or t.dtype != torch.float32):
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype or do.dtype != q.dtype:
+        raise TypeError("q, k, v and do must share a dtype")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    s = make_shape(q, v, g, cu_seqlens)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty(q.shape, **f32)
+    dk = torch.empty(k.shape, **f32)
+    dv = torch.empty(v.shape, **f32)
+    dbeta = torch.empty(beta.shape, **f32)
+    dg = torch.empty(g.shape, **f32)
+    dh0 = torch.empty(s.num_seqs, s.HV, s.K, s.V, **f32) if initial_state is not None else None
+    with torch.cuda.device(q.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
+        code = lib().gdn_chunk_bwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   ctypes.c_float(scale), _ptr(initial_state), _ptr(do), _ptr(dht),
+                                   _ptr(cu_seqlens), int(chunk_size), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta),
+                                   _ptr(dg), _ptr(dh0), stream)
+    _check(code, "gdn_chunk_bwd")
+    return dq, dk, dv, dbeta, dg, dh0
 
 
 def chunk_summary(k, v, g, beta, cu_seqlens=None, chunk_size=64, **opts):

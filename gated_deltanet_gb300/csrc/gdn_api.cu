@@ -604,6 +604,73 @@ gdn_status gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, c
     return gdn_chunk_fwd_ex(s, q, k, v, g, beta, scale, h0, cu, kChunk, o, ht, &opt, stream);
 }
 
+gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float scale, const float *h0, const void *dout, const float *dht,
+                         const int64_t *cu, int chunk_size, float *dq, float *dk, float *dv, float *dbeta,
+                         float *dg, float *dh0, gdn_stream_t stream)
+{
+    gdn_status st = validate_shape(s, chunk_size, nullptr);
+    if (st != GDN_OK) return st;
+    if (s->gate_kind != GDN_GATE_SCALAR) return GDN_ERR_UNSUPPORTED;
+    const bool varlen = cu != nullptr;
+    if (varlen && s->B != 1) return GDN_ERR_INVALID;
+    if (!varlen && s->num_seqs != s->B) return GDN_ERR_INVALID;
+    if (!std::isfinite(scale)) return GDN_ERR_INVALID;
+    const int64_t tokens = (int64_t)s->B * s->T;
+    if (tokens > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dbeta || !dg))
+        return GDN_ERR_INVALID;
+    const int N = s->num_seqs;
+    cudaStream_t cs = (cudaStream_t)stream;
+    // workspace: status word, the state entering every chunk (fp32), the per-row gate gradient dG
+    const size_t slots = (size_t)tile_slots(tokens, N);
+    const size_t off_states = kStatusBytes;
+    const size_t off_dG = align_up(off_states + slots * s->HV * (size_t)s->K * s->V * sizeof(float), 256);
+    const size_t bytes = align_up(off_dG + (size_t)tokens * s->HV * sizeof(float), 256);
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    if ((st = managed_ws(bytes, cs, &ws, &ws_bytes)) != GDN_OK) return st;
+    char *wsb = (char *)ws;
+    if (tokens == 0) {
+        // no token: dh0 = dht
+        if (dh0 && (size_t)N * s->HV > 0) {
+            const size_t sb = (size_t)N * s->HV * s->K * s->V * sizeof(float);
+            cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, sb, cudaMemcpyDeviceToDevice, cs)
+                                : cudaMemsetAsync(dh0, 0, sb, cs);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    // the sums (over value tiles, GVA heads) start at zero
+    if (cudaMemsetAsync(dq, 0, (size_t)tokens * s->H * s->K * sizeof(float), cs) != cudaSuccess ||
+        cudaMemsetAsync(dk, 0, (size_t)tokens * s->H * s->K * sizeof(float), cs) != cudaSuccess ||
+        cudaMemsetAsync(dbeta, 0, (size_t)tokens * s->HV * sizeof(float), cs) != cudaSuccess ||
+        cudaMemsetAsync(wsb + off_dG, 0, (size_t)tokens * s->HV * sizeof(float), cs) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    // Steps 1-2 of the backward: the states entering every chunk, by the CUDA-core engine's forward
+    // (no output, no split)
+    const int max_nt = ceil_div(s->T, kChunk);
+    ScanArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu_seqlens = cu;
+    a.o = nullptr; a.ht = nullptr;
+    a.B = s->B; a.T = s->T; a.H = s->H; a.HV = s->HV; a.K = s->K; a.V = s->V; a.N = N;
+    a.scale = scale;
+    a.seg_chunks = std::max(max_nt, 1);
+    a.n_seg = 1;
+    a.mode = kModeForward;
+    a.vext = s->V;
+    a.status = (unsigned *)wsb;
+    a.chunk_states = (float *)(wsb + off_states);
+    if (launch_simt_scan(a, s->qkv_dtype, GDN_GATE_SCALAR, cs) != cudaSuccess) return GDN_ERR_CUDA;
+    // Steps 3-7
+    BwdArgs b{};
+    b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.dht = dht; b.cu_seqlens = cu;
+    b.chunk_states = a.chunk_states;
+    b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dG = (float *)(wsb + off_dG); b.dg = dg; b.dh0 = dh0;
+    b.T = s->T; b.H = s->H; b.HV = s->HV; b.K = s->K; b.V = s->V; b.N = N; b.max_nt = max_nt;
+    b.scale = scale;
+    return launch_chunk_bwd(b, s->qkv_dtype, cs) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_read_device_status(void *workspace, gdn_stream_t stream)
 {
     cudaStream_t st = (cudaStream_t)stream;

@@ -1,0 +1,480 @@
+// Backward pass of the chunked gated delta rule (scalar gates): the gradients of o and of the final
+// state with respect to q, k, v, beta, g and h0.  The method is the chunked backward of the GDN-in-FLA
+// notes (backward, Steps 1-7) with the state gradient scanned in reverse time ("Flash Linear
+// Attention" page, sec. 7):
+//
+//   states    S0 of every chunk are recomputed by a forward pass (the CUDA-core engine, with a state
+//             dump) - Step 2;
+//   per chunk, newest first, with G the chunk-local inclusive log-gate cumsum, gam = exp(G),
+//   Gam_ij = exp(G_i - G_j), A = (I + StrictLower(diag(beta) Gam*K K^T))^-1 (Step 1, recomputed):
+//     R   = V - diag(gam) K S0,   B = diag(beta) R,   D = A B            (D: the chunk's v_new)
+//     dD  = P^T dO + diag(gam_C / gam) K dS,  P = scale Lower(Gam) * Q K^T          (Steps 3-4)
+//     dS0 = gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR,   dR = diag(beta) A^T dD  (Step 4)
+//     dq  = scale diag(gam) dO S0^T + F K,  F = scale Lower(Gam) * (dO D^T)                 (Step 5)
+//     dk  = F^T Q + diag(gam_C / gam) D dS^T - diag(gam) dR S0^T + E K + E^T K,           (Steps 5-6)
+//           E = StrictLower(diag(beta) Gam * dL),  dL = -A^T (dD B^T) A^T
+//     dv  = dR,  dbeta = rowsum((A^T dD) * R) + rowsum(dL * Gam * K K^T)                  (Step 6)
+//     dG  = the derivative with respect to each G_i of every factor exp(G) above         (Steps 5-6)
+//   dg = the suffix sum of dG within each chunk (Step 7); dh0 = the last dS.
+//
+// One CTA per (sequence, value head, 32-column value tile) walks the chunks in reverse with its tile
+// of dS in shared memory.  dq, dk, dbeta and dG sum over value tiles (and dq, dk over the value heads
+// of a GVA group) by atomic adds into fp32 buffers the host zeroes; dv and dh0 are tile-local.
+// CUDA cores, fp32 throughout.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kBThreads = 256;
+constexpr int kBC = 64;      // chunk
+constexpr int kBV = 32;      // value columns per CTA
+constexpr int kCP = kBC + 1;  // pitches (odd: strided reads are free of bank conflicts)
+constexpr int kVP = kBV + 1;
+
+template <int K>
+struct BwdLayout {
+    static constexpr int KP = K + 1;
+    static constexpr int oK = 0, oQ = oK + kBC * KP, oS0 = oQ + kBC * KP, odS = oS0 + K * kVP,
+                         oV = odS + K * kVP, odO = oV + kBC * kVP, oR = odO + kBC * kVP, oD = oR + kBC * kVP,
+                         odD = oD + kBC * kVP, oY = odD + kBC * kVP, oA = oY + kBC * kVP, oP = oA + kBC * kCP,
+                         oM1 = oP + kBC * kCP, oM2 = oM1 + kBC * kCP, oG = oM2 + kBC * kCP, oGam = oG + kBC,
+                         oBeta = oGam + kBC, odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC,
+                         total = oRed + 4 * kBC;
+};
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p) { return (float)*p; }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// out[m][n] = alpha * sum_x A(m, x) xs[x] B(x, n) (+ out when acc): A(m, x) = a[x lda + m] if TA else
+// a[m lda + x], B(x, n) = b[n ldb + x] if TB else b[x ldb + n]; xs optional
+template <bool TA, bool TB>
+__device__ void smm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
+                    float alpha, bool acc, const float *xs = nullptr)
+{
+    for (int e = threadIdx.x; e < M * N; e += kBThreads) {
+        const int m = e / N, n = e - m * N;
+        float s = 0.f;
+        for (int x = 0; x < X; ++x) {
+            const float av = TA ? a[x * lda + m] : a[m * lda + x];
+            const float bv = TB ? b[n * ldb + x] : b[x * ldb + n];
+            s = fmaf(xs ? av * xs[x] : av, bv, s);
+        }
+        out[m * ldo + n] = acc ? fmaf(alpha, s, out[m * ldo + n]) : alpha * s;
+    }
+}
+
+// A [kBC x K] register tile per CTA: warp w holds rows 8w .. 8w + 7, lane l the columns l + 32 j.
+// acc[r][j] += alpha * rs[m] * sum_x A(m, x) B(x, n) (rs optional)
+template <int K, bool TA, bool TB>
+__device__ void racc(float (&acc)[8][K / 32], const float *a, int lda, const float *b, int ldb, int X,
+                     float alpha = 1.f, const float *rs = nullptr)
+{
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    float s[8][K / 32];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < K / 32; ++j) s[r][j] = 0.f;
+    for (int x = 0; x < X; ++x) {
+        float av[8], bv[K / 32];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int m = 8 * w + r;
+            av[r] = TA ? a[x * lda + m] : a[m * lda + x];
+        }
+#pragma unroll
+        for (int j = 0; j < K / 32; ++j) {
+            const int n = l + 32 * j;
+            bv[j] = TB ? b[n * ldb + x] : b[x * ldb + n];
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < K / 32; ++j) s[r][j] = fmaf(av[r], bv[j], s[r][j]);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const float f = alpha * (rs ? rs[8 * w + r] : 1.f);
+#pragma unroll
+        for (int j = 0; j < K / 32; ++j) acc[r][j] = fmaf(f, s[r][j], acc[r][j]);
+    }
+}
+
+// per-row dot product of a register tile with a [kBC x K] shared-memory matrix (pitch ld): warp-reduced,
+// returned on every lane for the warp's eight rows
+template <int K>
+__device__ void rdot(const float (&t)[8][K / 32], const float *m, int ld, float (&out)[8])
+{
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < K / 32; ++j) s = fmaf(t[r][j], m[(8 * w + r) * ld + l + 32 * j], s);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        out[r] = s;
+    }
+}
+
+template <typename DT, int K>
+__global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a)
+{
+    using Lay = BwdLayout<K>;
+    constexpr int KP = Lay::KP, KJ = K / 32;
+    extern __shared__ float smem[];
+    float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sS0 = smem + Lay::oS0, *sdS = smem + Lay::odS;
+    float *sV = smem + Lay::oV, *sdO = smem + Lay::odO, *sR = smem + Lay::oR, *sD = smem + Lay::oD;
+    float *sdD = smem + Lay::odD, *sY = smem + Lay::oY, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
+    float *sM1 = smem + Lay::oM1, *sM2 = smem + Lay::oM2, *sG = smem + Lay::oG, *sGam = smem + Lay::oGam;
+    float *sBeta = smem + Lay::oBeta, *sdG = smem + Lay::odG, *sdB = smem + Lay::odB, *sRed = smem + Lay::oRed;
+
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int vt = blockIdx.x, pair = blockIdx.y;
+    const int HV = a.HV, V = a.V, n = pair / HV, hv = pair % HV, hq = hv / (HV / a.H);
+    const int64_t bos = a.cu_seqlens ? a.cu_seqlens[n] : (int64_t)n * a.T;
+    const int64_t len = a.cu_seqlens ? a.cu_seqlens[n + 1] - bos : a.T;
+    const int NT = (int)((len + kBC - 1) / kBC);
+    const int col0 = vt * kBV;
+    const float scale = a.scale;
+    const DT *q = (const DT *)a.q, *k = (const DT *)a.k, *v = (const DT *)a.v, *dout = (const DT *)a.dout;
+    const size_t pbase = ((size_t)n * HV + hv) * K * V;
+
+    // dS: the gradient with respect to the state after the last chunk (dht)
+    for (int e = tid; e < K * kBV; e += kBThreads) {
+        const int d = e / kBV, j = e - d * kBV, col = col0 + j;
+        sdS[d * kVP + j] = (a.dht && col < V) ? a.dht[pbase + (size_t)d * V + col] : 0.f;
+    }
+
+    for (int c = NT - 1; c >= 0; --c) {
+        const int64_t t0 = bos + (int64_t)c * kBC;
+        const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
+        __syncthreads();
+        // ---- loads (rows past the sequence end are inert zeros)
+        for (int e = tid; e < kBC * K; e += kBThreads) {
+            const int i = e / K, d = e - i * K;
+            float kv = 0.f, qv = 0.f;
+            if (i < rows) {
+                const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d;
+                kv = ldf(k + off);
+                qv = ldf(q + off);
+            }
+            sK[i * KP + d] = kv;
+            sQ[i * KP + d] = qv;
+        }
+        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+            const int i = e / kBV, j = e - i * kBV, col = col0 + j;
+            float vv = 0.f, dv = 0.f;
+            if (i < rows && col < V) {
+                const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
+                vv = ldf(v + off);
+                dv = ldf(dout + off);
+            }
+            sV[i * kVP + j] = vv;
+            sdO[i * kVP + j] = dv;
+        }
+        {
+            const float *src = a.chunk_states + ((size_t)tile_slot(bos, n, c) * HV + hv) * K * V;
+            for (int e = tid; e < K * kBV; e += kBThreads) {
+                const int d = e / kBV, j = e - d * kBV, col = col0 + j;
+                sS0[d * kVP + j] = col < V ? src[(size_t)d * V + col] : 0.f;
+            }
+        }
+        if (w == 0) {
+            // inclusive cumsum of the log-gate (natural log), two rows per lane
+            const int r0 = 2 * l, r1 = r0 + 1;
+            const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] : 0.f;
+            const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] : 0.f;
+            float sp = g0 + g1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sp, off);
+                if (l >= off) sp += y;
+            }
+            sG[r0] = sp - g1;
+            sG[r1] = sp;
+            sGam[r0] = __expf(sp - g1);
+            sGam[r1] = __expf(sp);
+            sBeta[r0] = r0 < rows ? a.beta[(size_t)(t0 + r0) * HV + hv] : 0.f;
+            sBeta[r1] = r1 < rows ? a.beta[(size_t)(t0 + r1) * HV + hv] : 0.f;
+            sdG[r0] = sdG[r1] = 0.f;
+            sdB[r0] = sdB[r1] = 0.f;
+        }
+        __syncthreads();
+        const float GC = sG[kBC - 1], gamC = sGam[kBC - 1];
+
+        // ---- Step 1: K K^T and Q K^T; L = StrictLower(diag(beta) Gam * K K^T), P = scale Lower(Gam) * Q K^T
+        smm<false, true>(sM1, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+        smm<false, true>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBC; e += kBThreads) {
+            const int i = e / kBC, j = e - i * kBC;
+            const float gm = i >= j ? __expf(sG[i] - sG[j]) : 0.f;
+            const float lraw = i > j ? gm * sM1[i * kCP + j] : 0.f;  // Gam * K K^T below the diagonal
+            sM1[i * kCP + j] = lraw;
+            sA[i * kCP + j] = sBeta[i] * lraw;
+            sP[i * kCP + j] = scale * gm * sP[i * kCP + j];
+        }
+        __syncthreads();
+        // A = (I + L)^-1 in place, one row at a time: A_i = e_i - sum_{j < i} L_ij A_j
+        for (int i = 0; i < kBC; ++i) {
+            const int col = tid & (kBC - 1), part = tid >> 6;
+            float s = 0.f;
+            for (int j = part; j < i; j += 4) s = fmaf(sA[i * kCP + j], sA[j * kCP + col], s);
+            sRed[part * kBC + col] = s;
+            __syncthreads();
+            if (tid < kBC) {
+                const float t = sRed[tid] + sRed[kBC + tid] + sRed[2 * kBC + tid] + sRed[3 * kBC + tid];
+                sA[i * kCP + tid] = tid < i ? -t : (tid == i ? 1.f : 0.f);
+            }
+            __syncthreads();
+        }
+
+        // ---- Step 2 (this chunk): R = V - diag(gam) K S0, B = diag(beta) R, D = A B
+        smm<false, false>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+            const int i = e / kBV, j = e - i * kBV;
+            const float r = sV[i * kVP + j] - sGam[i] * sR[i * kVP + j];
+            sR[i * kVP + j] = r;
+            sY[i * kVP + j] = sBeta[i] * r;
+        }
+        __syncthreads();
+        smm<false, false>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
+        __syncthreads();
+
+        // ---- Steps 3-5: dP = dO D^T; dD = P^T dO + diag(gam_C / gam) K dS
+        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
+        smm<true, false>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+            const int i = e / kBV, j = e - i * kBV;
+            float s = 0.f;
+            for (int d = 0; d < K; ++d) s = fmaf(sK[i * KP + d], sdS[d * kVP + j], s);
+            sdD[i * kVP + j] = fmaf(__expf(GC - sG[i]), s, sdD[i * kVP + j]);
+        }
+        // gate terms of P (dG_i += P_ij dP_ij, dG_j -= P_ij dP_ij), then F = scale Gam * dP below the diagonal
+        for (int e = tid; e < kBC * kBC; e += kBThreads) {
+            const int i = e / kBC, j = e - i * kBC;
+            const float dp = sM2[i * kCP + j];
+            const float pw = sP[i * kCP + j] * dp;
+            if (pw != 0.f) {
+                atomicAdd(&sdG[i], pw);
+                atomicAdd(&sdG[j], -pw);
+            }
+            sM2[i * kCP + j] = i >= j ? scale * __expf(sG[i] - sG[j]) * dp : 0.f;
+        }
+        __syncthreads();
+        float dq[8][KJ], dk[8][KJ], t[8][KJ], rd[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
+        racc<K, false, false>(dq, sM2, kCP, sK, KP, kBC);  // dq += F K
+        racc<K, true, false>(dk, sM2, kCP, sQ, KP, kBC);   // dk += F^T Q
+
+        // ---- Step 6: Y = A^T dD; dbeta += rowsum(Y R); dR = diag(beta) Y; dv = dR; dG_i += dR (R - V)
+        smm<true, false>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+            const int i = e / kBV, j = e - i * kBV;
+            const float y = sY[i * kVP + j], r = sR[i * kVP + j];
+            const float dr = sBeta[i] * y;
+            atomicAdd(&sdB[i], y * r);
+            atomicAdd(&sdG[i], dr * (r - sV[i * kVP + j]));
+            sY[i * kVP + j] = dr;
+            const int col = col0 + j;
+            if (i < rows && col < V) a.dv[((size_t)(t0 + i) * HV + hv) * V + col] = dr;
+        }
+        __syncthreads();
+        // dA = dD B^T (B = diag(beta) R: a column scale), then dL = -A^T (dA A^T)
+        smm<false, true>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBC; e += kBThreads) {
+            const int i = e / kBC, j = e - i * kBC;
+            sM2[i * kCP + j] *= sBeta[j];
+        }
+        __syncthreads();
+        smm<false, true>(sP, kCP, sM2, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
+        __syncthreads();
+        smm<true, false>(sM2, kCP, sA, kCP, sP, kCP, kBC, kBC, kBC, -1.f, false);
+        __syncthreads();
+        // L_ij = beta_i Lraw_ij (i > j): dbeta_i += dL_ij Lraw_ij, dG_i += dL_ij L_ij, dG_j -= dL_ij L_ij,
+        // E_ij = d(K K^T)_ij = beta_i Gam_ij dL_ij
+        for (int e = tid; e < kBC * kBC; e += kBThreads) {
+            const int i = e / kBC, j = e - i * kBC;
+            float ev = 0.f;
+            if (i > j) {
+                const float dl = sM2[i * kCP + j], lraw = sM1[i * kCP + j];
+                if (lraw != 0.f) {
+                    atomicAdd(&sdB[i], dl * lraw);
+                    const float wv = dl * sBeta[i] * lraw;
+                    atomicAdd(&sdG[i], wv);
+                    atomicAdd(&sdG[j], -wv);
+                }
+                ev = sBeta[i] * __expf(sG[i] - sG[j]) * dl;
+            }
+            sM2[i * kCP + j] = ev;
+        }
+        __syncthreads();
+        racc<K, false, false>(dk, sM2, kCP, sK, KP, kBC);  // dk_i += E_ij k_j
+        racc<K, true, false>(dk, sM2, kCP, sK, KP, kBC);   // dk_j += E_ij k_i
+
+        // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
+        //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) t[r][j] = 0.f;
+        racc<K, false, true>(t, sdO, kVP, sS0, kVP, kBV, scale, sGam);
+        rdot<K>(t, sQ, KP, rd);
+        if (l == 0)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) atomicAdd(&sdG[8 * w + r], rd[r]);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                dq[r][j] += t[r][j];
+                t[r][j] = 0.f;
+            }
+        racc<K, false, true>(t, sD, kVP, sdS, kVP, kBV);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float f = __expf(GC - sG[8 * w + r]);
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) t[r][j] *= f;
+        }
+        rdot<K>(t, sK, KP, rd);
+        if (l == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                atomicAdd(&sdG[8 * w + r], -rd[r]);
+                tot += rd[r];
+            }
+            atomicAdd(&sdG[kBC - 1], tot);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) dk[r][j] += t[r][j];
+        racc<K, false, true>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
+        {
+            float s = 0.f;
+            for (int e = tid; e < K * kBV; e += kBThreads) {
+                const int d = e / kBV, j = e - d * kBV;
+                s = fmaf(sdS[d * kVP + j], sS0[d * kVP + j], s);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (l == 0) atomicAdd(&sdG[kBC - 1], gamC * s);
+        }
+        // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int i = 8 * w + r;
+            if (i < rows) {
+                float *pq = a.dq + ((size_t)(t0 + i) * a.H + hq) * K, *pk = a.dk + ((size_t)(t0 + i) * a.H + hq) * K;
+#pragma unroll
+                for (int j = 0; j < KJ; ++j) {
+                    atomicAdd(pq + l + 32 * j, dq[r][j]);
+                    atomicAdd(pk + l + 32 * j, dk[r][j]);
+                }
+            }
+        }
+        __syncthreads();  // every shared-memory atomic of dG and dbeta is in; S0 is read for the last time
+
+        // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
+        smm<true, false>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
+        if (tid == 0) {
+            // G_C is the last row's G (rows past the end carry g = 0): its gradient belongs to the last row
+            float tail = 0.f;
+            for (int i = rows; i < kBC; ++i) tail += sdG[i];
+            sdG[rows - 1] += tail;
+        }
+        __syncthreads();
+        smm<true, false>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
+        for (int i = tid; i < rows; i += kBThreads) {
+            atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], sdB[i]);
+            atomicAdd(&a.dG[(size_t)(t0 + i) * HV + hv], sdG[i]);
+        }
+        __syncthreads();
+        for (int e = tid; e < K * kBV; e += kBThreads) {
+            const int d = e / kBV, j = e - d * kBV;
+            sS0[d * kVP + j] = fmaf(gamC, sdS[d * kVP + j], sS0[d * kVP + j]);
+        }
+        float *tmp = sS0;
+        sS0 = sdS;
+        sdS = tmp;
+    }
+    __syncthreads();
+    if (a.dh0) {
+        for (int e = tid; e < K * kBV; e += kBThreads) {
+            const int d = e / kBV, j = e - d * kBV, col = col0 + j;
+            if (col < V) a.dh0[pbase + (size_t)d * V + col] = sdS[d * kVP + j];
+        }
+    }
+}
+
+// dg = the suffix sum of dG within each chunk (one warp per (sequence, value head, chunk))
+__global__ void gate_suffix_kernel(const BwdArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int pair = (int)(item / a.max_nt), c = (int)(item % a.max_nt);
+    if (pair >= a.N * a.HV) return;
+    const int n = pair / a.HV, hv = pair % a.HV;
+    const int64_t bos = a.cu_seqlens ? a.cu_seqlens[n] : (int64_t)n * a.T;
+    const int64_t len = a.cu_seqlens ? a.cu_seqlens[n + 1] - bos : a.T;
+    if ((int64_t)c * kBC >= len) return;
+    const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
+    const int64_t t0 = bos + (int64_t)c * kBC;
+    // lane l holds rows 2l, 2l + 1; a reverse inclusive scan
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    const float x0 = r0 < rows ? a.dG[(size_t)(t0 + r0) * a.HV + hv] : 0.f;
+    const float x1 = r1 < rows ? a.dG[(size_t)(t0 + r1) * a.HV + hv] : 0.f;
+    float sp = x0 + x1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, sp, off);
+        if (lane + off < 32) sp += y;
+    }
+    if (r0 < rows) a.dg[(size_t)(t0 + r0) * a.HV + hv] = sp;
+    if (r1 < rows) a.dg[(size_t)(t0 + r1) * a.HV + hv] = sp - x0;
+}
+
+template <typename DT>
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st)
+{
+    auto go = [&](auto kern, size_t smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kBThreads, smem, st>>>(a);
+        return cudaGetLastError();
+    };
+    switch (a.K) {
+    case 32: return go(chunk_bwd_kernel<DT, 32>, sizeof(float) * BwdLayout<32>::total);
+    case 64: return go(chunk_bwd_kernel<DT, 64>, sizeof(float) * BwdLayout<64>::total);
+    case 128: return go(chunk_bwd_kernel<DT, 128>, sizeof(float) * BwdLayout<128>::total);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_bwd(const BwdArgs &a, gdn_dtype dt, cudaStream_t st)
+{
+    static_assert(sizeof(float) * BwdLayout<128>::total <= 227 * 1024, "shared memory budget");
+    if (a.N * a.HV == 0 || a.max_nt == 0) return cudaSuccess;
+    cudaError_t e = dt == GDN_BF16 ? launch_bwd_t<__nv_bfloat16>(a, st) : launch_bwd_t<float>(a, st);
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)a.N * a.HV * a.max_nt;
+    gate_suffix_kernel<<<(unsigned)((items + 7) / 8), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

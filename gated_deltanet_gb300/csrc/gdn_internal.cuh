@@ -66,6 +66,8 @@ struct ScanArgs {
     int tile_slots;         //   chunk slots of that buffer
     const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
     float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
+    float *chunk_states;    // CUDA-core engine, forward: the state entering every chunk, [slot][HV][K][V]
+                            //   (slot: tile_slot), for the backward pass; nullable
     int mode;               // Mode
     int vext;               // value columns processed: V (forward) or V + K (prepass)
     unsigned *status;
@@ -218,6 +220,24 @@ struct RecArgs {
     Act act;
 };
 cudaError_t launch_recurrent(const RecArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
+
+// Backward pass (scalar gates): one CTA per (sequence, value head, 32-column value tile), chunks newest
+// first; then the suffix sum of dG within each chunk into dg.
+struct BwdArgs {
+    const void *q, *k, *v, *dout;  // q, k [B,T,H,K]; v, dout [B,T,HV,V] (the dtype of v)
+    const float *g, *beta;         // [B,T,HV]
+    const float *dht;              // [N,HV,K,V], nullable
+    const int64_t *cu_seqlens;     // nullable
+    const float *chunk_states;     // [slot][HV][K][V]: the state entering every chunk (tile_slot)
+    float *dq, *dk;                // [B,T,H,K], zeroed by the host (sums of value tiles and GVA heads)
+    float *dv;                     // [B,T,HV,V]
+    float *dbeta, *dG;             // [B,T,HV], zeroed by the host (dG: per-row gate gradient before Step 7)
+    float *dg;                     // [B,T,HV]
+    float *dh0;                    // [N,HV,K,V], nullable
+    int T, H, HV, K, V, N, max_nt;
+    float scale;
+};
+cudaError_t launch_chunk_bwd(const BwdArgs &a, gdn_dtype dt, cudaStream_t st);
 // AUTO engine choice: packed or batched sequences of at most this many tokens go to the token-by-token
 // engine (decode, speculative continuations)
 constexpr int kAutoRecurrentTokens = 16;

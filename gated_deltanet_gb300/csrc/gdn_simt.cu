@@ -118,10 +118,18 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(const ScanArgs a)
     }
 
     for (int c = cs; c < c1; ++c) {
-        const bool emit = fwd && c >= c0;
+        const bool emit = fwd && c >= c0 && a.o != nullptr;  // (no o: a state dump for the backward pass)
         const int64_t t0 = bos + (int64_t)c * kChunk;
         const int nrow = (int)rows_in_chunk(len, c);
         __syncthreads();  // previous chunk done with every buffer
+        if (a.chunk_states) {
+            // the state entering chunk c, for the backward pass
+            float *dst = a.chunk_states + ((size_t)tile_slot(bos, n, c) * a.HV + hv) * K * V;
+            for (int e = tid; e < K * kBV; e += kThreads) {
+                const int d = e / kBV, col = col0 + e % kBV;
+                if (col < V) dst[(size_t)d * V + col] = sS[e];
+            }
+        }
 
         // ---- 1. loads (rows past the sequence end are inert zeros)
         for (int e = tid; e < 64 * K; e += kThreads) {

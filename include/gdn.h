@@ -292,6 +292,34 @@ gdn_status gdn_recurrent_fwd(const gdn_shape *s,
                              void *o, float *ht, gdn_stream_t stream);
 
 /*
+ * Backward pass of the chunked forward (GDN-in-FLA notes, backward: the gradients
+ * dq, dk, dv, db, dg, dh0 of chunk_gated_delta_rule_bwd, Steps 1-7; "Flash Linear
+ * Attention" page, sec. 7: the state gradient scanned in reverse time, the chunk
+ * states recomputed).  Given the same inputs as gdn_chunk_fwd (scalar gate) and
+ * `dout` [B,T,HV,V] (the dtype of v), the gradient of the loss with respect to o,
+ * and `dht` [N,HV,K,V] fp32 (nullable: zero), the gradient with respect to the
+ * final state, writes fp32
+ *     dq, dk [B,T,H,K]   (with HV > H: summed over the value heads of each head)
+ *     dv     [B,T,HV,V]
+ *     dbeta  [B,T,HV]
+ *     dg     [B,T,HV]    (natural-log gate, as g)
+ *     dh0    [N,HV,K,V]  (nullable: not written)
+ * The caller owns every buffer; the library-managed workspace of `stream` holds
+ * the recomputed states (4 K V bytes per chunk and value head) and a gate buffer.
+ * Errors: GDN_ERR_INVALID (arguments, a null required pointer),
+ * GDN_ERR_UNSUPPORTED (per-channel gates, chunk_size != 64, K not 32/64/128),
+ * GDN_ERR_NOMEM, GDN_ERR_CUDA; nothing is enqueued on an argument error.
+ * Asynchronous on `stream`.
+ */
+gdn_status gdn_chunk_bwd(const gdn_shape *s,
+                         const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float scale,
+                         const float *h0, const void *dout, const float *dht,
+                         const int64_t *cu_seqlens, int chunk_size,
+                         float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                         float *dh0, gdn_stream_t stream);
+
+/*
  * Context parallel across devices, step 1 (FlashQLA blog, "Key problems in
  * FLA's GDN chunked prefill": the S* / M pre-process; "KDA source
  * walkthrough", the cp_context pre-process of chunk_kda_fwd): the summary of
