@@ -47,6 +47,16 @@ def algorithmic_work(w, N, total_tokens, C=None):
     return float(flop), float(qk_bytes + hv_bytes + state)
 
 
+def backward_bytes(w, N, total_tokens):
+    """Bytes of one backward call, implementation-independent: read q, k, v, do (e each), g, beta;
+    write dq, dk, dv (fp32), dbeta, dg; per (sequence, head) read h0 and dht, write dh0."""
+    dk, dv, HV = w.K, w.V, w.hv
+    e = 2 if w.dtype == "bf16" else 4
+    qk = total_tokens * w.H * dk * (2 * e + 2 * 4)
+    hv = total_tokens * HV * (dv * (2 * e + 4) + 8 + 8)
+    return float(qk + hv + N * HV * dk * dv * 4 * 3)
+
+
 ENGINE_NAMES = ["auto", "simt", "tc", "recurrent"]
 
 
@@ -404,6 +414,64 @@ def cpu_baseline(w, seconds):
     return d
 
 
+def run_backward(args):
+    """One GPU: the backward pass (gdn_chunk_bwd) of the workload, timed like the forward step (L2
+    flushed before each call, CUDA events on the stream, clocks sampled)."""
+    import torch
+    import gated_deltanet_gb300 as gdn
+    from gdn_inputs import make_inputs, workload
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gdn.load_library()
+    w = workload(args.workload)
+    x = make_inputs(w, device=dev)
+    N, tokens = x["N"], int(x["q"].shape[0] * x["q"].shape[1])
+    gen = torch.Generator().manual_seed(5)
+    do = torch.randn(x["v"].shape, generator=gen).to(x["v"].dtype).to(dev)
+    dht = torch.randn(N, w.hv, w.K, w.V, generator=gen).to(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return gdn.chunk_gated_delta_rule_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, x["scale"], x["h0"],
+                                              dht, x["cu_seqlens"])
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    steps = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.05)
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+    byts = backward_bytes(w, N, tokens)
+    peaks, peak_kind = read_peaks()
+    achieved = byts / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "GDN chunked-prefill bwd tokens/s, 1 GB300",
+        "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": w.dtype, "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "B": int(x["q"].shape[0]), "T": int(x["q"].shape[1]), "H": w.H,
+                   "HV": w.hv, "dk": w.K, "dv": w.V, "h0": w.h0, "dht": True,
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind, "algorithmic_bytes": byts,
+                     "scope": "the whole backward call (state recompute, reverse scan, gate suffix sums)"},
+        "gpu_launches": 3 * steps,  # state recompute, reverse scan, gate suffix sums
+        "clocks": clocks,
+    }), flush=True)
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -443,10 +511,14 @@ def main():
     ap.add_argument("--workload", default="batched_bf16")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="backward: time gdn_chunk_bwd on one GPU instead of the forward step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.pass_ == "backward":
+        run_backward(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -49,20 +49,40 @@ template <>
 __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
 // out[m][n] = alpha * sum_x A(m, x) xs[x] B(x, n) (+ out when acc): A(m, x) = a[x lda + m] if TA else
-// a[m lda + x], B(x, n) = b[n ldb + x] if TB else b[x ldb + n]; xs optional
-template <bool TA, bool TB>
+// a[m lda + x], B(x, n) = b[n ldb + x] if TB else b[x ldb + n]; xs optional.  Each thread computes
+// 4 x TN blocks of outputs (M a multiple of 4, N of TN), sixteen or eight independent sums.
+template <bool TA, bool TB, int TN = 4>
 __device__ void smm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
                     float alpha, bool acc, const float *xs = nullptr)
 {
-    for (int e = threadIdx.x; e < M * N; e += kBThreads) {
-        const int m = e / N, n = e - m * N;
-        float s = 0.f;
+    const int nb = N / TN, blocks = (M / 4) * nb;
+    for (int e = threadIdx.x; e < blocks; e += kBThreads) {
+        const int m0 = (e / nb) * 4, n0 = (e % nb) * TN;
+        float s[4][TN];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) s[i][j] = 0.f;
+#pragma unroll 4
         for (int x = 0; x < X; ++x) {
-            const float av = TA ? a[x * lda + m] : a[m * lda + x];
-            const float bv = TB ? b[n * ldb + x] : b[x * ldb + n];
-            s = fmaf(xs ? av * xs[x] : av, bv, s);
+            const float f = xs ? xs[x] : 1.f;
+            float av[4], bv[TN];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) av[i] = f * (TA ? a[x * lda + m0 + i] : a[(m0 + i) * lda + x]);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) bv[j] = TB ? b[(n0 + j) * ldb + x] : b[x * ldb + n0 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) s[i][j] = fmaf(av[i], bv[j], s[i][j]);
         }
-        out[m * ldo + n] = acc ? fmaf(alpha, s, out[m * ldo + n]) : alpha * s;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                float *o = out + (m0 + i) * ldo + n0 + j;
+                *o = acc ? fmaf(alpha, s[i][j], *o) : alpha * s[i][j];
+            }
     }
 }
 
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         }
 
         // ---- Step 2 (this chunk): R = V - diag(gam) K S0, B = diag(beta) R, D = A B
-        smm<false, false>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        smm<false, false, 2>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
@@ -243,19 +263,23 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             sY[i * kVP + j] = sBeta[i] * r;
         }
         __syncthreads();
-        smm<false, false>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
+        smm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
 
-        // ---- Steps 3-5: dP = dO D^T; dD = P^T dO + diag(gam_C / gam) K dS
-        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
-        smm<true, false>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        // ---- Steps 3-5: dD = P^T dO + diag(gam_C / gam) K dS; dP = dO D^T
+        smm<true, false, 2>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        // (the row factors gam_C / gam into the scratch vector first)
+        if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);
+        __syncthreads();
+        smm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch in sM2)
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
-            float s = 0.f;
-            for (int d = 0; d < K; ++d) s = fmaf(sK[i * KP + d], sdS[d * kVP + j], s);
-            sdD[i * kVP + j] = fmaf(__expf(GC - sG[i]), s, sdD[i * kVP + j]);
+            sdD[i * kVP + j] = fmaf(sRed[i], sM2[i * kVP + j], sdD[i * kVP + j]);
         }
+        __syncthreads();
+        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);  // dP = dO D^T
+        __syncthreads();
         // gate terms of P (dG_i += P_ij dP_ij, dG_j -= P_ij dP_ij), then F = scale Gam * dP below the diagonal
         for (int e = tid; e < kBC * kBC; e += kBThreads) {
             const int i = e / kBC, j = e - i * kBC;
@@ -277,7 +301,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         racc<K, true, false>(dk, sM2, kCP, sQ, KP, kBC);   // dk += F^T Q
 
         // ---- Step 6: Y = A^T dD; dbeta += rowsum(Y R); dR = diag(beta) Y; dv = dR; dG_i += dR (R - V)
-        smm<true, false>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
+        smm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
