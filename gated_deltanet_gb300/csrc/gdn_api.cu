@@ -235,7 +235,8 @@ gdn_status prepare(const gdn_shape *s, const void *q, const void *k, const void 
 
 gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
                const float *beta, float scale, const float *h0, const int64_t *cu, int chunk_size, void *o,
-               float *ht, const gdn_options *optp, void *ws, size_t ws_bytes, cudaStream_t stream)
+               float *ht, const gdn_options *optp, void *ws, size_t ws_bytes, cudaStream_t stream,
+               float *chunk_states = nullptr)
 {
     Plan p;
     gdn_options opt;
@@ -272,6 +273,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
     a.scale = scale;
     a.seg_chunks = p.seg_chunks; a.n_seg = p.n_seg;
     a.mode = kModeForward; a.vext = s->V; a.status = status;
+    a.chunk_states = chunk_states;  // (the backward pass: the state entering every chunk; unsplit plans only)
     a.wait_ns = opt.wait_limit_us > 0 ? 1000ull * (unsigned long long)opt.wait_limit_us : 2000000000ull;
 
     cudaError_t e = cudaSuccess;
@@ -621,10 +623,22 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
         return GDN_ERR_INVALID;
     const int N = s->num_seqs;
     cudaStream_t cs = (cudaStream_t)stream;
-    // workspace: status word, the state entering every chunk (fp32), the per-row gate gradient dG
+    // the tensor-core forward recomputes the states when it can (bf16, d = 128, aligned), unsplit
+    gdn_options fopt;
+    gdn_default_options(&fopt);
+    fopt.engine = GDN_ENGINE_TC;
+    fopt.cp_mode = GDN_CP_OFF;
+    Plan fp;
+    const bool tc_engine = tc_shape_ok(s) && tc_supported(s, q, k, v, g, nullptr) &&
+                           make_plan(s, varlen, chunk_size, &fopt, current_sm_count(), &fp) == GDN_OK &&
+                           fp.engine == GDN_ENGINE_TC;
+    // workspace: the forward's (status word first), the state entering every chunk (fp32), the forward's
+    // output (scratch, tensor-core engine only), the per-row gate gradient dG
     const size_t slots = (size_t)tile_slots(tokens, N);
-    const size_t off_states = kStatusBytes;
-    const size_t off_dG = align_up(off_states + slots * s->HV * (size_t)s->K * s->V * sizeof(float), 256);
+    const size_t off_states = align_up(tc_engine ? fp.bytes : kStatusBytes, 256);
+    const size_t off_o = align_up(off_states + slots * s->HV * (size_t)s->K * s->V * sizeof(float), 256);
+    const size_t off_dG =
+        align_up(off_o + (tc_engine ? (size_t)tokens * s->HV * s->V * (s->qkv_dtype == GDN_BF16 ? 2 : 4) : 0), 256);
     const size_t bytes = align_up(off_dG + (size_t)tokens * s->HV * sizeof(float), 256);
     void *ws = nullptr;
     size_t ws_bytes = 0;
@@ -646,9 +660,16 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
         cudaMemsetAsync(dbeta, 0, (size_t)tokens * s->HV * sizeof(float), cs) != cudaSuccess ||
         cudaMemsetAsync(wsb + off_dG, 0, (size_t)tokens * s->HV * sizeof(float), cs) != cudaSuccess)
         return GDN_ERR_CUDA;
-    // Steps 1-2 of the backward: the states entering every chunk, by the CUDA-core engine's forward
-    // (no output, no split)
     const int max_nt = ceil_div(s->T, kChunk);
+    float *states = (float *)(wsb + off_states);
+    // Steps 1-2 of the backward: the states entering every chunk.  On the tensor-core engine when the
+    // shape and pointers allow (its forward, unsplit, with a state dump; o to scratch), else by the
+    // CUDA-core engine's forward (no output, no split).
+    if (tc_engine) {
+        if ((st = run(s, q, k, v, g, beta, scale, h0, cu, chunk_size, wsb + off_o, nullptr, &fopt, ws, ws_bytes, cs,
+                      states)) != GDN_OK)
+            return st;
+    } else {
     ScanArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu_seqlens = cu;
     a.o = nullptr; a.ht = nullptr;
@@ -659,12 +680,13 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
     a.mode = kModeForward;
     a.vext = s->V;
     a.status = (unsigned *)wsb;
-    a.chunk_states = (float *)(wsb + off_states);
+    a.chunk_states = states;
     if (launch_simt_scan(a, s->qkv_dtype, GDN_GATE_SCALAR, cs) != cudaSuccess) return GDN_ERR_CUDA;
+    }
     // Steps 3-7
     BwdArgs b{};
     b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.dht = dht; b.cu_seqlens = cu;
-    b.chunk_states = a.chunk_states;
+    b.chunk_states = states;
     b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dG = (float *)(wsb + off_dG); b.dg = dg; b.dh0 = dh0;
     b.T = s->T; b.H = s->H; b.HV = s->HV; b.K = s->K; b.V = s->V; b.N = N; b.max_nt = max_nt;
     b.scale = scale;

@@ -153,11 +153,12 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
     return 0;
 }
 
-template <bool KDA, bool ACT>
+template <bool KDA, bool ACT, bool DUMP = false>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a, const __grid_constant__ TcMaps m)
 {
     // ACT: the in-kernel input activations (raw gate input, L2 norm of q and k); a separate instance, so
-    // that the plain one carries none of their code
+    // that the plain one carries none of their code.  DUMP: also write the state entering every chunk
+    // (a.chunk_states, for the backward pass), in an instance of its own for the same reason.
     using Lay = TcLayout<KDA, ACT>;
     constexpr uint32_t kGateBytes = Lay::kGateBytes;
     const float *const rkp = ACT ? a.rk : nullptr;
@@ -805,6 +806,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tmem_ld32(tl + TM_S + 64 * hh, r);
                 tmem_ld32(tl + TM_S + 64 * hh + 32, r + 32);
                 tmem_ld_wait();
+                if constexpr (DUMP) {
+                    // S[dk][dv] entering chunk cs + i, dk = 64 hh .. 64 hh + 63 (coalesced over the warp's dv)
+                    float *dst = a.chunk_states + ((size_t)tile_slot(bos, n, cs + i) * HV + hv) * 128 * V +
+                                 (size_t)(64 * hh) * V + dv;
+#pragma unroll 8
+                    for (int j = 0; j < 64; ++j) dst[(size_t)j * V] = u2f(r[j]);
+                }
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t p[16];
@@ -1148,9 +1156,11 @@ cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStr
     };
     // the per-channel engine's operands come prepared (activated, normalised) from its preparation
     const bool act = !kda && (a.act.A_log != nullptr || a.act.qk_l2norm);
+    if (a.chunk_states && (kda || act || a.mode != kModeForward)) return cudaErrorInvalidValue;  // no dump there
     cudaError_t e;
     if (kda) e = go(tc_scan_kernel<true, false>, TcLayout<true, false>::kSmem);
     else if (act) e = go(tc_scan_kernel<false, true>, TcLayout<false, true>::kSmem);
+    else if (a.chunk_states) e = go(tc_scan_kernel<false, false, true>, TcLayout<false, false>::kSmem);
     else e = go(tc_scan_kernel<false, false>, TcLayout<false, false>::kSmem);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
