@@ -639,7 +639,12 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
     const size_t off_o = align_up(off_states + slots * s->HV * (size_t)s->K * s->V * sizeof(float), 256);
     const size_t off_dG =
         align_up(off_o + (tc_engine ? (size_t)tokens * s->HV * s->V * (s->qkv_dtype == GDN_BF16 ? 2 : 4) : 0), 256);
-    const size_t bytes = align_up(off_dG + (size_t)tokens * s->HV * sizeof(float), 256);
+    const size_t chunk_heads = slots * s->HV, tiles = (size_t)ceil_div(s->V, 32);
+    const size_t off_A = align_up(off_dG + (size_t)tokens * s->HV * sizeof(float), 256);
+    const size_t off_P = off_A + chunk_heads * 64 * 64 * sizeof(float);
+    const size_t off_dP = off_P + chunk_heads * 64 * 64 * sizeof(float);
+    const size_t off_dA = off_dP + tiles * chunk_heads * 64 * 64 * sizeof(float);
+    const size_t bytes = align_up(off_dA + tiles * chunk_heads * 64 * 64 * sizeof(float), 256);
     void *ws = nullptr;
     size_t ws_bytes = 0;
     if ((st = managed_ws(bytes, cs, &ws, &ws_bytes)) != GDN_OK) return st;
@@ -688,6 +693,8 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
     b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.dht = dht; b.cu_seqlens = cu;
     b.chunk_states = states;
     b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dG = (float *)(wsb + off_dG); b.dg = dg; b.dh0 = dh0;
+    b.Abuf = (float *)(wsb + off_A); b.Pbuf = (float *)(wsb + off_P);
+    b.dPbuf = (float *)(wsb + off_dP); b.dAbuf = (float *)(wsb + off_dA); b.chunk_heads = chunk_heads;
     b.T = s->T; b.H = s->H; b.HV = s->HV; b.K = s->K; b.V = s->V; b.N = N; b.max_nt = max_nt;
     b.scale = scale;
     return launch_chunk_bwd(b, s->qkv_dtype, cs) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

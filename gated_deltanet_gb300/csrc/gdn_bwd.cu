@@ -1,26 +1,31 @@
 // Backward pass of the chunked gated delta rule (scalar gates): the gradients of o and of the final
 // state with respect to q, k, v, beta, g and h0.  The method is the chunked backward of the GDN-in-FLA
 // notes (backward, Steps 1-7) with the state gradient scanned in reverse time ("Flash Linear
-// Attention" page, sec. 7):
+// Attention" page, sec. 7).  With G the chunk-local inclusive log-gate cumsum, gam = exp(G),
+// Gam_ij = exp(G_i - G_j), L = StrictLower(diag(beta) Gam * K K^T), A = (I + L)^-1,
+// P = scale Lower(Gam) * Q K^T and S0 the state entering the chunk:
 //
-//   states    S0 of every chunk are recomputed by a forward pass (the CUDA-core engine, with a state
-//             dump) - Step 2;
-//   per chunk, newest first, with G the chunk-local inclusive log-gate cumsum, gam = exp(G),
-//   Gam_ij = exp(G_i - G_j), A = (I + StrictLower(diag(beta) Gam*K K^T))^-1 (Step 1, recomputed):
-//     R   = V - diag(gam) K S0,   B = diag(beta) R,   D = A B            (D: the chunk's v_new)
-//     dD  = P^T dO + diag(gam_C / gam) K dS,  P = scale Lower(Gam) * Q K^T          (Steps 3-4)
-//     dS0 = gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR,   dR = diag(beta) A^T dD  (Step 4)
-//     dq  = scale diag(gam) dO S0^T + F K,  F = scale Lower(Gam) * (dO D^T)                 (Step 5)
-//     dk  = F^T Q + diag(gam_C / gam) D dS^T - diag(gam) dR S0^T + E K + E^T K,           (Steps 5-6)
-//           E = StrictLower(diag(beta) Gam * dL),  dL = -A^T (dD B^T) A^T
-//     dv  = dR,  dbeta = rowsum((A^T dD) * R) + rowsum(dL * Gam * K K^T)                  (Step 6)
-//     dG  = the derivative with respect to each G_i of every factor exp(G) above         (Steps 5-6)
-//   dg = the suffix sum of dG within each chunk (Step 7); dh0 = the last dS.
+//   R   = V - diag(gam) K S0,   B = diag(beta) R,   D = A B            (D: the chunk's v_new)
+//   dD  = P^T dO + diag(gam_C / gam) K dS                                             (Steps 3-4)
+//   dS0 = gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR,   dR = diag(beta) A^T dD  (Step 4)
+//   dq  = scale diag(gam) dO S0^T + F K,  F = scale Lower(Gam) * (dO D^T)                 (Step 5)
+//   dk  = F^T Q + diag(gam_C / gam) D dS^T - diag(gam) dR S0^T + E K + E^T K,           (Steps 5-6)
+//         E = StrictLower(diag(beta) Gam * dL),  dL = -A^T (dD B^T) A^T
+//   dv  = dR,  dbeta = rowsum((A^T dD) * R) + rowsum(dL * Gam * K K^T)                  (Step 6)
+//   dG  = the derivative with respect to each G_i of every factor exp(G) above         (Steps 5-6)
+//   dg  = the suffix sum of dG within each chunk (Step 7); dh0 = the last dS.
 //
-// One CTA per (sequence, value head, 32-column value tile) walks the chunks in reverse with its tile
-// of dS in shared memory.  dq, dk, dbeta and dG sum over value tiles (and dq, dk over the value heads
-// of a GVA group) by atomic adds into fp32 buffers the host zeroes; dv and dh0 are tile-local.
-// CUDA cores, fp32 throughout.
+// Kernels, after the chunk states are recomputed by a forward pass with a state dump (Step 2):
+//   bwd_prep_kernel     one CTA per chunk and value head: A and P (Step 1: nothing in them depends on
+//                       the state), fp32 into the workspace;
+//   chunk_bwd_kernel    one CTA per (sequence, value head, 32-column value tile), chunks newest first
+//                       with its tile of dS in shared memory: everything that needs S0 or dS, and the
+//                       tile's parts of dO D^T and dD B^T (sums over the value columns) to the workspace;
+//   bwd_finish_kernel   one CTA per chunk and value head: the tiles' parts summed, F, dL, E and their
+//                       products with K and Q, the gate and beta terms of P and L;
+//   gate_suffix_kernel  Step 7.
+// dq, dk, dbeta and dG are sums over value tiles and kernels (and dq, dk over a GVA group's value
+// heads): fp32 atomic adds into buffers the host zeroes.  CUDA cores, fp32 throughout.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -33,14 +38,20 @@ constexpr int kCP = kBC + 1;  // pitches (odd: strided reads are free of bank co
 constexpr int kVP = kBV + 1;
 
 template <int K>
-struct BwdLayout {
+struct BwdLayout {  // the reverse kernel
     static constexpr int KP = K + 1;
     static constexpr int oK = 0, oQ = oK + kBC * KP, oS0 = oQ + kBC * KP, odS = oS0 + K * kVP,
                          oV = odS + K * kVP, odO = oV + kBC * kVP, oR = odO + kBC * kVP, oD = oR + kBC * kVP,
                          odD = oD + kBC * kVP, oY = odD + kBC * kVP, oA = oY + kBC * kVP, oP = oA + kBC * kCP,
-                         oM1 = oP + kBC * kCP, oM2 = oM1 + kBC * kCP, oG = oM2 + kBC * kCP, oGam = oG + kBC,
-                         oBeta = oGam + kBC, odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC,
-                         total = oRed + 4 * kBC;
+                         oM2 = oP + kBC * kCP, oG = oM2 + kBC * kCP, oGam = oG + kBC, oBeta = oGam + kBC,
+                         odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC, total = oRed + 4 * kBC;
+};
+template <int K>
+struct ChunkLayout {  // the per-chunk kernels (A and P; the finish)
+    static constexpr int KP = K + 1;
+    static constexpr int oK = 0, oQ = oK + kBC * KP, oA = oQ + kBC * KP, oP = oA + kBC * kCP, odP = oP + kBC * kCP,
+                         odA = odP + kBC * kCP, oT = odA + kBC * kCP, oG = oT + kBC * kCP, oBeta = oG + kBC,
+                         oRed = oBeta + kBC, total = oRed + 4 * kBC;
 };
 
 template <typename T>
@@ -140,6 +151,115 @@ __device__ void rdot(const float (&t)[8][K / 32], const float *m, int ld, float 
     }
 }
 
+
+// The chunk (sequence n, value head hv, chunk c): k, q rows (zero past the sequence end), the
+// inclusive log-gate cumsum G and beta.  Every thread of the CTA takes part; returns the rows.
+template <typename DT, int K>
+__device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int hv, float *sK, float *sQ,
+                          float *sG, float *sGam, float *sBeta)
+{
+    constexpr int KP = K + 1;
+    const int HV = a.HV, hq = hv / (HV / a.H);
+    const int64_t t0 = bos + (int64_t)c * kBC;
+    const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
+    const DT *q = (const DT *)a.q, *k = (const DT *)a.k;
+    for (int e = threadIdx.x; e < kBC * K; e += kBThreads) {
+        const int i = e / K, d = e - i * K;
+        float kv = 0.f, qv = 0.f;
+        if (i < rows) {
+            const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d;
+            kv = ldf(k + off);
+            qv = ldf(q + off);
+        }
+        sK[i * KP + d] = kv;
+        sQ[i * KP + d] = qv;
+    }
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x, r0 = 2 * l, r1 = r0 + 1;
+        const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] : 0.f;
+        const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] : 0.f;
+        float sp = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sp, off);
+            if (l >= off) sp += y;
+        }
+        sG[r0] = sp - g1;
+        sG[r1] = sp;
+        if (sGam) {
+            sGam[r0] = __expf(sp - g1);
+            sGam[r1] = __expf(sp);
+        }
+        sBeta[r0] = r0 < rows ? a.beta[(size_t)(t0 + r0) * HV + hv] : 0.f;
+        sBeta[r1] = r1 < rows ? a.beta[(size_t)(t0 + r1) * HV + hv] : 0.f;
+    }
+    return rows;
+}
+
+// A = (I + L)^-1 in place (sA holds L below the diagonal, zero elsewhere), one row at a time:
+// A_i = e_i - sum_{j < i} L_ij A_j
+__device__ void unit_lower_inverse(float *sA, float *sRed)
+{
+    const int tid = threadIdx.x, col = tid & (kBC - 1), part = tid >> 6;
+    for (int i = 0; i < kBC; ++i) {
+        float s = 0.f;
+        for (int j = part; j < i; j += 4) s = fmaf(sA[i * kCP + j], sA[j * kCP + col], s);
+        sRed[part * kBC + col] = s;
+        __syncthreads();
+        if (tid < kBC) {
+            const float t = sRed[tid] + sRed[kBC + tid] + sRed[2 * kBC + tid] + sRed[3 * kBC + tid];
+            sA[i * kCP + tid] = tid < i ? -t : (tid == i ? 1.f : 0.f);
+        }
+        __syncthreads();
+    }
+}
+
+// (sequence, value head, chunk) of a per-chunk CTA: blockIdx.x = chunk, blockIdx.y = pair
+__device__ bool chunk_of_block(const BwdArgs &a, int &n, int &hv, int &c, int64_t &bos, int64_t &len)
+{
+    c = blockIdx.x;
+    const int pair = blockIdx.y;
+    n = pair / a.HV;
+    hv = pair % a.HV;
+    bos = a.cu_seqlens ? a.cu_seqlens[n] : (int64_t)n * a.T;
+    len = a.cu_seqlens ? a.cu_seqlens[n + 1] - bos : a.T;
+    return (int64_t)c * kBC < len;
+}
+
+// ---- Step 1: A and P of every chunk
+template <typename DT, int K>
+__global__ void __launch_bounds__(kBThreads, 1) bwd_prep_kernel(const BwdArgs a)
+{
+    using Lay = ChunkLayout<K>;
+    constexpr int KP = Lay::KP;
+    extern __shared__ float smem[];
+    float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
+    float *sG = smem + Lay::oG, *sBeta = smem + Lay::oBeta, *sRed = smem + Lay::oRed;
+    int n, hv, c;
+    int64_t bos, len;
+    if (!chunk_of_block(a, n, hv, c, bos, len)) return;
+    load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
+    __syncthreads();
+    smm<false, true>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    smm<false, true>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
+        const int i = e / kBC, j = e - i * kBC;
+        const float gm = i >= j ? __expf(sG[i] - sG[j]) : 0.f;
+        sA[i * kCP + j] = i > j ? sBeta[i] * gm * sA[i * kCP + j] : 0.f;  // L
+        sP[i * kCP + j] = a.scale * gm * sP[i * kCP + j];
+    }
+    __syncthreads();
+    unit_lower_inverse(sA, sRed);
+    const size_t base = ((size_t)tile_slot(bos, n, c) * a.HV + hv) * kBC * kBC;
+    for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
+        const int i = e / kBC, j = e - i * kBC;
+        a.Abuf[base + e] = sA[i * kCP + j];
+        a.Pbuf[base + e] = sP[i * kCP + j];
+    }
+}
+
+// ---- Steps 3-6, the state-dependent part: one CTA per (sequence, value head, value tile), newest chunk first
 template <typename DT, int K>
 __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a)
 {
@@ -149,7 +269,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
     float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sS0 = smem + Lay::oS0, *sdS = smem + Lay::odS;
     float *sV = smem + Lay::oV, *sdO = smem + Lay::odO, *sR = smem + Lay::oR, *sD = smem + Lay::oD;
     float *sdD = smem + Lay::odD, *sY = smem + Lay::oY, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
-    float *sM1 = smem + Lay::oM1, *sM2 = smem + Lay::oM2, *sG = smem + Lay::oG, *sGam = smem + Lay::oGam;
+    float *sM2 = smem + Lay::oM2, *sG = smem + Lay::oG, *sGam = smem + Lay::oGam;
     float *sBeta = smem + Lay::oBeta, *sdG = smem + Lay::odG, *sdB = smem + Lay::odB, *sRed = smem + Lay::oRed;
 
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -160,7 +280,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
     const int NT = (int)((len + kBC - 1) / kBC);
     const int col0 = vt * kBV;
     const float scale = a.scale;
-    const DT *q = (const DT *)a.q, *k = (const DT *)a.k, *v = (const DT *)a.v, *dout = (const DT *)a.dout;
+    const DT *v = (const DT *)a.v, *dout = (const DT *)a.dout;
     const size_t pbase = ((size_t)n * HV + hv) * K * V;
 
     // dS: the gradient with respect to the state after the last chunk (dht)
@@ -171,20 +291,10 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
 
     for (int c = NT - 1; c >= 0; --c) {
         const int64_t t0 = bos + (int64_t)c * kBC;
-        const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
+        const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
         __syncthreads();
         // ---- loads (rows past the sequence end are inert zeros)
-        for (int e = tid; e < kBC * K; e += kBThreads) {
-            const int i = e / K, d = e - i * K;
-            float kv = 0.f, qv = 0.f;
-            if (i < rows) {
-                const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d;
-                kv = ldf(k + off);
-                qv = ldf(q + off);
-            }
-            sK[i * KP + d] = kv;
-            sQ[i * KP + d] = qv;
-        }
+        const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV, col = col0 + j;
             float vv = 0.f, dv = 0.f;
@@ -197,63 +307,24 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             sdO[i * kVP + j] = dv;
         }
         {
-            const float *src = a.chunk_states + ((size_t)tile_slot(bos, n, c) * HV + hv) * K * V;
+            const float *src = a.chunk_states + cidx * K * V;
             for (int e = tid; e < K * kBV; e += kBThreads) {
                 const int d = e / kBV, j = e - d * kBV, col = col0 + j;
                 sS0[d * kVP + j] = col < V ? src[(size_t)d * V + col] : 0.f;
             }
-        }
-        if (w == 0) {
-            // inclusive cumsum of the log-gate (natural log), two rows per lane
-            const int r0 = 2 * l, r1 = r0 + 1;
-            const float g0 = r0 < rows ? a.g[(size_t)(t0 + r0) * HV + hv] : 0.f;
-            const float g1 = r1 < rows ? a.g[(size_t)(t0 + r1) * HV + hv] : 0.f;
-            float sp = g0 + g1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, sp, off);
-                if (l >= off) sp += y;
+            const float *ga = a.Abuf + cidx * kBC * kBC, *gp = a.Pbuf + cidx * kBC * kBC;
+            for (int e = tid; e < kBC * kBC; e += kBThreads) {
+                const int i = e / kBC, j = e - i * kBC;
+                sA[i * kCP + j] = ga[e];
+                sP[i * kCP + j] = gp[e];
             }
-            sG[r0] = sp - g1;
-            sG[r1] = sp;
-            sGam[r0] = __expf(sp - g1);
-            sGam[r1] = __expf(sp);
-            sBeta[r0] = r0 < rows ? a.beta[(size_t)(t0 + r0) * HV + hv] : 0.f;
-            sBeta[r1] = r1 < rows ? a.beta[(size_t)(t0 + r1) * HV + hv] : 0.f;
-            sdG[r0] = sdG[r1] = 0.f;
-            sdB[r0] = sdB[r1] = 0.f;
         }
+        if (tid < kBC) sdG[tid] = sdB[tid] = 0.f;
         __syncthreads();
         const float GC = sG[kBC - 1], gamC = sGam[kBC - 1];
+        if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);  // gam_C / gam
 
-        // ---- Step 1: K K^T and Q K^T; L = StrictLower(diag(beta) Gam * K K^T), P = scale Lower(Gam) * Q K^T
-        smm<false, true>(sM1, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
-        smm<false, true>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
-        __syncthreads();
-        for (int e = tid; e < kBC * kBC; e += kBThreads) {
-            const int i = e / kBC, j = e - i * kBC;
-            const float gm = i >= j ? __expf(sG[i] - sG[j]) : 0.f;
-            const float lraw = i > j ? gm * sM1[i * kCP + j] : 0.f;  // Gam * K K^T below the diagonal
-            sM1[i * kCP + j] = lraw;
-            sA[i * kCP + j] = sBeta[i] * lraw;
-            sP[i * kCP + j] = scale * gm * sP[i * kCP + j];
-        }
-        __syncthreads();
-        // A = (I + L)^-1 in place, one row at a time: A_i = e_i - sum_{j < i} L_ij A_j
-        for (int i = 0; i < kBC; ++i) {
-            const int col = tid & (kBC - 1), part = tid >> 6;
-            float s = 0.f;
-            for (int j = part; j < i; j += 4) s = fmaf(sA[i * kCP + j], sA[j * kCP + col], s);
-            sRed[part * kBC + col] = s;
-            __syncthreads();
-            if (tid < kBC) {
-                const float t = sRed[tid] + sRed[kBC + tid] + sRed[2 * kBC + tid] + sRed[3 * kBC + tid];
-                sA[i * kCP + tid] = tid < i ? -t : (tid == i ? 1.f : 0.f);
-            }
-            __syncthreads();
-        }
-
-        // ---- Step 2 (this chunk): R = V - diag(gam) K S0, B = diag(beta) R, D = A B
+        // ---- R = V - diag(gam) K S0, B = diag(beta) R, D = A B
         smm<false, false, 2>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
@@ -265,137 +336,81 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         __syncthreads();
         smm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
-
-        // ---- Steps 3-5: dD = P^T dO + diag(gam_C / gam) K dS; dP = dO D^T
+        // ---- dD = P^T dO + diag(gam_C / gam) K dS; this tile's part of dP = dO D^T
         smm<true, false, 2>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
-        // (the row factors gam_C / gam into the scratch vector first)
-        if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);
-        __syncthreads();
-        smm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch in sM2)
+        smm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
             sdD[i * kVP + j] = fmaf(sRed[i], sM2[i * kVP + j], sdD[i * kVP + j]);
         }
         __syncthreads();
-        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);  // dP = dO D^T
+        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
-        // gate terms of P (dG_i += P_ij dP_ij, dG_j -= P_ij dP_ij), then F = scale Gam * dP below the diagonal
-        for (int e = tid; e < kBC * kBC; e += kBThreads) {
-            const int i = e / kBC, j = e - i * kBC;
-            const float dp = sM2[i * kCP + j];
-            const float pw = sP[i * kCP + j] * dp;
-            if (pw != 0.f) {
-                atomicAdd(&sdG[i], pw);
-                atomicAdd(&sdG[j], -pw);
-            }
-            sM2[i * kCP + j] = i >= j ? scale * __expf(sG[i] - sG[j]) * dp : 0.f;
+        {
+            float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
+            for (int e = tid; e < kBC * kBC; e += kBThreads) dst[e] = sM2[(e / kBC) * kCP + (e % kBC)];
         }
-        __syncthreads();
-        float dq[8][KJ], dk[8][KJ], t[8][KJ], rd[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
-        racc<K, false, false>(dq, sM2, kCP, sK, KP, kBC);  // dq += F K
-        racc<K, true, false>(dk, sM2, kCP, sQ, KP, kBC);   // dk += F^T Q
-
-        // ---- Step 6: Y = A^T dD; dbeta += rowsum(Y R); dR = diag(beta) Y; dv = dR; dG_i += dR (R - V)
+        // ---- Y = A^T dD; dR = diag(beta) Y (= dv); dbeta_i += sum_v Y R, dG_i += sum_v dR (R - V)
         smm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
+        __syncthreads();
+        if (tid < kBC) {
+            const int i = tid;
+            float sb = 0.f, sg = 0.f;
+            for (int j = 0; j < kBV; ++j) {
+                const float y = sY[i * kVP + j], r = sR[i * kVP + j];
+                sb = fmaf(y, r, sb);
+                sg = fmaf(sBeta[i] * y, r - sV[i * kVP + j], sg);
+            }
+            sdB[i] += sb;
+            sdG[i] += sg;
+        }
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
-            const float y = sY[i * kVP + j], r = sR[i * kVP + j];
-            const float dr = sBeta[i] * y;
-            atomicAdd(&sdB[i], y * r);
-            atomicAdd(&sdG[i], dr * (r - sV[i * kVP + j]));
+            const float dr = sBeta[i] * sY[i * kVP + j];
             sY[i * kVP + j] = dr;
             const int col = col0 + j;
             if (i < rows && col < V) a.dv[((size_t)(t0 + i) * HV + hv) * V + col] = dr;
         }
-        __syncthreads();
-        // dA = dD B^T (B = diag(beta) R: a column scale), then dL = -A^T (dA A^T)
+        // this tile's part of dA = dD B^T (B = diag(beta) R: a column scale)
         smm<false, true>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
-        for (int e = tid; e < kBC * kBC; e += kBThreads) {
-            const int i = e / kBC, j = e - i * kBC;
-            sM2[i * kCP + j] *= sBeta[j];
-        }
-        __syncthreads();
-        smm<false, true>(sP, kCP, sM2, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
-        __syncthreads();
-        smm<true, false>(sM2, kCP, sA, kCP, sP, kCP, kBC, kBC, kBC, -1.f, false);
-        __syncthreads();
-        // L_ij = beta_i Lraw_ij (i > j): dbeta_i += dL_ij Lraw_ij, dG_i += dL_ij L_ij, dG_j -= dL_ij L_ij,
-        // E_ij = d(K K^T)_ij = beta_i Gam_ij dL_ij
-        for (int e = tid; e < kBC * kBC; e += kBThreads) {
-            const int i = e / kBC, j = e - i * kBC;
-            float ev = 0.f;
-            if (i > j) {
-                const float dl = sM2[i * kCP + j], lraw = sM1[i * kCP + j];
-                if (lraw != 0.f) {
-                    atomicAdd(&sdB[i], dl * lraw);
-                    const float wv = dl * sBeta[i] * lraw;
-                    atomicAdd(&sdG[i], wv);
-                    atomicAdd(&sdG[j], -wv);
-                }
-                ev = sBeta[i] * __expf(sG[i] - sG[j]) * dl;
+        {
+            float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
+            for (int e = tid; e < kBC * kBC; e += kBThreads) {
+                const int i = e / kBC, j = e - i * kBC;
+                dst[e] = sM2[i * kCP + j] * sBeta[j];
             }
-            sM2[i * kCP + j] = ev;
         }
-        __syncthreads();
-        racc<K, false, false>(dk, sM2, kCP, sK, KP, kBC);  // dk_i += E_ij k_j
-        racc<K, true, false>(dk, sM2, kCP, sK, KP, kBC);   // dk_j += E_ij k_i
 
         // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
         //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
+        float dq[8][KJ], dk[8][KJ], rd[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int j = 0; j < KJ; ++j) t[r][j] = 0.f;
-        racc<K, false, true>(t, sdO, kVP, sS0, kVP, kBV, scale, sGam);
-        rdot<K>(t, sQ, KP, rd);
+            for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
+        racc<K, false, true>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
+        rdot<K>(dq, sQ, KP, rd);
         if (l == 0)
 #pragma unroll
-            for (int r = 0; r < 8; ++r) atomicAdd(&sdG[8 * w + r], rd[r]);
+            for (int r = 0; r < 8; ++r) sRed[kBC + 8 * w + r] = rd[r];
+        racc<K, false, true>(dk, sD, kVP, sdS, kVP, kBV, 1.f, sRed);
+        rdot<K>(dk, sK, KP, rd);
+        if (l == 0)
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) {
-                dq[r][j] += t[r][j];
-                t[r][j] = 0.f;
-            }
-        racc<K, false, true>(t, sD, kVP, sdS, kVP, kBV);
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float f = __expf(GC - sG[8 * w + r]);
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) t[r][j] *= f;
-        }
-        rdot<K>(t, sK, KP, rd);
-        if (l == 0) {
-            float tot = 0.f;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                atomicAdd(&sdG[8 * w + r], -rd[r]);
-                tot += rd[r];
-            }
-            atomicAdd(&sdG[kBC - 1], tot);
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) dk[r][j] += t[r][j];
+            for (int r = 0; r < 8; ++r) sRed[2 * kBC + 8 * w + r] = rd[r];
         racc<K, false, true>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
         {
-            float s = 0.f;
+            float sum = 0.f;
             for (int e = tid; e < K * kBV; e += kBThreads) {
                 const int d = e / kBV, j = e - d * kBV;
-                s = fmaf(sdS[d * kVP + j], sS0[d * kVP + j], s);
+                sum = fmaf(sdS[d * kVP + j], sS0[d * kVP + j], sum);
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            if (l == 0) atomicAdd(&sdG[kBC - 1], gamC * s);
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (l == 0) sRed[3 * kBC + w] = sum;
         }
         // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
 #pragma unroll
@@ -410,23 +425,29 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
                 }
             }
         }
-        __syncthreads();  // every shared-memory atomic of dG and dbeta is in; S0 is read for the last time
-
-        // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
-        smm<true, false>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
+        __syncthreads();  // S0 is read for the last time; the row terms are in sRed
         if (tid == 0) {
-            // G_C is the last row's G (rows past the end carry g = 0): its gradient belongs to the last row
+            // gate terms of the state products; G_C is the last row's G (rows past the end carry g = 0),
+            // so its gradient belongs to the last row of the sequence
+            float gcsum = 0.f;
+            for (int i = 0; i < kBC; ++i) {
+                sdG[i] += sRed[kBC + i] - sRed[2 * kBC + i];
+                gcsum += sRed[2 * kBC + i];
+            }
+            for (int ww = 0; ww < kBThreads / 32; ++ww) gcsum += gamC * sRed[3 * kBC + ww];
+            sdG[kBC - 1] += gcsum;
             float tail = 0.f;
             for (int i = rows; i < kBC; ++i) tail += sdG[i];
             sdG[rows - 1] += tail;
         }
-        __syncthreads();
+        // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
+        smm<true, false>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
         smm<true, false>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
+        __syncthreads();
         for (int i = tid; i < rows; i += kBThreads) {
             atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], sdB[i]);
             atomicAdd(&a.dG[(size_t)(t0 + i) * HV + hv], sdG[i]);
         }
-        __syncthreads();
         for (int e = tid; e < K * kBV; e += kBThreads) {
             const int d = e / kBV, j = e - d * kBV;
             sS0[d * kVP + j] = fmaf(gamC, sdS[d * kVP + j], sS0[d * kVP + j]);
@@ -441,6 +462,113 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             const int d = e / kBV, j = e - d * kBV, col = col0 + j;
             if (col < V) a.dh0[pbase + (size_t)d * V + col] = sdS[d * kVP + j];
         }
+    }
+}
+
+// ---- Steps 5-6, the state-independent part: one CTA per chunk and value head, after the reverse scan
+template <typename DT, int K>
+__global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs a)
+{
+    using Lay = ChunkLayout<K>;
+    constexpr int KP = Lay::KP, KJ = K / 32;
+    extern __shared__ float smem[];
+    float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
+    float *sdP = smem + Lay::odP, *sdA = smem + Lay::odA, *sT = smem + Lay::oT, *sG = smem + Lay::oG;
+    float *sBeta = smem + Lay::oBeta, *sRed = smem + Lay::oRed;
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    int n, hv, c;
+    int64_t bos, len;
+    if (!chunk_of_block(a, n, hv, c, bos, len)) return;
+    const int HV = a.HV, hq = hv / (HV / a.H);
+    const int64_t t0 = bos + (int64_t)c * kBC;
+    const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
+    const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
+    const int tiles = (a.V + kBV - 1) / kBV;
+    for (int e = tid; e < kBC * kBC; e += kBThreads) {
+        const int i = e / kBC, j = e - i * kBC;
+        float dp = 0.f, da = 0.f;
+        for (int t = 0; t < tiles; ++t) {
+            dp += a.dPbuf[((size_t)t * a.chunk_heads + cidx) * kBC * kBC + e];
+            da += a.dAbuf[((size_t)t * a.chunk_heads + cidx) * kBC * kBC + e];
+        }
+        sdP[i * kCP + j] = dp;
+        sdA[i * kCP + j] = da;
+        sA[i * kCP + j] = a.Abuf[cidx * kBC * kBC + e];
+        sP[i * kCP + j] = a.Pbuf[cidx * kBC * kBC + e];
+    }
+    __syncthreads();
+    // P = scale Gam * Q K^T (i >= j): dG_i += rowsum(P dP), dG_j -= colsum(P dP); F = scale Gam * dP
+    if (tid < 2 * kBC) {
+        const int x = tid & (kBC - 1);
+        float sum = 0.f;
+        if (tid < kBC)
+            for (int j = 0; j < kBC; ++j) sum = fmaf(sP[x * kCP + j], sdP[x * kCP + j], sum);
+        else
+            for (int i = 0; i < kBC; ++i) sum = fmaf(sP[i * kCP + x], sdP[i * kCP + x], sum);
+        sRed[tid] = sum;  // [0, 64): rows, [64, 128): columns
+    }
+    __syncthreads();
+    for (int e = tid; e < kBC * kBC; e += kBThreads) {
+        const int i = e / kBC, j = e - i * kBC;
+        sdP[i * kCP + j] = i >= j ? a.scale * __expf(sG[i] - sG[j]) * sdP[i * kCP + j] : 0.f;  // F
+    }
+    // dL = -A^T (dA A^T)
+    smm<false, true>(sT, kCP, sdA, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
+    __syncthreads();
+    smm<true, false>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
+    // K K^T -> Lraw = Gam * K K^T below the diagonal (into A's buffer: A is no longer read)
+    __syncthreads();
+    smm<false, true>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    __syncthreads();
+    for (int e = tid; e < kBC * kBC; e += kBThreads) {
+        const int i = e / kBC, j = e - i * kBC;
+        const float gm = i > j ? __expf(sG[i] - sG[j]) : 0.f;
+        const float lraw = gm * sA[i * kCP + j];
+        const float dl = i > j ? sdA[i * kCP + j] : 0.f;
+        sT[i * kCP + j] = dl * lraw;                    // dL * Lraw (dbeta; times beta_i: the gate terms of L)
+        sdA[i * kCP + j] = sBeta[i] * gm * dl;          // E = d(K K^T)
+    }
+    __syncthreads();
+    // dbeta_i += rowsum(dL Lraw); dG_i += beta_i rowsum(dL Lraw) - beta_j colsum(dL Lraw) ... (L_ij = beta_i Lraw_ij)
+    if (tid < 2 * kBC) {
+        const int x = tid & (kBC - 1);
+        float sum = 0.f;
+        if (tid < kBC) {
+            for (int j = 0; j < kBC; ++j) sum += sT[x * kCP + j];
+        } else {
+            for (int i = 0; i < kBC; ++i) sum = fmaf(sBeta[i], sT[i * kCP + x], sum);
+        }
+        sRed[2 * kBC + tid] = sum;  // [128, 192): dL Lraw row sums, [192, 256): beta-weighted column sums
+    }
+    // dq += F K, dk += F^T Q + E K + E^T K
+    float dq[8][KJ], dk[8][KJ];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
+    racc<K, false, false>(dq, sdP, kCP, sK, KP, kBC);
+    racc<K, true, false>(dk, sdP, kCP, sQ, KP, kBC);
+    racc<K, false, false>(dk, sdA, kCP, sK, KP, kBC);
+    racc<K, true, false>(dk, sdA, kCP, sK, KP, kBC);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = 8 * w + r;
+        if (i < rows) {
+            float *pq = a.dq + ((size_t)(t0 + i) * a.H + hq) * K, *pk = a.dk + ((size_t)(t0 + i) * a.H + hq) * K;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                atomicAdd(pq + l + 32 * j, dq[r][j]);
+                atomicAdd(pk + l + 32 * j, dk[r][j]);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < rows) {
+        const int i = tid;
+        const float db = sRed[2 * kBC + i];
+        const float dgv = sRed[i] - sRed[kBC + i] + sBeta[i] * db - sRed[3 * kBC + i];
+        atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], db);
+        atomicAdd(&a.dG[(size_t)(t0 + i) * HV + hv], dgv);
     }
 }
 
@@ -471,19 +599,31 @@ __global__ void gate_suffix_kernel(const BwdArgs a)
     if (r1 < rows) a.dg[(size_t)(t0 + r1) * a.HV + hv] = sp - x0;
 }
 
+template <typename DT, int K>
+cudaError_t launch_bwd_k(const BwdArgs &a, cudaStream_t st)
+{
+    auto prep = bwd_prep_kernel<DT, K>;
+    auto scan = chunk_bwd_kernel<DT, K>;
+    auto fin = bwd_finish_kernel<DT, K>;
+    const size_t sc = sizeof(float) * ChunkLayout<K>::total, ss = sizeof(float) * BwdLayout<K>::total;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+    if (e != cudaSuccess) return e;
+    const dim3 gc(a.max_nt, a.N * a.HV);
+    prep<<<gc, kBThreads, sc, st>>>(a);
+    scan<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kBThreads, ss, st>>>(a);
+    fin<<<gc, kBThreads, sc, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename DT>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st)
 {
-    auto go = [&](auto kern, size_t smem) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kBThreads, smem, st>>>(a);
-        return cudaGetLastError();
-    };
     switch (a.K) {
-    case 32: return go(chunk_bwd_kernel<DT, 32>, sizeof(float) * BwdLayout<32>::total);
-    case 64: return go(chunk_bwd_kernel<DT, 64>, sizeof(float) * BwdLayout<64>::total);
-    case 128: return go(chunk_bwd_kernel<DT, 128>, sizeof(float) * BwdLayout<128>::total);
+    case 32: return launch_bwd_k<DT, 32>(a, st);
+    case 64: return launch_bwd_k<DT, 64>(a, st);
+    case 128: return launch_bwd_k<DT, 128>(a, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -492,7 +632,9 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st)
 
 cudaError_t launch_chunk_bwd(const BwdArgs &a, gdn_dtype dt, cudaStream_t st)
 {
-    static_assert(sizeof(float) * BwdLayout<128>::total <= 227 * 1024, "shared memory budget");
+    static_assert(sizeof(float) * BwdLayout<128>::total <= 227 * 1024 &&
+                      sizeof(float) * ChunkLayout<128>::total <= 227 * 1024,
+                  "shared memory budget");
     if (a.N * a.HV == 0 || a.max_nt == 0) return cudaSuccess;
     cudaError_t e = dt == GDN_BF16 ? launch_bwd_t<__nv_bfloat16>(a, st) : launch_bwd_t<float>(a, st);
     if (e != cudaSuccess) return e;

@@ -221,8 +221,9 @@ struct RecArgs {
 };
 cudaError_t launch_recurrent(const RecArgs &a, gdn_dtype dt, gdn_gate_kind gate, cudaStream_t st);
 
-// Backward pass (scalar gates): one CTA per (sequence, value head, 32-column value tile), chunks newest
-// first; then the suffix sum of dG within each chunk into dg.
+// Backward pass (scalar gates): A and P per chunk; the reverse scan, one CTA per (sequence, value head,
+// 32-column value tile), chunks newest first; the state-independent gradient terms per chunk; the
+// suffix sum of dG within each chunk into dg.
 struct BwdArgs {
     const void *q, *k, *v, *dout;  // q, k [B,T,H,K]; v, dout [B,T,HV,V] (the dtype of v)
     const float *g, *beta;         // [B,T,HV]
@@ -234,6 +235,9 @@ struct BwdArgs {
     float *dbeta, *dG;             // [B,T,HV], zeroed by the host (dG: per-row gate gradient before Step 7)
     float *dg;                     // [B,T,HV]
     float *dh0;                    // [N,HV,K,V], nullable
+    float *Abuf, *Pbuf;            // [slot][HV][64][64]: A = (I + L)^-1 and P of every chunk
+    float *dPbuf, *dAbuf;          // [value tile][slot][HV][64][64]: each tile's part of dO D^T and dD B^T
+    size_t chunk_heads;            // slots x HV
     int T, H, HV, K, V, N, max_nt;
     float scale;
 };
