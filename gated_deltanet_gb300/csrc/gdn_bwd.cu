@@ -25,7 +25,8 @@
 //                       products with K and Q, the gate and beta terms of P and L;
 //   gate_suffix_kernel  Step 7.
 // dq, dk, dbeta and dG are sums over value tiles and kernels (and dq, dk over a GVA group's value
-// heads): fp32 atomic adds into buffers the host zeroes.  CUDA cores, fp32 throughout.
+// heads): fp32 atomic adds into buffers the host zeroes.  The shared-memory products run on the tensor
+// cores in split tf32 (about fp32 accuracy), the rest on CUDA cores in fp32.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -34,12 +35,12 @@ namespace {
 constexpr int kBThreads = 256;
 constexpr int kBC = 64;      // chunk
 constexpr int kBV = 32;      // value columns per CTA
-constexpr int kCP = kBC + 1;  // pitches (odd: strided reads are free of bank conflicts)
-constexpr int kVP = kBV + 1;
+constexpr int kCP = kBC + 4;  // pitches (4 mod 32: the tensor-core fragments' strided reads hit at most
+constexpr int kVP = kBV + 4;  // two lanes per bank)
 
 template <int K>
 struct BwdLayout {  // the reverse kernel
-    static constexpr int KP = K + 1;
+    static constexpr int KP = K + 4;
     static constexpr int oK = 0, oQ = oK + kBC * KP, oS0 = oQ + kBC * KP, odS = oS0 + K * kVP,
                          oV = odS + K * kVP, odO = oV + kBC * kVP, oR = odO + kBC * kVP, oD = oR + kBC * kVP,
                          odD = oD + kBC * kVP, oY = odD + kBC * kVP, oA = oY + kBC * kVP, oP = oA + kBC * kCP,
@@ -48,7 +49,7 @@ struct BwdLayout {  // the reverse kernel
 };
 template <int K>
 struct ChunkLayout {  // the per-chunk kernels (A and P; the finish)
-    static constexpr int KP = K + 1;
+    static constexpr int KP = K + 4;
     static constexpr int oK = 0, oQ = oK + kBC * KP, oA = oQ + kBC * KP, oP = oA + kBC * kCP, odP = oP + kBC * kCP,
                          odA = odP + kBC * kCP, oT = odA + kBC * kCP, oG = oT + kBC * kCP, oBeta = oG + kBC,
                          oRed = oBeta + kBC, total = oRed + 4 * kBC;
@@ -59,41 +60,79 @@ __device__ __forceinline__ float ldf(const T *p) { return (float)*p; }
 template <>
 __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
-// out[m][n] = alpha * sum_x A(m, x) xs[x] B(x, n) (+ out when acc): A(m, x) = a[x lda + m] if TA else
-// a[m lda + x], B(x, n) = b[n ldb + x] if TB else b[x ldb + n]; xs optional.  Each thread computes
-// 4 x TN blocks of outputs (M a multiple of 4, N of TN), sixteen or eight independent sums.
-template <bool TA, bool TB, int TN = 4>
-__device__ void smm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
+// Shared-memory products: out[m][n] = alpha * sum_x A(m, x) xs[x] B(x, n) (+ out when acc), with
+// A(m, x) = a[x lda + m] if TA else a[m lda + x], B(x, n) = b[n ldb + x] if TB else b[x ldb + n], xs optional.
+__device__ __forceinline__ uint32_t tf32_of(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32x(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// On the tensor cores (mma.sync m16n8k8, tf32): each operand is split into a tf32
+// part and the tf32 rounding of its remainder, and hi*hi + hi*lo + lo*hi keeps the product to about fp32
+// accuracy.  A warp takes 16 x (8 NB) output blocks, NB tiles side by side sharing the A fragment (NB
+// independent accumulations in flight); M a multiple of 16, N of 8 NB, X of 8.
+template <bool TA, bool TB, int NB>
+__device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
                     float alpha, bool acc, const float *xs = nullptr)
 {
-    const int nb = N / TN, blocks = (M / 4) * nb;
-    for (int e = threadIdx.x; e < blocks; e += kBThreads) {
-        const int m0 = (e / nb) * 4, n0 = (e % nb) * TN;
-        float s[4][TN];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    const int bn = N / (8 * NB), blocks = (M / 16) * bn;
+    for (int blk = w; blk < blocks; blk += kBThreads / 32) {
+        const int m0 = (blk / bn) * 16, n0 = (blk % bn) * 8 * NB;
+        float d[NB][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < NB; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll 2
+        for (int x0 = 0; x0 < X; x0 += 8) {
+            const int xa = x0 + t, xb = x0 + t + 4;
+            const float fa = xs ? xs[xa] : 1.f, fb = xs ? xs[xb] : 1.f;
+            const float av[4] = {
+                fa * (TA ? a[xa * lda + m0 + g] : a[(m0 + g) * lda + xa]),
+                fa * (TA ? a[xa * lda + m0 + g + 8] : a[(m0 + g + 8) * lda + xa]),
+                fb * (TA ? a[xb * lda + m0 + g] : a[(m0 + g) * lda + xb]),
+                fb * (TA ? a[xb * lda + m0 + g + 8] : a[(m0 + g + 8) * lda + xb])};
+            uint32_t ah[4], al[4];
 #pragma unroll
-            for (int j = 0; j < TN; ++j) s[i][j] = 0.f;
-#pragma unroll 4
-        for (int x = 0; x < X; ++x) {
-            const float f = xs ? xs[x] : 1.f;
-            float av[4], bv[TN];
+            for (int i = 0; i < 4; ++i) {
+                ah[i] = tf32_of(av[i]);
+                al[i] = tf32_of(av[i] - __uint_as_float(ah[i]));
+            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) av[i] = f * (TA ? a[x * lda + m0 + i] : a[(m0 + i) * lda + x]);
-#pragma unroll
-            for (int j = 0; j < TN; ++j) bv[j] = TB ? b[(n0 + j) * ldb + x] : b[x * ldb + n0 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) s[i][j] = fmaf(av[i], bv[j], s[i][j]);
+            for (int j = 0; j < NB; ++j) {
+                const int nn = n0 + 8 * j + g;
+                const float bv0 = TB ? b[nn * ldb + xa] : b[xa * ldb + nn];
+                const float bv1 = TB ? b[nn * ldb + xb] : b[xb * ldb + nn];
+                const uint32_t bh0 = tf32_of(bv0), bh1 = tf32_of(bv1);
+                const uint32_t bl0 = tf32_of(bv0 - __uint_as_float(bh0)), bl1 = tf32_of(bv1 - __uint_as_float(bh1));
+                mma_tf32x(d[j], al, bh0, bh1);
+                mma_tf32x(d[j], ah, bl0, bl1);
+                mma_tf32x(d[j], ah, bh0, bh1);
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) {
-                float *o = out + (m0 + i) * ldo + n0 + j;
-                *o = acc ? fmaf(alpha, s[i][j], *o) : alpha * s[i][j];
+        for (int j = 0; j < NB; ++j) {
+            float *o0 = out + (m0 + g) * ldo + n0 + 8 * j + 2 * t, *o1 = o0 + 8 * ldo;
+            if (acc) {
+                o0[0] = fmaf(alpha, d[j][0], o0[0]);
+                o0[1] = fmaf(alpha, d[j][1], o0[1]);
+                o1[0] = fmaf(alpha, d[j][2], o1[0]);
+                o1[1] = fmaf(alpha, d[j][3], o1[1]);
+            } else {
+                o0[0] = alpha * d[j][0];
+                o0[1] = alpha * d[j][1];
+                o1[0] = alpha * d[j][2];
+                o1[1] = alpha * d[j][3];
             }
+        }
     }
 }
 
@@ -158,7 +197,7 @@ template <typename DT, int K>
 __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int hv, float *sK, float *sQ,
                           float *sG, float *sGam, float *sBeta)
 {
-    constexpr int KP = K + 1;
+    constexpr int KP = K + 4;
     const int HV = a.HV, hq = hv / (HV / a.H);
     const int64_t t0 = bos + (int64_t)c * kBC;
     const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
@@ -240,8 +279,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_prep_kernel(const BwdArgs a)
     if (!chunk_of_block(a, n, hv, c, bos, len)) return;
     load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
     __syncthreads();
-    smm<false, true>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
-    smm<false, true>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 4>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 4>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
     __syncthreads();
     for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
         const int i = e / kBC, j = e - i * kBC;
@@ -325,7 +364,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);  // gam_C / gam
 
         // ---- R = V - diag(gam) K S0, B = diag(beta) R, D = A B
-        smm<false, false, 2>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        tmm<false, false, 2>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
@@ -334,25 +373,25 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             sY[i * kVP + j] = sBeta[i] * r;
         }
         __syncthreads();
-        smm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
         // ---- dD = P^T dO + diag(gam_C / gam) K dS; this tile's part of dP = dO D^T
-        smm<true, false, 2>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
-        smm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
+        tmm<true, false, 2>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
             sdD[i * kVP + j] = fmaf(sRed[i], sM2[i * kVP + j], sdD[i * kVP + j]);
         }
         __syncthreads();
-        smm<false, true>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
+        tmm<false, true, 4>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
         {
             float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
             for (int e = tid; e < kBC * kBC; e += kBThreads) dst[e] = sM2[(e / kBC) * kCP + (e % kBC)];
         }
         // ---- Y = A^T dD; dR = diag(beta) Y (= dv); dbeta_i += sum_v Y R, dG_i += sum_v dR (R - V)
-        smm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
         if (tid < kBC) {
             const int i = tid;
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             if (i < rows && col < V) a.dv[((size_t)(t0 + i) * HV + hv) * V + col] = dr;
         }
         // this tile's part of dA = dD B^T (B = diag(beta) R: a column scale)
-        smm<false, true>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
+        tmm<false, true, 4>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
         {
             float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
@@ -441,8 +480,8 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             sdG[rows - 1] += tail;
         }
         // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
-        smm<true, false>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
-        smm<true, false>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
+        tmm<true, false, 2>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
+        tmm<true, false, 2>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
         __syncthreads();
         for (int i = tid; i < rows; i += kBThreads) {
             atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], sdB[i]);
@@ -513,12 +552,12 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
         sdP[i * kCP + j] = i >= j ? a.scale * __expf(sG[i] - sG[j]) * sdP[i * kCP + j] : 0.f;  // F
     }
     // dL = -A^T (dA A^T)
-    smm<false, true>(sT, kCP, sdA, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
+    tmm<false, true, 4>(sT, kCP, sdA, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
     __syncthreads();
-    smm<true, false>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
+    tmm<true, false, 4>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
     // K K^T -> Lraw = Gam * K K^T below the diagonal (into A's buffer: A is no longer read)
     __syncthreads();
-    smm<false, true>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 4>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
     __syncthreads();
     for (int e = tid; e < kBC * kBC; e += kBThreads) {
         const int i = e / kBC, j = e - i * kBC;
