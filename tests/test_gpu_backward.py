@@ -79,6 +79,27 @@ def test_backward_matches_oracle(gdn, w):
     _run(gdn, w)
 
 
+def test_backward_packed_edge_sequences(gdn):
+    """Packed sequences of 0, 1, 64 (one full chunk) and 65 tokens: the empty one's dh0 is its dht."""
+    from oracle import recurrence_backward
+    w = Workload("bwd_edges", B=1, T=130, H=2, HV=2, K=64, V=64, dtype="f32", h0=True, seed=68)
+    x = make_inputs(w, device="cuda")
+    cu = torch.tensor([0, 0, 1, 65, 130], dtype=torch.int64)
+    N = 4
+    gen = torch.Generator().manual_seed(9)
+    h0 = (0.1 * torch.randn(N, 2, 64, 64, generator=gen)).cuda()
+    do = torch.randn(x["v"].shape, generator=gen).cuda()
+    dht = torch.randn(N, 2, 64, 64, generator=gen).cuda()
+    got = gdn.chunk_gated_delta_rule_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, x["scale"], h0, dht,
+                                         cu.cuda())
+    torch.cuda.synchronize()
+    ref = recurrence_backward(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), to_f64(x["g"]), to_f64(x["beta"]),
+                              x["scale"], to_f64(do), to_f64(h0), to_f64(dht), cu)
+    for name, gv, rv in zip(NAMES, got, ref):
+        _close(name, gv, rv)
+    assert torch.equal(got[5][0].cpu(), dht[0].cpu())
+
+
 def test_backward_without_final_state_gradient(gdn):
     _run(gdn, Workload("bwd_nodht", B=2, T=64 * 2 + 9, H=2, HV=2, K=128, V=128, h0=True, seed=66), with_dht=False)
 
