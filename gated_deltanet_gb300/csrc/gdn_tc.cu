@@ -82,7 +82,7 @@ constexpr uint32_t TM_S = 0, TM_VP = 128, TM_O = 192, TM_W = 256, TM_SBF = 320, 
                    TM_KQ = 448;
 
 enum Bar {
-    B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_WF, B_WC, B_SBF, B_VPF, B_VTF, B_SF, B_PF,
+    B_TMA = 0, B_FULL = 3, B_EMPTY = 6, B_QS = 9, B_KQF = 12, B_KQE, B_WF, B_SBF, B_VPF, B_VTF, B_SF, B_PF,
     B_OF, B_OE, B_FIN, B_COUNT
 };
 static_assert(B_COUNT * 8 + 16 <= 512, "barrier block");  // + TMEM slot, cs, c0, c1
@@ -236,8 +236,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         mbar_init(&bars[B_KQF], 1);
         mbar_init(&bars[B_KQE], 2);
         mbar_init(&bars[B_WF], 1);
-        mbar_init(&bars[B_WC], 4);
-        mbar_init(&bars[B_SBF], 8);
+        mbar_init(&bars[B_SBF], KDA ? 8 : 12);  // the chain warps' state copy (+ the output warps' -W^T)
         mbar_init(&bars[B_VPF], 1);
         mbar_init(&bars[B_VTF], 8);
         mbar_init(&bars[B_SF], 1);
@@ -566,7 +565,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const bool em = emit_of(c);
                 const uint32_t st = stage(c);
                 // ---- V'^T (holding U^T, issued before) -= S^T W^T
-                if (!wait(B_SBF, c) || !wait(B_WC, c)) break;
+                if (!wait(B_SBF, c)) break;  // the state copy and -W^T (one barrier: one wait fewer per chunk)
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
@@ -965,7 +964,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_WC]);
+                if (lane == 0) mbar_arrive(&bars[B_SBF]);  // (with the chain warps' state copy)
             }
             if (it >= 1 && !emit_of(it - 1)) {
                 if (et == 0) mbar_arrive(&bars[B_EMPTY + (it - 1) % kStages]);  // nothing to store
