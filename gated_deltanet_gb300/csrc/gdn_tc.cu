@@ -433,14 +433,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             int e = 0;
             for (int c = 0; c < nch && ok; ++c) {
                 const uint32_t st = sbase + OFF_STAGE + (c % kStages) * kStageBytes;
+                // the stage's descriptors: a byte offset b adds b / 16 to the address field (no carry: shared
+                // memory addresses stay below 256 KB)
+                const uint64_t dw = kmaj(st + sTU), dq = kmaj(st + sQ0), dk = sdesc_sw128(st + sK0, 16384, 1024),
+                               dp = kmaj(st + sKdaP);
                 // ---- -(W S)^T = S^T (-W)^T: -W as K-major B (rows = tokens), fresh accumulator
                 if (!wait(B_SBF, c)) break;
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, kmaj(st + sTU + (ks >> 2) * 8192 + (ks & 3) * 32),
-                               idV1K, ks > 0 ? 1u : 0u);
+                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, dw + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), idV1K,
+                               ks > 0 ? 1u : 0u);
                     mma_commit(&bars[B_VPF]);
                 }
                 __syncwarp();
@@ -449,10 +453,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idV1K, ks > 0 ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, dq + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), idV1K,
+                               ks > 0 ? 1u : 0u);
                 }
                 __syncwarp();
                 // ---- S^T += V'^T K^  (B = K^, MN-major: dk atoms 16 KB apart; the per-channel decay is applied
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_S, tb + TM_VB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                        mma_ts(tb + TM_S, tb + TM_VB + ks * 8, dk + ks * 128, idS, 1u);
                     mma_commit(&bars[B_SF]);
                 }
                 __syncwarp();
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, kmaj(st + sKdaP + ks * 32), idV1K, 1u);
+                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, dp + ks * 2, idV1K, 1u);
                     mma_commit(&bars[B_OF]);
                 }
                 __syncwarp();
@@ -503,13 +506,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             const int ce0 = fwd ? min(max(c0 - cs, 0), nch) : nch;
             int kq = ce0;
             auto issue_kq = [&]() {
-                const uint32_t s2 = stage(kq);
+                const uint64_t d0 = kmaj(stage(kq));
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ss(tb + TM_KQ, kmaj(s2 + off), kmaj(s2 + off), idKQ, ks > 0 ? 1u : 0u);
+                        const uint64_t d = d0 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
+                        mma_ss(tb + TM_KQ, d, d, idKQ, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(&bars[B_KQF]);
                 }
@@ -531,12 +534,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             auto issue_w = [&](int i) {
                 // W^T = K^T (A_g diag(beta gam))^T   (A = K, MN-major: dk atoms 16 KB apart)
                 const uint32_t s2 = stage(i);
+                const uint64_t da = sdesc_sw128(s2 + sK0, 16384, 1024), db = kmaj(s2 + sTW);
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tb + TM_W, sdesc_sw128(s2 + sK0 + ks * 2048, 16384, 1024), kmaj(s2 + sTW + ks * 32),
-                               idMN, ks > 0 ? 1u : 0u);
+                        mma_ss(tb + TM_W, da + ks * 128, db + ks * 2, idMN, ks > 0 ? 1u : 0u);
                     mma_commit(&bars[B_WF]);
                 }
                 __syncwarp();
@@ -545,15 +548,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 // U^T = V^T (A_g diag(beta))^T into the V' accumulator (A = V, MN-major: dv atoms 8 KB apart)
                 if (zero_values) return;
                 const uint32_t s2 = stage(i);
+                const uint64_t da = sdesc_sw128(s2 + sV0, 8192, 1024), db = kmaj(s2 + sTU);
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tb + TM_VP, sdesc_sw128(s2 + sV0 + ks * 2048, 8192, 1024), kmaj(s2 + sTU + ks * 32),
-                               idMN, ks > 0 ? 1u : 0u);
+                        mma_ss(tb + TM_VP, da + ks * 128, db + ks * 2, idMN, ks > 0 ? 1u : 0u);
                 }
                 __syncwarp();
             };
+            // descriptors of the fixed operands (-W^T, P): a byte offset b adds b / 16 to the address field
+            // (shared-memory addresses stay below 256 KB: no carry out of it)
+            const uint64_t dws = sdesc_sw128(sbase + OFF_WS, 8192, 1024), dp = kmaj(sbase + OFF_P);
             // prologue: the first chunk's W and U, Q K^T of the first emitted chunks
             if (wait(B_FULL, 0)) {
                 issue_w(0);
@@ -570,8 +576,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, sdesc_sw128(sbase + OFF_WS + ks * 2048, 8192, 1024),
-                               idV1, (ks > 0 || !zero_values) ? 1u : 0u);
+                        mma_ts(tb + TM_VP, tb + TM_SBF + ks * 8, dws + ks * 128, idV1, (ks > 0 || !zero_values) ? 1u : 0u);
                     mma_commit(&bars[B_VPF]);
                 }
                 __syncwarp();
@@ -582,23 +587,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     kq_upto(c, true);
                     if ((!factored(c) && !wait(B_QS + c % kStages, c / kStages)) || (e > 0 && !wait(B_OE, e - 1)))
                         break;
+                    const uint64_t dq0 = kmaj(st + sQ0);
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, kmaj(st + sQ0 + off), idO, ks > 0 ? 1u : 0u);
-                        }
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, dq0 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), idO,
+                                   ks > 0 ? 1u : 0u);
                     }
                     __syncwarp();
                 }
                 // ---- S^T += (V'^T diag(gC/gam)) K   (B = K, MN-major: dk atoms 16 KB apart)
+                const uint64_t dks = sdesc_sw128(st + sK0, 16384, 1024);
                 if (!wait(B_VTF, c)) break;
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, sdesc_sw128(st + sK0 + ks * 2048, 16384, 1024), idS, 1u);
+                        mma_ts(tb + TM_S, tb + TM_VTB + ks * 8, dks + ks * 128, idS, 1u);
                     mma_commit(&bars[B_SF]);
                 }
                 __syncwarp();
@@ -616,7 +622,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(tb + TM_O, va + ks * 8, kmaj(sbase + OFF_P + ks * 32), idO, 1u);
+                            mma_ts(tb + TM_O, va + ks * 8, dp + ks * 2, idO, 1u);
                         mma_commit(&bars[B_OF]);
                     }
                     __syncwarp();
@@ -809,7 +815,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     // S[dk][dv] entering chunk cs + i, dk = 64 hh .. 64 hh + 63 (coalesced over the warp's dv)
                     float *dst = a.chunk_states + ((size_t)tile_slot(bos, n, cs + i) * HV + hv) * 128 * V +
                                  (size_t)(64 * hh) * V + dv;
-#pragma unroll 8
+#pragma unroll
                     for (int j = 0; j < 64; ++j) dst[(size_t)j * V] = u2f(r[j]);
                 }
 #pragma unroll
