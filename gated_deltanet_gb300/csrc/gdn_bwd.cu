@@ -26,7 +26,8 @@
 //   gate_suffix_kernel  Step 7.
 // dq, dk, dbeta and dG are sums over value tiles and kernels (and dq, dk over a GVA group's value
 // heads): fp32 atomic adds into buffers the host zeroes.  The shared-memory products run on the tensor
-// cores in split tf32 (about fp32 accuracy), the rest on CUDA cores in fp32.
+// cores in split tf32 (about fp32 accuracy; the remainder terms of bf16 inputs, exact in tf32, left out), and
+// so do the row tiles of dq and dk, kept in accumulator fragments; the rest runs on CUDA cores in fp32.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -45,10 +46,16 @@ struct BwdLayout {  // the reverse kernel
                          oV = odS + K * kVP, odO = oV + kBC * kVP, oR = odO + kBC * kVP, oD = oR + kBC * kVP,
                          odD = oD + kBC * kVP, oY = odD + kBC * kVP, oA = oY + kBC * kVP, oP = oA + kBC * kCP,
                          oM2 = oP + kBC * kCP, oG = oM2 + kBC * kCP, oGam = oG + kBC, oBeta = oGam + kBC,
-                         odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC, total = oRed + 4 * kBC;
+                         odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC, total = oRed + 6 * kBC;
 };
 template <int K>
-struct ChunkLayout {  // the per-chunk kernels (A and P; the finish)
+struct PrepLayout {  // A and P of a chunk (two CTAs per SM at K = 128)
+    static constexpr int KP = K + 4;
+    static constexpr int oK = 0, oQ = oK + kBC * KP, oA = oQ + kBC * KP, oP = oA + kBC * kCP, oG = oP + kBC * kCP,
+                         oBeta = oG + kBC, oRed = oBeta + kBC, total = oRed + 4 * kBC;
+};
+template <int K>
+struct ChunkLayout {  // the finish
     static constexpr int KP = K + 4;
     static constexpr int oK = 0, oQ = oK + kBC * KP, oA = oQ + kBC * KP, oP = oA + kBC * kCP, odP = oP + kBC * kCP,
                          odA = odP + kBC * kCP, oT = odA + kBC * kCP, oG = oT + kBC * kCP, oBeta = oG + kBC,
@@ -57,6 +64,11 @@ struct ChunkLayout {  // the per-chunk kernels (A and P; the finish)
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T *p) { return (float)*p; }
+// bf16 inputs (k, q, v, dO) are exact in tf32: their products need no remainder term
+template <typename T>
+constexpr bool kExactOf = false;
+template <>
+constexpr bool kExactOf<__nv_bfloat16> = true;
 template <>
 __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
@@ -78,9 +90,11 @@ __device__ __forceinline__ void mma_tf32x(float (&d)[4], const uint32_t (&a)[4],
 
 // On the tensor cores (mma.sync m16n8k8, tf32): each operand is split into a tf32
 // part and the tf32 rounding of its remainder, and hi*hi + hi*lo + lo*hi keeps the product to about fp32
-// accuracy.  A warp takes 16 x (8 NB) output blocks, NB tiles side by side sharing the A fragment (NB
-// independent accumulations in flight); M a multiple of 16, N of 8 NB, X of 8.
-template <bool TA, bool TB, int NB>
+// accuracy.  An operand that is exact in tf32 (EA, EB: bf16 inputs, unscaled) has no remainder, and its
+// term is left out.  A warp takes 16 x (8 NB) output blocks, NB tiles side by side sharing the A fragment
+// (NB independent accumulations in flight); M a multiple of 16, N of 8 NB, X of 8.  xs scales the
+// contraction index on A's side, or on B's with XB (so that the other operand stays exact).
+template <bool TA, bool TB, int NB, bool EA = false, bool EB = false, bool XB = false>
 __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
                     float alpha, bool acc, const float *xs = nullptr)
 {
@@ -94,7 +108,8 @@ __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b
 #pragma unroll 2
         for (int x0 = 0; x0 < X; x0 += 8) {
             const int xa = x0 + t, xb = x0 + t + 4;
-            const float fa = xs ? xs[xa] : 1.f, fb = xs ? xs[xb] : 1.f;
+            const float sa = xs ? xs[xa] : 1.f, sb = xs ? xs[xb] : 1.f;
+            const float fa = XB ? 1.f : sa, fb = XB ? 1.f : sb, ga = XB ? sa : 1.f, gb = XB ? sb : 1.f;
             const float av[4] = {
                 fa * (TA ? a[xa * lda + m0 + g] : a[(m0 + g) * lda + xa]),
                 fa * (TA ? a[xa * lda + m0 + g + 8] : a[(m0 + g + 8) * lda + xa]),
@@ -104,17 +119,19 @@ __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 ah[i] = tf32_of(av[i]);
-                al[i] = tf32_of(av[i] - __uint_as_float(ah[i]));
+                al[i] = EA ? 0u : tf32_of(av[i] - __uint_as_float(ah[i]));
             }
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int nn = n0 + 8 * j + g;
-                const float bv0 = TB ? b[nn * ldb + xa] : b[xa * ldb + nn];
-                const float bv1 = TB ? b[nn * ldb + xb] : b[xb * ldb + nn];
+                const float bv0 = ga * (TB ? b[nn * ldb + xa] : b[xa * ldb + nn]);
+                const float bv1 = gb * (TB ? b[nn * ldb + xb] : b[xb * ldb + nn]);
                 const uint32_t bh0 = tf32_of(bv0), bh1 = tf32_of(bv1);
-                const uint32_t bl0 = tf32_of(bv0 - __uint_as_float(bh0)), bl1 = tf32_of(bv1 - __uint_as_float(bh1));
-                mma_tf32x(d[j], al, bh0, bh1);
-                mma_tf32x(d[j], ah, bl0, bl1);
+                if (!EA) mma_tf32x(d[j], al, bh0, bh1);
+                if (!EB) {
+                    const uint32_t bl0 = tf32_of(bv0 - __uint_as_float(bh0)), bl1 = tf32_of(bv1 - __uint_as_float(bh1));
+                    mma_tf32x(d[j], ah, bl0, bl1);
+                }
                 mma_tf32x(d[j], ah, bh0, bh1);
             }
         }
@@ -136,60 +153,101 @@ __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b
     }
 }
 
-// A [kBC x K] register tile per CTA: warp w holds rows 8w .. 8w + 7, lane l the columns l + 32 j.
-// acc[r][j] += alpha * rs[m] * sum_x A(m, x) B(x, n) (rs optional)
-template <int K, bool TA, bool TB>
-__device__ void racc(float (&acc)[8][K / 32], const float *a, int lda, const float *b, int ldb, int X,
+// A [kBC x K] tile in tensor-core accumulator fragments: warp w holds rows 16 (w & 3) .. + 15 and the
+// columns (K / 2)(w >> 2) .. + K / 2 - 1 as K / 16 blocks of m16n8; thread (g = lane / 4, t = lane % 4)
+// holds, in block j, rows r = 16 (w & 3) + g and r + 8 at columns c = (K / 2)(w >> 2) + 8 j + 2 t and c + 1.
+// facc: acc[m][n] += alpha * rs[m] * sum_x A(m, x) B(x, n) (rs optional), split tf32 as in tmm, X a
+// multiple of 8.
+template <int K, bool TA, bool TB, bool EA = false, bool EB = false>
+__device__ void facc(float (&acc)[K / 16][4], const float *a, int lda, const float *b, int ldb, int X,
                      float alpha = 1.f, const float *rs = nullptr)
 {
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    float s[8][K / 32];
+    constexpr int NT = K / 16;
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    const int m0 = 16 * (w & 3), n0 = (K / 2) * (w >> 2);
+    float d[NT][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int j = 0; j < NT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll 2
+    for (int x0 = 0; x0 < X; x0 += 8) {
+        const int xa = x0 + t, xb = x0 + t + 4;
+        const float av[4] = {TA ? a[xa * lda + m0 + g] : a[(m0 + g) * lda + xa],
+                             TA ? a[xa * lda + m0 + g + 8] : a[(m0 + g + 8) * lda + xa],
+                             TA ? a[xb * lda + m0 + g] : a[(m0 + g) * lda + xb],
+                             TA ? a[xb * lda + m0 + g + 8] : a[(m0 + g + 8) * lda + xb]};
+        uint32_t ah[4], al[4];
 #pragma unroll
-        for (int j = 0; j < K / 32; ++j) s[r][j] = 0.f;
-    for (int x = 0; x < X; ++x) {
-        float av[8], bv[K / 32];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int m = 8 * w + r;
-            av[r] = TA ? a[x * lda + m] : a[m * lda + x];
+        for (int i = 0; i < 4; ++i) {
+            ah[i] = tf32_of(av[i]);
+            al[i] = EA ? 0u : tf32_of(av[i] - __uint_as_float(ah[i]));
         }
 #pragma unroll
-        for (int j = 0; j < K / 32; ++j) {
-            const int n = l + 32 * j;
-            bv[j] = TB ? b[n * ldb + x] : b[x * ldb + n];
+        for (int j = 0; j < NT; ++j) {
+            const int nn = n0 + 8 * j + g;
+            const float bv0 = TB ? b[nn * ldb + xa] : b[xa * ldb + nn];
+            const float bv1 = TB ? b[nn * ldb + xb] : b[xb * ldb + nn];
+            const uint32_t bh0 = tf32_of(bv0), bh1 = tf32_of(bv1);
+            if (!EA) mma_tf32x(d[j], al, bh0, bh1);
+            if (!EB) {
+                const uint32_t bl0 = tf32_of(bv0 - __uint_as_float(bh0)), bl1 = tf32_of(bv1 - __uint_as_float(bh1));
+                mma_tf32x(d[j], ah, bl0, bl1);
+            }
+            mma_tf32x(d[j], ah, bh0, bh1);
         }
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < K / 32; ++j) s[r][j] = fmaf(av[r], bv[j], s[r][j]);
     }
+    const float f0 = alpha * (rs ? rs[m0 + g] : 1.f), f1 = alpha * (rs ? rs[m0 + g + 8] : 1.f);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const float f = alpha * (rs ? rs[8 * w + r] : 1.f);
-#pragma unroll
-        for (int j = 0; j < K / 32; ++j) acc[r][j] = fmaf(f, s[r][j], acc[r][j]);
+    for (int j = 0; j < NT; ++j) {
+        acc[j][0] = fmaf(f0, d[j][0], acc[j][0]);
+        acc[j][1] = fmaf(f0, d[j][1], acc[j][1]);
+        acc[j][2] = fmaf(f1, d[j][2], acc[j][2]);
+        acc[j][3] = fmaf(f1, d[j][3], acc[j][3]);
     }
 }
 
-// per-row dot product of a register tile with a [kBC x K] shared-memory matrix (pitch ld): warp-reduced,
-// returned on every lane for the warp's eight rows
+// the warp's part of the row dot products of a fragment tile with a [kBC x K] shared-memory matrix (pitch
+// ld) over its K / 2 columns: out[0] for row 16 (w & 3) + g, out[1] for that + 8, on every lane of the quad
 template <int K>
-__device__ void rdot(const float (&t)[8][K / 32], const float *m, int ld, float (&out)[8])
+__device__ void frdot(const float (&acc)[K / 16][4], const float *m, int ld, float (&out)[2])
 {
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    const int r0 = 16 * (w & 3) + g, n0 = (K / 2) * (w >> 2);
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < K / 32; ++j) s = fmaf(t[r][j], m[(8 * w + r) * ld + l + 32 * j], s);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        out[r] = s;
+    for (int j = 0; j < K / 16; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        s0 = fmaf(acc[j][0], m[r0 * ld + c], fmaf(acc[j][1], m[r0 * ld + c + 1], s0));
+        s1 = fmaf(acc[j][2], m[(r0 + 8) * ld + c], fmaf(acc[j][3], m[(r0 + 8) * ld + c + 1], s1));
     }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    out[0] = s0;
+    out[1] = s1;
 }
 
+// fragment tiles dq, dk into the fp32 sums of rows t0 + r (r < rows) of [T, H, K] tensors (head hq): pairs of
+// columns by 8-byte atomic adds
+template <int K>
+__device__ void fatomic_rows(const float (&dq)[K / 16][4], const float (&dk)[K / 16][4], float *gq, float *gk,
+                             int64_t t0, int rows, int H, int hq)
+{
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    const int n0 = (K / 2) * (w >> 2);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int i = 16 * (w & 3) + g + 8 * hr;
+        if (i >= rows) continue;
+        float *pq = gq + ((size_t)(t0 + i) * H + hq) * K, *pk = gk + ((size_t)(t0 + i) * H + hq) * K;
+#pragma unroll
+        for (int j = 0; j < K / 16; ++j) {
+            const int c = n0 + 8 * j + 2 * t;
+            atomicAdd((float2 *)(pq + c), make_float2(dq[j][2 * hr], dq[j][2 * hr + 1]));
+            atomicAdd((float2 *)(pk + c), make_float2(dk[j][2 * hr], dk[j][2 * hr + 1]));
+        }
+    }
+}
 
 // The chunk (sequence n, value head hv, chunk c): k, q rows (zero past the sequence end), the
 // inclusive log-gate cumsum G and beta.  Every thread of the CTA takes part; returns the rows.
@@ -267,9 +325,9 @@ __device__ bool chunk_of_block(const BwdArgs &a, int &n, int &hv, int &c, int64_
 
 // ---- Step 1: A and P of every chunk
 template <typename DT, int K>
-__global__ void __launch_bounds__(kBThreads, 1) bwd_prep_kernel(const BwdArgs a)
+__global__ void __launch_bounds__(kBThreads, 2) bwd_prep_kernel(const BwdArgs a)
 {
-    using Lay = ChunkLayout<K>;
+    using Lay = PrepLayout<K>;
     constexpr int KP = Lay::KP;
     extern __shared__ float smem[];
     float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
@@ -279,8 +337,9 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_prep_kernel(const BwdArgs a)
     if (!chunk_of_block(a, n, hv, c, bos, len)) return;
     load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
     __syncthreads();
-    tmm<false, true, 4>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
-    tmm<false, true, 4>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    constexpr bool EX = kExactOf<DT>;
+    tmm<false, true, 4, EX, EX>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 4, EX, EX>(sP, kCP, sQ, KP, sK, KP, kBC, kBC, K, 1.f, false);
     __syncthreads();
     for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
         const int i = e / kBC, j = e - i * kBC;
@@ -303,7 +362,8 @@ template <typename DT, int K>
 __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a)
 {
     using Lay = BwdLayout<K>;
-    constexpr int KP = Lay::KP, KJ = K / 32;
+    constexpr int KP = Lay::KP;
+    constexpr bool EX = kExactOf<DT>;
     extern __shared__ float smem[];
     float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sS0 = smem + Lay::oS0, *sdS = smem + Lay::odS;
     float *sV = smem + Lay::oV, *sdO = smem + Lay::odO, *sR = smem + Lay::oR, *sD = smem + Lay::oD;
@@ -364,7 +424,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);  // gam_C / gam
 
         // ---- R = V - diag(gam) K S0, B = diag(beta) R, D = A B
-        tmm<false, false, 2>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        tmm<false, false, 2, EX>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
@@ -376,15 +436,15 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         tmm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
         // ---- dD = P^T dO + diag(gam_C / gam) K dS; this tile's part of dP = dO D^T
-        tmm<true, false, 2>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
-        tmm<false, false, 2>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
+        tmm<true, false, 2, false, EX>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 2, EX>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
             sdD[i * kVP + j] = fmaf(sRed[i], sM2[i * kVP + j], sdD[i * kVP + j]);
         }
         __syncthreads();
-        tmm<false, true, 4>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
+        tmm<false, true, 4, EX>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
         {
             float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
@@ -425,22 +485,25 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
 
         // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
         //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
-        float dq[8][KJ], dk[8][KJ], rd[8];
+        // (row dots: the two column halves of a row land in [kBC, 2 kBC) and [4 kBC, 5 kBC) for q, in
+        // [2 kBC, 3 kBC) and [5 kBC, 6 kBC) for k)
+        float dq[K / 16][4], dk[K / 16][4], rd[2];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
-        racc<K, false, true>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
-        rdot<K>(dq, sQ, KP, rd);
-        if (l == 0)
-#pragma unroll
-            for (int r = 0; r < 8; ++r) sRed[kBC + 8 * w + r] = rd[r];
-        racc<K, false, true>(dk, sD, kVP, sdS, kVP, kBV, 1.f, sRed);
-        rdot<K>(dk, sK, KP, rd);
-        if (l == 0)
-#pragma unroll
-            for (int r = 0; r < 8; ++r) sRed[2 * kBC + 8 * w + r] = rd[r];
-        racc<K, false, true>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
+        for (int j = 0; j < K / 16; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+        const int fr = 16 * (w & 3) + (l >> 2), fh = 3 * kBC * (w >> 2);
+        facc<K, false, true, EX>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
+        frdot<K>(dq, sQ, KP, rd);
+        if ((l & 3) == 0) {
+            sRed[kBC + fh + fr] = rd[0];
+            sRed[kBC + fh + fr + 8] = rd[1];
+        }
+        facc<K, false, true>(dk, sD, kVP, sdS, kVP, kBV, 1.f, sRed);
+        frdot<K>(dk, sK, KP, rd);
+        if ((l & 3) == 0) {
+            sRed[2 * kBC + fh + fr] = rd[0];
+            sRed[2 * kBC + fh + fr + 8] = rd[1];
+        }
+        facc<K, false, true>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
         {
             float sum = 0.f;
             for (int e = tid; e < K * kBV; e += kBThreads) {
@@ -452,26 +515,16 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             if (l == 0) sRed[3 * kBC + w] = sum;
         }
         // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int i = 8 * w + r;
-            if (i < rows) {
-                float *pq = a.dq + ((size_t)(t0 + i) * a.H + hq) * K, *pk = a.dk + ((size_t)(t0 + i) * a.H + hq) * K;
-#pragma unroll
-                for (int j = 0; j < KJ; ++j) {
-                    atomicAdd(pq + l + 32 * j, dq[r][j]);
-                    atomicAdd(pk + l + 32 * j, dk[r][j]);
-                }
-            }
-        }
+        fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
         __syncthreads();  // S0 is read for the last time; the row terms are in sRed
         if (tid == 0) {
             // gate terms of the state products; G_C is the last row's G (rows past the end carry g = 0),
             // so its gradient belongs to the last row of the sequence
             float gcsum = 0.f;
             for (int i = 0; i < kBC; ++i) {
-                sdG[i] += sRed[kBC + i] - sRed[2 * kBC + i];
-                gcsum += sRed[2 * kBC + i];
+                const float qd = sRed[kBC + i] + sRed[4 * kBC + i], kd = sRed[2 * kBC + i] + sRed[5 * kBC + i];
+                sdG[i] += qd - kd;
+                gcsum += kd;
             }
             for (int ww = 0; ww < kBThreads / 32; ++ww) gcsum += gamC * sRed[3 * kBC + ww];
             sdG[kBC - 1] += gcsum;
@@ -480,8 +533,8 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             sdG[rows - 1] += tail;
         }
         // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
-        tmm<true, false, 2>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
-        tmm<true, false, 2>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
+        tmm<true, false, 2, EX, false, true>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
+        tmm<true, false, 2, EX, false, true>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
         __syncthreads();
         for (int i = tid; i < rows; i += kBThreads) {
             atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], sdB[i]);
@@ -509,12 +562,13 @@ template <typename DT, int K>
 __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs a)
 {
     using Lay = ChunkLayout<K>;
-    constexpr int KP = Lay::KP, KJ = K / 32;
+    constexpr int KP = Lay::KP;
+    constexpr bool EX = kExactOf<DT>;
     extern __shared__ float smem[];
     float *sK = smem + Lay::oK, *sQ = smem + Lay::oQ, *sA = smem + Lay::oA, *sP = smem + Lay::oP;
     float *sdP = smem + Lay::odP, *sdA = smem + Lay::odA, *sT = smem + Lay::oT, *sG = smem + Lay::oG;
     float *sBeta = smem + Lay::oBeta, *sRed = smem + Lay::oRed;
-    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int tid = threadIdx.x;
     int n, hv, c;
     int64_t bos, len;
     if (!chunk_of_block(a, n, hv, c, bos, len)) return;
@@ -557,7 +611,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
     tmm<true, false, 4>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
     // K K^T -> Lraw = Gam * K K^T below the diagonal (into A's buffer: A is no longer read)
     __syncthreads();
-    tmm<false, true, 4>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 4, EX, EX>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
     __syncthreads();
     for (int e = tid; e < kBC * kBC; e += kBThreads) {
         const int i = e / kBC, j = e - i * kBC;
@@ -580,27 +634,14 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
         sRed[2 * kBC + tid] = sum;  // [128, 192): dL Lraw row sums, [192, 256): beta-weighted column sums
     }
     // dq += F K, dk += F^T Q + E K + E^T K
-    float dq[8][KJ], dk[8][KJ];
+    float dq[K / 16][4], dk[K / 16][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int j = 0; j < KJ; ++j) dq[r][j] = dk[r][j] = 0.f;
-    racc<K, false, false>(dq, sdP, kCP, sK, KP, kBC);
-    racc<K, true, false>(dk, sdP, kCP, sQ, KP, kBC);
-    racc<K, false, false>(dk, sdA, kCP, sK, KP, kBC);
-    racc<K, true, false>(dk, sdA, kCP, sK, KP, kBC);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int i = 8 * w + r;
-        if (i < rows) {
-            float *pq = a.dq + ((size_t)(t0 + i) * a.H + hq) * K, *pk = a.dk + ((size_t)(t0 + i) * a.H + hq) * K;
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) {
-                atomicAdd(pq + l + 32 * j, dq[r][j]);
-                atomicAdd(pk + l + 32 * j, dk[r][j]);
-            }
-        }
-    }
+    for (int j = 0; j < K / 16; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+    facc<K, false, false, false, EX>(dq, sdP, kCP, sK, KP, kBC);
+    facc<K, true, false, false, EX>(dk, sdP, kCP, sQ, KP, kBC);
+    facc<K, false, false, false, EX>(dk, sdA, kCP, sK, KP, kBC);
+    facc<K, true, false, false, EX>(dk, sdA, kCP, sK, KP, kBC);
+    fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
     __syncthreads();
     if (tid < rows) {
         const int i = tid;
@@ -644,13 +685,14 @@ cudaError_t launch_bwd_k(const BwdArgs &a, cudaStream_t st)
     auto prep = bwd_prep_kernel<DT, K>;
     auto scan = chunk_bwd_kernel<DT, K>;
     auto fin = bwd_finish_kernel<DT, K>;
-    const size_t sc = sizeof(float) * ChunkLayout<K>::total, ss = sizeof(float) * BwdLayout<K>::total;
-    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+    const size_t sp = sizeof(float) * PrepLayout<K>::total, sc = sizeof(float) * ChunkLayout<K>::total,
+                 ss = sizeof(float) * BwdLayout<K>::total;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
     if (e != cudaSuccess) return e;
     const dim3 gc(a.max_nt, a.N * a.HV);
-    prep<<<gc, kBThreads, sc, st>>>(a);
+    prep<<<gc, kBThreads, sp, st>>>(a);
     scan<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kBThreads, ss, st>>>(a);
     fin<<<gc, kBThreads, sc, st>>>(a);
     return cudaGetLastError();
@@ -672,7 +714,8 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st)
 cudaError_t launch_chunk_bwd(const BwdArgs &a, gdn_dtype dt, cudaStream_t st)
 {
     static_assert(sizeof(float) * BwdLayout<128>::total <= 227 * 1024 &&
-                      sizeof(float) * ChunkLayout<128>::total <= 227 * 1024,
+                      sizeof(float) * ChunkLayout<128>::total <= 227 * 1024 &&
+                      2 * (sizeof(float) * PrepLayout<128>::total + 1024) <= 228 * 1024,
                   "shared memory budget");
     if (a.N * a.HV == 0 || a.max_nt == 0) return cudaSuccess;
     cudaError_t e = dt == GDN_BF16 ? launch_bwd_t<__nv_bfloat16>(a, st) : launch_bwd_t<float>(a, st);
