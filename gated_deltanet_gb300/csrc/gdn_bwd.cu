@@ -64,6 +64,30 @@ struct ChunkLayout {  // the finish
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T *p) { return (float)*p; }
+// eight consecutive elements as fp32 (one 16-byte load for bf16, two for fp32; p 16-byte aligned), and
+// eight fp32 into shared memory (p 16-byte aligned)
+__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&f)[8])
+{
+    const uint4 u = __ldg((const uint4 *)p);
+    const __nv_bfloat162 *h = (const __nv_bfloat162 *)&u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(h[q]);
+        f[2 * q] = x.x;
+        f[2 * q + 1] = x.y;
+    }
+}
+__device__ __forceinline__ void ld8(const float *p, float (&f)[8])
+{
+    const float4 x = __ldg((const float4 *)p), y = __ldg((const float4 *)p + 1);
+    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+}
+__device__ __forceinline__ void st8(float *p, const float (&f)[8])
+{
+    *(float4 *)p = make_float4(f[0], f[1], f[2], f[3]);
+    *(float4 *)(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+}
 // bf16 inputs (k, q, v, dO) are exact in tf32: their products need no remainder term
 template <typename T>
 constexpr bool kExactOf = false;
@@ -260,16 +284,21 @@ __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int
     const int64_t t0 = bos + (int64_t)c * kBC;
     const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
     const DT *q = (const DT *)a.q, *k = (const DT *)a.k;
-    for (int e = threadIdx.x; e < kBC * K; e += kBThreads) {
-        const int i = e / K, d = e - i * K;
-        float kv = 0.f, qv = 0.f;
+    constexpr int P8 = K / 8;  // eight-element pieces of a row (rows are K * sizeof(DT) >= 64 bytes)
+#pragma unroll 4
+    for (int e = threadIdx.x; e < kBC * P8; e += kBThreads) {
+        const int i = e / P8, d8 = (e - i * P8) * 8;
+        float kv[8], qv[8];
         if (i < rows) {
-            const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d;
-            kv = ldf(k + off);
-            qv = ldf(q + off);
+            const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d8;
+            ld8(k + off, kv);
+            ld8(q + off, qv);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kv[u] = qv[u] = 0.f;
         }
-        sK[i * KP + d] = kv;
-        sQ[i * KP + d] = qv;
+        st8(sK + i * KP + d8, kv);
+        st8(sQ + i * KP + d8, qv);
     }
     if (threadIdx.x < 32) {
         const int l = threadIdx.x, r0 = 2 * l, r1 = r0 + 1;
@@ -350,10 +379,10 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_prep_kernel(const BwdArgs a)
     __syncthreads();
     unit_lower_inverse(sA, sRed);
     const size_t base = ((size_t)tile_slot(bos, n, c) * a.HV + hv) * kBC * kBC;
-    for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
-        const int i = e / kBC, j = e - i * kBC;
-        a.Abuf[base + e] = sA[i * kCP + j];
-        a.Pbuf[base + e] = sP[i * kCP + j];
+    for (int e4 = threadIdx.x; e4 < kBC * kBC / 4; e4 += kBThreads) {
+        const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
+        *(float4 *)(a.Abuf + base + 4 * e4) = *(const float4 *)(sA + i * kCP + j);
+        *(float4 *)(a.Pbuf + base + 4 * e4) = *(const float4 *)(sP + i * kCP + j);
     }
 }
 
@@ -394,28 +423,53 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         __syncthreads();
         // ---- loads (rows past the sequence end are inert zeros)
         const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
-        for (int e = tid; e < kBC * kBV; e += kBThreads) {
-            const int i = e / kBV, j = e - i * kBV, col = col0 + j;
-            float vv = 0.f, dv = 0.f;
-            if (i < rows && col < V) {
-                const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
-                vv = ldf(v + off);
-                dv = ldf(dout + off);
+        const float *src = a.chunk_states + cidx * K * V;
+        if (V % 8 == 0) {
+            // eight-column pieces: 16-byte loads (a piece is either inside the value range or past it)
+            for (int e = tid; e < kBC * (kBV / 8); e += kBThreads) {
+                const int i = e / (kBV / 8), j = (e % (kBV / 8)) * 8, col = col0 + j;
+                float vv[8], dv[8];
+                if (i < rows && col < V) {
+                    const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
+                    ld8(v + off, vv);
+                    ld8(dout + off, dv);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) vv[u] = dv[u] = 0.f;
+                }
+                st8(sV + i * kVP + j, vv);
+                st8(sdO + i * kVP + j, dv);
             }
-            sV[i * kVP + j] = vv;
-            sdO[i * kVP + j] = dv;
-        }
-        {
-            const float *src = a.chunk_states + cidx * K * V;
+#pragma unroll 4
+            for (int e = tid; e < K * (kBV / 4); e += kBThreads) {
+                const int d = e / (kBV / 4), j = (e % (kBV / 4)) * 4, col = col0 + j;
+                *(float4 *)(sS0 + d * kVP + j) =
+                    col < V ? __ldg((const float4 *)(src + (size_t)d * V + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        } else {
+            for (int e = tid; e < kBC * kBV; e += kBThreads) {
+                const int i = e / kBV, j = e - i * kBV, col = col0 + j;
+                float vv = 0.f, dv = 0.f;
+                if (i < rows && col < V) {
+                    const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
+                    vv = ldf(v + off);
+                    dv = ldf(dout + off);
+                }
+                sV[i * kVP + j] = vv;
+                sdO[i * kVP + j] = dv;
+            }
             for (int e = tid; e < K * kBV; e += kBThreads) {
                 const int d = e / kBV, j = e - d * kBV, col = col0 + j;
                 sS0[d * kVP + j] = col < V ? src[(size_t)d * V + col] : 0.f;
             }
+        }
+        {
             const float *ga = a.Abuf + cidx * kBC * kBC, *gp = a.Pbuf + cidx * kBC * kBC;
-            for (int e = tid; e < kBC * kBC; e += kBThreads) {
-                const int i = e / kBC, j = e - i * kBC;
-                sA[i * kCP + j] = ga[e];
-                sP[i * kCP + j] = gp[e];
+#pragma unroll 4
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+                const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
+                *(float4 *)(sA + i * kCP + j) = __ldg((const float4 *)ga + e4);
+                *(float4 *)(sP + i * kCP + j) = __ldg((const float4 *)gp + e4);
             }
         }
         if (tid < kBC) sdG[tid] = sdB[tid] = 0.f;
@@ -448,7 +502,8 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         __syncthreads();
         {
             float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e = tid; e < kBC * kBC; e += kBThreads) dst[e] = sM2[(e / kBC) * kCP + (e % kBC)];
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads)
+                *(float4 *)(dst + 4 * e4) = *(const float4 *)(sM2 + (e4 / (kBC / 4)) * kCP + (e4 % (kBC / 4)) * 4);
         }
         // ---- Y = A^T dD; dR = diag(beta) Y (= dv); dbeta_i += sum_v Y R, dG_i += sum_v dR (R - V)
         tmm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
@@ -477,9 +532,10 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         __syncthreads();
         {
             float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e = tid; e < kBC * kBC; e += kBThreads) {
-                const int i = e / kBC, j = e - i * kBC;
-                dst[e] = sM2[i * kCP + j] * sBeta[j];
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+                const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
+                const float4 m = *(const float4 *)(sM2 + i * kCP + j), b = *(const float4 *)(sBeta + j);
+                *(float4 *)(dst + 4 * e4) = make_float4(m.x * b.x, m.y * b.y, m.z * b.z, m.w * b.w);
             }
         }
 
@@ -577,17 +633,22 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
     const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
     const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
     const int tiles = (a.V + kBV - 1) / kBV;
-    for (int e = tid; e < kBC * kBC; e += kBThreads) {
-        const int i = e / kBC, j = e - i * kBC;
-        float dp = 0.f, da = 0.f;
+    // the value tiles' parts of dP and dA summed (16-byte loads, all of a thread's issued together)
+#pragma unroll 4
+    for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+        const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
+        float4 dp = make_float4(0.f, 0.f, 0.f, 0.f), da = dp;
+#pragma unroll 4
         for (int t = 0; t < tiles; ++t) {
-            dp += a.dPbuf[((size_t)t * a.chunk_heads + cidx) * kBC * kBC + e];
-            da += a.dAbuf[((size_t)t * a.chunk_heads + cidx) * kBC * kBC + e];
+            const float4 x = __ldg((const float4 *)(a.dPbuf + ((size_t)t * a.chunk_heads + cidx) * kBC * kBC) + e4);
+            const float4 y = __ldg((const float4 *)(a.dAbuf + ((size_t)t * a.chunk_heads + cidx) * kBC * kBC) + e4);
+            dp.x += x.x; dp.y += x.y; dp.z += x.z; dp.w += x.w;
+            da.x += y.x; da.y += y.y; da.z += y.z; da.w += y.w;
         }
-        sdP[i * kCP + j] = dp;
-        sdA[i * kCP + j] = da;
-        sA[i * kCP + j] = a.Abuf[cidx * kBC * kBC + e];
-        sP[i * kCP + j] = a.Pbuf[cidx * kBC * kBC + e];
+        *(float4 *)(sdP + i * kCP + j) = dp;
+        *(float4 *)(sdA + i * kCP + j) = da;
+        *(float4 *)(sA + i * kCP + j) = __ldg((const float4 *)(a.Abuf + cidx * kBC * kBC) + e4);
+        *(float4 *)(sP + i * kCP + j) = __ldg((const float4 *)(a.Pbuf + cidx * kBC * kBC) + e4);
     }
     __syncthreads();
     // P = scale Gam * Q K^T (i >= j): dG_i += rowsum(P dP), dG_j -= colsum(P dP); F = scale Gam * dP

@@ -116,3 +116,17 @@ def test_backward_rejects_channel_gates(gdn):
     do = torch.zeros_like(x["v"])
     with pytest.raises(gdn.GdnError):
         gdn.chunk_gated_delta_rule_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, x["scale"])
+
+
+def test_backward_rejects_misaligned_rows(gdn):
+    """q as a contiguous view four bf16 elements (8 bytes) into its buffer: the 16-byte row loads would be
+    misaligned, so the call is refused before anything is enqueued."""
+    w = Workload("bwd_mis", B=1, T=64, H=1, HV=1, K=64, V=64, seed=69)
+    x = make_inputs(w, device="cuda")
+    buf = torch.empty(x["q"].numel() + 4, dtype=x["q"].dtype, device="cuda")
+    q = buf[4:].view(x["q"].shape)
+    q.copy_(x["q"])
+    assert q.data_ptr() % 16 == 8
+    do = torch.zeros_like(x["v"])
+    with pytest.raises(gdn.GdnError):
+        gdn.chunk_gated_delta_rule_bwd(q, x["k"], x["v"], x["g"], x["beta"], do, x["scale"])
