@@ -322,22 +322,35 @@ __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int
     return rows;
 }
 
-// A = (I + L)^-1 in place (sA holds L below the diagonal, zero elsewhere), one row at a time:
-// A_i = e_i - sum_{j < i} L_ij A_j
-__device__ void unit_lower_inverse(float *sA, float *sRed)
+// A = (I + L)^-1 in place (sA holds L below the diagonal, zero elsewhere) by forward substitution per
+// column: column j solves x_i = [i == j] - sum_{k < i} L_ik x_k.  Four threads share a column, thread p
+// keeping x_k for k = p mod 4 and summing those terms; the four partial sums meet by shuffles, so no
+// barrier runs between rows.
+__device__ void unit_lower_inverse(float *sA)
 {
-    const int tid = threadIdx.x, col = tid & (kBC - 1), part = tid >> 6;
+    const int tid = threadIdx.x, j = tid >> 2, p = tid & 3;
+    float xq[kBC / 4];  // x_{4 q + p}
+#pragma unroll
+    for (int q = 0; q < kBC / 4; ++q) xq[q] = 0.f;
+#pragma unroll
     for (int i = 0; i < kBC; ++i) {
-        float s = 0.f;
-        for (int j = part; j < i; j += 4) s = fmaf(sA[i * kCP + j], sA[j * kCP + col], s);
-        sRed[part * kBC + col] = s;
-        __syncthreads();
-        if (tid < kBC) {
-            const float t = sRed[tid] + sRed[kBC + tid] + sRed[2 * kBC + tid] + sRed[3 * kBC + tid];
-            sA[i * kCP + tid] = tid < i ? -t : (tid == i ? 1.f : 0.f);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kBC / 4; ++q) {
+            if (4 * q + 3 < i || 4 * q + p < i) {  // (the first test is constant: the full groups)
+                const float v = sA[i * kCP + 4 * q + p] * xq[q];
+                if (q & 1) s1 += v; else s0 += v;
+            }
         }
-        __syncthreads();
+        float sum = s0 + s1;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (p == (i & 3)) xq[i >> 2] = (i == j ? 1.f : 0.f) - sum;
     }
+    __syncthreads();  // every thread has read L
+#pragma unroll
+    for (int q = 0; q < kBC / 4; ++q) sA[(4 * q + p) * kCP + j] = xq[q];
+    __syncthreads();
 }
 
 // (sequence, value head, chunk) of a per-chunk CTA: blockIdx.x = chunk, blockIdx.y = pair
@@ -377,7 +390,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_prep_kernel(const BwdArgs a)
         sP[i * kCP + j] = a.scale * gm * sP[i * kCP + j];
     }
     __syncthreads();
-    unit_lower_inverse(sA, sRed);
+    unit_lower_inverse(sA);
     const size_t base = ((size_t)tile_slot(bos, n, c) * a.HV + hv) * kBC * kBC;
     for (int e4 = threadIdx.x; e4 < kBC * kBC / 4; e4 += kBThreads) {
         const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
@@ -508,16 +521,25 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         // ---- Y = A^T dD; dR = diag(beta) Y (= dv); dbeta_i += sum_v Y R, dG_i += sum_v dR (R - V)
         tmm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
-        if (tid < kBC) {
-            const int i = tid;
+        {
+            // four threads per row, columns p, p + 4, ... (conflict-free), reduced over the quad
+            const int i = tid >> 2, p = tid & 3;
             float sb = 0.f, sg = 0.f;
-            for (int j = 0; j < kBV; ++j) {
+#pragma unroll
+            for (int jj = 0; jj < kBV / 4; ++jj) {
+                const int j = p + 4 * jj;
                 const float y = sY[i * kVP + j], r = sR[i * kVP + j];
                 sb = fmaf(y, r, sb);
-                sg = fmaf(sBeta[i] * y, r - sV[i * kVP + j], sg);
+                sg = fmaf(y, r - sV[i * kVP + j], sg);
             }
-            sdB[i] += sb;
-            sdG[i] += sg;
+            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+            sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+            sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+            if (p == 0) {
+                sdB[i] += sb;
+                sdG[i] += sBeta[i] * sg;
+            }
         }
         __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
@@ -573,20 +595,26 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
         fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
         __syncthreads();  // S0 is read for the last time; the row terms are in sRed
-        if (tid == 0) {
-            // gate terms of the state products; G_C is the last row's G (rows past the end carry g = 0),
-            // so its gradient belongs to the last row of the sequence
-            float gcsum = 0.f;
-            for (int i = 0; i < kBC; ++i) {
+        if (w == 0) {
+            // gate terms of the state products (lane: rows l, l + 32); G_C is the last row's G (rows past the
+            // end carry g = 0), so its gradient belongs to the last row of the sequence
+            float gcsum = l < kBThreads / 32 ? gamC * sRed[3 * kBC + l] : 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = l + 32 * h;
                 const float qd = sRed[kBC + i] + sRed[4 * kBC + i], kd = sRed[2 * kBC + i] + sRed[5 * kBC + i];
                 sdG[i] += qd - kd;
                 gcsum += kd;
             }
-            for (int ww = 0; ww < kBThreads / 32; ++ww) gcsum += gamC * sRed[3 * kBC + ww];
-            sdG[kBC - 1] += gcsum;
-            float tail = 0.f;
-            for (int i = rows; i < kBC; ++i) tail += sdG[i];
-            sdG[rows - 1] += tail;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) gcsum += __shfl_xor_sync(0xffffffffu, gcsum, off);
+            __syncwarp();
+            if (l == 0) sdG[kBC - 1] += gcsum;
+            __syncwarp();
+            float tail = (l >= rows ? sdG[l] : 0.f) + (l + 32 >= rows ? sdG[l + 32] : 0.f);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) tail += __shfl_xor_sync(0xffffffffu, tail, off);
+            if (l == 0) sdG[rows - 1] += tail;
         }
         // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
         tmm<true, false, 2, EX, false, true>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
