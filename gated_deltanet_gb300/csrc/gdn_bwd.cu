@@ -490,37 +490,30 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         const float GC = sG[kBC - 1], gamC = sGam[kBC - 1];
         if (tid < kBC) sRed[tid] = __expf(GC - sG[tid]);  // gam_C / gam
 
-        // ---- R = V - diag(gam) K S0, B = diag(beta) R, D = A B
+        // Phases between barriers (each line one phase; the products inside a phase are independent):
+        //   K S0, P^T dO, K dS | R, B = diag(beta) R, dD | D = A B, Y = A^T dD | dO D^T, row sums, dR |
+        //   dD B^T, the state terms of dq and dk | the gate terms, the dS update | the sums, dS
+        // ---- K S0 (-> R), P^T dO (-> dD), K dS (scratch)
         tmm<false, false, 2, EX>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        tmm<true, false, 2, false, EX>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 2, EX>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
+        // ---- R = V - diag(gam) K S0, B = diag(beta) R (-> Y), dD = P^T dO + diag(gam_C / gam) K dS
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
             const float r = sV[i * kVP + j] - sGam[i] * sR[i * kVP + j];
             sR[i * kVP + j] = r;
             sY[i * kVP + j] = sBeta[i] * r;
-        }
-        __syncthreads();
-        tmm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
-        __syncthreads();
-        // ---- dD = P^T dO + diag(gam_C / gam) K dS; this tile's part of dP = dO D^T
-        tmm<true, false, 2, false, EX>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
-        tmm<false, false, 2, EX>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);  // K dS (scratch)
-        __syncthreads();
-        for (int e = tid; e < kBC * kBV; e += kBThreads) {
-            const int i = e / kBV, j = e - i * kBV;
             sdD[i * kVP + j] = fmaf(sRed[i], sM2[i * kVP + j], sdD[i * kVP + j]);
         }
         __syncthreads();
-        tmm<false, true, 4, EX>(sM2, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
+        // ---- D = A B; Y2 = A^T dD (-> the scratch)
+        tmm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<true, false, 2>(sM2, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
-        {
-            float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads)
-                *(float4 *)(dst + 4 * e4) = *(const float4 *)(sM2 + (e4 / (kBC / 4)) * kCP + (e4 % (kBC / 4)) * 4);
-        }
-        // ---- Y = A^T dD; dR = diag(beta) Y (= dv); dbeta_i += sum_v Y R, dG_i += sum_v dR (R - V)
-        tmm<true, false, 2>(sY, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
-        __syncthreads();
+        // ---- this tile's part of dP = dO D^T (-> P's buffer: P is read); dbeta_i += sum_v Y2 R,
+        //      dG_i += beta_i sum_v Y2 (R - V); dR = diag(beta) Y2 (= dv, -> Y: B is read)
+        tmm<false, true, 4, EX>(sP, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
         {
             // four threads per row, columns p, p + 4, ... (conflict-free), reduced over the quad
             const int i = tid >> 2, p = tid & 3;
@@ -528,7 +521,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
 #pragma unroll
             for (int jj = 0; jj < kBV / 4; ++jj) {
                 const int j = p + 4 * jj;
-                const float y = sY[i * kVP + j], r = sR[i * kVP + j];
+                const float y = sM2[i * kVP + j], r = sR[i * kVP + j];
                 sb = fmaf(y, r, sb);
                 sg = fmaf(y, r - sV[i * kVP + j], sg);
             }
@@ -541,25 +534,21 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
                 sdG[i] += sBeta[i] * sg;
             }
         }
-        __syncthreads();
         for (int e = tid; e < kBC * kBV; e += kBThreads) {
             const int i = e / kBV, j = e - i * kBV;
-            const float dr = sBeta[i] * sY[i * kVP + j];
+            const float dr = sBeta[i] * sM2[i * kVP + j];
             sY[i * kVP + j] = dr;
             const int col = col0 + j;
             if (i < rows && col < V) a.dv[((size_t)(t0 + i) * HV + hv) * V + col] = dr;
         }
-        // this tile's part of dA = dD B^T (B = diag(beta) R: a column scale)
-        tmm<false, true, 4>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
         __syncthreads();
         {
-            float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
-                const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
-                const float4 m = *(const float4 *)(sM2 + i * kCP + j), b = *(const float4 *)(sBeta + j);
-                *(float4 *)(dst + 4 * e4) = make_float4(m.x * b.x, m.y * b.y, m.z * b.z, m.w * b.w);
-            }
+            float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads)
+                *(float4 *)(dst + 4 * e4) = *(const float4 *)(sP + (e4 / (kBC / 4)) * kCP + (e4 % (kBC / 4)) * 4);
         }
+        // ---- this tile's part of dA = dD B^T (B = diag(beta) R: a column scale; -> the scratch, Y2 is read)
+        tmm<false, true, 4>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
 
         // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
         //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
@@ -594,7 +583,15 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         }
         // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
         fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
-        __syncthreads();  // S0 is read for the last time; the row terms are in sRed
+        __syncthreads();  // S0 is read for the last time; the row terms are in sRed; dA's part is complete
+        {
+            float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+                const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
+                const float4 m = *(const float4 *)(sM2 + i * kCP + j), b = *(const float4 *)(sBeta + j);
+                *(float4 *)(dst + 4 * e4) = make_float4(m.x * b.x, m.y * b.y, m.z * b.z, m.w * b.w);
+            }
+        }
         if (w == 0) {
             // gate terms of the state products (lane: rows l, l + 32); G_C is the last row's G (rows past the
             // end carry g = 0), so its gradient belongs to the last row of the sequence
