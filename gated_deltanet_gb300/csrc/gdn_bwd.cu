@@ -33,7 +33,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kBThreads = 256;
+constexpr int kBThreads = 256;  // the per-chunk kernels
+constexpr int kRThreads = 512;  // the reverse scan (sixteen warps: every product has a block per warp)
 constexpr int kBC = 64;      // chunk
 constexpr int kBV = 32;      // value columns per CTA
 constexpr int kCP = kBC + 4;  // pitches (4 mod 32: the tensor-core fragments' strided reads hit at most
@@ -46,7 +47,7 @@ struct BwdLayout {  // the reverse kernel
                          oV = odS + K * kVP, odO = oV + kBC * kVP, oR = odO + kBC * kVP, oD = oR + kBC * kVP,
                          odD = oD + kBC * kVP, oY = odD + kBC * kVP, oA = oY + kBC * kVP, oP = oA + kBC * kCP,
                          oM2 = oP + kBC * kCP, oG = oM2 + kBC * kCP, oGam = oG + kBC, oBeta = oGam + kBC,
-                         odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC, total = oRed + 6 * kBC;
+                         odG = oBeta + kBC, odB = odG + kBC, oRed = odB + kBC, total = oRed + 12 * kBC;
 };
 template <int K>
 struct PrepLayout {  // A and P of a chunk (two CTAs per SM at K = 128)
@@ -118,13 +119,13 @@ __device__ __forceinline__ void mma_tf32x(float (&d)[4], const uint32_t (&a)[4],
 // term is left out.  A warp takes 16 x (8 NB) output blocks, NB tiles side by side sharing the A fragment
 // (NB independent accumulations in flight); M a multiple of 16, N of 8 NB, X of 8.  xs scales the
 // contraction index on A's side, or on B's with XB (so that the other operand stays exact).
-template <bool TA, bool TB, int NB, bool EA = false, bool EB = false, bool XB = false>
+template <bool TA, bool TB, int NB, bool EA = false, bool EB = false, bool XB = false, int NTH = kBThreads>
 __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b, int ldb, int M, int N, int X,
                     float alpha, bool acc, const float *xs = nullptr)
 {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
     const int bn = N / (8 * NB), blocks = (M / 16) * bn;
-    for (int blk = w; blk < blocks; blk += kBThreads / 32) {
+    for (int blk = w; blk < blocks; blk += NTH / 32) {
         const int m0 = (blk / bn) * 16, n0 = (blk % bn) * 8 * NB;
         float d[NB][4];
 #pragma unroll
@@ -177,18 +178,21 @@ __device__ void tmm(float *out, int ldo, const float *a, int lda, const float *b
     }
 }
 
-// A [kBC x K] tile in tensor-core accumulator fragments: warp w holds rows 16 (w & 3) .. + 15 and the
-// columns (K / 2)(w >> 2) .. + K / 2 - 1 as K / 16 blocks of m16n8; thread (g = lane / 4, t = lane % 4)
-// holds, in block j, rows r = 16 (w & 3) + g and r + 8 at columns c = (K / 2)(w >> 2) + 8 j + 2 t and c + 1.
+// A [kBC x K] tile in tensor-core accumulator fragments over NTH threads: the warps form 4 row groups x
+// NTH / 128 column parts; warp w holds rows 16 (w & 3) .. + 15 and the K / parts columns of part w >> 2
+// as NT = K * 16 / NTH blocks of m16n8; thread (g = lane / 4, t = lane % 4) holds, in block j, rows
+// r = 16 (w & 3) + g and r + 8 at columns c = (part start) + 8 j + 2 t and c + 1.
 // facc: acc[m][n] += alpha * rs[m] * sum_x A(m, x) B(x, n) (rs optional), split tf32 as in tmm, X a
 // multiple of 8.
-template <int K, bool TA, bool TB, bool EA = false, bool EB = false>
-__device__ void facc(float (&acc)[K / 16][4], const float *a, int lda, const float *b, int ldb, int X,
+template <int K, int NTH>
+constexpr int kFragNT = K * 16 / NTH;
+template <int K, bool TA, bool TB, bool EA = false, bool EB = false, int NTH = kBThreads>
+__device__ void facc(float (&acc)[kFragNT<K, NTH>][4], const float *a, int lda, const float *b, int ldb, int X,
                      float alpha = 1.f, const float *rs = nullptr)
 {
-    constexpr int NT = K / 16;
+    constexpr int NT = kFragNT<K, NTH>;
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
-    const int m0 = 16 * (w & 3), n0 = (K / 2) * (w >> 2);
+    const int m0 = 16 * (w & 3), n0 = 8 * NT * (w >> 2);
     float d[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
@@ -230,15 +234,16 @@ __device__ void facc(float (&acc)[K / 16][4], const float *a, int lda, const flo
 }
 
 // the warp's part of the row dot products of a fragment tile with a [kBC x K] shared-memory matrix (pitch
-// ld) over its K / 2 columns: out[0] for row 16 (w & 3) + g, out[1] for that + 8, on every lane of the quad
-template <int K>
-__device__ void frdot(const float (&acc)[K / 16][4], const float *m, int ld, float (&out)[2])
+// ld) over its columns: out[0] for row 16 (w & 3) + g, out[1] for that + 8, on every lane of the quad
+template <int K, int NTH = kBThreads>
+__device__ void frdot(const float (&acc)[kFragNT<K, NTH>][4], const float *m, int ld, float (&out)[2])
 {
+    constexpr int NT = kFragNT<K, NTH>;
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
-    const int r0 = 16 * (w & 3) + g, n0 = (K / 2) * (w >> 2);
+    const int r0 = 16 * (w & 3) + g, n0 = 8 * NT * (w >> 2);
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < K / 16; ++j) {
+    for (int j = 0; j < NT; ++j) {
         const int c = n0 + 8 * j + 2 * t;
         s0 = fmaf(acc[j][0], m[r0 * ld + c], fmaf(acc[j][1], m[r0 * ld + c + 1], s0));
         s1 = fmaf(acc[j][2], m[(r0 + 8) * ld + c], fmaf(acc[j][3], m[(r0 + 8) * ld + c + 1], s1));
@@ -253,19 +258,20 @@ __device__ void frdot(const float (&acc)[K / 16][4], const float *m, int ld, flo
 
 // fragment tiles dq, dk into the fp32 sums of rows t0 + r (r < rows) of [T, H, K] tensors (head hq): pairs of
 // columns by 8-byte atomic adds
-template <int K>
-__device__ void fatomic_rows(const float (&dq)[K / 16][4], const float (&dk)[K / 16][4], float *gq, float *gk,
-                             int64_t t0, int rows, int H, int hq)
+template <int K, int NTH = kBThreads>
+__device__ void fatomic_rows(const float (&dq)[kFragNT<K, NTH>][4], const float (&dk)[kFragNT<K, NTH>][4],
+                             float *gq, float *gk, int64_t t0, int rows, int H, int hq)
 {
+    constexpr int NT = kFragNT<K, NTH>;
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
-    const int n0 = (K / 2) * (w >> 2);
+    const int n0 = 8 * NT * (w >> 2);
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
         const int i = 16 * (w & 3) + g + 8 * hr;
         if (i >= rows) continue;
         float *pq = gq + ((size_t)(t0 + i) * H + hq) * K, *pk = gk + ((size_t)(t0 + i) * H + hq) * K;
 #pragma unroll
-        for (int j = 0; j < K / 16; ++j) {
+        for (int j = 0; j < NT; ++j) {
             const int c = n0 + 8 * j + 2 * t;
             atomicAdd((float2 *)(pq + c), make_float2(dq[j][2 * hr], dq[j][2 * hr + 1]));
             atomicAdd((float2 *)(pk + c), make_float2(dk[j][2 * hr], dk[j][2 * hr + 1]));
@@ -275,7 +281,7 @@ __device__ void fatomic_rows(const float (&dq)[K / 16][4], const float (&dk)[K /
 
 // The chunk (sequence n, value head hv, chunk c): k, q rows (zero past the sequence end), the
 // inclusive log-gate cumsum G and beta.  Every thread of the CTA takes part; returns the rows.
-template <typename DT, int K>
+template <typename DT, int K, int NTH = kBThreads>
 __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int hv, float *sK, float *sQ,
                           float *sG, float *sGam, float *sBeta)
 {
@@ -286,7 +292,7 @@ __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int
     const DT *q = (const DT *)a.q, *k = (const DT *)a.k;
     constexpr int P8 = K / 8;  // eight-element pieces of a row (rows are K * sizeof(DT) >= 64 bytes)
 #pragma unroll 4
-    for (int e = threadIdx.x; e < kBC * P8; e += kBThreads) {
+    for (int e = threadIdx.x; e < kBC * P8; e += NTH) {
         const int i = e / P8, d8 = (e - i * P8) * 8;
         float kv[8], qv[8];
         if (i < rows) {
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_prep_kernel(const BwdArgs a)
 
 // ---- Steps 3-6, the state-dependent part: one CTA per (sequence, value head, value tile), newest chunk first
 template <typename DT, int K>
-__global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a)
+__global__ void __launch_bounds__(kRThreads, 1) chunk_bwd_kernel(const BwdArgs a)
 {
     using Lay = BwdLayout<K>;
     constexpr int KP = Lay::KP;
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
     const size_t pbase = ((size_t)n * HV + hv) * K * V;
 
     // dS: the gradient with respect to the state after the last chunk (dht)
-    for (int e = tid; e < K * kBV; e += kBThreads) {
+    for (int e = tid; e < K * kBV; e += kRThreads) {
         const int d = e / kBV, j = e - d * kBV, col = col0 + j;
         sdS[d * kVP + j] = (a.dht && col < V) ? a.dht[pbase + (size_t)d * V + col] : 0.f;
     }
@@ -435,11 +441,11 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
         __syncthreads();
         // ---- loads (rows past the sequence end are inert zeros)
-        const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
+        const int rows = load_chunk<DT, K, kRThreads>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
         const float *src = a.chunk_states + cidx * K * V;
         if (V % 8 == 0) {
             // eight-column pieces: 16-byte loads (a piece is either inside the value range or past it)
-            for (int e = tid; e < kBC * (kBV / 8); e += kBThreads) {
+            for (int e = tid; e < kBC * (kBV / 8); e += kRThreads) {
                 const int i = e / (kBV / 8), j = (e % (kBV / 8)) * 8, col = col0 + j;
                 float vv[8], dv[8];
                 if (i < rows && col < V) {
@@ -454,13 +460,13 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
                 st8(sdO + i * kVP + j, dv);
             }
 #pragma unroll 4
-            for (int e = tid; e < K * (kBV / 4); e += kBThreads) {
+            for (int e = tid; e < K * (kBV / 4); e += kRThreads) {
                 const int d = e / (kBV / 4), j = (e % (kBV / 4)) * 4, col = col0 + j;
                 *(float4 *)(sS0 + d * kVP + j) =
                     col < V ? __ldg((const float4 *)(src + (size_t)d * V + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         } else {
-            for (int e = tid; e < kBC * kBV; e += kBThreads) {
+            for (int e = tid; e < kBC * kBV; e += kRThreads) {
                 const int i = e / kBV, j = e - i * kBV, col = col0 + j;
                 float vv = 0.f, dv = 0.f;
                 if (i < rows && col < V) {
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
                 sV[i * kVP + j] = vv;
                 sdO[i * kVP + j] = dv;
             }
-            for (int e = tid; e < K * kBV; e += kBThreads) {
+            for (int e = tid; e < K * kBV; e += kRThreads) {
                 const int d = e / kBV, j = e - d * kBV, col = col0 + j;
                 sS0[d * kVP + j] = col < V ? src[(size_t)d * V + col] : 0.f;
             }
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         {
             const float *ga = a.Abuf + cidx * kBC * kBC, *gp = a.Pbuf + cidx * kBC * kBC;
 #pragma unroll 4
-            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kRThreads) {
                 const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
                 *(float4 *)(sA + i * kCP + j) = __ldg((const float4 *)ga + e4);
                 *(float4 *)(sP + i * kCP + j) = __ldg((const float4 *)gp + e4);
@@ -494,12 +500,12 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         //   K S0, P^T dO, K dS | R, B = diag(beta) R, dD | D = A B, Y = A^T dD | dO D^T, row sums, dR |
         //   dD B^T, the state terms of dq and dk | the gate terms, the dS update | the sums, dS
         // ---- K S0 (-> R), P^T dO (-> dD), K dS (scratch)
-        tmm<false, false, 2, EX>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
-        tmm<true, false, 2, false, EX>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
-        tmm<false, false, 2, EX>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);
+        tmm<false, false, 1, EX, false, false, kRThreads>(sR, kVP, sK, KP, sS0, kVP, kBC, kBV, K, 1.f, false);
+        tmm<true, false, 1, false, EX, false, kRThreads>(sdD, kVP, sP, kCP, sdO, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 1, EX, false, false, kRThreads>(sM2, kVP, sK, KP, sdS, kVP, kBC, kBV, K, 1.f, false);
         __syncthreads();
         // ---- R = V - diag(gam) K S0, B = diag(beta) R (-> Y), dD = P^T dO + diag(gam_C / gam) K dS
-        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+        for (int e = tid; e < kBC * kBV; e += kRThreads) {
             const int i = e / kBV, j = e - i * kBV;
             const float r = sV[i * kVP + j] - sGam[i] * sR[i * kVP + j];
             sR[i * kVP + j] = r;
@@ -508,33 +514,35 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         }
         __syncthreads();
         // ---- D = A B; Y2 = A^T dD (-> the scratch)
-        tmm<false, false, 2>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
-        tmm<true, false, 2>(sM2, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<false, false, 1, false, false, false, kRThreads>(sD, kVP, sA, kCP, sY, kVP, kBC, kBV, kBC, 1.f, false);
+        tmm<true, false, 1, false, false, false, kRThreads>(sM2, kVP, sA, kCP, sdD, kVP, kBC, kBV, kBC, 1.f, false);
         __syncthreads();
         // ---- this tile's part of dP = dO D^T (-> P's buffer: P is read); dbeta_i += sum_v Y2 R,
         //      dG_i += beta_i sum_v Y2 (R - V); dR = diag(beta) Y2 (= dv, -> Y: B is read)
-        tmm<false, true, 4, EX>(sP, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
+        tmm<false, true, 2, EX, false, false, kRThreads>(sP, kCP, sdO, kVP, sD, kVP, kBC, kBC, kBV, 1.f, false);
         {
-            // four threads per row, columns p, p + 4, ... (conflict-free), reduced over the quad
-            const int i = tid >> 2, p = tid & 3;
+            // kRThreads / 64 threads per row, columns p, p + that, ..., reduced over the group
+            constexpr int TR = kRThreads / kBC;
+            const int i = tid / TR, p = tid % TR;
             float sb = 0.f, sg = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < kBV / 4; ++jj) {
-                const int j = p + 4 * jj;
+            for (int jj = 0; jj < kBV / TR; ++jj) {
+                const int j = p + TR * jj;
                 const float y = sM2[i * kVP + j], r = sR[i * kVP + j];
                 sb = fmaf(y, r, sb);
                 sg = fmaf(y, r - sV[i * kVP + j], sg);
             }
-            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-            sb += __shfl_xor_sync(0xffffffffu, sb, 2);
-            sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-            sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+#pragma unroll
+            for (int off = 1; off < TR; off <<= 1) {
+                sb += __shfl_xor_sync(0xffffffffu, sb, off);
+                sg += __shfl_xor_sync(0xffffffffu, sg, off);
+            }
             if (p == 0) {
                 sdB[i] += sb;
                 sdG[i] += sBeta[i] * sg;
             }
         }
-        for (int e = tid; e < kBC * kBV; e += kBThreads) {
+        for (int e = tid; e < kBC * kBV; e += kRThreads) {
             const int i = e / kBV, j = e - i * kBV;
             const float dr = sBeta[i] * sM2[i * kVP + j];
             sY[i * kVP + j] = dr;
@@ -544,36 +552,36 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         __syncthreads();
         {
             float *dst = a.dPbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads)
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kRThreads)
                 *(float4 *)(dst + 4 * e4) = *(const float4 *)(sP + (e4 / (kBC / 4)) * kCP + (e4 % (kBC / 4)) * 4);
         }
         // ---- this tile's part of dA = dD B^T (B = diag(beta) R: a column scale; -> the scratch, Y2 is read)
-        tmm<false, true, 4>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
+        tmm<false, true, 2, false, false, false, kRThreads>(sM2, kCP, sdD, kVP, sR, kVP, kBC, kBC, kBV, 1.f, false);
 
         // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
         //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
-        // (row dots: the two column halves of a row land in [kBC, 2 kBC) and [4 kBC, 5 kBC) for q, in
-        // [2 kBC, 3 kBC) and [5 kBC, 6 kBC) for k)
-        float dq[K / 16][4], dk[K / 16][4], rd[2];
+        // (row dots: column part p of a row lands at kBC + 3 kBC p for q, at 2 kBC + 3 kBC p for k)
+        constexpr int NT = kFragNT<K, kRThreads>, NP = kRThreads / 128;
+        float dq[NT][4], dk[NT][4], rd[2];
 #pragma unroll
-        for (int j = 0; j < K / 16; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+        for (int j = 0; j < NT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
         const int fr = 16 * (w & 3) + (l >> 2), fh = 3 * kBC * (w >> 2);
-        facc<K, false, true, EX>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
-        frdot<K>(dq, sQ, KP, rd);
+        facc<K, false, true, EX, false, kRThreads>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
+        frdot<K, kRThreads>(dq, sQ, KP, rd);
         if ((l & 3) == 0) {
             sRed[kBC + fh + fr] = rd[0];
             sRed[kBC + fh + fr + 8] = rd[1];
         }
-        facc<K, false, true>(dk, sD, kVP, sdS, kVP, kBV, 1.f, sRed);
-        frdot<K>(dk, sK, KP, rd);
+        facc<K, false, true, false, false, kRThreads>(dk, sD, kVP, sdS, kVP, kBV, 1.f, sRed);
+        frdot<K, kRThreads>(dk, sK, KP, rd);
         if ((l & 3) == 0) {
             sRed[2 * kBC + fh + fr] = rd[0];
             sRed[2 * kBC + fh + fr + 8] = rd[1];
         }
-        facc<K, false, true>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
+        facc<K, false, true, false, false, kRThreads>(dk, sY, kVP, sS0, kVP, kBV, -1.f, sGam);
         {
             float sum = 0.f;
-            for (int e = tid; e < K * kBV; e += kBThreads) {
+            for (int e = tid; e < K * kBV; e += kRThreads) {
                 const int d = e / kBV, j = e - d * kBV;
                 sum = fmaf(sdS[d * kVP + j], sS0[d * kVP + j], sum);
             }
@@ -582,11 +590,11 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             if (l == 0) sRed[3 * kBC + w] = sum;
         }
         // this chunk's dq, dk into the sums over value tiles (and a GVA group's value heads)
-        fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
+        fatomic_rows<K, kRThreads>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
         __syncthreads();  // S0 is read for the last time; the row terms are in sRed; dA's part is complete
         {
             float *dst = a.dAbuf + ((size_t)vt * a.chunk_heads + cidx) * kBC * kBC;
-            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+            for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kRThreads) {
                 const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
                 const float4 m = *(const float4 *)(sM2 + i * kCP + j), b = *(const float4 *)(sBeta + j);
                 *(float4 *)(dst + 4 * e4) = make_float4(m.x * b.x, m.y * b.y, m.z * b.z, m.w * b.w);
@@ -595,11 +603,16 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
         if (w == 0) {
             // gate terms of the state products (lane: rows l, l + 32); G_C is the last row's G (rows past the
             // end carry g = 0), so its gradient belongs to the last row of the sequence
-            float gcsum = l < kBThreads / 32 ? gamC * sRed[3 * kBC + l] : 0.f;
+            float gcsum = l < kRThreads / 32 ? gamC * sRed[3 * kBC + l] : 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int i = l + 32 * h;
-                const float qd = sRed[kBC + i] + sRed[4 * kBC + i], kd = sRed[2 * kBC + i] + sRed[5 * kBC + i];
+                float qd = 0.f, kd = 0.f;
+#pragma unroll
+                for (int pp = 0; pp < NP; ++pp) {
+                    qd += sRed[kBC + 3 * kBC * pp + i];
+                    kd += sRed[2 * kBC + 3 * kBC * pp + i];
+                }
                 sdG[i] += qd - kd;
                 gcsum += kd;
             }
@@ -614,14 +627,14 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
             if (l == 0) sdG[rows - 1] += tail;
         }
         // ---- Step 4: dS <- gam_C dS + scale Q^T diag(gam) dO - K^T diag(gam) dR (into S0's buffer)
-        tmm<true, false, 2, EX, false, true>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
-        tmm<true, false, 2, EX, false, true>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
+        tmm<true, false, 2, EX, false, true, kRThreads>(sS0, kVP, sQ, KP, sdO, kVP, K, kBV, kBC, scale, false, sGam);
+        tmm<true, false, 2, EX, false, true, kRThreads>(sS0, kVP, sK, KP, sY, kVP, K, kBV, kBC, -1.f, true, sGam);
         __syncthreads();
-        for (int i = tid; i < rows; i += kBThreads) {
+        for (int i = tid; i < rows; i += kRThreads) {
             atomicAdd(&a.dbeta[(size_t)(t0 + i) * HV + hv], sdB[i]);
             atomicAdd(&a.dG[(size_t)(t0 + i) * HV + hv], sdG[i]);
         }
-        for (int e = tid; e < K * kBV; e += kBThreads) {
+        for (int e = tid; e < K * kBV; e += kRThreads) {
             const int d = e / kBV, j = e - d * kBV;
             sS0[d * kVP + j] = fmaf(gamC, sdS[d * kVP + j], sS0[d * kVP + j]);
         }
@@ -631,7 +644,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chunk_bwd_kernel(const BwdArgs a
     }
     __syncthreads();
     if (a.dh0) {
-        for (int e = tid; e < K * kBV; e += kBThreads) {
+        for (int e = tid; e < K * kBV; e += kRThreads) {
             const int d = e / kBV, j = e - d * kBV, col = col0 + j;
             if (col < V) a.dh0[pbase + (size_t)d * V + col] = sdS[d * kVP + j];
         }
@@ -779,7 +792,7 @@ cudaError_t launch_bwd_k(const BwdArgs &a, cudaStream_t st)
     if (e != cudaSuccess) return e;
     const dim3 gc(a.max_nt, a.N * a.HV);
     prep<<<gc, kBThreads, sp, st>>>(a);
-    scan<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kBThreads, ss, st>>>(a);
+    scan<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kRThreads, ss, st>>>(a);
     fin<<<gc, kBThreads, sc, st>>>(a);
     return cudaGetLastError();
 }
