@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(kRThreads, 1) chunk_bwd_kernel(const BwdArgs a
 
 // ---- Steps 5-6, the state-independent part: one CTA per chunk and value head, after the reverse scan
 template <typename DT, int K>
-__global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs a)
+__global__ void __launch_bounds__(kRThreads, 1) bwd_finish_kernel(const BwdArgs a)
 {
     using Lay = ChunkLayout<K>;
     constexpr int KP = Lay::KP;
@@ -669,11 +669,11 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
     const int HV = a.HV, hq = hv / (HV / a.H);
     const int64_t t0 = bos + (int64_t)c * kBC;
     const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
-    const int rows = load_chunk<DT, K>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
+    const int rows = load_chunk<DT, K, kRThreads>(a, bos, len, c, hv, sK, sQ, sG, nullptr, sBeta);
     const int tiles = (a.V + kBV - 1) / kBV;
     // the value tiles' parts of dP and dA summed (16-byte loads, all of a thread's issued together)
 #pragma unroll 4
-    for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kBThreads) {
+    for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kRThreads) {
         const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
         float4 dp = make_float4(0.f, 0.f, 0.f, 0.f), da = dp;
 #pragma unroll 4
@@ -700,19 +700,19 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
         sRed[tid] = sum;  // [0, 64): rows, [64, 128): columns
     }
     __syncthreads();
-    for (int e = tid; e < kBC * kBC; e += kBThreads) {
+    for (int e = tid; e < kBC * kBC; e += kRThreads) {
         const int i = e / kBC, j = e - i * kBC;
         sdP[i * kCP + j] = i >= j ? a.scale * __expf(sG[i] - sG[j]) * sdP[i * kCP + j] : 0.f;  // F
     }
     // dL = -A^T (dA A^T)
-    tmm<false, true, 4>(sT, kCP, sdA, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
+    tmm<false, true, 2, false, false, false, kRThreads>(sT, kCP, sdA, kCP, sA, kCP, kBC, kBC, kBC, 1.f, false);
     __syncthreads();
-    tmm<true, false, 4>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
+    tmm<true, false, 2, false, false, false, kRThreads>(sdA, kCP, sA, kCP, sT, kCP, kBC, kBC, kBC, -1.f, false);
     // K K^T -> Lraw = Gam * K K^T below the diagonal (into A's buffer: A is no longer read)
     __syncthreads();
-    tmm<false, true, 4, EX, EX>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
+    tmm<false, true, 2, EX, EX, false, kRThreads>(sA, kCP, sK, KP, sK, KP, kBC, kBC, K, 1.f, false);
     __syncthreads();
-    for (int e = tid; e < kBC * kBC; e += kBThreads) {
+    for (int e = tid; e < kBC * kBC; e += kRThreads) {
         const int i = e / kBC, j = e - i * kBC;
         const float gm = i > j ? __expf(sG[i] - sG[j]) : 0.f;
         const float lraw = gm * sA[i * kCP + j];
@@ -733,14 +733,15 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_finish_kernel(const BwdArgs 
         sRed[2 * kBC + tid] = sum;  // [128, 192): dL Lraw row sums, [192, 256): beta-weighted column sums
     }
     // dq += F K, dk += F^T Q + E K + E^T K
-    float dq[K / 16][4], dk[K / 16][4];
+    constexpr int NT = kFragNT<K, kRThreads>;
+    float dq[NT][4], dk[NT][4];
 #pragma unroll
-    for (int j = 0; j < K / 16; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
-    facc<K, false, false, false, EX>(dq, sdP, kCP, sK, KP, kBC);
-    facc<K, true, false, false, EX>(dk, sdP, kCP, sQ, KP, kBC);
-    facc<K, false, false, false, EX>(dk, sdA, kCP, sK, KP, kBC);
-    facc<K, true, false, false, EX>(dk, sdA, kCP, sK, KP, kBC);
-    fatomic_rows<K>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
+    for (int j = 0; j < NT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+    facc<K, false, false, false, EX, kRThreads>(dq, sdP, kCP, sK, KP, kBC);
+    facc<K, true, false, false, EX, kRThreads>(dk, sdP, kCP, sQ, KP, kBC);
+    facc<K, false, false, false, EX, kRThreads>(dk, sdA, kCP, sK, KP, kBC);
+    facc<K, true, false, false, EX, kRThreads>(dk, sdA, kCP, sK, KP, kBC);
+    fatomic_rows<K, kRThreads>(dq, dk, a.dq, a.dk, t0, rows, a.H, hq);
     __syncthreads();
     if (tid < rows) {
         const int i = tid;
@@ -793,7 +794,7 @@ cudaError_t launch_bwd_k(const BwdArgs &a, cudaStream_t st)
     const dim3 gc(a.max_nt, a.N * a.HV);
     prep<<<gc, kBThreads, sp, st>>>(a);
     scan<<<dim3(ceil_div(a.V, kBV), a.N * a.HV), kRThreads, ss, st>>>(a);
-    fin<<<gc, kBThreads, sc, st>>>(a);
+    fin<<<gc, kRThreads, sc, st>>>(a);
     return cudaGetLastError();
 }
 
