@@ -561,10 +561,10 @@ __global__ void __launch_bounds__(kRThreads, 1) chunk_bwd_kernel(const BwdArgs a
         // ---- state terms: dq += scale diag(gam) dO S0^T (dG_i += q_i . that), dk += diag(gam_C / gam) D dS^T
         //      (dG_C += k_j . that, dG_j -= k_j . that), dk -= diag(gam) dR S0^T, dG_C += gam_C <dS, S0>
         // (row dots: column part p of a row lands at kBC + 3 kBC p for q, at 2 kBC + 3 kBC p for k)
-        constexpr int NT = kFragNT<K, kRThreads>, NP = kRThreads / 128;
-        float dq[NT][4], dk[NT][4], rd[2];
+        constexpr int FNT = kFragNT<K, kRThreads>, NP = kRThreads / 128;
+        float dq[FNT][4], dk[FNT][4], rd[2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+        for (int j = 0; j < FNT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
         const int fr = 16 * (w & 3) + (l >> 2), fh = 3 * kBC * (w >> 2);
         facc<K, false, true, EX, false, kRThreads>(dq, sdO, kVP, sS0, kVP, kBV, scale, sGam);
         frdot<K, kRThreads>(dq, sQ, KP, rd);
@@ -733,10 +733,10 @@ __global__ void __launch_bounds__(kRThreads, 1) bwd_finish_kernel(const BwdArgs 
         sRed[2 * kBC + tid] = sum;  // [128, 192): dL Lraw row sums, [192, 256): beta-weighted column sums
     }
     // dq += F K, dk += F^T Q + E K + E^T K
-    constexpr int NT = kFragNT<K, kRThreads>;
-    float dq[NT][4], dk[NT][4];
+    constexpr int FNT = kFragNT<K, kRThreads>;
+    float dq[FNT][4], dk[FNT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
+    for (int j = 0; j < FNT; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
     facc<K, false, false, false, EX, kRThreads>(dq, sdP, kCP, sK, KP, kBC);
     facc<K, true, false, false, EX, kRThreads>(dk, sdP, kCP, sQ, KP, kBC);
     facc<K, false, false, false, EX, kRThreads>(dk, sdA, kCP, sK, KP, kBC);
