@@ -621,10 +621,11 @@ gdn_status gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const
     const int64_t tokens = (int64_t)s->B * s->T;
     if (tokens > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dbeta || !dg))
         return GDN_ERR_INVALID;
-    // rows of q, k, v and dO are read by 16-byte loads, dq and dk summed in column pairs by 8-byte atomics
+    // rows of q, k, v and dO are read by 16-byte loads, dq and dk summed four columns at a time by 16-byte
+    // atomics
     auto aligned = [](const void *p, uintptr_t m) { return ((uintptr_t)p & (m - 1)) == 0; };
     if (tokens > 0 && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) ||
-                       !aligned(dq, 8) || !aligned(dk, 8)))
+                       !aligned(dq, 16) || !aligned(dk, 16)))
         return GDN_ERR_INVALID;
     const int N = s->num_seqs;
     cudaStream_t cs = (cudaStream_t)stream;

@@ -256,8 +256,8 @@ __device__ void frdot(const float (&acc)[kFragNT<K, NTH>][4], const float *m, in
     out[1] = s1;
 }
 
-// fragment tiles dq, dk into the fp32 sums of rows t0 + r (r < rows) of [T, H, K] tensors (head hq): pairs of
-// columns by 8-byte atomic adds
+// fragment tiles dq, dk into the fp32 sums of rows t0 + r (r < rows) of [T, H, K] tensors (head hq): four
+// columns by one 16-byte atomic add
 template <int K, int NTH = kBThreads>
 __device__ void fatomic_rows(const float (&dq)[kFragNT<K, NTH>][4], const float (&dk)[kFragNT<K, NTH>][4],
                              float *gq, float *gk, int64_t t0, int rows, int H, int hq)
@@ -265,16 +265,22 @@ __device__ void fatomic_rows(const float (&dq)[kFragNT<K, NTH>][4], const float 
     constexpr int NT = kFragNT<K, NTH>;
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
     const int n0 = 8 * NT * (w >> 2);
+    // lanes t and t ^ 1 trade halves: the even one gathers four columns of row r0 = 16 (w & 3) + g, the odd
+    // one four columns of r0 + 8, and each adds them by one 16-byte atomic
+    const bool odd = t & 1;
+    const int i = 16 * (w & 3) + g + (odd ? 8 : 0);
+    const bool live = i < rows;
+    float *pq = gq + ((size_t)(t0 + i) * H + hq) * K, *pk = gk + ((size_t)(t0 + i) * H + hq) * K;
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int i = 16 * (w & 3) + g + 8 * hr;
-        if (i >= rows) continue;
-        float *pq = gq + ((size_t)(t0 + i) * H + hq) * K, *pk = gk + ((size_t)(t0 + i) * H + hq) * K;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int c = n0 + 8 * j + 2 * t;
-            atomicAdd((float2 *)(pq + c), make_float2(dq[j][2 * hr], dq[j][2 * hr + 1]));
-            atomicAdd((float2 *)(pk + c), make_float2(dk[j][2 * hr], dk[j][2 * hr + 1]));
+    for (int j = 0; j < NT; ++j) {
+        const float q0 = __shfl_xor_sync(0xffffffffu, odd ? dq[j][0] : dq[j][2], 1);
+        const float q1 = __shfl_xor_sync(0xffffffffu, odd ? dq[j][1] : dq[j][3], 1);
+        const float k0 = __shfl_xor_sync(0xffffffffu, odd ? dk[j][0] : dk[j][2], 1);
+        const float k1 = __shfl_xor_sync(0xffffffffu, odd ? dk[j][1] : dk[j][3], 1);
+        const int c = n0 + 8 * j + 4 * (t >> 1);
+        if (live) {
+            atomicAdd((float4 *)(pq + c), odd ? make_float4(q0, q1, dq[j][2], dq[j][3]) : make_float4(dq[j][0], dq[j][1], q0, q1));
+            atomicAdd((float4 *)(pk + c), odd ? make_float4(k0, k1, dk[j][2], dk[j][3]) : make_float4(dk[j][0], dk[j][1], k0, k1));
         }
     }
 }
@@ -324,6 +330,120 @@ __device__ int load_chunk(const BwdArgs &a, int64_t bos, int64_t len, int c, int
         }
         sBeta[r0] = r0 < rows ? a.beta[(size_t)(t0 + r0) * HV + hv] : 0.f;
         sBeta[r1] = r1 < rows ? a.beta[(size_t)(t0 + r1) * HV + hv] : 0.f;
+    }
+    return rows;
+}
+
+// One reverse step's inputs with every global load issued before the first shared-memory store (one
+// memory round trip): the chunk's k, q rows and gates, the value tile's v and dO columns and state rows,
+// A and P.  V a multiple of 8.  Returns the rows.
+template <typename DT, int K>
+__device__ int load_step(const BwdArgs &a, int64_t bos, int64_t len, int c, int hv, int col0, size_t cidx,
+                         float *sK, float *sQ, float *sG, float *sGam, float *sBeta, float *sV, float *sdO,
+                         float *sS0, float *sA, float *sP)
+{
+    constexpr int KP = K + 4, P8 = K / 8, NTH = kRThreads;
+    constexpr int KQI = (kBC * P8 + NTH - 1) / NTH, VI = (kBC * (kBV / 8) + NTH - 1) / NTH,
+                  SI = (K * (kBV / 4) + NTH - 1) / NTH, AI = (kBC * kBC / 4 + NTH - 1) / NTH;
+    const int tid = threadIdx.x, HV = a.HV, V = a.V, hq = hv / (HV / a.H);
+    const int64_t t0 = bos + (int64_t)c * kBC;
+    const int rows = (int)min((int64_t)kBC, len - (int64_t)c * kBC);
+    const DT *q = (const DT *)a.q, *k = (const DT *)a.k, *v = (const DT *)a.v, *dout = (const DT *)a.dout;
+    float kv[KQI][8], qv[KQI][8], vv[VI][8], dv[VI][8];
+    float4 s4[SI], a4[AI], p4[AI];
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < KQI; ++u) {
+        const int e = tid + u * NTH, i = e / P8, d8 = (e % P8) * 8;
+        if (e < kBC * P8 && i < rows) {
+            const size_t off = ((size_t)(t0 + i) * a.H + hq) * K + d8;
+            ld8(k + off, kv[u]);
+            ld8(q + off, qv[u]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) kv[u][x] = qv[u][x] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < VI; ++u) {
+        const int e = tid + u * NTH, i = e / (kBV / 8), j = (e % (kBV / 8)) * 8, col = col0 + j;
+        if (e < kBC * (kBV / 8) && i < rows && col < V) {
+            const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
+            ld8(v + off, vv[u]);
+            ld8(dout + off, dv[u]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) vv[u][x] = dv[u][x] = 0.f;
+        }
+    }
+    const float *src = a.chunk_states + cidx * K * V;
+#pragma unroll
+    for (int u = 0; u < SI; ++u) {
+        const int e = tid + u * NTH, d = e / (kBV / 4), j = (e % (kBV / 4)) * 4, col = col0 + j;
+        s4[u] = (e < K * (kBV / 4) && col < V) ? __ldg((const float4 *)(src + (size_t)d * V + col)) : z4;
+    }
+    const float4 *ga = (const float4 *)(a.Abuf + cidx * kBC * kBC), *gp = (const float4 *)(a.Pbuf + cidx * kBC * kBC);
+#pragma unroll
+    for (int u = 0; u < AI; ++u) {
+        const int e = tid + u * NTH;
+        a4[u] = e < kBC * kBC / 4 ? __ldg(ga + e) : z4;
+        p4[u] = e < kBC * kBC / 4 ? __ldg(gp + e) : z4;
+    }
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    const int l = tid & 31, r0 = 2 * l, r1 = r0 + 1;
+    if (tid < 32) {
+        if (r0 < rows) {
+            g0 = a.g[(size_t)(t0 + r0) * HV + hv];
+            b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
+        }
+        if (r1 < rows) {
+            g1 = a.g[(size_t)(t0 + r1) * HV + hv];
+            b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
+        }
+    }
+    // ---- stores
+#pragma unroll
+    for (int u = 0; u < KQI; ++u) {
+        const int e = tid + u * NTH, i = e / P8, d8 = (e % P8) * 8;
+        if (e < kBC * P8) {
+            st8(sK + i * KP + d8, kv[u]);
+            st8(sQ + i * KP + d8, qv[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < VI; ++u) {
+        const int e = tid + u * NTH, i = e / (kBV / 8), j = (e % (kBV / 8)) * 8;
+        if (e < kBC * (kBV / 8)) {
+            st8(sV + i * kVP + j, vv[u]);
+            st8(sdO + i * kVP + j, dv[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < SI; ++u) {
+        const int e = tid + u * NTH, d = e / (kBV / 4), j = (e % (kBV / 4)) * 4;
+        if (e < K * (kBV / 4)) *(float4 *)(sS0 + d * kVP + j) = s4[u];
+    }
+#pragma unroll
+    for (int u = 0; u < AI; ++u) {
+        const int e = tid + u * NTH, i = e / (kBC / 4), j = (e % (kBC / 4)) * 4;
+        if (e < kBC * kBC / 4) {
+            *(float4 *)(sA + i * kCP + j) = a4[u];
+            *(float4 *)(sP + i * kCP + j) = p4[u];
+        }
+    }
+    if (tid < 32) {
+        float sp = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sp, off);
+            if (l >= off) sp += y;
+        }
+        sG[r0] = sp - g1;
+        sG[r1] = sp;
+        sGam[r0] = __expf(sp - g1);
+        sGam[r1] = __expf(sp);
+        sBeta[r0] = b0;
+        sBeta[r1] = b1;
     }
     return rows;
 }
@@ -441,31 +561,12 @@ __global__ void __launch_bounds__(kRThreads, 1) chunk_bwd_kernel(const BwdArgs a
         const size_t cidx = (size_t)tile_slot(bos, n, c) * HV + hv;
         __syncthreads();
         // ---- loads (rows past the sequence end are inert zeros)
-        const int rows = load_chunk<DT, K, kRThreads>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
-        const float *src = a.chunk_states + cidx * K * V;
+        int rows;
         if (V % 8 == 0) {
-            // eight-column pieces: 16-byte loads (a piece is either inside the value range or past it)
-            for (int e = tid; e < kBC * (kBV / 8); e += kRThreads) {
-                const int i = e / (kBV / 8), j = (e % (kBV / 8)) * 8, col = col0 + j;
-                float vv[8], dv[8];
-                if (i < rows && col < V) {
-                    const size_t off = ((size_t)(t0 + i) * HV + hv) * V + col;
-                    ld8(v + off, vv);
-                    ld8(dout + off, dv);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) vv[u] = dv[u] = 0.f;
-                }
-                st8(sV + i * kVP + j, vv);
-                st8(sdO + i * kVP + j, dv);
-            }
-#pragma unroll 4
-            for (int e = tid; e < K * (kBV / 4); e += kRThreads) {
-                const int d = e / (kBV / 4), j = (e % (kBV / 4)) * 4, col = col0 + j;
-                *(float4 *)(sS0 + d * kVP + j) =
-                    col < V ? __ldg((const float4 *)(src + (size_t)d * V + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            rows = load_step<DT, K>(a, bos, len, c, hv, col0, cidx, sK, sQ, sG, sGam, sBeta, sV, sdO, sS0, sA, sP);
         } else {
+            rows = load_chunk<DT, K, kRThreads>(a, bos, len, c, hv, sK, sQ, sG, sGam, sBeta);
+            const float *src = a.chunk_states + cidx * K * V;
             for (int e = tid; e < kBC * kBV; e += kRThreads) {
                 const int i = e / kBV, j = e - i * kBV, col = col0 + j;
                 float vv = 0.f, dv = 0.f;
@@ -481,10 +582,7 @@ __global__ void __launch_bounds__(kRThreads, 1) chunk_bwd_kernel(const BwdArgs a
                 const int d = e / kBV, j = e - d * kBV, col = col0 + j;
                 sS0[d * kVP + j] = col < V ? src[(size_t)d * V + col] : 0.f;
             }
-        }
-        {
             const float *ga = a.Abuf + cidx * kBC * kBC, *gp = a.Pbuf + cidx * kBC * kBC;
-#pragma unroll 4
             for (int e4 = tid; e4 < kBC * kBC / 4; e4 += kRThreads) {
                 const int i = e4 / (kBC / 4), j = (e4 % (kBC / 4)) * 4;
                 *(float4 *)(sA + i * kCP + j) = __ldg((const float4 *)ga + e4);

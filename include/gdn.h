@@ -306,8 +306,8 @@ gdn_status gdn_recurrent_fwd(const gdn_shape *s,
  *     dh0    [N,HV,K,V]  (nullable: not written)
  * The caller owns every buffer; the library-managed workspace of `stream` holds
  * the recomputed states (4 K V bytes per chunk and value head) and a gate buffer.
- * q, k, v and dout must be 16-byte aligned (rows are read by 16-byte loads) and
- * dq, dk 8-byte aligned (pairs of columns are added by 8-byte atomics).
+ * q, k, v, dout, dq and dk must be 16-byte aligned (rows are read by 16-byte loads,
+ * four columns of dq and dk added by one 16-byte atomic).
  * Errors: GDN_ERR_INVALID (arguments, a null required pointer, a misaligned one),
  * GDN_ERR_UNSUPPORTED (per-channel gates, chunk_size != 64, K not 32/64/128),
  * GDN_ERR_NOMEM, GDN_ERR_CUDA; nothing is enqueued on an argument error.
