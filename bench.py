@@ -220,6 +220,15 @@ def run_ours(args):
     N = x["N"]
     tokens = int(x["q"].shape[0] * x["q"].shape[1])
     opts = bench_options(w)
+    if args.activations:
+        # the same step from raw inputs with the activations inside the kernels: the gate input x with
+        # -exp(A_log) softplus(x + dt_bias) = g (A_log = dt_bias = 0), beta as logits, q and k
+        # L2-normalised in the kernels (they are unit vectors already: the work is the same)
+        x["g"] = torch.log(torch.expm1(-x["g"].double())).float().contiguous()
+        x["beta"] = torch.log(x["beta"] / (1.0 - x["beta"])).contiguous()
+        zeros = torch.zeros(w.hv if w.gate == "scalar" else w.hv * w.K, dtype=torch.float32, device=dev)
+        opts = dict(max_seq_len=opts["max_seq_len"], gate_A_log=torch.zeros(w.hv, dtype=torch.float32, device=dev),
+                    gate_dt_bias=zeros, beta_logits=True, qk_l2norm=True)
     info = gdn.plan(int(x["q"].shape[0]), int(x["q"].shape[1]), w.H, w.hv, w.K, w.V, w.dtype, w.gate,
                     num_seqs=N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count, **opts)
     o = torch.empty_like(x["v"])
@@ -317,6 +326,8 @@ def run_ours(args):
         "config": {"workload": w.name, "B": int(x["q"].shape[0]), "T": int(x["q"].shape[1]), "H": w.H,
                    "HV": w.hv, "dk": w.K, "dv": w.V, "chunk": w.chunk, "gate": w.gate, "h0": w.h0,
                    "sequences": N, "l2": "flushed (512 MiB write) before every timed step",
+                   "activations": ("in the kernels: gate -exp(A_log) softplus(x + dt_bias), sigmoid(beta), "
+                                   "L2 norm of q and k") if args.activations else "none (inputs as given)",
                    "plan": {"engine": ENGINE_NAMES[info.engine],
                             "cp": ["auto", "off", "exact", "warmup"][info.cp_mode],
                             "segments": info.segments, "kernels": info.kernels},
@@ -331,7 +342,9 @@ def run_ours(args):
                               "its launch time); whole_forward_frac, step: every kernel of the forward",
                      "dominant_kernel_frac": achieved / peaks["hbm_gbs"],
                      "whole_forward_frac": step_achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic(w.name, KERNEL_KEYS[names[dom]]) if names[dom] in KERNEL_KEYS else None,
+                     # (the committed captures are of the instances without in-kernel activations)
+                     "traffic": (ncu_traffic(w.name, KERNEL_KEYS[names[dom]])
+                                 if names[dom] in KERNEL_KEYS and not args.activations else None),
                      "kernel_ms": {names[j]: kernel_ms[j] for j in range(len(kernel_ms))},
                      "step": {"achieved": step_achieved, "frac": step_achieved / peaks["hbm_gbs"]},
                      "algorithmic_bytes": byts, "algorithmic_flop": flop,
@@ -511,6 +524,9 @@ def main():
     ap.add_argument("--workload", default="batched_bf16")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--activations", action="store_true",
+                    help="forward from raw inputs with the gate activation, sigmoid(beta) and the L2 norm of "
+                         "q and k inside the kernels")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="backward: time gdn_chunk_bwd on one GPU instead of the forward step")
     args = ap.parse_args()

@@ -112,8 +112,11 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         // pre-pass over the whole sequence plus a serial combine, so it needs
         // a larger idle share to pay off.
         const long base = pairs * p->value_tiles;
+        // the warmup split needs ||k|| <= 1 and beta <= 2: asserted by the caller, or made so by the
+        // kernels (keys L2-normalised, beta = sigmoid of its logit)
+        const bool unit_keys = opt.keys_unit_norm || (opt.qk_l2norm && opt.beta_logits);
         cp = GDN_CP_OFF;
-        if (pairs > 0 && opt.keys_unit_norm && base * 2 <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
+        if (pairs > 0 && unit_keys && base * 2 <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
         else if (pairs > 0 && base * 4 <= num_sms && max_nt >= 16) cp = GDN_CP_EXACT;
     }
     if (max_nt <= 1 || p->kda) cp = GDN_CP_OFF;

@@ -43,6 +43,13 @@ __device__ __forceinline__ float act_gate(const Act &a, float x, int hv, int d, 
     if (a.lower_bound < 0.f) return a.lower_bound / (1.f + expf(-ea * z));
     return -ea * (z > 20.f ? z : log1pf(expf(z)));  // softplus, linear past 20 like the usual threshold
 }
+// act_gate with the per-head factor exp(A_log) and the bias taken once by the caller (the same arithmetic)
+__device__ __forceinline__ float act_gate_pre(const Act &a, float x, float bias, float ea)
+{
+    const float z = x + bias;
+    if (a.lower_bound < 0.f) return a.lower_bound / (1.f + expf(-ea * z));
+    return -ea * (z > 20.f ? z : log1pf(expf(z)));
+}
 __device__ __forceinline__ float act_beta(const Act &a, float x) { return a.beta_logits ? 1.f / (1.f + expf(-x)) : x; }
 constexpr float kNormEps = 1e-12f;
 

@@ -89,6 +89,17 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     {
         uint4 kv[4], qv[4];
         float4 gv[8];
+        // a thread's four channels are the same in every row: the activation's per-channel bias and the
+        // head's exp(A_log) are taken once
+        float ea = 0.f;
+        float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.act.A_log) {
+            ea = expf(a.act.A_log[hv]);
+            if (a.act.dt_bias) {
+                const float *bp = a.act.dt_bias + (size_t)hv * 128 + (tid & 31) * 4;
+                bias = make_float4(bp[0], bp[1], bp[2], bp[3]);
+            }
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int e = tid + kThreadsKda * i, r = e >> 4, c8 = (e & 15) * 8;
@@ -106,10 +117,10 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
             if (r < rows) {
                 gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
                 if (a.act.A_log) {  // raw gate input: the activation, per channel
-                    gv[i].x = act_gate(a.act, gv[i].x, hv, c4, 128);
-                    gv[i].y = act_gate(a.act, gv[i].y, hv, c4 + 1, 128);
-                    gv[i].z = act_gate(a.act, gv[i].z, hv, c4 + 2, 128);
-                    gv[i].w = act_gate(a.act, gv[i].w, hv, c4 + 3, 128);
+                    gv[i].x = act_gate_pre(a.act, gv[i].x, bias.x, ea);
+                    gv[i].y = act_gate_pre(a.act, gv[i].y, bias.y, ea);
+                    gv[i].z = act_gate_pre(a.act, gv[i].z, bias.z, ea);
+                    gv[i].w = act_gate_pre(a.act, gv[i].w, bias.w, ea);
                 }
             }
         }
@@ -130,18 +141,32 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     __syncthreads();
     if (a.act.qk_l2norm) {
         // in-kernel L2 norm: the rows of k and q to unit length (fp32 arithmetic, one bf16 rounding, as
-        // every operand of the products below is bf16)
-        if (tid < 128) {
-            __nv_bfloat16 *row = (tid < 64 ? sh.k : sh.q) + (tid & 63) * QP;
-            float ss = 0.f;
-#pragma unroll 4
-            for (int c = 0; c < 128; ++c) {
-                const float x = __bfloat162float(row[c]);
-                ss = fmaf(x, x, ss);
+        // every operand of the products below is bf16); two threads per row, eight 16-byte pieces each
+        const int rr = tid >> 1, h = tid & 1;
+        __nv_bfloat16 *row = (rr < 64 ? sh.k : sh.q) + (rr & 63) * QP + 64 * h;
+        uint4 x[8];
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            x[j] = *(const uint4 *)(row + 8 * j);
+            const __nv_bfloat162 *b2 = (const __nv_bfloat162 *)&x[j];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(b2[u]);
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
             }
-            const float rn = 1.f / fmaxf(sqrtf(ss), kNormEps);
-#pragma unroll 4
-            for (int c = 0; c < 128; ++c) row[c] = __float2bfloat16_rn(__bfloat162float(row[c]) * rn);
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        const float rn = 1.f / fmaxf(sqrtf(ss), kNormEps);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __nv_bfloat162 *b2 = (__nv_bfloat162 *)&x[j];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(b2[u]);
+                b2[u] = __floats2bfloat162_rn(f.x * rn, f.y * rn);
+            }
+            *(uint4 *)(row + 8 * j) = x[j];
         }
         __syncthreads();
     }

@@ -106,7 +106,8 @@ typedef struct {
     gdn_engine engine;
     int keys_unit_norm;    /* caller asserts ||k_t||_2 <= 1 and 0 <= beta_t <= 2, so
                               every transition has spectral norm <= its decay; lets
-                              AUTO choose the warmup split                           */
+                              AUTO choose the warmup split (qk_l2norm together with
+                              beta_logits implies it)                               */
     float warmup_log2_eps; /* warmup stops once the window's decay <= 2^this (0 = -24) */
     int max_seq_len;       /* packed input: bound on one sequence's length, used to
                               size the split grid (0 = T)                             */

@@ -73,6 +73,12 @@ def test_plans(gdn):
     # 64 pairs leave half the SMs idle: with unit-norm keys asserted, the warmup split
     p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152, keys_unit_norm=True)
     assert p.cp_mode == 3 and p.segments == 2
+    # keys L2-normalised and beta a sigmoid inside the kernels: unit-norm keys by construction; with beta
+    # as given (it may exceed 2) no such guarantee
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152, qk_l2norm=True, beta_logits=True)
+    assert p.cp_mode == 3 and p.segments == 2
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, num_sms=152, qk_l2norm=True)
+    assert p.cp_mode == 1
     # fp32 or other head dims: CUDA-core engine
     p = gdn.plan(4, 4096, 16, 16, 128, 128, dtype="f32", num_sms=152)
     assert p.engine == 1 and p.value_tiles == 4

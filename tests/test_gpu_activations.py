@@ -70,6 +70,9 @@ CASES = [
     ("tc_scalar_exact", dict(B=1, T=64 * 12 + 5, H=2, HV=2, K=128, V=128, dtype="bf16", gate="scalar"), "tc",
      dict(cp_mode="exact", segment_chunks=4)),
     ("tc_varlen", dict(B=1, T=400, H=2, HV=2, K=128, V=128, dtype="bf16", gate="scalar", varlen=5), "tc", {}),
+    # the planner's own choice: few pairs, normalised keys and sigmoid beta -> the warmup split
+    ("tc_scalar_auto_split", dict(B=1, T=64 * 20 + 5, H=2, HV=2, K=128, V=128, dtype="bf16", gate="scalar"), "tc",
+     {}),
     ("tc_channel", dict(B=1, T=64 * 3 + 7, H=2, HV=2, K=128, V=128, dtype="bf16", gate="channel",
                         lower_bound=-5.0), "tc", {}),
     ("recurrent_bf16", dict(B=3, T=5, H=2, HV=4, K=128, V=128, dtype="bf16", gate="scalar"), "recurrent", {}),
