@@ -121,6 +121,9 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
                                           float log2_eps, const Act &act)
 {
     const int lane = threadIdx.x & 31;
+    // the head's activation parameters, taken once
+    const float ea = ACT && act.A_log ? expf(act.A_log[hv]) : 0.f;
+    const float bias = ACT && act.A_log && act.dt_bias ? act.dt_bias[hv] : 0.f;
     float acc = 0.f;
     for (int c = c0; c > 0; c -= 8) {
         // lane l: tokens l and l + 32 of the chunks c - 1, ..., c - 8 (loads issued together)
@@ -131,8 +134,13 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
             const int rows = cc >= 0 ? rows_in(len, cc) : 0;
             const float *gp = g + ((size_t)(bos + (int64_t)(cc >= 0 ? cc : 0) * kChunk) + lane) * HV + hv;
             if constexpr (ACT) {
-                v[2 * b] = lane < rows ? act_gate(act, gp[0], hv, -1, 128) : 0.f;
-                v[2 * b + 1] = lane + 32 < rows ? act_gate(act, gp[(size_t)32 * HV], hv, -1, 128) : 0.f;
+                if (act.A_log) {
+                    v[2 * b] = lane < rows ? act_gate_pre(act, gp[0], bias, ea) : 0.f;
+                    v[2 * b + 1] = lane + 32 < rows ? act_gate_pre(act, gp[(size_t)32 * HV], bias, ea) : 0.f;
+                } else {
+                    v[2 * b] = lane < rows ? gp[0] : 0.f;
+                    v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+                }
             } else {
                 v[2 * b] = lane < rows ? gp[0] : 0.f;
                 v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
@@ -268,6 +276,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
         // chunk's loads before issuing the next would leave one chunk of HBM traffic in flight.
         bool ok = true;
         int ni = 0, nl = 0;  // next chunk to issue, next chunk to land
+        // the head's gate-activation parameters (raw gate input), taken once
+        const float act_ea = ACT && a.act.A_log ? expf(a.act.A_log[hv]) : 0.f;
+        const float act_bias = ACT && a.act.A_log && a.act.dt_bias ? a.act.dt_bias[hv] : 0.f;
         uint64_t t_last = globaltimer();
         uint32_t idle = 0;
         auto rdy = [&](int b, int ph) {
@@ -351,8 +362,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     // (activated in place when the gate input is raw; rows past the end stay exactly 0)
                     float g0 = gr.x * kRcpLn2, g1 = gr.y * kRcpLn2;
                     if constexpr (ACT) {
-                        g0 = (r0 < rows ? act_gate(a.act, gr.x, hv, -1, 128) : 0.f) * kRcpLn2;
-                        g1 = (r1 < rows ? act_gate(a.act, gr.y, hv, -1, 128) : 0.f) * kRcpLn2;
+                        if (a.act.A_log) {
+                            g0 = (r0 < rows ? act_gate_pre(a.act, gr.x, act_bias, act_ea) : 0.f) * kRcpLn2;
+                            g1 = (r1 < rows ? act_gate_pre(a.act, gr.y, act_bias, act_ea) : 0.f) * kRcpLn2;
+                        }
                     }
                     float sp = g0 + g1;
     #pragma unroll
@@ -669,9 +682,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (lane == 0) mbar_arrive(&bars[B_KQE]);
             const bool fac = gt[GT_G + 63] >= kFactorFloor;
             float rq = 1.f;
-            if (nrm) {
-                // in-kernel L2 norm: 1 / ||q_r|| from row r of the chunk's Q boxes (before a steep chunk's
-                // in-place Q~), for the O epilogue's row factor
+            if (nrm && !fac) {
+                // in-kernel L2 norm, steep chunk: 1 / ||q_r|| from row r of the chunk's Q boxes (before the
+                // in-place Q~), for Q~, P and the O epilogue's row factor (a factored chunk's are the
+                // output warps')
                 const uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
                 float ss = 0.f;
 #pragma unroll 1
@@ -979,6 +993,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const int ci = it - 1, c = cs + ci;
                 const int64_t t0 = bos + (int64_t)c * kChunk;
                 const int rows = rows_in(len, c);
+                if (!KDA && nrm && factored(ci)) {
+                    // in-kernel L2 norm: 1 / ||q_t|| of the chunk's rows for the row factors below, taken here
+                    // while the products run (two threads per row, eight 16-byte pieces each; a steep chunk's
+                    // are the aux warps', which need them first)
+                    ok = mbar_wait(&bars[B_FULL + ci % kStages], (ci / kStages) & 1, status, kStatusTimeout, kWaitNs);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    const int rr = et >> 1, hb = et & 1;
+                    const uint8_t *row = sm + OFF_STAGE + (ci % kStages) * kStageBytes + (hb ? sQ1 : sQ0) + rr * 128;
+                    float ss = 0.f;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 x = *(const uint4 *)(row + ((c8 + rr) & 7) * 16);
+                        const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 fv = __bfloat1622float2(h2[q]);
+                            ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
+                        }
+                    }
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    if (hb == 0) gates(ci)[GT_RQ + rr] = 1.f / fmaxf(sqrtf(ss), kNormEps);
+                    bar_sync(1, 128);  // the four output warps
+                }
                 ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
