@@ -34,21 +34,26 @@ struct Act {
     int beta_logits;       // beta = sigmoid(input)
     int qk_l2norm;         // q, k scaled to unit L2 norm per (token, head) (x / max(||x||, 1e-12))
 };
+// the log-decay of z = x + bias with ea = exp(A_log): lower_bound sigmoid(ea z), or -ea softplus(z) (linear
+// past z = 20 like the usual threshold).  By the fast exponential and logarithm: the softplus of z below
+// about -17 rounds to 0 (its value is under 6e-8), and the gate's relative error stays far below the
+// bf16 resolution of the operands it scales
+__device__ __forceinline__ float act_gate_z(const Act &a, float z, float ea)
+{
+    if (a.lower_bound < 0.f) return a.lower_bound / (1.f + __expf(-ea * z));
+    return -ea * (z > 20.f ? z : __logf(1.f + __expf(z)));
+}
 // the log-decay of gate input x for value head hv (channel d, or d < 0 for a scalar gate)
 __device__ __forceinline__ float act_gate(const Act &a, float x, int hv, int d, int K)
 {
     if (!a.A_log) return x;
     const float z = x + (a.dt_bias ? a.dt_bias[d < 0 ? hv : hv * K + d] : 0.f);
-    const float ea = expf(a.A_log[hv]);
-    if (a.lower_bound < 0.f) return a.lower_bound / (1.f + expf(-ea * z));
-    return -ea * (z > 20.f ? z : log1pf(expf(z)));  // softplus, linear past 20 like the usual threshold
+    return act_gate_z(a, z, expf(a.A_log[hv]));
 }
 // act_gate with the per-head factor exp(A_log) and the bias taken once by the caller (the same arithmetic)
 __device__ __forceinline__ float act_gate_pre(const Act &a, float x, float bias, float ea)
 {
-    const float z = x + bias;
-    if (a.lower_bound < 0.f) return a.lower_bound / (1.f + expf(-ea * z));
-    return -ea * (z > 20.f ? z : log1pf(expf(z)));
+    return act_gate_z(a, x + bias, ea);
 }
 __device__ __forceinline__ float act_beta(const Act &a, float x) { return a.beta_logits ? 1.f / (1.f + expf(-x)) : x; }
 constexpr float kNormEps = 1e-12f;
