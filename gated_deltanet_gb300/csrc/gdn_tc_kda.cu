@@ -114,9 +114,14 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
         for (int i = 0; i < 8; ++i) {
             const int e = tid + kThreadsKda * i, r = e >> 5, c4 = (e & 31) * 4;
             gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < rows) {
-                gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
-                if (a.act.A_log) {  // raw gate input: the activation, per channel
+            if (r < rows) gv[i] = *(const float4 *)(a.gk + ((size_t)(t0 + r) * HV + hv) * 128 + c4);
+        }
+        if (a.act.A_log) {
+            // raw gate input: the activation, per channel, once every load is issued (rows past the end
+            // stay 0)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (((tid + kThreadsKda * i) >> 5) < rows) {
                     gv[i].x = act_gate_pre(a.act, gv[i].x, bias.x, ea);
                     gv[i].y = act_gate_pre(a.act, gv[i].y, bias.y, ea);
                     gv[i].z = act_gate_pre(a.act, gv[i].z, bias.z, ea);
