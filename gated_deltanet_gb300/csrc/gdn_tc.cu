@@ -993,30 +993,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const int ci = it - 1, c = cs + ci;
                 const int64_t t0 = bos + (int64_t)c * kChunk;
                 const int rows = rows_in(len, c);
-                if (!KDA && nrm && factored(ci)) {
-                    // in-kernel L2 norm: 1 / ||q_t|| of the chunk's rows for the row factors below, taken here
-                    // while the products run (two threads per row, eight 16-byte pieces each; a steep chunk's
-                    // are the aux warps', which need them first)
-                    ok = mbar_wait(&bars[B_FULL + ci % kStages], (ci / kStages) & 1, status, kStatusTimeout, kWaitNs);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    const int rr = et >> 1, hb = et & 1;
-                    const uint8_t *row = sm + OFF_STAGE + (ci % kStages) * kStageBytes + (hb ? sQ1 : sQ0) + rr * 128;
-                    float ss = 0.f;
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 x = *(const uint4 *)(row + ((c8 + rr) & 7) * 16);
-                        const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 fv = __bfloat1622float2(h2[q]);
-                            ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
-                        }
-                    }
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                    if (hb == 0) gates(ci)[GT_RQ + rr] = 1.f / fmaxf(sqrtf(ss), kNormEps);
-                    bar_sync(1, 128);  // the four output warps
-                }
                 ok = mbar_wait(&bars[B_OF], e & 1, status, kStatusTimeout, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -1028,15 +1004,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const float *gt = gates(ci);
                 if (!KDA && factored(ci)) {
                     // the row factors scale * gam_t of the factored form (per-channel gates: inside Q~ and P),
-                    // with 1 / ||q_t|| of the in-kernel L2 norm
-                    const bool nq = nrm;
+                    // with 1 / ||q_t|| of the in-kernel L2 norm folded in above
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
-                        float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
-                        if (nq) {
-                            const float4 rq4 = *(const float4 *)(gt + GT_RQ + 4 * j4);
-                            f.x *= rq4.x; f.y *= rq4.y; f.z *= rq4.z; f.w *= rq4.w;
-                        }
+                        const float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
                         r[4 * j4] = f2u(u2f(r[4 * j4]) * f.x);
                         r[4 * j4 + 1] = f2u(u2f(r[4 * j4 + 1]) * f.y);
                         r[4 * j4 + 2] = f2u(u2f(r[4 * j4 + 2]) * f.z);
@@ -1081,6 +1052,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     if (et == 0) mbar_arrive(&bars[B_EMPTY + ci % kStages]);
                 }
                 ++e;
+            }
+            if (!KDA && nrm && it < nch && emit_of(it) && factored(it)) {
+                // in-kernel L2 norm: 1 / ||q_t|| of the next chunk's rows, folded into its row factors
+                // scale * gam_t, here, between this chunk's store and the next -W^T, so that it delays neither
+                // (two threads per row, eight 16-byte pieces each; a steep chunk's are the aux warps', which
+                // need them first for Q~ and P)
+                ok = mbar_wait(&bars[B_FULL + it % kStages], (it / kStages) & 1, status, kStatusTimeout, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const int rr = et >> 1, hb = et & 1;
+                const uint8_t *row = sm + OFF_STAGE + (it % kStages) * kStageBytes + (hb ? sQ1 : sQ0) + rr * 128;
+                float ss = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 x = *(const uint4 *)(row + ((c8 + rr) & 7) * 16);
+                    const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 fv = __bfloat1622float2(h2[q]);
+                        ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (hb == 0) gates(it)[GT_SGAM + rr] *= 1.f / fmaxf(sqrtf(ss), kNormEps);
+                bar_sync(1, 128);  // the four output warps
             }
         }
     }
