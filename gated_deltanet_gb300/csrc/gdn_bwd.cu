@@ -17,7 +17,7 @@
 //
 // Kernels, after the chunk states are recomputed by a forward pass with a state dump (Step 2):
 //   bwd_prep_kernel     one CTA per chunk and value head: A and P (Step 1: nothing in them depends on
-//                       the state), fp32 into the workspace;
+//                       the state; A by forward substitution per column), fp32 into the workspace;
 //   chunk_bwd_kernel    one CTA per (sequence, value head, 32-column value tile), chunks newest first
 //                       with its tile of dS in shared memory: everything that needs S0 or dS, and the
 //                       tile's parts of dO D^T and dD B^T (sums over the value columns) to the workspace;
@@ -33,8 +33,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kBThreads = 256;  // the per-chunk kernels
-constexpr int kRThreads = 512;  // the reverse scan (sixteen warps: every product has a block per warp)
+constexpr int kBThreads = 256;  // the A and P kernel (two CTAs per SM)
+constexpr int kRThreads = 512;  // the reverse scan and the finish (sixteen warps: a product block per warp)
 constexpr int kBC = 64;      // chunk
 constexpr int kBV = 32;      // value columns per CTA
 constexpr int kCP = kBC + 4;  // pitches (4 mod 32: the tensor-core fragments' strided reads hit at most
