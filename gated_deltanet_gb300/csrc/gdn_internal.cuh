@@ -167,6 +167,9 @@ constexpr size_t kKdaTileBytesPerChunk = 9 * 64 * 64 * 2 + 128 * 4;  // nine bf1
 cudaError_t launch_tc_scan(const ScanArgs &a, int value_tiles, bool kda, cudaStream_t st);
 // 2-D TMA map over the operand tiles, bf16 rows of 64, box 64 x box_rows, 128-byte swizzle
 bool encode_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t box_rows);
+// 3-D TMA map over a [rows][heads][128] bf16 tensor (q, k, v, o), box 64 elements x 1 head x 64 rows, 128-byte
+// swizzle
+bool encode_rows_map(CUtensorMap *map, const void *base, int heads, int64_t rows);
 cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st);
 constexpr size_t kTcTileBytesPerChunk = 2 * 64 * 64 * 2;  // T_U and T_W, bf16
 

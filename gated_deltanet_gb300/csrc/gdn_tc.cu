@@ -1138,6 +1138,8 @@ bool make_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t b
 
 }  // namespace
 
+bool encode_rows_map(CUtensorMap *map, const void *base, int heads, int64_t rows) { return make_map(map, base, heads, rows); }
+
 bool encode_tiles_map(CUtensorMap *map, const void *base, int64_t rows, uint32_t box_rows)
 {
     return make_tiles_map(map, base, rows, box_rows);

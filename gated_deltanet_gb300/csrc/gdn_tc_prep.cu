@@ -32,7 +32,7 @@ struct PrepSmem {
     __align__(1024) uint8_t buf[8192 + 64 * kLdX * 4];
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
     __align__(16) float bw[64], rk[64];  // beta / ||k|| (T_W's column factor), 1 / ||k|| (in-kernel L2 norm)
-    uint64_t bar;
+    uint64_t bar, kbar;  // the product's completion; the K boxes' arrival
     uint32_t tslot;
 };
 
@@ -43,7 +43,8 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 }
 
 template <bool ACT>
-__global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tmap)
+__global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tmap,
+                                                                   const __grid_constant__ CUtensorMap kmap)
 {
     // ACT: the in-kernel input activations (raw gate input, sigmoid(beta), L2 norm of k); a separate
     // instance, so that the plain one carries none of their code
@@ -73,11 +74,17 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
 
     if (warp == 0) tmem_alloc(&sh.tslot, kTmemCols);
     if (tid == 32) {
+        // the chunk's K rows by two TMA boxes (dk 0-63, 64-127) straight into the swizzled operand layout
         mbar_init(&sh.bar, 1);
+        mbar_init(&sh.kbar, 1);
         fence_mbar_init();
+        fence_proxy_async();  // (block (0, 0) used the buffer as scratch above)
+        mbar_arrive_expect_tx(&sh.kbar, 16384u);
+        tma_load_3d(sh.buf, &kmap, 0, hq, (int)t0, &sh.kbar);
+        tma_load_3d(sh.buf + 8192, &kmap, 64, hq, (int)t0, &sh.kbar);
     }
-    // ---- K rows into the swizzled boxes (rows past the end of the sequence are zero), gates; every global
-    //      load (warp 0's gates included) is issued before the first store waits for one
+    __syncthreads();  // the barriers are initialised before any thread waits on them
+    // ---- gates (warp 0; issued while the K boxes are in flight), then the K boxes' tail rows
     const int r0 = 2 * lane, r1 = r0 + 1;
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp == 0) {
@@ -101,18 +108,12 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         }
     }
     {
-        const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k;
-        uint4 kv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
-            kv[i] = make_uint4(0, 0, 0, 0);
-            if (r < rows) kv[i] = *(const uint4 *)(kg + ((size_t)(t0 + r) * a.H + hq) * 128 + ch * 8);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + kThreadsPrep * i, r = e >> 4, ch = e & 15;
-            *(uint4 *)(sh.buf + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = kv[i];
+        // the K boxes have landed; rows past the end of the sequence (the next one's, or zero fill past the
+        // tensor) become zeros (a wait that runs out leaves the status flag and a wrong chunk, never a hang)
+        mbar_wait(&sh.kbar, 0, a.status, kStatusTimeout, a.wait_ns);
+        for (int e = tid; e < (kChunk - rows) * 16; e += kThreadsPrep) {
+            const int r = rows + (e >> 4), piece = e & 15;
+            *(uint4 *)(sh.buf + (piece >> 3) * 8192 + r * 128 + (piece & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();  // the tensor core reads them
     }
@@ -432,9 +433,12 @@ cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
     // T_W leaves through a TMA store: the same tile map as the scan reads it with
     alignas(64) CUtensorMap tmap;
     if (!encode_tiles_map(&tmap, a.tiles, (int64_t)a.slots * a.HV * 128, 64)) return cudaErrorInvalidValue;
+    // the chunks' K rows arrive by TMA: the map the scan reads K with
+    alignas(64) CUtensorMap kmap;
+    if (!encode_rows_map(&kmap, a.k, a.H, a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T)) return cudaErrorInvalidValue;
     dim3 grid(a.slots, a.HV);
-    if (a.act.A_log || a.act.beta_logits || a.act.qk_l2norm) tc_prep_kernel<true><<<grid, kThreadsPrep, 0, st>>>(a, tmap);
-    else tc_prep_kernel<false><<<grid, kThreadsPrep, 0, st>>>(a, tmap);
+    if (a.act.A_log || a.act.beta_logits || a.act.qk_l2norm) tc_prep_kernel<true><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap);
+    else tc_prep_kernel<false><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap);
     return cudaGetLastError();
 }
 
