@@ -359,56 +359,43 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     __syncthreads();
 
     // ---- operand tiles, each staged in the dead K box (128-byte swizzle) and written by one TMA store:
-    //      T_W, then T_U once the first copy has read the box.  Warp = (32 rows, 32 columns), lane = row,
-    //      one 16-byte piece per step: a warp reads consecutive rows of X^T (no conflicts) and its
-    //      quadrant of the lower-triangular tiles is all zeros (rows 0-31, columns 32-63: written once,
-    //      both tiles share them), all below the diagonal (rows 32-63, columns 0-31: no masks) or a
-    //      diagonal block
+    //      T_W, then T_U once the first copy has read the box.  Warp w takes the 8-column piece w of each
+    //      of the three nonzero quadrants (rows 0-31 x columns 0-31 and rows 32-63 x columns 32-63: diagonal
+    //      blocks; rows 32-63 x columns 0-31: all below the diagonal, no masks), lane = row within the
+    //      quadrant, one 16-byte piece per quadrant: consecutive rows of X^T (no conflicts), equal work per
+    //      warp.  The all-zero quadrant (rows 0-31, columns 32-63) is written once, piece 4 + w by warp w,
+    //      and both tiles share it
     {
-        const int r = 32 * (warp & 1) + lane, h = warp >> 1;
-        const bool zeros = warp == 2, below = warp == 1;  // warp-uniform
-        const float gr = sh.gam[r], Gr = sh.G[r];
         const bool factored = sh.G[63] >= kFactorFloor;
         const int row0 = (int)(((size_t)slot * HV + hv) * 2 * 64);  // T_U rows; T_W follows
-        uint8_t *srow = sh.buf + r * 128;
+        const float ga = sh.gam[lane], gb = sh.gam[32 + lane], Ga = sh.G[lane], Gb = sh.G[32 + lane];
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {  // 0: T_W, 1: T_U
             if (pass == 1) {
                 if (tid == 0) tma_store_wait_read0();
                 __syncthreads();
-            }
-            if (zeros) {
-                if (pass == 0) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) *(uint4 *)(srow + (((4 + q) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-                }
             } else {
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    const int j0 = 32 * h + 8 * q;
-                    const float *bsrc = pass == 0 ? (ACT ? sh.bw : sh.beta) : !factored ? sh.beta : sh.br;
-                    const float4 b0 = *(const float4 *)(bsrc + j0), b1 = *(const float4 *)(bsrc + j0 + 4);
-                    const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                    float v[8];
-                    if (below) {
+                *(uint4 *)(sh.buf + lane * 128 + (((4 + warp) ^ (lane & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+            const float *bsrc = pass == 0 ? (ACT ? sh.bw : sh.beta) : !factored ? sh.beta : sh.br;
+            const bool plain = pass == 0 || factored;  // T_W, or T_U with the factored form: gam_r X beta'_j
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const float xv = lx[(j0 + u) * kLdX + r];
-                            // T_W = gam_r X beta_j; T_U = gam_r X beta_j / gam_j (factored: br = beta / gam;
-                            // else the power 2^(G_r - G_j) per element)
-                            v[u] = pass == 0 || factored ? gr * bj[u] * xv : ex2(Gr - sh.G[j0 + u]) * bj[u] * xv;
-                        }
-                    } else {
+            for (int qd = 0; qd < 3; ++qd) {  // 0: upper diagonal block, 1: below the diagonal, 2: lower one
+                const int r = qd == 0 ? lane : 32 + lane;
+                const int j0 = (qd == 2 ? 32 : 0) + 8 * warp;
+                const float gr = qd == 0 ? ga : gb, Gr = qd == 0 ? Ga : Gb;
+                const float4 b0 = *(const float4 *)(bsrc + j0), b1 = *(const float4 *)(bsrc + j0 + 4);
+                const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float v[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int jj = j0 + u;
-                            const float xv = jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f);
-                            v[u] = pass == 0 || factored ? gr * bj[u] * xv
-                                                         : (jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv : 0.f);
-                        }
-                    }
-                    *(uint4 *)(srow + (((4 * h + q) ^ (r & 7)) << 4)) = pack8(v);
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = j0 + u;
+                    // T_W = gam_r X beta_j; T_U = gam_r X beta_j / gam_j (factored: br = beta / gam; else the
+                    // power 2^(G_r - G_j) per element)
+                    const float xv = qd == 1 ? lx[jj * kLdX + r] : (jj < r ? lx[jj * kLdX + r] : (jj == r ? 1.f : 0.f));
+                    v[u] = plain ? gr * bj[u] * xv : (qd == 1 || jj <= r ? ex2(Gr - sh.G[jj]) * bj[u] * xv : 0.f);
                 }
+                *(uint4 *)(sh.buf + r * 128 + (((j0 >> 3) ^ (r & 7)) << 4)) = pack8(v);
             }
             fence_proxy_async();  // the tensor-memory-access unit reads the staging box
             __syncthreads();
