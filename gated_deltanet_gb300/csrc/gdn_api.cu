@@ -180,9 +180,9 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
     }
     if (p->engine == GDN_ENGINE_TC) p->kernels += 1;  // the chunk preparation
     if (opt.qk_l2norm && p->engine == GDN_ENGINE_TC && !p->kda) {
-        // 1 / ||k_t|| of every row, from the chunk preparation to the scan
+        // 1 / ||k_t|| and 1 / ||q_t|| of every row, from the chunk preparation to the scan
         p->off_rk = off;
-        off = align_up(off + p->tile_slots * s->HV * 64 * sizeof(float), 256);
+        off = align_up(off + 2 * p->tile_slots * s->HV * 64 * sizeof(float), 256);
     }
     if (opt.state_v_first) {
         const size_t sb = (size_t)N * s->HV * s->K * s->V * sizeof(float);
@@ -328,8 +328,13 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         pa.status = status;
         pa.wait_ns = a.wait_ns;
         pa.act = act;
-        if (p.off_rk) pa.rk = (float *)(wsb + p.off_rk);
+        if (p.off_rk) {
+            pa.rk = (float *)(wsb + p.off_rk);
+            pa.rq = pa.rk + p.tile_slots * s->HV * 64;
+            pa.q = q;
+        }
         a.rk = pa.rk;
+        a.rq = pa.rq;
         mark();
         e = launch_tc_prep(pa, stream);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -576,8 +581,13 @@ gdn_status gdn_chunk_summary(const gdn_shape *s, const void *k, const void *v, c
         pa.status = a.status;
         pa.wait_ns = a.wait_ns;
         pa.act = a.act;
-        if (p.off_rk) pa.rk = (float *)(wsb + p.off_rk);
+        if (p.off_rk) {
+            pa.rk = (float *)(wsb + p.off_rk);
+            pa.rq = pa.rk + p.tile_slots * s->HV * 64;
+            pa.q = a.q;
+        }
         a.rk = pa.rk;
+        a.rq = pa.rq;
         if ((e = launch_tc_prep(pa, cs)) != cudaSuccess) return GDN_ERR_CUDA;
         a.tiles = pa.tiles;
         a.tile_slots = pa.slots;

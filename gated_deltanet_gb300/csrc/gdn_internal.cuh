@@ -88,6 +88,7 @@ struct ScanArgs {
     int withhold_full0;     // timeout-path test: the load warp never signals its first chunk
     Act act;
     const float *rk;        // tensor-core engine, in-kernel L2 norm: 1 / ||k_t|| per (slot, value head, row)
+    const float *rq;        //   and 1 / ||q_t|| (same layout), both from the chunk preparation
 };
 
 struct CombineArgs {
@@ -124,6 +125,8 @@ struct PrepArgs {
     unsigned long long wait_ns; // wall-clock limit of the product-completion wait
     Act act;
     float *rk;                  // qk_l2norm: 1 / ||k_t|| per (slot, value head, row), written for the scan
+    float *rq;                  //   and 1 / ||q_t|| (same layout; rows past the end of the sequence 0)
+    const void *q;              //   read only for rq
 };
 
 // Start states of consecutive pieces of sequences from their (S*, M) summaries (context parallel).

@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
     constexpr uint32_t kGateBytes = Lay::kGateBytes;
     const float *const rkp = ACT ? a.rk : nullptr;
     const bool nrm = ACT && a.act.qk_l2norm;
+    const float *const rqp = nrm ? a.rq : nullptr;  // 1 / ||q_t|| from the preparation
     constexpr uint32_t kStageBytes = Lay::kStageBytes, OFF_P = Lay::OFF_P, OFF_WS = Lay::OFF_WS,
                        OFF_GATE = Lay::OFF_GATE, OFF_BAR = Lay::OFF_BAR;
     extern __shared__ __align__(1024) uint8_t smraw[];
@@ -341,6 +342,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                         cp_async4(gates(ni) + GT_RK + 2 * lane, rsrc + 2 * lane, 4u);
                         cp_async4(gates(ni) + GT_RK + 2 * lane + 1, rsrc + 2 * lane + 1, 4u);
                     }
+                    if (rqp && emit) {
+                        const float *qsrc = rqp + ((size_t)tile_slot(bos, n, c) * HV + hv) * 64;
+                        cp_async4(gates(ni) + GT_RQ + 2 * lane, qsrc + 2 * lane, 4u);
+                        cp_async4(gates(ni) + GT_RQ + 2 * lane + 1, qsrc + 2 * lane + 1, 4u);
+                    }
                 }
                 cp_async_commit();
                 ++ni;
@@ -383,7 +389,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     if (rkp) rk2 = *(const float2 *)(gt + GT_RK + r0);
                     *(float2 *)(gt + GT_RDEC + r0) = make_float2(ex2(GC - G0) * rk2.x, ex2(GC - G1) * rk2.y);
                     *(float2 *)(gt + GT_GINV + r0) = make_float2(ex2(-G0), ex2(-G1));  // read only if G_C >= kFactorFloor
-                    *(float2 *)(gt + GT_SGAM + r0) = make_float2(a.scale * gm0, a.scale * gm1);
+                    // the output's row factors scale * gam (a factored chunk's with 1 / ||q|| of the in-kernel L2
+                    // norm folded in; a steep chunk's Q~ and P take it themselves)
+                    float2 sg = make_float2(a.scale * gm0, a.scale * gm1);
+                    if (rqp && emit_of(nl) && GC >= kFactorFloor) {
+                        const float2 q2 = *(const float2 *)(gt + GT_RQ + r0);
+                        sg.x *= q2.x;
+                        sg.y *= q2.y;
+                    }
+                    *(float2 *)(gt + GT_SGAM + r0) = sg;
                     if (rows < kChunk) {
                         // rows past the end of the sequence belong to the next one: make them inert zeros
                         uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
@@ -682,29 +696,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             if (lane == 0) mbar_arrive(&bars[B_KQE]);
             const bool fac = gt[GT_G + 63] >= kFactorFloor;
             float rq = 1.f;
-            if (nrm && !fac) {
-                // in-kernel L2 norm, steep chunk: 1 / ||q_r|| from row r of the chunk's Q boxes (before the
-                // in-place Q~), for Q~, P and the O epilogue's row factor (a factored chunk's are the
-                // output warps')
-                const uint8_t *st = sm + OFF_STAGE + s * kStageBytes;
-                float ss = 0.f;
-#pragma unroll 1
-                for (int bx = 0; bx < 2; ++bx) {
-                    const uint8_t *row = st + (bx ? sQ1 : sQ0) + r * 128;
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 x = *(const uint4 *)(row + ((c8 + r) & 7) * 16);
-                        const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 fv = __bfloat1622float2(h2[q]);
-                            ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
-                        }
-                    }
-                }
-                rq = 1.f / fmaxf(sqrtf(ss), kNormEps);
-                ((float *)gt)[GT_RQ + r] = rq;
-            }
+            // in-kernel L2 norm, steep chunk: 1 / ||q_r|| (from the preparation) for Q~ and P
+            if (nrm && !fac) rq = gt[GT_RQ + r];
             if (!fac) {
                 // steep chunk: Q~ row r = scale * gam_r * q_r, in place (the Q K^T product has read Q);
                 // the 16-byte pieces go in a row-rotated order to spread the banks, all loads first
@@ -1004,7 +997,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 const float *gt = gates(ci);
                 if (!KDA && factored(ci)) {
                     // the row factors scale * gam_t of the factored form (per-channel gates: inside Q~ and P),
-                    // with 1 / ||q_t|| of the in-kernel L2 norm folded in above
+                    // with 1 / ||q_t|| of the in-kernel L2 norm folded in by the load warp
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         const float4 f = *(const float4 *)(gt + GT_SGAM + 4 * j4);
@@ -1052,31 +1045,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     if (et == 0) mbar_arrive(&bars[B_EMPTY + ci % kStages]);
                 }
                 ++e;
-            }
-            if (!KDA && nrm && it < nch && emit_of(it) && factored(it)) {
-                // in-kernel L2 norm: 1 / ||q_t|| of the next chunk's rows, folded into its row factors
-                // scale * gam_t, here, between this chunk's store and the next -W^T, so that it delays neither
-                // (two threads per row, eight 16-byte pieces each; a steep chunk's are the aux warps', which
-                // need them first for Q~ and P)
-                ok = mbar_wait(&bars[B_FULL + it % kStages], (it / kStages) & 1, status, kStatusTimeout, kWaitNs);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const int rr = et >> 1, hb = et & 1;
-                const uint8_t *row = sm + OFF_STAGE + (it % kStages) * kStageBytes + (hb ? sQ1 : sQ0) + rr * 128;
-                float ss = 0.f;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint4 x = *(const uint4 *)(row + ((c8 + rr) & 7) * 16);
-                    const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 fv = __bfloat1622float2(h2[q]);
-                        ss = fmaf(fv.x, fv.x, fmaf(fv.y, fv.y, ss));
-                    }
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (hb == 0) gates(it)[GT_SGAM + rr] *= 1.f / fmaxf(sqrtf(ss), kNormEps);
-                bar_sync(1, 128);  // the four output warps
             }
         }
     }

@@ -32,7 +32,7 @@ struct PrepSmem {
     __align__(1024) uint8_t buf[8192 + 64 * kLdX * 4];
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
     __align__(16) float bw[64], rk[64];  // beta / ||k|| (T_W's column factor), 1 / ||k|| (in-kernel L2 norm)
-    uint64_t bar, kbar;  // the product's completion; the K boxes' arrival
+    uint64_t bar, kbar, qbar;  // the product's completion; the K boxes' arrival; the second Q box's (L2 norm)
     uint32_t tslot;
 };
 
@@ -44,7 +44,8 @@ __device__ __forceinline__ int rows_in(int64_t len, int c)
 
 template <bool ACT>
 __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tmap,
-                                                                   const __grid_constant__ CUtensorMap kmap)
+                                                                   const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap qmap)
 {
     // ACT: the in-kernel input activations (raw gate input, sigmoid(beta), L2 norm of k); a separate
     // instance, so that the plain one carries none of their code
@@ -77,11 +78,14 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         // the chunk's K rows by two TMA boxes (dk 0-63, 64-127) straight into the swizzled operand layout
         mbar_init(&sh.bar, 1);
         mbar_init(&sh.kbar, 1);
+        mbar_init(&sh.qbar, 1);
         fence_mbar_init();
         fence_proxy_async();  // (block (0, 0) used the buffer as scratch above)
-        mbar_arrive_expect_tx(&sh.kbar, 16384u);
+        const bool qn = ACT && a.rq;  // in-kernel L2 norm of q: its first box (dk 0-63) beside K's, where L goes later
+        mbar_arrive_expect_tx(&sh.kbar, qn ? 24576u : 16384u);
         tma_load_3d(sh.buf, &kmap, 0, hq, (int)t0, &sh.kbar);
         tma_load_3d(sh.buf + 8192, &kmap, 64, hq, (int)t0, &sh.kbar);
+        if (qn) tma_load_3d(sh.buf + 16384, &qmap, 0, hq, (int)t0, &sh.kbar);
     }
     __syncthreads();  // the barriers are initialised before any thread waits on them
     // ---- gates (warp 0; issued while the K boxes are in flight), then the K boxes' tail rows
@@ -117,6 +121,26 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         }
         fence_proxy_async();  // the tensor core reads them
     }
+    // in-kernel L2 norm of q, first half: row qr's sum of squares over dk 0-63 (two threads per row, four of its
+    // eight 16-byte pieces each: the swizzle only permutes a row's pieces)
+    const int qr = tid >> 1, qh = tid & 1;
+    float qss = 0.f;
+    auto q_sumsq = [&](const uint8_t *box) {
+        const uint4 *src = (const uint4 *)(box + qr * 128 + qh * 64);
+        uint4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = src[j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x[j];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                qss = fmaf(f.x, f.x, fmaf(f.y, f.y, qss));
+            }
+        }
+    };
+    if (ACT && a.rq) q_sumsq(sh.buf + 16384);
     if (warp == 0) {
         float sp = g0 + g1;
 #pragma unroll
@@ -159,6 +183,11 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     if (warp < 2) {
         const bool ok = mbar_wait(&sh.bar, 0, a.status, kStatusTimeout, a.wait_ns);
         const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (ACT && a.rq && tid == 0 && ok) {
+            // the product has read K's first box: q's second box (dk 64-127) lands there for the norm
+            mbar_arrive_expect_tx(&sh.qbar, 8192u);
+            tma_load_3d(sh.buf, &qmap, 64, hq, (int)t0, &sh.qbar);
+        }
         const int r = 32 * warp + lane;
         // in-kernel L2 norm: ||k_r||^2 is the diagonal of K K^T (column r, in this warp's half); every
         // entry of L takes beta_r / (||k_r|| ||k_j||) and T_W's columns 1 / ||k_j|| (W = T_W K^, K^ = diag(rk) K)
@@ -356,6 +385,13 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
             lx[(n0 + 2 * t + 1) * kLdX + m0 + g + 8] = -u[mt][3];
         }
     }
+    if (ACT && a.rq) {
+        // in-kernel L2 norm of q, second half, and 1 / ||q_r|| for the scan's row factors (rows past the end
+        // of the sequence 0); the box is read before the barrier after which the tiles are staged there
+        if (mbar_wait(&sh.qbar, 0, a.status, kStatusTimeout, a.wait_ns)) q_sumsq(sh.buf);
+        qss += __shfl_xor_sync(0xffffffffu, qss, 1);
+        if (qh == 0) a.rq[((size_t)slot * HV + hv) * 64 + qr] = qr < rows ? 1.f / fmaxf(sqrtf(qss), kNormEps) : 0.f;
+    }
     __syncthreads();
 
     // ---- operand tiles, each staged in the dead K box (128-byte swizzle) and written by one TMA store:
@@ -423,9 +459,13 @@ cudaError_t launch_tc_prep(const PrepArgs &a, cudaStream_t st)
     // the chunks' K rows arrive by TMA: the map the scan reads K with
     alignas(64) CUtensorMap kmap;
     if (!encode_rows_map(&kmap, a.k, a.H, a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T)) return cudaErrorInvalidValue;
+    // and, for the in-kernel L2 norm of q, its rows (the K map again when there is none: never read)
+    alignas(64) CUtensorMap qmap = kmap;
+    if (a.rq && !encode_rows_map(&qmap, a.q, a.H, a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T))
+        return cudaErrorInvalidValue;
     dim3 grid(a.slots, a.HV);
-    if (a.act.A_log || a.act.beta_logits || a.act.qk_l2norm) tc_prep_kernel<true><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap);
-    else tc_prep_kernel<false><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap);
+    if (a.act.A_log || a.act.beta_logits || a.act.qk_l2norm) tc_prep_kernel<true><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap, qmap);
+    else tc_prep_kernel<false><<<grid, kThreadsPrep, 0, st>>>(a, tmap, kmap, qmap);
     return cudaGetLastError();
 }
 
