@@ -133,17 +133,20 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
             const int cc = c - 1 - b;
             const int rows = cc >= 0 ? rows_in(len, cc) : 0;
             const float *gp = g + ((size_t)(bos + (int64_t)(cc >= 0 ? cc : 0) * kChunk) + lane) * HV + hv;
-            if constexpr (ACT) {
-                if (act.A_log) {
-                    v[2 * b] = lane < rows ? act_gate_pre(act, gp[0], bias, ea) : 0.f;
-                    v[2 * b + 1] = lane + 32 < rows ? act_gate_pre(act, gp[(size_t)32 * HV], bias, ea) : 0.f;
-                } else {
-                    v[2 * b] = lane < rows ? gp[0] : 0.f;
-                    v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+            v[2 * b] = lane < rows ? gp[0] : 0.f;
+            v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
+        }
+        if constexpr (ACT) {
+            if (act.A_log) {
+                // raw gate input: the activation once every load of the round is issued (rows past the end
+                // stay 0)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const int cc = c - 1 - b;
+                    const int rows = cc >= 0 ? rows_in(len, cc) : 0;
+                    if (lane < rows) v[2 * b] = act_gate_pre(act, v[2 * b], bias, ea);
+                    if (lane + 32 < rows) v[2 * b + 1] = act_gate_pre(act, v[2 * b + 1], bias, ea);
                 }
-            } else {
-                v[2 * b] = lane < rows ? gp[0] : 0.f;
-                v[2 * b + 1] = lane + 32 < rows ? gp[(size_t)32 * HV] : 0.f;
             }
         }
 #pragma unroll 1

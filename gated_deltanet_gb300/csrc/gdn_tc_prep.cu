@@ -92,24 +92,31 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
     const int r0 = 2 * lane, r1 = r0 + 1;
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp == 0) {
+        // every load first (the head's activation parameters with them), then the activations
+        float ea = 0.f, bias = 0.f;
+        if (ACT && a.act.A_log) {
+            ea = a.act.A_log[hv];
+            if (a.act.dt_bias) bias = a.act.dt_bias[hv];
+        }
         if (r0 < rows) {
             g0 = a.g[(size_t)(t0 + r0) * HV + hv];
             b0 = a.beta[(size_t)(t0 + r0) * HV + hv];
-            if constexpr (ACT) {
-                g0 = act_gate(a.act, g0, hv, -1, 128);
-                b0 = act_beta(a.act, b0);
-            }
-            g0 *= kRcpLn2;
         }
         if (r1 < rows) {
             g1 = a.g[(size_t)(t0 + r1) * HV + hv];
             b1 = a.beta[(size_t)(t0 + r1) * HV + hv];
-            if constexpr (ACT) {
-                g1 = act_gate(a.act, g1, hv, -1, 128);
-                b1 = act_beta(a.act, b1);
-            }
-            g1 *= kRcpLn2;
         }
+        if constexpr (ACT) {
+            if (a.act.A_log) {
+                ea = expf(ea);
+                if (r0 < rows) g0 = act_gate_pre(a.act, g0, bias, ea);
+                if (r1 < rows) g1 = act_gate_pre(a.act, g1, bias, ea);
+            }
+            if (r0 < rows) b0 = act_beta(a.act, b0);
+            if (r1 < rows) b1 = act_beta(a.act, b1);
+        }
+        g0 *= kRcpLn2;
+        g1 *= kRcpLn2;
     }
     {
         // the K boxes have landed; rows past the end of the sequence (the next one's, or zero fill past the
