@@ -25,10 +25,12 @@ constexpr uint32_t kTmemCols = 64;  // the K K^T accumulator; eight CTAs per SM 
 constexpr float kFactorFloor = -100.f;  // G_C >= this: Gam_ij = gam_i * 2^-G_j without overflow
 
 struct PrepSmem {
-    // bytes 0-24575: the chunk's K rows, 128-byte swizzled boxes of 64 rows x 64 dk (dk 0-63, then
-    // 64-127), until K K^T is formed (the 128-row operand of the product reads one box past the second).
-    // Then bytes 0-8191: the T_W tile, 128-byte swizzled, for its TMA store; from byte 8192 the fp32 L / X
-    // tile: L in the lower triangle, X^T in the upper (X(r, j), j < r, at lx[j * kLdX + r]).
+    // bytes 0-16383: the chunk's K rows, 128-byte swizzled boxes of 64 rows x 64 dk (dk 0-63, then
+    // 64-127), until K K^T is formed (the 128-row operand of the product reads one box past the second:
+    // bytes 16384-24575, where the in-kernel L2 norm puts q's first box, dk 0-63).  Then bytes 0-8191:
+    // q's second box (L2 norm only) until the last merge, then the T_W and T_U tiles, 128-byte swizzled,
+    // for their TMA stores; from byte 8192 the fp32 L / X tile: L in the lower triangle, X^T in the upper
+    // (X(r, j), j < r, at lx[j * kLdX + r]).
     __align__(1024) uint8_t buf[8192 + 64 * kLdX * 4];
     __align__(16) float G[64], beta[64], gam[64], br[64];  // br = beta / gam
     __align__(16) float bw[64], rk[64];  // beta / ||k|| (T_W's column factor), 1 / ||k|| (in-kernel L2 norm)
@@ -47,8 +49,8 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
                                                                    const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap qmap)
 {
-    // ACT: the in-kernel input activations (raw gate input, sigmoid(beta), L2 norm of k); a separate
-    // instance, so that the plain one carries none of their code
+    // ACT: the in-kernel input activations (raw gate input, sigmoid(beta), L2 norm of k and q); a
+    // separate instance, so that the plain one carries none of their code
     __shared__ __align__(1024) PrepSmem sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (a.seq_order && blockIdx.x == 0 && blockIdx.y == 0) {  // the scan's CTA order (K's buffer as scratch)
