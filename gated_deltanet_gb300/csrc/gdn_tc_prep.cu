@@ -131,14 +131,15 @@ __global__ void __launch_bounds__(kThreadsPrep, 8) tc_prep_kernel(const PrepArgs
         fence_proxy_async();  // the tensor core reads them
     }
     // in-kernel L2 norm of q, first half: row qr's sum of squares over dk 0-63 (two threads per row, four of its
-    // eight 16-byte pieces each: the swizzle only permutes a row's pieces)
+    // eight 16-byte pieces each: the swizzle only permutes a row's pieces; each row takes its pieces in an
+    // order rotated by the row, so that the eight lanes of a quarter warp read eight different bank groups)
     const int qr = tid >> 1, qh = tid & 1;
     float qss = 0.f;
     auto q_sumsq = [&](const uint8_t *box) {
-        const uint4 *src = (const uint4 *)(box + qr * 128 + qh * 64);
+        const uint8_t *src = box + qr * 128 + qh * 64;
         uint4 x[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = src[j];
+        for (int j = 0; j < 4; ++j) x[j] = *(const uint4 *)(src + ((j + qr) & 3) * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x[j];
