@@ -25,6 +25,7 @@ struct Plan {
     float log2_eps;
     // workspace layout
     size_t off_warm, off_segout, off_seginit, off_tiles, off_gc, off_order, tile_slots, bytes;
+    size_t off_wdec;  // per-channel gates, warmup split: each chunk's bound on the state's log2-decay
     size_t off_h0t, off_htt, off_rk;  // transposed-state copies; 1 / ||k|| per row (in-kernel L2 norm)
     int n_buckets;
     bool kda;  // tensor-core engine with per-channel gates
@@ -95,8 +96,8 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         }
         return GDN_OK;
     }
-    // per-channel gates on the tensor-core engine run without the chunk-parallel split
-    const bool tc_ok = tc_shape_ok(s) && !(channel && (opt.cp_mode == GDN_CP_EXACT || opt.cp_mode == GDN_CP_WARMUP));
+    // per-channel gates on the tensor-core engine take the warmup split, not the exact one
+    const bool tc_ok = tc_shape_ok(s) && !(channel && opt.cp_mode == GDN_CP_EXACT);
     if (opt.engine == GDN_ENGINE_TC && !tc_ok) return GDN_ERR_UNSUPPORTED;
     p->engine = (opt.engine != GDN_ENGINE_SIMT && tc_ok) ? GDN_ENGINE_TC : GDN_ENGINE_SIMT;
     p->kda = p->engine == GDN_ENGINE_TC && channel;
@@ -116,10 +117,14 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
         // kernels (keys L2-normalised, beta = sigmoid of its logit)
         const bool unit_keys = opt.keys_unit_norm || (opt.qk_l2norm && opt.beta_logits);
         cp = GDN_CP_OFF;
-        if (pairs > 0 && unit_keys && base * 2 <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
+        // per-channel gates bound a window's decay by the slowest channel of every token, so their warmup
+        // windows run long and a warmup chunk costs about an emitted one: split them only for four or more
+        // segments per pair
+        const long need = p->kda ? 4 : 2;
+        if (pairs > 0 && unit_keys && base * need <= num_sms && max_nt >= 8) cp = GDN_CP_WARMUP;
         else if (pairs > 0 && base * 4 <= num_sms && max_nt >= 16) cp = GDN_CP_EXACT;
     }
-    if (max_nt <= 1 || p->kda) cp = GDN_CP_OFF;
+    if (max_nt <= 1 || (p->kda && cp == GDN_CP_EXACT)) cp = GDN_CP_OFF;
     int L;
     if (cp == GDN_CP_OFF) {
         L = std::max(max_nt, 1);
@@ -142,6 +147,7 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
 
     size_t off = kStatusBytes;
     p->off_warm = p->off_segout = p->off_seginit = p->off_tiles = p->off_gc = p->off_order = p->tile_slots = 0;
+    p->off_wdec = 0;
     p->n_buckets = 0;
     if (p->engine == GDN_ENGINE_TC) {
         // operand tiles of every chunk, written by the preparation kernel
@@ -151,6 +157,11 @@ gdn_status make_plan(const gdn_shape *s, bool varlen, int chunk_size, const gdn_
             off = align_up(off + p->tile_slots * s->HV * (kKdaTileBytesPerChunk - 512), 256);
             p->off_gc = off;
             off = align_up(off + p->tile_slots * s->HV * 512, 256);
+            if (p->cp == GDN_CP_WARMUP) {
+                // the preparation's per-chunk decay bounds, from which each scan CTA finds its warmup start
+                p->off_wdec = off;
+                off = align_up(off + p->tile_slots * s->HV * sizeof(float), 256);
+            }
         } else {
             off = align_up(off + p->tile_slots * s->HV * kTcTileBytesPerChunk, 256);
         }
@@ -310,6 +321,10 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         ka.T = s->T; ka.H = s->H; ka.HV = s->HV; ka.N = N; ka.slots = (int)p.tile_slots;
         if (p.off_order) { ka.seq_order = (int *)(wsb + p.off_order); ka.n_buckets = p.n_buckets; }
         ka.act = act;
+        if (p.off_wdec) ka.wdec = (float *)(wsb + p.off_wdec);
+        // the warmup split needs beta ||k||^2 <= 2: checked unless the keys are normalised in the kernel
+        ka.check_norm = p.cp == GDN_CP_WARMUP && !opt.qk_l2norm;
+        ka.status = status;
         a.seq_order = ka.seq_order;
         mark();
         e = launch_kda_prep(ka, stream);
@@ -317,6 +332,7 @@ gdn_status run(const gdn_shape *s, const void *q, const void *k, const void *v, 
         a.tiles = ka.tiles;
         a.tile_slots = ka.slots;
         a.kda_gc = ka.gc;
+        a.kda_wdec = ka.wdec;
     } else if (tc) {
         PrepArgs pa{};
         pa.k = k; pa.g = g; pa.beta = beta; pa.cu_seqlens = cu;

@@ -75,6 +75,7 @@ struct ScanArgs {
     float warm_log2_eps;    // threshold of that search (accumulated log2-decay)
     const void *tiles;      // tensor-core engine: operand tiles of tc_prep_kernel / kda_prep_kernel (see tile_slot)
     const float *kda_gc;    // per-channel gates: 2^G_C per (slot, value head, channel)
+    const float *kda_wdec;  //   and, for the warmup split, each chunk's log2-decay bound per (slot, value head)
     int tile_slots;         //   chunk slots of that buffer
     const float *seg_init;  // [N*HV*n_seg][K][V] start state per segment (exact split), nullable
     float *seg_out;         // prepass: [N*HV*n_seg][K][V+K] (S* | M)
@@ -159,6 +160,10 @@ struct KdaPrepArgs {
     const int64_t *cu_seqlens;  // nullable
     void *tiles;                // bf16 [slot][HV][9][64][64] (see gdn_tc_kda.cu)
     float *gc;                  // [slot][HV][128] per-channel chunk decay 2^G_C
+    float *wdec;                // warmup split: [slot][HV] the chunk's bound on the state's log2-decay (the sum
+                                //   over its tokens of the slowest channel's log2-gate); nullable
+    int check_norm;             // warmup split: flag beta ||k||^2 > 2 in the status word
+    unsigned *status;
     int T, H, HV, N, slots;
     int *seq_order;             // as PrepArgs
     int n_buckets;

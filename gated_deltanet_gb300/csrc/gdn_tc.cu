@@ -164,6 +164,29 @@ __device__ __noinline__ int warm_start_of(const float *g, int64_t bos, int64_t l
     return 0;
 }
 
+// The same walk for per-channel gates over the preparation's bound of each chunk's log2-decay
+// (wdec[slot * HV + hv], slot = slot0 + chunk): one warp, lane l takes chunk c - 1 - l, 32 chunks
+// per round trip; an inclusive sum over the lanes finds the first chunk where the window reaches
+// log2_eps.
+__device__ __noinline__ int warm_start_chunks(const float *wdec, int64_t slot0, int HV, int hv, int c0, float log2_eps)
+{
+    const int lane = threadIdx.x & 31;
+    float acc = 0.f;
+    for (int c = c0; c > 0; c -= 32) {
+        const int cc = c - 1 - lane;
+        float v = cc >= 0 ? wdec[(size_t)(slot0 + cc) * HV + hv] : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, cc >= 0 && acc + v <= log2_eps);
+        if (hit) return c - __ffs(hit);
+        acc += __shfl_sync(0xffffffffu, v, 31);
+    }
+    return 0;
+}
+
 template <bool KDA, bool ACT, bool DUMP = false>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a, const __grid_constant__ TcMaps m)
 {
@@ -212,16 +235,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
             // it (which also scans its warmup) and the one before do about equal work: a warmup chunk
             // costs about half an emitted one (no q, no output products, no P, no O epilogue).
             const int L = a.seg_chunks;
+            // per-channel gates: the preparation's per-chunk bounds; scalar gates: the gates themselves
+            auto start = [&](int c) -> int {
+                if constexpr (KDA)
+                    return warm_start_chunks(a.kda_wdec, tile_slot(bos, n, 0), HV, hv, c, a.warm_log2_eps);
+                else
+                    return warm_start_of<ACT>(a.g, bos, len, HV, hv, c, a.warm_log2_eps, a.act);
+            };
             auto bnd = [&](int j) -> int {
                 const int cj = j * L;
                 if (j == 0) return 0;
                 if (cj >= NT) return NT;
-                const int w = cj - warm_start_of<ACT>(a.g, bos, len, HV, hv, cj, a.warm_log2_eps, a.act);
+                const int w = cj - start(cj);
                 return min(cj + (min(w, L) + 2) / 4, NT);
             };
             c0 = bnd(seg);
             c1 = bnd(seg + 1);
-            if (seg > 0) cs = warm_start_of<ACT>(a.g, bos, len, HV, hv, c0, a.warm_log2_eps, a.act);
+            if (seg > 0) cs = start(c0);
         } else if (fwd && seg > 0) {
             if (a.warm_start) {
                 cs = a.warm_start[sidx];
@@ -478,16 +508,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                     mma_commit(&bars[B_VPF]);
                 }
                 __syncwarp();
-                // ---- O^T = S^T Q~^T
-                if (e > 0 && !wait(B_OE, e - 1)) break;
-                tc_fence_after();
-                if (elect_one()) {
+                // ---- O^T = S^T Q~^T (emitted chunks only: a warmup chunk of the split only carries the state)
+                const bool em = emit_of(c);
+                if (em) {
+                    if (e > 0 && !wait(B_OE, e - 1)) break;
+                    tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, dq + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), idV1K,
-                               ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ts(tb + TM_O, tb + TM_SBF + ks * 8, dq + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                   idV1K, ks > 0 ? 1u : 0u);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
                 // ---- S^T += V'^T K^  (B = K^, MN-major: dk atoms 16 KB apart; the per-channel decay is applied
                 //      to S^T by the chain)
                 if (!wait(B_VTF, c)) break;
@@ -500,16 +533,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 }
                 __syncwarp();
                 // ---- O^T += V'^T P^T
-                tc_fence_after();
-                if (elect_one()) {
+                if (em) {
+                    tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ts(tb + TM_O, tb + TM_VB + ks * 8, dp + ks * 2, idV1K, 1u);
-                    mma_commit(&bars[B_OF]);
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ts(tb + TM_O, tb + TM_VB + ks * 8, dp + ks * 2, idV1K, 1u);
+                        mma_commit(&bars[B_OF]);
+                    }
+                    __syncwarp();
+                    ++e;
                 }
-                __syncwarp();
-                ++e;
-                if (elect_one()) mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                if (elect_one()) {
+                    mma_commit(&bars[B_EMPTY + c % kStages]);  // every product reading stage c is issued
+                    // a warmup chunk stores no output: its second arrival is made here, in chunk order (the
+                    // output warps, with no -W^T to wait for, would run ahead of the stage ring)
+                    if (!em) mbar_arrive(&bars[B_EMPTY + c % kStages]);
+                }
                 __syncwarp();
             }
             if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
@@ -983,7 +1023,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_scan_kernel(const ScanArgs a
                 if (lane == 0) mbar_arrive(&bars[B_SBF]);  // (with the chain warps' state copy)
             }
             if (it >= 1 && !emit_of(it - 1)) {
-                if (et == 0) mbar_arrive(&bars[B_EMPTY + (it - 1) % kStages]);  // nothing to store
+                // nothing to store (per-channel gates: the issuer releases a warmup chunk's stage)
+                if (!KDA && et == 0) mbar_arrive(&bars[B_EMPTY + (it - 1) % kStages]);
             } else if (it >= 1) {
                 // ---- O of chunk it - 1 (lane = dv)
                 const int ci = it - 1, c = cs + ci;

@@ -40,6 +40,7 @@ struct KdaSmem {
     __nv_bfloat16 kj[64 * QP];   // k_j 2^(G_r - G_j), r = first row of j's 16-row block
     float beta[64];
     float gc[128];
+    float wpart[8];              // warmup split: each warp's share of the chunk's log-decay bound
 };
 static_assert(64 * KP * sizeof(float) >= 4 * 8192 + 1024, "the U / -W staging boxes fit the G buffer");
 
@@ -129,6 +130,20 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
                 }
             }
         }
+        if (a.wdec) {
+            // warmup split: the chunk's bound on the state's decay, per token the slowest channel's (largest)
+            // log-gate summed over the tokens, as the CUDA-core engine's gate statistics take it; warp w holds
+            // every channel of rows w + 8 i (rows past the end of the sequence are 0)
+            float part = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float m = fmaxf(fmaxf(gv[i].x, gv[i].y), fmaxf(gv[i].z, gv[i].w));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                part += m;
+            }
+            if ((tid & 31) == 0) sh.wpart[tid >> 5] = part;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int e = tid + kThreadsKda * i, r = e >> 4, c8 = (e & 15) * 8;
@@ -144,6 +159,31 @@ __global__ void __launch_bounds__(kThreadsKda, 2) kda_prep_kernel(const KdaPrepA
     }
     if (tid < 64) sh.beta[tid] = tid < rows ? act_beta(a.act, a.beta[(size_t)(t0 + tid) * HV + hv]) : 0.f;
     __syncthreads();
+    if (a.wdec && tid == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreadsKda / 32; ++w) sum += sh.wpart[w];
+        a.wdec[(size_t)slot * HV + hv] = sum * kRcpLn2;
+    }
+    if (a.check_norm) {
+        // the warmup split relies on beta ||k||^2 <= 2 (non-expansive transitions): four threads per row
+        const int r = tid >> 2, pc = tid & 3;
+        const __nv_bfloat16 *row = sh.k + r * QP + 32 * pc;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = *(const uint4 *)(row + 8 * j);
+            const __nv_bfloat162 *h2 = (const __nv_bfloat162 *)&x;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (pc == 0 && r < rows && sh.beta[r] * ss > 2.0001f) atomicOr(a.status, kStatusNormBound);
+    }
     if (a.act.qk_l2norm) {
         // in-kernel L2 norm: the rows of k and q to unit length (fp32 arithmetic, one bf16 rounding, as
         // every operand of the products below is bf16); two threads per row, eight 16-byte pieces each

@@ -82,10 +82,27 @@ def test_plans(gdn):
     # fp32 or other head dims: CUDA-core engine
     p = gdn.plan(4, 4096, 16, 16, 128, 128, dtype="f32", num_sms=152)
     assert p.engine == 1 and p.value_tiles == 4
-    # per-key-channel gates, bf16, dk = dv = 128: tensor-core engine with its own chunk preparation,
-    # never split; a requested split keeps them on the CUDA-core engine
+    # per-key-channel gates, bf16, dk = dv = 128: tensor-core engine with its own chunk preparation;
+    # with unit-norm keys and few pairs the warmup split (each scan CTA walks the preparation's per-chunk
+    # decay bounds), without that assertion no split; a requested exact split keeps them on the
+    # CUDA-core engine
+    # (AUTO splits them for four or more segments per pair: 64 pairs stay whole, 8 pairs split)
     p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152, keys_unit_norm=True)
     assert p.engine == 2 and p.cp_mode == 1 and p.segments == 1 and p.kernels == 2
+    p = gdn.plan(2, 8192, 32, 32, 128, 128, gate="channel", num_sms=152, keys_unit_norm=True)
+    assert p.engine == 2 and p.cp_mode == 1
+    p = gdn.plan(1, 16384, 8, 8, 128, 128, gate="channel", num_sms=152, keys_unit_norm=True)
+    assert p.engine == 2 and p.cp_mode == 3 and p.segments >= 4 and p.kernels == 2
+    p = gdn.plan(1, 16384, 8, 8, 128, 128, gate="channel", num_sms=152, qk_l2norm=True, beta_logits=True)
+    assert p.engine == 2 and p.cp_mode == 3
+    p = gdn.plan(2, 8192, 32, 32, 128, 128, gate="channel", num_sms=152, cp_mode="warmup", keys_unit_norm=True)
+    assert p.engine == 2 and p.cp_mode == 3 and p.segments == 2
+    p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152)
+    assert p.engine == 2 and p.cp_mode == 1 and p.segments == 1 and p.kernels == 2
+    p = gdn.plan(32, 4096, 16, 16, 128, 128, gate="channel", num_sms=152, keys_unit_norm=True)
+    assert p.engine == 2 and p.cp_mode == 1
+    p = gdn.plan(1, 64 * 14, 2, 2, 128, 128, gate="channel", num_sms=152, cp_mode="warmup", segment_chunks=3)
+    assert p.engine == 2 and p.cp_mode == 3 and p.segments == 5
     p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", num_sms=152, cp_mode="exact")
     assert p.engine == 1
     p = gdn.plan(4, 4096, 16, 16, 128, 128, gate="channel", dtype="f32", num_sms=152)

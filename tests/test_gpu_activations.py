@@ -75,6 +75,10 @@ CASES = [
      {}),
     ("tc_channel", dict(B=1, T=64 * 3 + 7, H=2, HV=2, K=128, V=128, dtype="bf16", gate="channel",
                         lower_bound=-5.0), "tc", {}),
+    # per-channel gates, few pairs, normalised keys and sigmoid beta: the planner's warmup split on the
+    # tensor-core engine (three segments), with decay bounds taken from the activated gates
+    ("tc_channel_auto_split", dict(B=1, T=64 * 12 + 5, H=2, HV=2, K=128, V=128, dtype="bf16", gate="channel",
+                                   lower_bound=-5.0), "tc", {}),
     ("recurrent_bf16", dict(B=3, T=5, H=2, HV=4, K=128, V=128, dtype="bf16", gate="scalar"), "recurrent", {}),
     ("recurrent_channel", dict(B=2, T=3, H=2, HV=2, K=64, V=64, dtype="f32", gate="channel"), "recurrent", {}),
 ]

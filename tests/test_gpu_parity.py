@@ -167,6 +167,41 @@ def test_split_modes_varlen(gdn):
         check(gdn, w, cp_mode=mode, segment_chunks=2, keys_unit_norm=True, max_seq_len=900)
 
 
+@pytest.mark.parametrize("seg", [3, 5])
+def test_channel_warmup_split_tc(gdn, seg):
+    """Per-key-channel gates with the warmup split on the tensor-core engine: each scan CTA walks back
+    over the preparation's per-chunk decay bounds (per token the slowest channel's log-gate) from its
+    start.  Gates with g = logsigmoid(N(0, 1)) bound the decay at about 2^-6.6 per chunk, so the later
+    segments start from a truncated warmup window (about four chunks), the earlier ones from the
+    sequence start."""
+    w = Workload("ch_warm", B=1, T=64 * 14 + 9, H=2, K=128, V=128, gate="channel", h0=True, g_mu=0.0,
+                 seed=41)
+    opts = dict(engine="tc", cp_mode="warmup", segment_chunks=seg, keys_unit_norm=True)
+    info = gdn.plan(w.B, w.T, w.H, w.hv, w.K, w.V, w.dtype, w.gate, num_seqs=w.B, num_sms=_sms(), **opts)
+    assert info.engine == 2 and info.cp_mode == 3 and info.segments > 2
+    check(gdn, w, **opts)
+
+
+def test_channel_warmup_split_tc_varlen(gdn):
+    w = Workload("ch_warm_varlen", B=1, T=900, H=2, K=128, V=128, gate="channel", h0=True, g_mu=0.0,
+                 varlen=4, seed=42)
+    check(gdn, w, engine="tc", cp_mode="warmup", segment_chunks=2, keys_unit_norm=True, max_seq_len=900)
+
+
+def test_channel_warmup_flags_long_keys(gdn):
+    """The warmup split relies on beta ||k||^2 <= 2; the per-channel preparation flags keys that break
+    it (GDN_ERR_INVALID from the status word, which reading clears)."""
+    w = Workload("ch_norm", B=1, T=64 * 6, H=2, K=128, V=128, gate="channel", seed=43)
+    x = make_inputs(w, device="cuda")
+    x["k"] = (x["k"].float() * 3.0).to(torch.bfloat16)
+    gdn.chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], True,
+                               x["cu_seqlens"], engine="tc", cp_mode="warmup", segment_chunks=2,
+                               keys_unit_norm=True)
+    torch.cuda.synchronize()
+    assert gdn.read_device_status() == -1
+    assert gdn.read_device_status() == 0
+
+
 @pytest.mark.parametrize("gate", ["scalar", "channel"])
 def test_empty_and_single_token_sequences_tc(gdn, gate):
     """The tensor-core engine (bf16, d = 128) on empty, one-token and exact-chunk sequences."""
@@ -275,8 +310,19 @@ def test_workload_varlen_bf16(gdn):
     check(gdn, w, **bench_options(w))
 
 
-def test_workload_channel_bf16(gdn):
-    check(gdn, WORKLOADS["channel_bf16"])
+@pytest.mark.parametrize("split", [False, True])
+def test_workload_channel_bf16(gdn, split):
+    """The full per-channel workload in the plan bench.py times (64 pairs: no split), and with the
+    warmup split requested (two segments, warmup windows of about 70 chunks by the slowest channel's
+    bound)."""
+    from bench import bench_options
+    w = WORKLOADS["channel_bf16"]
+    opts = bench_options(w)
+    if split:
+        opts["cp_mode"] = "warmup"
+    info = gdn.plan(w.B, w.T, w.H, w.hv, w.K, w.V, w.dtype, w.gate, num_seqs=w.B, num_sms=_sms(), **opts)
+    assert info.engine == 2 and info.cp_mode == (3 if split else 1)
+    check(gdn, w, **opts)
 
 
 @pytest.mark.parametrize("name", ["bf16_varlen_many", "bf16_channel_varlen", "bf16_mixed_decay", "bf16_gva"])
