@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "local_cumsum", "fla_form", "qla_form", "channel_form", "forward_substitution",
     "blocked_inverse", "cp_exact_deltanet", "cp_exact_qla", "cp_warmup",
-    "warmup_start", "run_pairs",
+    "warmup_start", "chunk_decay_bounds", "run_pairs",
 ]
 
 
@@ -291,13 +291,29 @@ def warmup_start(chunk_gate_sums, seg_first_chunk, log_eps, max_chunks=None):
     return 0
 
 
+def chunk_decay_bounds(g, C):
+    """Per chunk, the log of a bound on how far the chunk's transitions contract
+    the state (the gate statistics of the warmup split).  One token's transition
+    A_t = (I - beta_t k_t k_t^T) Diag(alpha_t) has spectral norm at most
+    max_d alpha_{t,d}, since ||k|| <= 1 and beta in [0, 2] keep the first factor's
+    norm at most 1; a chunk therefore contracts the state by at most the product of
+    those maxima.  In logs: the sum over the chunk's tokens of the largest
+    per-channel log-gate; for a scalar gate, of the gate itself.  (Reading for
+    per-channel gates: the per-channel products over a chunk are not a bound,
+    because the delta-rule factor moves state between channels.)"""
+    gt = g if g.ndim == 1 else g.max(axis=1)
+    return [float(np.sum(gt[s:e])) for (s, e) in _chunk_bounds(gt.shape[0], C)]
+
+
 def cp_warmup(q, k, v, g, beta, scale, S0, C, seg_chunks, log_eps):
     """Gate-driven warmup split: each segment j > 0 recomputes its start state
-    from zero over the warmup chunks chosen by :func:`warmup_start` (or from the
-    true initial state when the walk reaches the sequence start), then emits
-    its own chunks.  Scalar gate only."""
+    from zero over the warmup chunks chosen by :func:`warmup_start` on the
+    :func:`chunk_decay_bounds` (or from the true initial state when the walk
+    reaches the sequence start), then emits its own chunks.  Scalar gate
+    (:func:`qla_form`) or per-key-channel gate (:func:`channel_form`)."""
     bounds = _chunk_bounds(q.shape[0], C)
-    sums = [float(np.sum(g[s:e])) for (s, e) in bounds]
+    sums = chunk_decay_bounds(g, C)
+    form = qla_form if g.ndim == 1 else channel_form
     o = np.zeros((q.shape[0], v.shape[1]))
     S_end = None
     starts = []
@@ -307,10 +323,10 @@ def cp_warmup(q, k, v, g, beta, scale, S0, C, seg_chunks, log_eps):
         S = np.array(S0, dtype=np.float64) if w == 0 else np.zeros_like(S0, dtype=np.float64)
         ws, s0, e1 = bounds[w][0], bounds[c0][0], bounds[c1 - 1][1]
         if s0 > ws:
-            _, S = qla_form(q[ws:s0], k[ws:s0], v[ws:s0], g[ws:s0], beta[ws:s0], scale, S, C)
+            _, S = form(q[ws:s0], k[ws:s0], v[ws:s0], g[ws:s0], beta[ws:s0], scale, S, C)
         starts.append(S)
-        o[s0:e1], S_end = qla_form(q[s0:e1], k[s0:e1], v[s0:e1], g[s0:e1], beta[s0:e1],
-                                   scale, S, C)
+        o[s0:e1], S_end = form(q[s0:e1], k[s0:e1], v[s0:e1], g[s0:e1], beta[s0:e1],
+                               scale, S, C)
     return o, S_end, starts
 
 

@@ -331,6 +331,70 @@ def test_warmup_start_walk():
     assert cw.warmup_start(sums, 2, -100.0) == 0
 
 
+def test_transition_norm_is_bounded_by_the_slowest_channel():
+    """||(I - beta k k^T) Diag(alpha)||_2 <= max_d alpha_d for ||k|| = 1, beta in [0, 2] (the
+    inequality behind the warmup split's gate statistics), checked by SVD, beta = 0 and 2 included;
+    with beta = 0 it is attained."""
+    rng = np.random.default_rng(61)
+    for trial in range(200):
+        K = int(rng.integers(2, 17))
+        kv = rng.standard_normal(K)
+        kv /= np.linalg.norm(kv)
+        beta = [0.0, 2.0, float(rng.uniform(0, 2))][trial % 3]
+        alpha = rng.uniform(0.0, 1.0, K)
+        A = (np.eye(K) - beta * np.outer(kv, kv)) @ np.diag(alpha)
+        nrm = np.linalg.norm(A, 2)
+        assert nrm <= alpha.max() * (1 + 1e-12)
+        if beta == 0.0:
+            assert abs(nrm - alpha.max()) <= 1e-12
+
+
+def test_per_channel_products_are_not_a_decay_bound():
+    """Two channels that take turns decaying, and a reflection (beta = 2, k = (e0 - e1)/sqrt 2) that swaps
+    them every token: every channel's own product decays by 0.1 every other token, yet the state keeps
+    its norm, since it always sits in the channel that does not decay.  chunk_decay_bounds (per token the
+    slowest channel) gives no decay here, as it must."""
+    T = 16
+    kv = np.array([1.0, -1.0]) / np.sqrt(2.0)
+    P = np.eye(2) - 2.0 * np.outer(kv, kv)
+    assert np.allclose(P, [[0.0, 1.0], [1.0, 0.0]])
+    g = np.log(np.array([[1.0, 0.1] if t % 2 == 0 else [0.1, 1.0] for t in range(T)]))
+    S = np.array([1.0, 0.0])
+    for t in range(T):
+        S = P @ (np.exp(g[t]) * S)
+    assert abs(np.linalg.norm(S) - 1.0) < 1e-12
+    per_channel = g.sum(axis=0)
+    assert per_channel.max() < -18.0  # each channel alone would claim a decay of 1e-8
+    assert cw.chunk_decay_bounds(g, C=T) == [0.0]
+
+
+def test_chunk_decay_bounds_scalar_is_the_gate_sum():
+    g = np.array([-0.5, -1.0, -0.25, -2.0, -0.125])
+    assert cw.chunk_decay_bounds(g, C=2) == [-1.5, -2.25, -0.125]
+    gc = np.array([[-0.5, -3.0], [-2.0, -1.0], [-0.25, -0.75]])
+    assert cw.chunk_decay_bounds(gc, C=2) == [-1.5, -0.25]
+
+
+def test_cp_warmup_channel_error_within_bound():
+    """The warmup split with per-channel gates, windows chosen on the slowest-channel bound: within
+    the bound's attenuation of the exact result, and exact when every window reaches the sequence start."""
+    x = small_case(seed=53, B=1, H=1, T=640, K=16, V=8, gate="channel", g_mu=0.0)
+    o, ht = run_oracle(x)
+    log_eps = math.log(2.0 ** -24)
+    o2, ht2 = cw.run_pairs(cw.cp_warmup, x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
+                           x["h0"], C=16, seg_chunks=8, log_eps=log_eps)
+    assert rel(ht2, ht) < 1e-6 and rel(o2, o) < 1e-6
+    # the windows are truncated here (the bound reaches 2^-24 within the sequence), so the split is not
+    # the exact recurrence
+    g0 = np.asarray(x["g"])[0, :, 0]
+    sums = cw.chunk_decay_bounds(g0, 16)
+    assert cw.warmup_start(sums, 32, log_eps) > 0
+    # with a threshold no window reaches, every segment starts from the true initial state: exact
+    o3, ht3 = cw.run_pairs(cw.cp_warmup, x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
+                           x["h0"], C=16, seg_chunks=8, log_eps=-1e9)
+    assert rel(o3, o) < 1e-10 and rel(ht3, ht) < 1e-10
+
+
 # ---------------------------------------------------------------- step a1: the chunk-local gate cumsum
 def test_local_cumsum_golden():
     """Hand-worked cumsums ("Flash Linear Attention" page, sec. 3, chunk_local_cumsum; sec. 2 for
