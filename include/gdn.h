@@ -81,9 +81,13 @@ typedef struct {
 typedef enum {
     GDN_CP_AUTO = 0,   /* planner decides (split only when (seq, head) pairs are few) */
     GDN_CP_OFF = 1,    /* one serial scan per (sequence, head)                        */
-    GDN_CP_EXACT = 2,  /* segments start from S* = 0, M = I; serial S* / M combine      */
+    GDN_CP_EXACT = 2,  /* segments start from S* = 0, M = I; serial S* / M combine
+                          (per-channel gates: on the SIMT engine)                    */
     GDN_CP_WARMUP = 3  /* segments re-derive their start state from zero over a
-                          warmup window sized from the gate statistics               */
+                          warmup window sized from the gate statistics (per-channel
+                          gates: each token's slowest channel bounds its decay; AUTO
+                          picks it for them on the TC engine only when the (sequence,
+                          head) pairs fill at most a quarter of the SMs)             */
 } gdn_cp_mode;
 
 typedef enum {
