@@ -73,7 +73,7 @@ struct TcLayout {
 
 // gate arrays inside a stage's gate block
 constexpr int GT_G = 0, GT_GRAW = 64, GT_GAM = 128, GT_RDEC = 192, GT_GINV = 256, GT_SGAM = 320,
-              GT_RK = 384, GT_RQ = 448;  // in-kernel L2 norm: 1 / ||k_t|| (from the preparation), 1 / ||q_t||
+              GT_RK = 384, GT_RQ = 448;  // in-kernel L2 norm: 1 / ||k_t||, 1 / ||q_t|| (both from the preparation)
 // G_C >= this: Gam_ij = gam_i * 2^-G_j with every factor inside the fp32 range
 constexpr float kFactorFloor = -100.f;
 
